@@ -1,0 +1,126 @@
+"""FP64 CPU oracle for the row-normalisation kernels (ctypes over ``oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline / reference leg import this package.  The CUDA library never
+imports, links or calls it, and there is no CPU fallback anywhere in the
+product path.
+
+The C source (``oracle.c``) is the authority; this module only compiles it
+with gcc, loads it and marshals numpy arrays.  Every function takes the exact
+FP32 inputs given to the GPU and returns FP64 outputs.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(HERE, "oracle.c")
+LIBRARY = os.path.join(HERE, "liboracle.so")
+
+#: gcc flags: IEEE FP64, no FMA contraction, so x86 and Arm agree bit for bit.
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+_lock = threading.Lock()
+_default = None
+
+
+def build(source: str = SOURCE, output: str = LIBRARY, force: bool = False) -> str:
+    """Compile ``source`` into the shared library ``output`` (if stale)."""
+    if (not force and os.path.exists(output)
+            and os.path.getmtime(output) >= os.path.getmtime(source)):
+        return output
+    tmp = output + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, "-o", tmp, source, "-lm"], check=True)
+    os.replace(tmp, output)
+    return output
+
+
+class Oracle:
+    """One loaded copy of the oracle library."""
+
+    def __init__(self, path: str):
+        self.path = path
+        lib = ctypes.CDLL(path)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        L, D = ctypes.c_long, ctypes.c_double
+        lib.oracle_residual_layernorm.argtypes = [f32p, f32p, f64p, L, L, D]
+        lib.oracle_layernorm.argtypes = [f32p, f64p, L, L, D]
+        lib.oracle_rmsnorm.argtypes = [f32p, f64p, L, L, D]
+        lib.oracle_softmax.argtypes = [f32p, f64p, L, L]
+        for fn in (lib.oracle_residual_layernorm, lib.oracle_layernorm,
+                   lib.oracle_rmsnorm, lib.oracle_softmax):
+            fn.restype = None
+        self._lib = lib
+
+    @staticmethod
+    def _f32(a):
+        a = np.ascontiguousarray(a, dtype=np.float32)
+        if a.ndim != 2:
+            raise ValueError("oracle inputs are 2-D [rows, width]")
+        return a
+
+    @staticmethod
+    def _p(a, ct):
+        return a.ctypes.data_as(ctypes.POINTER(ct))
+
+    def residual_layernorm(self, x, r, eps=1e-5):
+        x, r = self._f32(x), self._f32(r)
+        if x.shape != r.shape:
+            raise ValueError("x and residual shapes differ")
+        y = np.empty(x.shape, dtype=np.float64)
+        if x.size:
+            self._lib.oracle_residual_layernorm(
+                self._p(x, ctypes.c_float), self._p(r, ctypes.c_float),
+                self._p(y, ctypes.c_double), x.shape[0], x.shape[1], float(eps))
+        return y
+
+    def layernorm(self, x, eps=1e-5):
+        x = self._f32(x)
+        y = np.empty(x.shape, dtype=np.float64)
+        if x.size:
+            self._lib.oracle_layernorm(self._p(x, ctypes.c_float), self._p(y, ctypes.c_double),
+                                       x.shape[0], x.shape[1], float(eps))
+        return y
+
+    def rmsnorm(self, x, eps=1e-5):
+        x = self._f32(x)
+        y = np.empty(x.shape, dtype=np.float64)
+        if x.size:
+            self._lib.oracle_rmsnorm(self._p(x, ctypes.c_float), self._p(y, ctypes.c_double),
+                                     x.shape[0], x.shape[1], float(eps))
+        return y
+
+    def softmax(self, x, eps=None):
+        x = self._f32(x)
+        y = np.empty(x.shape, dtype=np.float64)
+        if x.size:
+            self._lib.oracle_softmax(self._p(x, ctypes.c_float), self._p(y, ctypes.c_double),
+                                     x.shape[0], x.shape[1])
+        return y
+
+    def run(self, op: str, x, r=None, eps=1e-5):
+        """Dispatch by library op name."""
+        if op == "residual_layernorm":
+            return self.residual_layernorm(x, r, eps)
+        return getattr(self, op)(x, eps)
+
+
+def get() -> Oracle:
+    """The oracle built from ``oracle.c`` (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+        return _default
+
+
+def kernel_eps(eps: float = 1e-5) -> float:
+    """The FP32 value of ``eps`` widened to FP64: what the kernel receives."""
+    return float(np.float32(eps))

@@ -1,0 +1,249 @@
+"""Pins of the FP64 oracle against things other than itself.
+
+``check_all(orc)`` runs every pin against one loaded oracle and returns the
+list of failures (empty when the oracle is right).  The same checks run on
+the real oracle (all must pass) and on copies of it with a planted mistake
+(at least one must fail), see ``test_oracle_mutations.py``.
+
+Pins used:
+  * hand-worked golden cases in ``tests/golden`` (exact rationals derived by
+    hand from the definitions on the pages);
+  * closed forms: constant rows, +-a rows, softmax of logarithms;
+  * invariants that follow from the definitions: LayerNorm output has mean 0
+    and variance var/(var+eps); RMSNorm output has mean square
+    ms/(ms+eps); softmax rows sum to 1 and y_i/y_j = exp(x_i - x_j); shift
+    and scale invariance; permutation equivariance; residual symmetry;
+    row independence;
+  * a library special case: torch's CPU FP64 layer_norm / rms_norm / softmax.
+"""
+
+from __future__ import annotations
+
+import glob
+import math
+import os
+from decimal import Decimal, getcontext
+from fractions import Fraction
+
+import numpy as np
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+getcontext().prec = 50
+
+
+# ---------------------------------------------------------------------------
+# golden fixtures
+# ---------------------------------------------------------------------------
+
+def load_golden(path):
+    case = {"x": [], "r": [], "numer": [], "den": [], "expect": [], "atol": 0.0}
+    with open(path) as fh:
+        for line in fh:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, val = [s.strip() for s in line.split(":", 1)]
+            if key == "op":
+                case["op"] = val
+            elif key == "eps":
+                case["eps"] = val
+            elif key == "atol":
+                case["atol"] = float(val)
+            elif key in ("x", "r"):
+                case[key].append([float(v) for v in val.split()])
+            elif key in ("numer", "expect"):
+                case[key].append([Fraction(v) for v in val.split()])
+            elif key == "den":
+                case[key].append(Fraction(val))
+            else:
+                raise ValueError(f"{path}: unknown key {key}")
+    return case
+
+
+def golden_expected(case):
+    """Expected outputs of a golden case, evaluated to 50 digits."""
+    if case["op"] == "softmax":
+        return np.array([[float(Decimal(f.numerator) / Decimal(f.denominator)) for f in row]
+                         for row in case["expect"]])
+    eps = Decimal(case["eps"])
+    out = []
+    for numer, den in zip(case["numer"], case["den"]):
+        root = (Decimal(den.numerator) / Decimal(den.denominator) + eps).sqrt()
+        out.append([float(Decimal(f.numerator) / Decimal(f.denominator) / root) for f in numer])
+    return np.array(out)
+
+
+def golden_cases():
+    return sorted(p for p in glob.glob(os.path.join(GOLDEN, "*.txt"))
+                  if os.path.basename(p) != "README.txt")
+
+
+def _run_golden(orc, path):
+    case = load_golden(path)
+    if "op" not in case:
+        return None
+    x = np.array(case["x"], dtype=np.float32)
+    eps = float(case.get("eps", "1e-5"))
+    if case["op"] == "residual_layernorm":
+        y = orc.residual_layernorm(x, np.array(case["r"], dtype=np.float32), eps)
+    else:
+        y = orc.run(case["op"], x, eps=eps)
+    want = golden_expected(case)
+    tol = 1e-12 + case["atol"] + 1e-12 * np.abs(want)
+    if y.shape != want.shape or not np.all(np.abs(y - want) <= tol):
+        return f"golden {os.path.basename(path)}: got {y.tolist()} want {want.tolist()}"
+    return None
+
+
+# ---------------------------------------------------------------------------
+# closed forms and invariants on seeded inputs
+# ---------------------------------------------------------------------------
+
+def _seeded(rows, width, seed, sigma=None):
+    n = rows * width
+    v = synth.uniform_pm1(seed, n) if sigma is None else synth.normal(seed, n, sigma)
+    return v.reshape(rows, width)
+
+
+def _close(a, b, tol):
+    return a.shape == b.shape and bool(np.all(np.abs(a - b) <= tol))
+
+
+def _pins_layernorm(orc):
+    fails = []
+    eps = 1e-5
+    x = _seeded(9, 257, 11)
+    y = orc.layernorm(x, eps)
+    var_x = x.astype(np.float64).var(axis=1)
+    if not np.all(np.abs(y.mean(axis=1)) <= 1e-12):
+        fails.append("layernorm: row mean of output is not 0")
+    if not _close(y.var(axis=1), var_x / (var_x + eps), 1e-12):
+        fails.append("layernorm: output variance != var/(var+eps)")
+    # shift by an exactly representable constant, scale by 2 (eps = 0)
+    if not _close(orc.layernorm(x + np.float32(0.5), eps), y, 1e-12):
+        fails.append("layernorm: not shift invariant")
+    if not _close(orc.layernorm(2 * x, 0.0), orc.layernorm(x, 0.0), 1e-12):
+        fails.append("layernorm: not scale invariant at eps=0")
+    # permutation equivariance and row independence
+    if not _close(orc.layernorm(x[:, ::-1], eps), y[:, ::-1], 1e-13):
+        fails.append("layernorm: not permutation equivariant")
+    single = np.vstack([orc.layernorm(x[i:i + 1], eps) for i in range(x.shape[0])])
+    if not np.array_equal(single, y):
+        fails.append("layernorm: rows not independent")
+    # constant rows of non-dyadic values give exactly 0
+    c = np.full((3, 1000), np.float32(0.1), dtype=np.float32)
+    if not np.all(np.abs(orc.layernorm(c, eps)) <= 1e-9):
+        fails.append("layernorm: constant row is not 0")
+    return fails
+
+
+def _pins_residual(orc):
+    fails = []
+    eps = 1e-5
+    x = _seeded(7, 1537, 21)
+    r = _seeded(7, 1537, 22)
+    y = orc.residual_layernorm(x, r, eps)
+    if not _close(orc.residual_layernorm(r, x, eps), y, 1e-13):
+        fails.append("residual_layernorm: not symmetric in (x, residual)")
+    zero = np.zeros_like(x)
+    if not _close(orc.residual_layernorm(x, zero, eps), orc.layernorm(x, eps), 1e-13):
+        fails.append("residual_layernorm(x, 0) != layernorm(x)")
+    c = (x.astype(np.float64) + r.astype(np.float64))
+    var_c = c.var(axis=1)
+    if not np.all(np.abs(y.mean(axis=1)) <= 1e-12):
+        fails.append("residual_layernorm: row mean of output is not 0")
+    if not _close(y.var(axis=1), var_c / (var_c + eps), 1e-12):
+        fails.append("residual_layernorm: output variance != var/(var+eps)")
+    single = np.vstack([orc.residual_layernorm(x[i:i + 1], r[i:i + 1], eps) for i in range(7)])
+    if not np.array_equal(single, y):
+        fails.append("residual_layernorm: rows not independent")
+    return fails
+
+
+def _pins_rmsnorm(orc):
+    fails = []
+    eps = 1e-5
+    x = _seeded(5, 4096, 31, sigma=3.0)
+    y = orc.rmsnorm(x, eps)
+    ms = (x.astype(np.float64) ** 2).mean(axis=1)
+    if not _close((y ** 2).mean(axis=1), ms / (ms + eps), 1e-12):
+        fails.append("rmsnorm: output mean square != ms/(ms+eps)")
+    if not _close(orc.rmsnorm(x[:, ::-1], eps), y[:, ::-1], 1e-13):
+        fails.append("rmsnorm: not permutation equivariant")
+    # +-a rows: y = +-a / sqrt(a^2 + eps)
+    a = np.float32(0.3)
+    pm = np.where(np.arange(64) % 3 == 0, a, -a).astype(np.float32)[None, :]
+    want = np.sign(pm.astype(np.float64)) * float(a) / math.sqrt(float(a) ** 2 + eps)
+    if not _close(orc.rmsnorm(pm, eps), want, 1e-14):
+        fails.append("rmsnorm: +-a row is not +-a/sqrt(a^2+eps)")
+    single = np.vstack([orc.rmsnorm(x[i:i + 1], eps) for i in range(x.shape[0])])
+    if not np.array_equal(single, y):
+        fails.append("rmsnorm: rows not independent")
+    return fails
+
+
+def _pins_softmax(orc):
+    fails = []
+    x = _seeded(6, 8192, 41, sigma=3.0)
+    x[1, 100] = np.float32(40.0)
+    y = orc.softmax(x)
+    if not _close(y.sum(axis=1), np.ones(6), 1e-12):
+        fails.append("softmax: rows do not sum to 1")
+    if not np.all(y > 0):
+        fails.append("softmax: non-positive output")
+    i, j = 17, 4000
+    ratio = y[:, i] / y[:, j]
+    want = np.exp(x[:, i].astype(np.float64) - x[:, j].astype(np.float64))
+    if not _close(ratio / want, np.ones(6), 1e-12):
+        fails.append("softmax: y_i/y_j != exp(x_i - x_j)")
+    u = _seeded(3, 1000, 42)       # values k/2^23 in [-1, 1): +0.5 is exact
+    if not _close(orc.softmax(u + np.float32(0.5)), orc.softmax(u), 1e-15):
+        fails.append("softmax: not shift invariant")
+    if not _close(orc.softmax(x[:, ::-1]), y[:, ::-1], 1e-12):
+        fails.append("softmax: not permutation equivariant")
+    c = np.full((2, 300), np.float32(-1.7), dtype=np.float32)
+    if not _close(orc.softmax(c), np.full((2, 300), 1.0 / 300), 1e-15):
+        fails.append("softmax: constant row is not 1/width")
+    single = np.vstack([orc.softmax(x[k:k + 1]) for k in range(x.shape[0])])
+    if not np.array_equal(single, y):
+        fails.append("softmax: rows not independent")
+    return fails
+
+
+def _pins_torch(orc):
+    """Library special case: torch's CPU FP64 functional ops."""
+    import torch
+    import torch.nn.functional as F
+    fails = []
+    eps = 1e-5
+    x = _seeded(8, 1537, 51)
+    r = _seeded(8, 1537, 52)
+    tx = torch.from_numpy(x).double()
+    tr = torch.from_numpy(r).double()
+    checks = [
+        ("layernorm", orc.layernorm(x, eps), F.layer_norm(tx, (1537,), eps=eps)),
+        ("residual_layernorm", orc.residual_layernorm(x, r, eps),
+         F.layer_norm(tx + tr, (1537,), eps=eps)),
+        ("rmsnorm", orc.rmsnorm(x, eps), F.rms_norm(tx, (1537,), eps=eps)),
+        ("softmax", orc.softmax(x), torch.softmax(tx, dim=1)),
+    ]
+    for name, got, want in checks:
+        if not _close(got, want.numpy(), 1e-12):
+            fails.append(f"{name}: differs from torch FP64")
+    return fails
+
+
+def check_all(orc):
+    fails = []
+    for path in golden_cases():
+        f = _run_golden(orc, path)
+        if f:
+            fails.append(f)
+    for group in (_pins_layernorm, _pins_residual, _pins_rmsnorm, _pins_softmax, _pins_torch):
+        try:
+            fails.extend(group(orc))
+        except Exception as exc:  # a mutant may produce NaN shapes etc.
+            fails.append(f"{group.__name__}: raised {exc!r}")
+    return fails
