@@ -1,0 +1,456 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused FP32 row-normalisation library on one GB300.
+
+One step = one call of ``tile_residual_layernorm_f32`` on a 65536x4096 FP32
+matrix (x and residual read once, y written once: 12 bytes per element,
+3 GiB per step).  Inputs are seeded synthetic uniform[-1, 1) values, resident
+in HBM before the timed region; the 3 GiB working set is far larger than the
+129 MB L2, so no flush is needed between steps.
+
+Printed: one JSON line with the device-timed throughput (algorithmic GB/s),
+the end-to-end throughput through the C ABI with host buffers (copies in the
+timed region), the roofline of the kernel against the measured HBM copy
+bandwidth, the SM clocks seen during the run, and the FP64 CPU oracle timed
+on this host as a baseline.
+
+  python bench.py [--gpus N --steps K --warmup W]        our CUDA library
+  python bench.py --impl reference ...                    the CPU oracle
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent replicas, no collective on the data path); the timed region is
+bracketed by barriers and the maximum time over ranks is used.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "HBM GB/s (% of GB300 peak) and µs/call, residual LayerNorm FP32 65536×4096"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+BYTES_PER_ELEM = {"residual_layernorm": 12, "layernorm": 8, "rmsnorm": 8, "softmax": 8}
+EPS = 1e-5
+SEED_CFG = 5
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--rows", type=int, default=65536, help="rows (profiling runs use fewer)")
+    ap.add_argument("--width", type=int, default=4096)
+    ap.add_argument("--op", default="residual_layernorm", choices=sorted(BYTES_PER_ELEM))
+    ap.add_argument("--no-extra", action="store_true", help="skip the RMSNorm/softmax lines")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--plan", type=int, default=None, help="force a built plan (sweeps)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self, gpus):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if gpus != self.world and self.world > 1:
+            raise SystemExit(f"--gpus {gpus} but WORLD_SIZE={self.world}")
+
+    def init(self, backend="nccl"):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            import torch
+            self.pg.barrier(device_ids=[torch.cuda.current_device()])
+
+    def max(self, value):
+        if self.pg is None:
+            return value
+        import torch
+        t = torch.tensor([value], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 50 ms while the GPU is under load."""
+
+    def __init__(self, gpu_selector):
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.selector = gpu_selector
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.selector:
+            cmd += ["-i", self.selector]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)       # let the first samples arrive
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                self.samples.append({
+                    "t": time.perf_counter(), "sm": float(parts[1]), "sm_max": float(parts[2]),
+                    "power": float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else None,
+                    "hw_slowdown": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7],
+                    "sw_power_cap": parts[8]})
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s["t"] <= t1]
+        use = inside if inside else self.samples
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi gave no samples"}
+        reasons = set()
+        for s in use:
+            for key, name in (("hw_slowdown", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power_cap", "sw_power_cap")):
+                if s[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s["sm"] for s in use),
+                "sm_max_mhz": max(s["sm_max"] for s in use),
+                "reasons": sorted(reasons), "samples": len(use),
+                "window": "timed region" if inside else "warm-up and timed region"}
+
+
+def gpu_selector():
+    try:
+        import torch
+        uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            mp = json.load(fh)
+        return float(mp["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(op, rows, width):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source that is built now (else None)."""
+    from tile_compiler_row_gb300 import _build
+    path = os.path.join(ROOT, "profiles", f"{op}_{rows}x{width}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        line = line.strip().lstrip("-* ").strip()
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip().strip("`")] = v.strip().strip("`")
+    if fields.get("source_sha256") != _build.source_hash():
+        return None
+    try:
+        return int(float(fields["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+def time_calls(fn, steps, stream):
+    """Per-call CUDA-event durations (ms) of ``steps`` back-to-back calls on
+    ``stream``, plus the total elapsed (ms) between the first and last event."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record(stream)
+    for i in range(steps):
+        fn()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+    return per, evs[0].elapsed_time(evs[-1])
+
+
+# ---------------------------------------------------------------------------
+# our CUDA library
+# ---------------------------------------------------------------------------
+
+def run_ours(args, dist):
+    import numpy as np
+    import torch
+
+    import synth
+    import tile_compiler_row_gb300 as tile
+    from tile_compiler_row_gb300 import _build
+
+    _build.build()
+    lib = tile.load()
+    torch.cuda.set_device(dist.local_rank)
+    dist.init("nccl")
+    stream = torch.cuda.current_stream()
+    rows, width, op = args.rows, args.width, args.op
+    elems = rows * width
+    nbytes = BYTES_PER_ELEM[op] * elems
+
+    x_h = synth.rows_of(SEED_CFG, rows, width, which="x")
+    r_h = synth.rows_of(SEED_CFG, rows, width, which="r")
+    x = torch.from_numpy(x_h).cuda()
+    r = torch.from_numpy(r_h).cuda()
+    y = torch.empty_like(x)
+    s = stream.cuda_stream
+
+    def call_op(name, out, plan=None):
+        px, pr, po = x.data_ptr(), r.data_ptr(), out.data_ptr()
+        if plan is not None:
+            st = lib.tile_run_plan_f32(tile.OPS[name], plan, px, pr, po, rows, width, EPS, s)
+        elif name == "residual_layernorm":
+            st = lib.tile_residual_layernorm_f32(px, pr, po, rows, width, EPS, s)
+        else:
+            st = getattr(lib, f"tile_{name}_f32")(px, po, rows, width, EPS, s)
+        if st != 0:
+            raise tile.TileError(st, name)
+
+    plan = tile.tile_describe_plan(op, rows, width) if args.plan is None else \
+        tile.tile_plan_info(args.plan, op, rows, width)
+    sampler = ClockSampler(gpu_selector())
+    sampler.start()
+
+    step = lambda: call_op(op, y, args.plan)       # noqa: E731
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    per, total_ms = time_calls(step, args.steps, stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    t1 = time.perf_counter()
+    total_ms = dist.max(total_ms)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    if tile.tile_check_device_status() != 0:
+        raise SystemExit("device status word set after the timed region")
+
+    ms_per_step = total_ms / args.steps
+    value = dist.world * nbytes * args.steps / (total_ms / 1e3) / 1e9
+    kernel_ms = statistics.mean(per)
+    peak, peak_src = measured_peaks()
+    achieved = nbytes / (kernel_ms / 1e3) / 1e9
+    traffic = profile_traffic(op, rows, width)
+    line = {
+        "metric": METRIC if (op, rows, width) == ("residual_layernorm", 65536, 4096) else
+        f"HBM GB/s and µs/call, {op} FP32 {rows}×{width}",
+        "value": round(value, 2), "unit": UNIT, "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "us_per_call": round(ms_per_step * 1e3, 3),
+        "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": f"synthetic: SplitMix64 uniform[-1,1), seeds {synth.x_seed(SEED_CFG)}/"
+                f"{synth.r_seed(SEED_CFG)}",
+        "config": {
+            "workload": f"{op.replace('_', ' ')} FP32 {rows}x{width}",
+            "rows": rows, "width": width, "eps": EPS,
+            "plan": {k: plan[k] for k in ("id", "path", "vec", "warps_per_program",
+                                          "programs_per_cta", "chunks", "cluster", "threads",
+                                          "grid")},
+            "l2": f"inputs larger than L2: {3 * elems * 4 / 2**30:.2f} GiB working set, no flush",
+            "parallelism": f"replicas x{dist.world}",
+        },
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} HBM copy bandwidth",
+                     "algorithmic_bytes_per_launch": nbytes,
+                     "kernel_ms_mean": round(kernel_ms, 6),
+                     "kernel_ms_median": round(statistics.median(per), 6),
+                     "frac_of_8TBps_nominal": round(achieved / 8000.0, 4)},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+    }
+
+    # --- the other two large-shape ops (same inputs; one launch per call) ---
+    if not args.no_extra and (rows, width) == (65536, 4096) and args.plan is None:
+        extra = {}
+        for name in ("rmsnorm", "softmax"):
+            if name == op:
+                continue
+            f = lambda name=name: call_op(name, y)      # noqa: E731
+            for _ in range(max(3, args.warmup)):
+                f()
+            per_x, tot_x = time_calls(f, max(20, min(args.steps, 200)), stream)
+            k_ms = statistics.mean(per_x)
+            b = BYTES_PER_ELEM[name] * elems
+            extra[name] = {"us_per_call": round(k_ms * 1e3, 3),
+                           "achieved_gbs": round(b / (k_ms / 1e3) / 1e9, 1),
+                           "frac": round(b / (k_ms / 1e3) / 1e9 / peak, 4),
+                           "plan_id": tile.tile_describe_plan(name, rows, width)["id"]}
+        line["other_ops"] = extra
+
+    # --- end to end through the C ABI with pinned host buffers -------------
+    if not args.no_e2e:
+        xp = torch.from_numpy(x_h).pin_memory()
+        rp = torch.from_numpy(r_h).pin_memory()
+        yp = torch.empty_like(xp).pin_memory()
+
+        def e2e_step():
+            x.copy_(xp, non_blocking=True)
+            r.copy_(rp, non_blocking=True)
+            call_op(op, y, args.plan)
+            yp.copy_(y, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 10))
+        dist.barrier()
+        _, e2e_ms = time_calls(e2e_step, n_e2e, stream)
+        e2e_ms = dist.max(e2e_ms)
+        h2d = (2 if op == "residual_layernorm" else 1) * elems * 4
+        line["e2e"] = {"value": round(dist.world * nbytes * n_e2e / (e2e_ms / 1e3) / 1e9, 2),
+                       "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": elems * 4,
+                       "steps": n_e2e, "ms_per_step": round(e2e_ms / n_e2e, 4),
+                       "path": "pinned host -> cudaMemcpyAsync -> C-ABI call -> cudaMemcpyAsync "
+                               "-> pinned host, one stream"}
+        if not np.array_equal(yp[:2].numpy(), y[:2].cpu().numpy()):
+            raise SystemExit("e2e output mismatch")
+
+    # --- the FP64 CPU oracle on this host (rank 0, N = 1 only) -------------
+    if not args.no_cpu and dist.world == 1 and dist.rank == 0:
+        line["cpu_baseline"] = cpu_baseline(op, x_h, r_h)
+
+    dist.close()
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(op, x_h, r_h):
+    import oracle
+    orc = oracle.get()
+    rows, width = x_h.shape
+    t = time.perf_counter()
+    orc.run(op, x_h, r_h, oracle.kernel_eps(EPS))
+    dt = time.perf_counter() - t
+    b = BYTES_PER_ELEM[op] * rows * width
+    return {"value": round(b / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"all {rows} rows x {width}, one pass, single-threaded FP64 C",
+            "seconds": round(dt, 3)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the FP64 CPU oracle as it stands, on host cores
+# ---------------------------------------------------------------------------
+
+SAMPLE_ROWS = 1024
+
+
+def run_reference(args, dist):
+    if dist.rank != 0:
+        return                               # rank 0 alone runs and prints
+    import oracle
+    import synth
+
+    rows, width, op = args.rows, args.width, args.op
+    n = min(SAMPLE_ROWS, rows)
+    x_h = synth.rows_of(SEED_CFG, rows, width, row_ids=range(n), which="x")
+    r_h = synth.rows_of(SEED_CFG, rows, width, row_ids=range(n), which="r")
+    orc = oracle.get()
+    eps = oracle.kernel_eps(EPS)
+    for _ in range(args.warmup):
+        orc.run(op, x_h, r_h, eps)
+    per = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        orc.run(op, x_h, r_h, eps)
+        per.append(time.perf_counter() - t)
+    total = time.perf_counter() - t0
+    b = BYTES_PER_ELEM[op] * n * width
+    value = b * args.steps / total / 1e9
+    sample = f"{n} of {rows} rows x {width} per step, single-threaded FP64 C"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: SplitMix64 uniform[-1,1), seeds 1005/2005",
+        "config": {"workload": f"{op.replace('_', ' ')} FP32 {rows}x{width}", "rows": rows,
+                   "width": width, "eps": EPS, "parallelism": "host, 1 thread"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    dist = Dist(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, dist)
+        return
+    run_ours(args, dist)
+
+
+if __name__ == "__main__":
+    main()

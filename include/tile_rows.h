@@ -1,0 +1,167 @@
+/*
+ * tile_rows.h -- C ABI of the fused FP32 row-normalisation library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Four operations, each applied independently to every row of a row-major
+ * FP32 matrix [rows][width] (row i starts at element i*width):
+ *
+ *   residual LayerNorm  y = (c - mean(c)) / sqrt(var(c) + eps),  c = x + r
+ *   LayerNorm           y = (x - mean(x)) / sqrt(var(x) + eps)
+ *   RMSNorm             y = x / sqrt(mean(x^2) + eps)
+ *   softmax             y = exp(x - max(x)) / sum(exp(x - max(x)))
+ *
+ * var is the centred, biased variance (divided by width); there are no
+ * affine weights.  The definitions follow the notes "Residual LayerNorm
+ * shared-Tile materialization search" (section "Structural finding": the
+ * residual LayerNorm expression, eps = 1e-5 inside the square root) and
+ * "Immutable input reuse in Metal reductions" (softmax, RMSNorm and
+ * LayerNorm rows; each input element read once and kept in worker-private
+ * stripes across the reduction phases).  Several rows may be packed into one
+ * CTA as cooperating programs, as in "Cooperating-program packing",
+ * section "Implementation boundary".
+ *
+ * Common contract of the four compute entry points
+ * ------------------------------------------------
+ *  - Pointers are DEVICE pointers (or managed/host-mapped memory the device
+ *    can read), FP32, 4-byte aligned.  16-byte alignment is not required:
+ *    rows whose start is not 16-byte aligned take a scalar head and tail.
+ *  - The caller owns every buffer.  The library allocates nothing, writes
+ *    exactly rows*width elements of `out` and nothing else, and never writes
+ *    `in` or `residual`.
+ *  - `out` must not overlap `in` or `residual` (the caller guarantees
+ *    no aliasing; an overlap that the library can see from the address
+ *    ranges is rejected with TILE_ERR_ALIAS).  `in` and `residual` may
+ *    overlap each other.
+ *  - Work is enqueued on `stream` (0 = the legacy default stream); the call
+ *    returns without synchronising.  Results are bitwise reproducible for a
+ *    given (op, rows, width, pointer alignment) on the same GPU.
+ *  - rows == 0 is a no-op returning TILE_OK.  1 <= width <= tile_max_width().
+ *  - Return value: TILE_OK (0) or a negative TILE_ERR_* code; on error
+ *    nothing is launched, except TILE_ERR_CUDA, which reports the launch
+ *    error returned by the CUDA runtime.
+ */
+#ifndef TILE_ROWS_H
+#define TILE_ROWS_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define TILE_OK               0
+#define TILE_ERR_NULL        -1  /* a required pointer is NULL (rows > 0)       */
+#define TILE_ERR_SHAPE       -2  /* rows < 0, width < 1 or width > max width   */
+#define TILE_ERR_ALIAS       -3  /* out overlaps in or residual               */
+#define TILE_ERR_EPS         -4  /* eps negative or not finite (normalisers)  */
+#define TILE_ERR_CUDA        -5  /* the CUDA runtime reported a launch error  */
+#define TILE_ERR_OP          -6  /* unknown operation code                    */
+#define TILE_ERR_ALIGN       -7  /* a pointer is not 4-byte aligned           */
+#define TILE_ERR_PLAN        -8  /* an explicit plan is not one of the built  */
+#define TILE_ERR_DEVICE      -9  /* a kernel recorded an error on the device  */
+
+/* ---- operation codes (tile_describe_plan, tile_run_plan_f32) ----------- */
+#define TILE_OP_RESIDUAL_LAYERNORM 0
+#define TILE_OP_LAYERNORM          1
+#define TILE_OP_RMSNORM            2
+#define TILE_OP_SOFTMAX            3
+
+/* ---- launch paths ------------------------------------------------------ */
+#define TILE_PATH_CTA      0  /* P programs x S warps per CTA, one row each  */
+#define TILE_PATH_CLUSTER  1  /* one row split over a cluster of C CTAs,     */
+                              /* partials exchanged through DSMEM            */
+
+/*
+ * A launch plan: how rows map onto the GPU.  Worker w of program p in a CTA
+ * owns the row elements e = (chunk * W * C + rank * W + w) * V + v of its
+ * row (chunk < K, v < V; rank = CTA rank in the cluster), keeps them in
+ * registers across every reduction phase, and reduces with warp shuffles,
+ * then P*S shared partials, then (C > 1) the C CTA partials of the cluster.
+ */
+typedef struct tile_plan {
+    int op;                 /* TILE_OP_*                                      */
+    int rows, width;        /* the shape the plan was made for                */
+    int id;                 /* index in the built plan table                  */
+    int path;               /* TILE_PATH_*                                    */
+    int vec;                /* V: 4 = float4 body (+ scalar head/tail), or 1  */
+    int warps_per_program;  /* S                                              */
+    int programs_per_cta;   /* P                                              */
+    int chunks;             /* K: V-vectors per worker                        */
+    int cluster;            /* C: CTAs per row (1 = no cluster)               */
+    int threads;            /* T = 32 * S * P                                 */
+    int workers;            /* W = 32 * S                                     */
+    int stripe_floats;      /* K * V registers of row data per thread         */
+    int max_width;          /* widest row this plan covers                    */
+    int smem_bytes;         /* static shared memory per CTA                   */
+    int barriers_per_row;   /* CTA or cluster barriers on a row's path        */
+    long long grid;         /* CTAs launched for `rows`                       */
+} tile_plan_t;
+
+/* ---- compute entry points --------------------------------------------- */
+
+/* Residual LayerNorm, no affine: c = in + residual, then LayerNorm of c.
+ * "Residual LayerNorm shared-Tile materialization search", "Structural
+ * finding".  in, residual, out: [rows][width] FP32 on the device. */
+int tile_residual_layernorm_f32(const float *in, const float *residual, float *out,
+                                int rows, int width, float eps, cudaStream_t stream);
+
+/* LayerNorm, no affine.  "Cooperating-program packing", "Validation"
+ * (no-affine LayerNorm); "Immutable input reuse in Metal reductions". */
+int tile_layernorm_f32(const float *in, float *out, int rows, int width, float eps,
+                       cudaStream_t stream);
+
+/* RMSNorm, no weight: y = x / sqrt(mean(x^2) + eps).  Named in "Immutable
+ * input reuse in Metal reductions" (fixed-width results table). */
+int tile_rmsnorm_f32(const float *in, float *out, int rows, int width, float eps,
+                     cudaStream_t stream);
+
+/* softmax over each row with the row maximum subtracted first (the max
+ * collective of "Cooperating-program packing", "Implementation boundary").
+ * `eps` is accepted for a uniform signature and ignored. */
+int tile_softmax_f32(const float *in, float *out, int rows, int width, float eps,
+                     cudaStream_t stream);
+
+/* ---- plans and diagnostics -------------------------------------------- */
+
+/* The plan the library would launch for (op, rows, width) with 16-byte
+ * co-aligned pointers (the common case).  Host only; touches no GPU.
+ * Returns TILE_OK, TILE_ERR_OP or TILE_ERR_SHAPE.  `plan` is written on
+ * success only. */
+int tile_describe_plan(int op, int rows, int width, tile_plan_t *plan);
+
+/* Number of plans built into the library, and plan `id` of that table
+ * described for (op, rows, width).  Returns TILE_ERR_PLAN for a bad id and
+ * TILE_ERR_SHAPE if the plan cannot cover `width`.  Host only. */
+int tile_plan_count(void);
+int tile_plan_info(int id, int op, int rows, int width, tile_plan_t *plan);
+
+/* Run `op` with the built plan `plan_id` instead of the selector's choice
+ * (used by the measured plan sweep and by tests that check every plan).
+ * Same contract as the compute entry points; `residual` is used only by
+ * TILE_OP_RESIDUAL_LAYERNORM.  Returns TILE_ERR_PLAN if the plan does not
+ * exist, cannot cover `width`, or needs 16-byte co-alignment (V = 4) that
+ * the pointers do not have. */
+int tile_run_plan_f32(int op, int plan_id, const float *in, const float *residual,
+                      float *out, int rows, int width, float eps, cudaStream_t stream);
+
+/* Widest row any built plan covers. */
+int tile_max_width(void);
+
+/* The cudaError_t value behind the last TILE_ERR_CUDA returned on this host
+ * thread (0 if none). */
+int tile_last_cuda_error(void);
+
+/* A static, human-readable description of a status code. */
+const char *tile_status_string(int status);
+
+/* Synchronise `stream`, then read and clear the device error word that
+ * kernels set instead of trapping.  Returns TILE_OK, TILE_ERR_DEVICE (a
+ * kernel recorded an error since the last check) or TILE_ERR_CUDA. */
+int tile_check_device_status(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TILE_ROWS_H */

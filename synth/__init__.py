@@ -28,6 +28,9 @@ Value maps:
 
 from __future__ import annotations
 
+import concurrent.futures as cf
+import os
+
 import numpy as np
 
 GOLDEN_GAMMA = np.uint64(0x9E3779B97F4A7C15)
@@ -47,26 +50,43 @@ def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
         return z ^ (z >> np.uint64(31))
 
 
+def _chunked(count: int, fill) -> None:
+    """Call ``fill(lo, n)`` over chunks of ``count``; large requests use a
+    thread pool (numpy releases the GIL inside these array operations)."""
+    spans = [(lo, min(_CHUNK, count - lo)) for lo in range(0, count, _CHUNK)]
+    if len(spans) <= 2:
+        for lo, n in spans:
+            fill(lo, n)
+        return
+    workers = max(1, min(16, os.cpu_count() or 1))
+    with cf.ThreadPoolExecutor(max_workers=workers) as pool:
+        list(pool.map(lambda s: fill(*s), spans))
+
+
 def uniform_pm1(seed: int, count: int, start: int = 0) -> np.ndarray:
     """``count`` FP32 values on [-1, 1), elements ``start..`` of stream ``seed``."""
     out = np.empty(count, dtype=np.float32)
-    for lo in range(0, count, _CHUNK):
-        n = min(_CHUNK, count - lo)
+
+    def fill(lo, n):
         k = (splitmix64(seed, start + lo, n) >> np.uint64(40)).astype(np.int64)
         out[lo:lo + n] = (k - (1 << 23)).astype(np.float32) * np.float32(2.0 ** -23)
+
+    _chunked(count, fill)
     return out
 
 
 def normal(seed: int, count: int, sigma: float, start: int = 0) -> np.ndarray:
     """``count`` FP32 draws of N(0, sigma**2); element ``j`` uses outputs 2j, 2j+1."""
     out = np.empty(count, dtype=np.float32)
-    for lo in range(0, count, _CHUNK):
-        n = min(_CHUNK, count - lo)
+
+    def fill(lo, n):
         h = splitmix64(seed, 2 * (start + lo), 2 * n)
         u1 = ((h[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53
         u2 = (h[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
         z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
         out[lo:lo + n] = (sigma * z).astype(np.float32)
+
+    _chunked(count, fill)
     return out
 
 

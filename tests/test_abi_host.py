@@ -1,0 +1,157 @@
+"""Host-only checks of the C ABI: the library loads, exports every function
+declared in include/*.h, and rejects bad arguments before any CUDA call.
+Nothing here launches a kernel, so it runs without a GPU."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import tile_compiler_row_gb300 as tile
+from tile_compiler_row_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, NULL, SHAPE, ALIAS, EPS, CUDA, OP, ALIGN, PLAN, DEVICE = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return tile.load()
+
+
+def declared_functions():
+    names = set()
+    for hdr in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(hdr).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(tile_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_four_ops():
+    names = declared_functions()
+    for n in ("tile_residual_layernorm_f32", "tile_layernorm_f32", "tile_rmsnorm_f32",
+              "tile_softmax_f32", "tile_describe_plan", "tile_status_string",
+              "tile_check_device_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_python_binding_has_the_same_names():
+    for name in declared_functions():
+        assert hasattr(tile, name), f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    for code in (OK, NULL, SHAPE, ALIAS, EPS, CUDA, OP, ALIGN, PLAN, DEVICE):
+        s = tile.tile_status_string(code)
+        assert s and s != "unknown status"
+    assert tile.tile_status_string(12345) == "unknown status"
+
+
+A = 0x10000000      # fake, never dereferenced: every call below fails validation
+B = 0x20000000
+
+
+def _resln(lib, x, r, y, rows, width, eps=1e-5):
+    return lib.tile_residual_layernorm_f32(x, r, y, rows, width, eps, None)
+
+
+def test_shape_errors(lib):
+    assert _resln(lib, A, A, B, -1, 8) == SHAPE
+    assert _resln(lib, A, A, B, 4, 0) == SHAPE
+    assert _resln(lib, A, A, B, 4, tile.tile_max_width() + 1) == SHAPE
+    assert lib.tile_softmax_f32(A, B, 1, -3, 0.0, None) == SHAPE
+
+
+def test_rows_zero_is_a_noop(lib):
+    assert _resln(lib, None, None, None, 0, 8) == OK
+    assert lib.tile_softmax_f32(None, None, 0, 8, 0.0, None) == OK
+
+
+def test_null_pointers(lib):
+    assert _resln(lib, None, A, B, 2, 8) == NULL
+    assert _resln(lib, A, None, B, 2, 8) == NULL
+    assert _resln(lib, A, A, None, 2, 8) == NULL
+    assert lib.tile_layernorm_f32(None, B, 2, 8, 1e-5, None) == NULL
+
+
+def test_eps_checked_for_normalisers_only(lib):
+    assert lib.tile_rmsnorm_f32(A, B, 2, 8, -1.0, None) == EPS
+    assert lib.tile_layernorm_f32(A, B, 2, 8, float("nan"), None) == EPS
+    assert _resln(lib, A, A, B, 2, 8, float("inf")) == EPS
+
+
+def test_alignment(lib):
+    assert lib.tile_rmsnorm_f32(A + 2, B, 2, 8, 1e-5, None) == ALIGN
+    assert lib.tile_rmsnorm_f32(A, B + 1, 2, 8, 1e-5, None) == ALIGN
+
+
+def test_alias(lib):
+    # out overlaps in: [A, A+64) vs [A+32, A+96)
+    assert lib.tile_layernorm_f32(A, A + 32, 2, 8, 1e-5, None) == ALIAS
+    assert _resln(lib, A, B, B + 60, 2, 8) == ALIAS
+    assert lib.tile_softmax_f32(A, A, 1, 1, 0.0, None) == ALIAS
+
+
+def test_run_plan_rejects_bad_plans(lib):
+    n = lib.tile_plan_count()
+    assert lib.tile_run_plan_f32(0, -1, A, A, B, 2, 8, 1e-5, None) == PLAN
+    assert lib.tile_run_plan_f32(0, n, A, A, B, 2, 8, 1e-5, None) == PLAN
+    # plan 0 covers at most 131 columns
+    assert lib.tile_run_plan_f32(1, 0, A, None, B, 2, 4096, 1e-5, None) == PLAN
+    # a float4 plan needs co-aligned pointers (A and B+4 differ mod 16)
+    assert lib.tile_run_plan_f32(1, 0, A, None, B + 4, 2, 8, 1e-5, None) == PLAN
+    assert lib.tile_run_plan_f32(9, 0, A, None, B, 2, 8, 1e-5, None) == OP
+
+
+def test_every_width_has_a_covering_plan(lib):
+    widths = list(range(1, 600)) + [1023, 1024, 1025, 1537, 4095, 4096, 4097, 8192, 8195,
+                                      16384, 16388, 32768, 32772, 65536, 65540, 131071, 131072]
+    for op in range(4):
+        for w in widths:
+            p = tile.tile_describe_plan(op, 5, w)
+            assert p["max_width"] >= w
+            assert p["threads"] == 32 * p["warps_per_program"] * p["programs_per_cta"] <= 1024
+            cap = p["chunks"] * p["workers"] * p["cluster"]
+            assert (w // 4 if p["vec"] == 4 else w) <= cap
+            assert p["grid"] == -(-5 // p["programs_per_cta"]) * p["cluster"]
+
+
+def test_plan_info_table(lib):
+    n = tile.tile_plan_count()
+    assert n >= 20
+    seen_vec1 = False
+    for pid in range(n):
+        info = tile.tile_plan_info(pid, 0, 3, 1)
+        assert info is not None and info["id"] == pid
+        assert tile.tile_plan_info(pid, 0, 3, info["max_width"]) is not None
+        if info["max_width"] < tile.tile_max_width():
+            assert tile.tile_plan_info(pid, 0, 3, info["max_width"] + 1) is None
+        seen_vec1 |= info["vec"] == 1
+        if info["cluster"] > 1:
+            assert info["programs_per_cta"] == 1 and info["cluster"] <= 8
+    assert seen_vec1
+
+
+def test_describe_plan_errors(lib):
+    plan = tile.TilePlan()
+    assert lib.tile_describe_plan(7, 4, 8, ctypes.byref(plan)) == OP
+    assert lib.tile_describe_plan(0, 4, 0, ctypes.byref(plan)) == SHAPE
+    assert lib.tile_describe_plan(0, 4, 8, None) == NULL
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    x = torch.zeros(2, 8)
+    with pytest.raises(ValueError):
+        tile.tile_rmsnorm_f32(x, torch.zeros(2, 8))

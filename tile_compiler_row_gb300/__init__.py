@@ -1,0 +1,262 @@
+"""Python binding of ``libtile_rows.so``: fused FP32 row normalisation on GB300.
+
+Argument marshalling only.  Every function here checks tensor metadata, takes
+device pointers and the current CUDA stream from PyTorch, and calls the C ABI
+of the same name (declared in ``include/tile_rows.h``); all arithmetic runs in
+the library's CUDA kernels.  There is no CPU path: CPU tensors are rejected,
+and importing the binding without the built library raises.
+
+    import torch, tile_compiler_row_gb300 as tile
+    y = torch.empty_like(x)
+    tile.tile_residual_layernorm_f32(x, r, y, eps=1e-5)
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIBRARY
+
+__all__ = [
+    "TileError", "OPS", "load", "library_path",
+    "tile_residual_layernorm_f32", "tile_layernorm_f32", "tile_rmsnorm_f32",
+    "tile_softmax_f32", "tile_run_plan_f32", "tile_describe_plan", "tile_plan_info",
+    "tile_plan_count", "tile_max_width", "tile_status_string",
+    "tile_check_device_status", "tile_last_cuda_error",
+    "residual_layernorm", "layernorm", "rmsnorm", "softmax", "run",
+]
+
+#: Library operation codes, by name.
+OPS = {"residual_layernorm": 0, "layernorm": 1, "rmsnorm": 2, "softmax": 3}
+
+TILE_OK = 0
+
+
+class TileError(RuntimeError):
+    """A non-zero status returned by the C ABI."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: status {status} ({tile_status_string(status)})"
+        if status == -5:
+            msg += f", cudaError {tile_last_cuda_error()}"
+        super().__init__(msg)
+
+
+class TilePlan(ctypes.Structure):
+    _fields_ = [
+        ("op", ctypes.c_int), ("rows", ctypes.c_int), ("width", ctypes.c_int),
+        ("id", ctypes.c_int), ("path", ctypes.c_int), ("vec", ctypes.c_int),
+        ("warps_per_program", ctypes.c_int), ("programs_per_cta", ctypes.c_int),
+        ("chunks", ctypes.c_int), ("cluster", ctypes.c_int), ("threads", ctypes.c_int),
+        ("workers", ctypes.c_int), ("stripe_floats", ctypes.c_int),
+        ("max_width", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+        ("barriers_per_row", ctypes.c_int), ("grid", ctypes.c_longlong),
+    ]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return LIBRARY
+
+
+def load():
+    """Load the shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIBRARY):
+        raise RuntimeError(
+            f"{LIBRARY} is not built: run `python -c 'import __graft_entry__ as g; g.build()'` "
+            "(the library has no CPU fallback)")
+    lib = ctypes.CDLL(LIBRARY)
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    sigs = {
+        "tile_residual_layernorm_f32": [P, P, P, I, I, F, P],
+        "tile_layernorm_f32": [P, P, I, I, F, P],
+        "tile_rmsnorm_f32": [P, P, I, I, F, P],
+        "tile_softmax_f32": [P, P, I, I, F, P],
+        "tile_run_plan_f32": [I, I, P, P, P, I, I, F, P],
+        "tile_describe_plan": [I, I, I, ctypes.POINTER(TilePlan)],
+        "tile_plan_info": [I, I, I, I, ctypes.POINTER(TilePlan)],
+        "tile_plan_count": [],
+        "tile_max_width": [],
+        "tile_check_device_status": [P],
+        "tile_last_cuda_error": [],
+    }
+    for name, argtypes in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = argtypes
+        fn.restype = ctypes.c_int
+    lib.tile_status_string.argtypes = [I]
+    lib.tile_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _matrix(t, name):
+    """(pointer, rows, width) of a CUDA FP32 row-major matrix tensor."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != torch.float32:
+        raise ValueError(f"{name} must be float32")
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D [rows, width]")
+    rows, width = t.shape
+    if rows > 1 and t.stride(0) != width or width > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major with row stride == width")
+    return t.data_ptr(), rows, width
+
+
+def _check(status, where):
+    if status != TILE_OK:
+        raise TileError(status, where)
+
+
+def _same_shape(a, b, names):
+    if tuple(a.shape) != tuple(b.shape):
+        raise ValueError(f"{names}: shapes {tuple(a.shape)} and {tuple(b.shape)} differ")
+
+
+# ---------------------------------------------------------------------------
+# the C ABI, one Python function per entry point
+# ---------------------------------------------------------------------------
+
+def tile_residual_layernorm_f32(x, residual, out, eps=1e-5, stream=None):
+    px, rows, width = _matrix(x, "x")
+    pr, _, _ = _matrix(residual, "residual")
+    po, _, _ = _matrix(out, "out")
+    _same_shape(x, residual, "x/residual")
+    _same_shape(x, out, "x/out")
+    _check(load().tile_residual_layernorm_f32(px, pr, po, rows, width, eps, _stream(stream)),
+           "tile_residual_layernorm_f32")
+
+
+def _unary(name):
+    def fn(x, out, eps=1e-5, stream=None):
+        px, rows, width = _matrix(x, "x")
+        po, _, _ = _matrix(out, "out")
+        _same_shape(x, out, "x/out")
+        _check(getattr(load(), name)(px, po, rows, width, eps, _stream(stream)), name)
+    fn.__name__ = name
+    fn.__doc__ = f"Calls ``{name}`` (see include/tile_rows.h)."
+    return fn
+
+
+tile_layernorm_f32 = _unary("tile_layernorm_f32")
+tile_rmsnorm_f32 = _unary("tile_rmsnorm_f32")
+tile_softmax_f32 = _unary("tile_softmax_f32")
+
+
+def tile_run_plan_f32(op, plan_id, x, residual, out, eps=1e-5, stream=None):
+    op = OPS[op] if isinstance(op, str) else op
+    px, rows, width = _matrix(x, "x")
+    po, _, _ = _matrix(out, "out")
+    _same_shape(x, out, "x/out")
+    pr = None
+    if residual is not None:
+        pr, _, _ = _matrix(residual, "residual")
+        _same_shape(x, residual, "x/residual")
+    _check(load().tile_run_plan_f32(op, plan_id, px, pr, po, rows, width, eps, _stream(stream)),
+           "tile_run_plan_f32")
+
+
+def tile_describe_plan(op, rows, width):
+    op = OPS[op] if isinstance(op, str) else op
+    plan = TilePlan()
+    _check(load().tile_describe_plan(op, rows, width, ctypes.byref(plan)), "tile_describe_plan")
+    return plan.as_dict()
+
+
+def tile_plan_info(plan_id, op, rows, width):
+    """The built plan ``plan_id`` for (op, rows, width), or None if it cannot cover ``width``."""
+    op = OPS[op] if isinstance(op, str) else op
+    plan = TilePlan()
+    st = load().tile_plan_info(plan_id, op, rows, width, ctypes.byref(plan))
+    if st == -2:
+        return None
+    _check(st, "tile_plan_info")
+    return plan.as_dict()
+
+
+def tile_plan_count():
+    return load().tile_plan_count()
+
+
+def tile_max_width():
+    return load().tile_max_width()
+
+
+def tile_status_string(status):
+    return load().tile_status_string(status).decode()
+
+
+def tile_check_device_status(stream=None):
+    return load().tile_check_device_status(_stream(stream))
+
+
+def tile_last_cuda_error():
+    return load().tile_last_cuda_error()
+
+
+# ---------------------------------------------------------------------------
+# convenience wrappers (allocate the output with torch when not given)
+# ---------------------------------------------------------------------------
+
+def residual_layernorm(x, residual, out=None, eps=1e-5, stream=None):
+    import torch
+    out = torch.empty_like(x) if out is None else out
+    tile_residual_layernorm_f32(x, residual, out, eps, stream)
+    return out
+
+
+def layernorm(x, out=None, eps=1e-5, stream=None):
+    import torch
+    out = torch.empty_like(x) if out is None else out
+    tile_layernorm_f32(x, out, eps, stream)
+    return out
+
+
+def rmsnorm(x, out=None, eps=1e-5, stream=None):
+    import torch
+    out = torch.empty_like(x) if out is None else out
+    tile_rmsnorm_f32(x, out, eps, stream)
+    return out
+
+
+def softmax(x, out=None, stream=None):
+    import torch
+    out = torch.empty_like(x) if out is None else out
+    tile_softmax_f32(x, out, 0.0, stream)
+    return out
+
+
+def run(op, x, residual=None, out=None, eps=1e-5, stream=None):
+    """Dispatch by op name."""
+    if op == "residual_layernorm":
+        return residual_layernorm(x, residual, out, eps, stream)
+    if op == "softmax":
+        return softmax(x, out, stream)
+    return {"layernorm": layernorm, "rmsnorm": rmsnorm}[op](x, out, eps, stream)

@@ -1,0 +1,88 @@
+// Instantiates every built plan for one operation and provides its host-side
+// launcher and device error word.  Included once per op by ops_<op>.cu with
+// TILE_INST_OP (tile::OP_*) and TILE_INST_NAME (a C identifier) defined, so
+// the four ops compile as four translation units in parallel.
+#include "row_kernel.cuh"
+#include "plans.h"
+#include "launch.h"
+
+#include <atomic>
+
+#define TILE_CAT2(a, b) a##b
+#define TILE_CAT(a, b) TILE_CAT2(a, b)
+
+namespace tile {
+namespace {
+__device__ unsigned int g_status;   // this op's device error word
+
+// Device address of g_status, looked up once per device.
+unsigned int *status_address(cudaError_t *err) {
+    static std::atomic<unsigned int *> cache[kMaxDevices];
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    unsigned int *p = cache[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        *err = cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_status);
+        if (*err != cudaSuccess) return nullptr;
+        cache[dev].store(p, std::memory_order_release);
+    }
+    return p;
+}
+
+template <int V, int S, int P, int K, int C>
+cudaError_t launch_plan(const float *x, const float *r, float *y, long long rows, int width,
+                        float eps, cudaStream_t stream) {
+    cudaError_t err = cudaSuccess;
+    unsigned int *status = status_address(&err);
+    if (status == nullptr) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned int>(((rows + P - 1) / P) * C), 1, 1);
+    cfg.blockDim = dim3(32 * S * P, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (C > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, row_kernel<TILE_INST_OP, V, S, P, K, C>, x, r, y, rows,
+                              width, eps, status);
+}
+}  // namespace
+
+cudaError_t TILE_CAT(launch_, TILE_INST_NAME)(int plan_id, const float *x, const float *r,
+                                              float *y, long long rows, int width, float eps,
+                                              cudaStream_t stream) {
+    switch (plan_id) {
+#define TILE_CASE(id, V, S, P, K, C) \
+    case id: return launch_plan<V, S, P, K, C>(x, r, y, rows, width, eps, stream);
+        TILE_PLAN_LIST(TILE_CASE)
+#undef TILE_CASE
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t TILE_CAT(status_, TILE_INST_NAME)(unsigned int *value, cudaStream_t stream) {
+    cudaError_t err = cudaMemcpyFromSymbolAsync(value, g_status, sizeof(unsigned int), 0,
+                                                cudaMemcpyDeviceToHost, stream);
+    if (err != cudaSuccess) return err;
+    err = cudaStreamSynchronize(stream);
+    if (err != cudaSuccess) return err;
+    if (*value == 0) return cudaSuccess;
+    const unsigned int zero = 0;
+    err = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(unsigned int), 0,
+                                  cudaMemcpyHostToDevice, stream);
+    if (err != cudaSuccess) return err;
+    return cudaStreamSynchronize(stream);
+}
+
+}  // namespace tile

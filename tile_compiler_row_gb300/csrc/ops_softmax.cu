@@ -1,0 +1,4 @@
+// softmax: every built plan (see ops_inst.cuh).
+#define TILE_INST_OP tile::OP_SOFTMAX
+#define TILE_INST_NAME softmax
+#include "ops_inst.cuh"

@@ -1,0 +1,59 @@
+// Built launch plans: X(id, V, S, P, K, C).
+//
+//   V  elements per vector access (4 = float4 body with scalar head/tail,
+//      1 = scalar, for pointers whose 16-byte phases differ)
+//   S  warps per program (W = 32*S cooperating workers per row)
+//   P  programs (rows) packed per CTA, T = 32*S*P threads
+//   K  V-vectors per worker: the register stripe holds K*V floats
+//   C  CTAs per row (a thread-block cluster when C > 1)
+//
+// A plan covers a row of `width` when its workers can own every element:
+// V = 4: floor(width/4) <= K*W*C (head/tail scalars are extra);
+// V = 1: width <= K*W*C.
+//
+// The selector in tile_api.cu picks from this table by width and row count;
+// every plan can also be forced through tile_run_plan_f32 (plan sweeps and
+// the per-plan parity tests use that).
+#pragma once
+
+#define TILE_PLAN_LIST(X)                                                     \
+    /* one warp per row, packed 4-8 rows per CTA */                           \
+    X(0, 4, 1, 8, 1, 1)                                                       \
+    X(1, 4, 1, 8, 2, 1)                                                       \
+    X(2, 4, 1, 4, 4, 1)                                                       \
+    /* 2-8 warps per row, packed */                                           \
+    X(3, 4, 2, 4, 4, 1)                                                       \
+    X(4, 4, 2, 2, 4, 1)                                                       \
+    X(5, 4, 4, 2, 4, 1)                                                       \
+    X(6, 4, 4, 1, 4, 1)                                                       \
+    X(7, 4, 4, 1, 8, 1)                                                       \
+    X(8, 4, 8, 1, 4, 1)                                                       \
+    X(9, 4, 16, 1, 2, 1)                                                      \
+    X(10, 4, 8, 1, 8, 1)                                                      \
+    X(11, 4, 16, 1, 4, 1)                                                     \
+    X(12, 4, 32, 1, 2, 1)                                                     \
+    X(13, 4, 32, 1, 4, 1)                                                     \
+    X(14, 4, 16, 1, 8, 1)                                                     \
+    /* one row over a cluster of 2-8 CTAs */                                  \
+    X(15, 4, 16, 1, 4, 2)                                                     \
+    X(16, 4, 16, 1, 4, 4)                                                     \
+    X(17, 4, 8, 1, 8, 4)                                                      \
+    X(18, 4, 16, 1, 4, 8)                                                     \
+    X(19, 4, 8, 1, 8, 8)                                                      \
+    X(20, 4, 32, 1, 4, 8)                                                     \
+    /* more packings around the common widths */                              \
+    X(21, 4, 4, 4, 2, 1)                                                      \
+    X(22, 4, 8, 2, 2, 1)                                                      \
+    X(23, 4, 32, 1, 1, 1)                                                     \
+    X(24, 4, 8, 2, 4, 1)                                                      \
+    /* scalar plans for pointers that are not co-aligned */                   \
+    X(25, 1, 1, 8, 4, 1)                                                      \
+    X(26, 1, 4, 2, 8, 1)                                                      \
+    X(27, 1, 8, 1, 16, 1)                                                     \
+    X(28, 1, 32, 1, 16, 1)                                                    \
+    X(29, 1, 32, 1, 16, 8)
+
+#define TILE_PLAN_COUNT 30
+
+// Widest row covered by both a V = 4 and a V = 1 plan.
+#define TILE_MAX_WIDTH 131072

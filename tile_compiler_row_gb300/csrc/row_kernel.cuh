@@ -1,0 +1,347 @@
+// Fused FP32 row-normalisation kernel for sm_103a: one template, four ops.
+//
+// Mapping (after "Cooperating-program packing", section "Implementation
+// boundary"): a CTA of T = 32*S*P threads runs P row programs of W = 32*S
+// cooperating workers each.  With C > 1 one row is split over a thread-block
+// cluster of C CTAs (P = 1), which is how rows too wide for one CTA's
+// registers are handled.
+//
+// Every worker loads its elements of the row exactly once into a register
+// stripe (float4 accesses where the row is 16-byte aligned, a scalar head
+// and tail otherwise), and every later phase reads the stripe, never global
+// memory -- the input-reuse scheme of "Immutable input reuse in Metal
+// reductions" (execution map e = (chunk*W + worker)*V + v, resource map
+// stripe_slot = chunk*V + v).  Reductions go warp shuffle -> P*S shared
+// partials -> (C > 1) C cluster partials read through distributed shared
+// memory; every level combines in a fixed order, so a plan is bitwise
+// deterministic.  A packed CTA whose last programs fall past the final row
+// replays the last row and predicates only its stores, so every barrier is
+// unconditional.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+namespace tile {
+
+enum { OP_RESLN = 0, OP_LN = 1, OP_RMS = 2, OP_SOFTMAX = 3 };
+
+// Bits of the per-library device error word (read by tile_check_device_status).
+enum { STATUS_BAD_LAUNCH = 1u };
+
+// ---------------------------------------------------------------------------
+// memory access: inputs are read once and outputs written once, so both use
+// the streaming cache hint (evict-first).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 load4(const float *p) {
+    return __ldcs(reinterpret_cast<const float4 *>(p));
+}
+__device__ __forceinline__ float load1(const float *p) { return __ldcs(p); }
+__device__ __forceinline__ void store4(float *p, float4 v) {
+    __stcs(reinterpret_cast<float4 *>(p), v);
+}
+__device__ __forceinline__ void store1(float *p, float v) { __stcs(p, v); }
+
+// ---------------------------------------------------------------------------
+// cluster primitives (inline PTX)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+// Read a float from the shared memory of CTA `rank` of this cluster, at the
+// address `local` has in this CTA's shared window.
+__device__ __forceinline__ float load_dsmem(const float *local, uint32_t rank) {
+    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// reductions
+// ---------------------------------------------------------------------------
+struct Sum {
+    __device__ static float apply(float a, float b) { return a + b; }
+};
+struct Max {
+    __device__ static float apply(float a, float b) { return fmaxf(a, b); }
+};
+
+// xor butterfly: every lane ends with the same value (IEEE + and max are
+// commutative, so lane i and lane i^o compute the same pair).
+template <class Op, int N>
+__device__ __forceinline__ void warp_allreduce(float (&v)[N]) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            v[i] = Op::apply(v[i], __shfl_xor_sync(0xffffffffu, v[i], o));
+    }
+}
+
+// All-reduce of N values over one row program: warp -> S shared partials of
+// this program -> C cluster partials.  part: [N][P*S] floats, cpart: [N].
+// Each call site passes its own part/cpart so no phase overwrites a buffer
+// another thread may still be reading.
+template <class Op, int N, int S, int P, int C>
+__device__ __forceinline__ void row_allreduce(float (&v)[N], float *part, float *cpart,
+                                              int program, int warp, int lane) {
+    warp_allreduce<Op, N>(v);
+    if constexpr (S > 1) {
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) part[i * P * S + program * S + warp] = v[i];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            float t = part[i * P * S + program * S];
+#pragma unroll
+            for (int w = 1; w < S; ++w) t = Op::apply(t, part[i * P * S + program * S + w]);
+            v[i] = t;
+        }
+    }
+    if constexpr (C > 1) {
+        if (threadIdx.x == 0) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) cpart[i] = v[i];
+        }
+        cluster_arrive();
+        cluster_wait();
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            float t = load_dsmem(&cpart[i], 0);
+#pragma unroll
+            for (int q = 1; q < C; ++q) t = Op::apply(t, load_dsmem(&cpart[i], q));
+            v[i] = t;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int OP, int V, int S, int P, int K, int C>
+__global__ void __launch_bounds__(32 * S * P)
+    row_kernel(const float *__restrict__ x, const float *__restrict__ r, float *__restrict__ y,
+               long long rows, int width, float eps, unsigned int *status) {
+    static_assert(V == 1 || V == 4, "V is 1 or 4");
+    static_assert(C == 1 || P == 1, "a cluster row has one program per CTA");
+    static_assert(32 * S * P <= 1024, "at most 1024 threads per CTA");
+    constexpr int W = 32 * S;
+    constexpr int NPH = (OP == OP_RMS) ? 1 : 2;   // reduction phases
+    constexpr float kFill = (OP == OP_SOFTMAX) ? -INFINITY : 0.0f;
+
+    __shared__ float part1[S > 1 ? P * S : 1];
+    __shared__ float part2[S > 1 ? 2 * P * S : 1];
+    __shared__ float cpart[C > 1 ? 4 : 1];
+
+    if (blockDim.x != 32 * S * P) {           // uniform over the grid
+        if (threadIdx.x == 0) atomicOr(status, STATUS_BAD_LAUNCH);
+        return;
+    }
+
+    const int tid = threadIdx.x;
+    const int program = tid / W;
+    const int worker = tid - program * W;
+    const int warp = worker >> 5;
+    const int lane = tid & 31;
+    int rank = 0;
+    long long group = blockIdx.x;
+    if constexpr (C > 1) {
+        rank = static_cast<int>(cluster_rank());
+        group = cluster_index();
+    }
+    long long row = group * P + program;
+    const bool active = row < rows;
+    if (!active) row = rows - 1;                  // replay the last row
+
+    const long long base = row * static_cast<long long>(width);
+    const float *xr = x + base;
+    const float *rr = (OP == OP_RESLN) ? r + base : nullptr;
+    float *yr = y + base;
+
+    // Row geometry.  V = 4: h scalars up to the first 16-byte boundary, then
+    // nb float4s, then tl scalars.  All pointers share the 16-byte phase.
+    int h = 0, tl = 0, nb;
+    if constexpr (V == 4) {
+        const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(xr) >> 2) & 3);
+        h = (4 - mis) & 3;
+        if (h > width) h = width;
+        nb = (width - h) >> 2;
+        tl = width - h - (nb << 2);
+    } else {
+        nb = width;
+    }
+    const int gw = rank * W + worker;
+
+    // ---- a1: load the row once into the register stripe ----------------
+    float v[K][V];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int i = k * (C * W) + gw;
+        if (i < nb) {
+            if constexpr (V == 4) {
+                float4 a = load4(xr + h + 4 * i);
+                if constexpr (OP == OP_RESLN) {
+                    const float4 b = load4(rr + h + 4 * i);
+                    a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+                }
+                v[k][0] = a.x; v[k][1] = a.y; v[k][2] = a.z; v[k][3] = a.w;
+            } else {
+                float a = load1(xr + i);
+                if constexpr (OP == OP_RESLN) a += load1(rr + i);
+                v[k][0] = a;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < V; ++j) v[k][j] = kFill;
+        }
+    }
+    bool has_h = false, has_t = false;
+    float hv = kFill, tv = kFill;
+    int te = 0;
+    if constexpr (V == 4) {
+        has_h = (rank == 0) && (worker < h);
+        has_t = (rank == 0) && (worker < tl);
+        te = h + 4 * nb + worker;
+        if (has_h) {
+            hv = load1(xr + worker);
+            if constexpr (OP == OP_RESLN) hv += load1(rr + worker);
+        }
+        if (has_t) {
+            tv = load1(xr + te);
+            if constexpr (OP == OP_RESLN) tv += load1(rr + te);
+        }
+    }
+
+    const float n = static_cast<float>(width);
+    if constexpr (OP == OP_RESLN || OP == OP_LN) {
+        // ---- a2: mean estimate -------------------------------------------
+        float s[1] = {hv + tv};
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            float t = v[k][0];
+#pragma unroll
+            for (int j = 1; j < V; ++j) t += v[k][j];
+            s[0] += t;
+        }
+        row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
+        const float mean0 = s[0] / n;
+        // ---- a3: centre in place; reduce (sum d, sum d^2) -----------------
+        float q[2] = {0.0f, 0.0f};
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const bool ok = k * (C * W) + gw < nb;
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                const float d = ok ? v[k][j] - mean0 : 0.0f;
+                v[k][j] = d;
+                q[0] += d;
+                q[1] = fmaf(d, d, q[1]);
+            }
+        }
+        hv = has_h ? hv - mean0 : 0.0f;
+        tv = has_t ? tv - mean0 : 0.0f;
+        q[0] += hv + tv;
+        q[1] = fmaf(hv, hv, fmaf(tv, tv, q[1]));
+        row_allreduce<Sum, 2, S, P, C>(q, part2, cpart + 1, program, warp, lane);
+        // corrected two-pass: mean = mean0 + mu1, var = E[d^2] - mu1^2
+        const float mu1 = q[0] / n;
+        const float var = fmaxf(q[1] / n - mu1 * mu1, 0.0f);
+        const float rstd = 1.0f / sqrtf(var + eps);
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < V; ++j) v[k][j] = (v[k][j] - mu1) * rstd;
+        hv = (hv - mu1) * rstd;
+        tv = (tv - mu1) * rstd;
+    } else if constexpr (OP == OP_RMS) {
+        // ---- a2: mean square ---------------------------------------------
+        float s[1] = {fmaf(hv, hv, tv * tv)};
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < V; ++j) s[0] = fmaf(v[k][j], v[k][j], s[0]);
+        row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
+        const float rstd = 1.0f / sqrtf(s[0] / n + eps);
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < V; ++j) v[k][j] *= rstd;
+        hv *= rstd;
+        tv *= rstd;
+    } else {
+        // ---- a2: row maximum (empty slots hold -inf) ---------------------
+        float m[1] = {fmaxf(hv, tv)};
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < V; ++j) m[0] = fmaxf(m[0], v[k][j]);
+        row_allreduce<Max, 1, S, P, C>(m, part1, cpart, program, warp, lane);
+        const float mx = m[0];
+        // ---- a3: exponentiate in place (exp(-inf) = 0), reduce the sum ---
+        float s[1] = {0.0f};
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                const float e = expf(v[k][j] - mx);
+                v[k][j] = e;
+                s[0] += e;
+            }
+        hv = expf(hv - mx);
+        tv = expf(tv - mx);
+        s[0] += hv + tv;
+        row_allreduce<Sum, 1, S, P, C>(s, part2, cpart + 1, program, warp, lane);
+        const float inv = 1.0f / s[0];
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < V; ++j) v[k][j] *= inv;
+        hv *= inv;
+        tv *= inv;
+    }
+    (void)NPH;
+
+    // Our cluster partials must stay readable until every CTA of the
+    // cluster has read them: arrive now, wait after the stores.
+    if constexpr (C > 1) cluster_arrive();
+
+    // ---- a4: streaming stores, predicated for replayed programs ---------
+    if (active) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int i = k * (C * W) + gw;
+            if (i < nb) {
+                if constexpr (V == 4)
+                    store4(yr + h + 4 * i, make_float4(v[k][0], v[k][1], v[k][2], v[k][3]));
+                else
+                    store1(yr + i, v[k][0]);
+            }
+        }
+        if constexpr (V == 4) {
+            if (has_h) store1(yr + worker, hv);
+            if (has_t) store1(yr + te, tv);
+        }
+    }
+    if constexpr (C > 1) cluster_wait();
+}
+
+}  // namespace tile

@@ -1,0 +1,264 @@
+// C ABI of the row-normalisation library: argument checks, the width->plan
+// selector and dispatch to the per-op launchers.  See include/tile_rows.h for
+// the contract of every entry point.
+#include "../../include/tile_rows.h"
+
+#include <cmath>
+#include <cstdint>
+
+#include "launch.h"
+#include "plans.h"
+
+namespace {
+
+struct PlanDesc {
+    int id, V, S, P, K, C;
+};
+
+constexpr PlanDesc kPlans[TILE_PLAN_COUNT] = {
+#define TILE_ROW(id, V, S, P, K, C) {id, V, S, P, K, C},
+    TILE_PLAN_LIST(TILE_ROW)
+#undef TILE_ROW
+};
+
+// Vector slots a plan's workers own for one row.
+constexpr long long capacity(const PlanDesc &p) {
+    return static_cast<long long>(p.K) * 32 * p.S * p.C;
+}
+
+bool covers(const PlanDesc &p, int width) {
+    if (width < 1) return false;
+    return p.V == 4 ? (width / 4) <= capacity(p) : width <= capacity(p);
+}
+
+int max_width_of(const PlanDesc &p) {
+    const long long w = p.V == 4 ? capacity(p) * 4 + 3 : capacity(p);
+    return w > TILE_MAX_WIDTH ? TILE_MAX_WIDTH : static_cast<int>(w);
+}
+
+// Selector: for each op, the first entry whose width bound covers the row.
+// Separate tables for 16-byte co-aligned pointers (V = 4 plans) and for the
+// rest (V = 1 plans).
+struct Bucket {
+    int max_width;
+    int plan;
+};
+
+constexpr Bucket kVec4[] = {
+    {131, 0}, {259, 1}, {515, 2}, {1027, 3}, {2051, 5}, {4099, 8},
+    {8195, 11}, {16387, 13}, {32771, 16}, {65539, 18}, {TILE_MAX_WIDTH, 20},
+};
+constexpr Bucket kVec1[] = {
+    {128, 25}, {1024, 26}, {4096, 27}, {16384, 28}, {TILE_MAX_WIDTH, 29},
+};
+
+template <int N>
+int pick(const Bucket (&table)[N], int width) {
+    for (int i = 0; i < N; ++i)
+        if (width <= table[i].max_width) return table[i].plan;
+    return -1;
+}
+
+int select_plan(int op, long long rows, int width, bool vec4) {
+    (void)op;
+    (void)rows;
+    return vec4 ? pick(kVec4, width) : pick(kVec1, width);
+}
+
+long long grid_of(const PlanDesc &p, long long rows) {
+    return ((rows + p.P - 1) / p.P) * p.C;
+}
+
+void fill_plan(const PlanDesc &p, int op, int rows, int width, tile_plan_t *out) {
+    out->op = op;
+    out->rows = rows;
+    out->width = width;
+    out->id = p.id;
+    out->path = p.C > 1 ? TILE_PATH_CLUSTER : TILE_PATH_CTA;
+    out->vec = p.V;
+    out->warps_per_program = p.S;
+    out->programs_per_cta = p.P;
+    out->chunks = p.K;
+    out->cluster = p.C;
+    out->threads = 32 * p.S * p.P;
+    out->workers = 32 * p.S;
+    out->stripe_floats = p.K * p.V;
+    out->max_width = max_width_of(p);
+    const int part = p.S > 1 ? 3 * p.P * p.S : 0;
+    out->smem_bytes = 4 * (part + (p.C > 1 ? 4 : 0));
+    const int phases = op == TILE_OP_RMSNORM ? 1 : 2;
+    out->barriers_per_row = (p.S > 1 ? phases : 0) + (p.C > 1 ? phases + 1 : 0);
+    out->grid = rows > 0 ? grid_of(p, rows) : 0;
+}
+
+thread_local int t_last_cuda_error = 0;
+
+bool overlaps(const void *a, const void *b, size_t bytes) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bytes && y < x + bytes;
+}
+
+bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; }
+
+bool coaligned16(const float *in, const float *res, const float *out, bool residual) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(in), c = reinterpret_cast<uintptr_t>(out);
+    if (((a ^ c) & 15u) != 0) return false;
+    if (residual && ((a ^ reinterpret_cast<uintptr_t>(res)) & 15u) != 0) return false;
+    return true;
+}
+
+// Checks shared by every compute entry point.  Returns TILE_OK with *noop set
+// when there is nothing to launch.
+int validate(int op, const float *in, const float *res, const float *out, int rows, int width,
+             float eps, bool *noop) {
+    *noop = false;
+    if (op < TILE_OP_RESIDUAL_LAYERNORM || op > TILE_OP_SOFTMAX) return TILE_ERR_OP;
+    if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH) return TILE_ERR_SHAPE;
+    if (op != TILE_OP_SOFTMAX && !(std::isfinite(eps) && eps >= 0.0f)) return TILE_ERR_EPS;
+    if (rows == 0) {
+        *noop = true;
+        return TILE_OK;
+    }
+    const bool residual = op == TILE_OP_RESIDUAL_LAYERNORM;
+    if (in == nullptr || out == nullptr || (residual && res == nullptr)) return TILE_ERR_NULL;
+    if (misaligned(in) || misaligned(out) || (residual && misaligned(res))) return TILE_ERR_ALIGN;
+    const size_t bytes = static_cast<size_t>(rows) * static_cast<size_t>(width) * sizeof(float);
+    if (overlaps(out, in, bytes) || (residual && overlaps(out, res, bytes))) return TILE_ERR_ALIAS;
+    return TILE_OK;
+}
+
+int launch(int op, int plan_id, const float *in, const float *res, float *out, int rows,
+           int width, float eps, cudaStream_t stream) {
+    const PlanDesc &p = kPlans[plan_id];
+    if (grid_of(p, rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
+    cudaError_t err;
+    switch (op) {
+        case TILE_OP_RESIDUAL_LAYERNORM:
+            err = tile::launch_residual_layernorm(plan_id, in, res, out, rows, width, eps, stream);
+            break;
+        case TILE_OP_LAYERNORM:
+            err = tile::launch_layernorm(plan_id, in, nullptr, out, rows, width, eps, stream);
+            break;
+        case TILE_OP_RMSNORM:
+            err = tile::launch_rmsnorm(plan_id, in, nullptr, out, rows, width, eps, stream);
+            break;
+        default:
+            err = tile::launch_softmax(plan_id, in, nullptr, out, rows, width, eps, stream);
+            break;
+    }
+    if (err != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(err);
+        return TILE_ERR_CUDA;
+    }
+    return TILE_OK;
+}
+
+int run_selected(int op, const float *in, const float *res, float *out, int rows, int width,
+                 float eps, cudaStream_t stream) {
+    bool noop = false;
+    const int st = validate(op, in, res, out, rows, width, eps, &noop);
+    if (st != TILE_OK || noop) return st;
+    const bool vec4 = coaligned16(in, res, out, op == TILE_OP_RESIDUAL_LAYERNORM);
+    const int plan = select_plan(op, rows, width, vec4);
+    if (plan < 0) return TILE_ERR_SHAPE;
+    return launch(op, plan, in, res, out, rows, width, eps, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int tile_residual_layernorm_f32(const float *in, const float *residual, float *out, int rows,
+                                int width, float eps, cudaStream_t stream) {
+    return run_selected(TILE_OP_RESIDUAL_LAYERNORM, in, residual, out, rows, width, eps, stream);
+}
+
+int tile_layernorm_f32(const float *in, float *out, int rows, int width, float eps,
+                       cudaStream_t stream) {
+    return run_selected(TILE_OP_LAYERNORM, in, nullptr, out, rows, width, eps, stream);
+}
+
+int tile_rmsnorm_f32(const float *in, float *out, int rows, int width, float eps,
+                     cudaStream_t stream) {
+    return run_selected(TILE_OP_RMSNORM, in, nullptr, out, rows, width, eps, stream);
+}
+
+int tile_softmax_f32(const float *in, float *out, int rows, int width, float eps,
+                     cudaStream_t stream) {
+    return run_selected(TILE_OP_SOFTMAX, in, nullptr, out, rows, width, eps, stream);
+}
+
+int tile_describe_plan(int op, int rows, int width, tile_plan_t *plan) {
+    if (op < TILE_OP_RESIDUAL_LAYERNORM || op > TILE_OP_SOFTMAX) return TILE_ERR_OP;
+    if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH) return TILE_ERR_SHAPE;
+    if (plan == nullptr) return TILE_ERR_NULL;
+    const int id = select_plan(op, rows, width, true);
+    if (id < 0) return TILE_ERR_SHAPE;
+    fill_plan(kPlans[id], op, rows, width, plan);
+    return TILE_OK;
+}
+
+int tile_plan_count(void) { return TILE_PLAN_COUNT; }
+
+int tile_plan_info(int id, int op, int rows, int width, tile_plan_t *plan) {
+    if (id < 0 || id >= TILE_PLAN_COUNT) return TILE_ERR_PLAN;
+    if (op < TILE_OP_RESIDUAL_LAYERNORM || op > TILE_OP_SOFTMAX) return TILE_ERR_OP;
+    if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH || !covers(kPlans[id], width))
+        return TILE_ERR_SHAPE;
+    if (plan == nullptr) return TILE_ERR_NULL;
+    fill_plan(kPlans[id], op, rows, width, plan);
+    return TILE_OK;
+}
+
+int tile_run_plan_f32(int op, int plan_id, const float *in, const float *residual, float *out,
+                      int rows, int width, float eps, cudaStream_t stream) {
+    bool noop = false;
+    const int st = validate(op, in, residual, out, rows, width, eps, &noop);
+    if (st != TILE_OK) return st;
+    if (plan_id < 0 || plan_id >= TILE_PLAN_COUNT || !covers(kPlans[plan_id], width))
+        return TILE_ERR_PLAN;
+    if (noop) return TILE_OK;
+    if (kPlans[plan_id].V == 4 &&
+        !coaligned16(in, residual, out, op == TILE_OP_RESIDUAL_LAYERNORM))
+        return TILE_ERR_PLAN;
+    return launch(op, plan_id, in, residual, out, rows, width, eps, stream);
+}
+
+int tile_max_width(void) { return TILE_MAX_WIDTH; }
+
+int tile_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char *tile_status_string(int status) {
+    switch (status) {
+        case TILE_OK: return "ok";
+        case TILE_ERR_NULL: return "a required pointer is NULL";
+        case TILE_ERR_SHAPE: return "rows < 0, width < 1, width above the maximum, or grid too large";
+        case TILE_ERR_ALIAS: return "out overlaps in or residual";
+        case TILE_ERR_EPS: return "eps is negative or not finite";
+        case TILE_ERR_CUDA: return "the CUDA runtime reported an error (see tile_last_cuda_error)";
+        case TILE_ERR_OP: return "unknown operation code";
+        case TILE_ERR_ALIGN: return "a pointer is not 4-byte aligned";
+        case TILE_ERR_PLAN: return "the plan does not exist, cannot cover the width, or needs 16-byte co-aligned pointers";
+        case TILE_ERR_DEVICE: return "a kernel recorded an error in the device status word";
+        default: return "unknown status";
+    }
+}
+
+int tile_check_device_status(cudaStream_t stream) {
+    unsigned int word = 0, v = 0;
+    cudaError_t (*fetch[])(unsigned int *, cudaStream_t) = {
+        tile::status_residual_layernorm, tile::status_layernorm, tile::status_rmsnorm,
+        tile::status_softmax};
+    for (auto f : fetch) {
+        v = 0;
+        const cudaError_t err = f(&v, stream);
+        if (err != cudaSuccess) {
+            t_last_cuda_error = static_cast<int>(err);
+            return TILE_ERR_CUDA;
+        }
+        word |= v;
+    }
+    return word ? TILE_ERR_DEVICE : TILE_OK;
+}
+
+}  // extern "C"
