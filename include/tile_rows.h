@@ -43,6 +43,7 @@
 #ifndef TILE_ROWS_H
 #define TILE_ROWS_H
 
+#include <stddef.h>
 #include <cuda_runtime_api.h>
 
 #ifdef __cplusplus
@@ -60,6 +61,7 @@ extern "C" {
 #define TILE_ERR_ALIGN       -7  /* a pointer is not 4-byte aligned           */
 #define TILE_ERR_PLAN        -8  /* an explicit plan is not one of the built  */
 #define TILE_ERR_DEVICE      -9  /* a kernel recorded an error on the device  */
+#define TILE_ERR_WORKSPACE  -10  /* device workspace too small for one row    */
 
 /* ---- operation codes (tile_describe_plan, tile_run_plan_f32) ----------- */
 #define TILE_OP_RESIDUAL_LAYERNORM 0
@@ -121,6 +123,33 @@ int tile_rmsnorm_f32(const float *in, float *out, int rows, int width, float eps
  * `eps` is accepted for a uniform signature and ignored. */
 int tile_softmax_f32(const float *in, float *out, int rows, int width, float eps,
                      cudaStream_t stream);
+
+/* ---- end to end on host buffers ---------------------------------------- */
+
+/* Run `op` on HOST buffers h_in[, h_residual] -> h_out ([rows][width] FP32
+ * each).  Rows stream through the caller's device workspace `d_work`
+ * (`work_bytes` bytes, 256-byte aligned) in chunks, double-buffered: the
+ * host->device copy of one chunk, the kernel on the previous chunk and the
+ * device->host copy of the one before overlap on three streams (the caller's
+ * `stream` runs the kernels; two internal non-blocking streams per device,
+ * created on first use, run the copies).  Host buffers should be pinned
+ * (cudaHostAlloc / cudaHostRegister) for the copies to overlap; pageable
+ * memory gives the same results more slowly.  Ownership: the caller owns all
+ * buffers and must keep them alive and untouched until `stream` has passed
+ * this call (the call returns once everything is enqueued; `stream` is
+ * ordered after the last copy).  Results are bitwise equal to the device
+ * entry point on the same rows.  `h_residual` is read only by
+ * TILE_OP_RESIDUAL_LAYERNORM.  Errors: as the compute entry points, plus
+ * TILE_ERR_NULL for a NULL d_work, TILE_ERR_ALIGN for a misaligned d_work and
+ * TILE_ERR_WORKSPACE when not even one row fits twice.  Calls from several
+ * host threads on one device are serialised inside the library. */
+int tile_run_host_f32(int op, const float *h_in, const float *h_residual, float *h_out,
+                      int rows, int width, float eps, void *d_work, size_t work_bytes,
+                      cudaStream_t stream);
+
+/* Workspace bytes tile_run_host_f32 needs to move `chunk_rows` rows per
+ * chunk (0 for invalid arguments).  Host only. */
+size_t tile_host_workspace_bytes(int op, int width, int chunk_rows);
 
 /* ---- plans and diagnostics -------------------------------------------- */
 

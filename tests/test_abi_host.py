@@ -14,7 +14,7 @@ from tile_compiler_row_gb300 import _build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-OK, NULL, SHAPE, ALIAS, EPS, CUDA, OP, ALIGN, PLAN, DEVICE = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
+OK, NULL, SHAPE, ALIAS, EPS, CUDA, OP, ALIGN, PLAN, DEVICE, WORKSPACE = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10
 
 
 @pytest.fixture(scope="module")
@@ -52,7 +52,7 @@ def test_python_binding_has_the_same_names():
 
 
 def test_status_strings(lib):
-    for code in (OK, NULL, SHAPE, ALIAS, EPS, CUDA, OP, ALIGN, PLAN, DEVICE):
+    for code in (OK, NULL, SHAPE, ALIAS, EPS, CUDA, OP, ALIGN, PLAN, DEVICE, WORKSPACE):
         s = tile.tile_status_string(code)
         assert s and s != "unknown status"
     assert tile.tile_status_string(12345) == "unknown status"
@@ -155,3 +155,26 @@ def test_binding_rejects_cpu_tensors():
     x = torch.zeros(2, 8)
     with pytest.raises(ValueError):
         tile.tile_rmsnorm_f32(x, torch.zeros(2, 8))
+
+
+def test_host_entry_rejects_bad_arguments(lib):
+    ws = 1 << 20
+    W = 0x30000000                       # fake device workspace, 256-aligned
+    f = lib.tile_run_host_f32
+    assert f(0, A, A, B, 0, 8, 1e-5, None, 0, None) == OK          # rows == 0
+    assert f(5, A, A, B, 2, 8, 1e-5, W, ws, None) == OP
+    assert f(0, A, A, B, 2, 0, 1e-5, W, ws, None) == SHAPE
+    assert f(1, A, None, B, 2, 8, -1.0, W, ws, None) == EPS
+    assert f(0, A, None, B, 2, 8, 1e-5, W, ws, None) == NULL
+    assert f(1, A, None, B, 2, 8, 1e-5, None, ws, None) == NULL
+    assert f(1, A, None, B, 2, 8, 1e-5, W + 16, ws, None) == ALIGN
+    assert f(1, A, None, A + 8, 2, 8, 1e-5, W, ws, None) == ALIAS
+    # one row of 4096 floats needs 2 x 2 x 16 KiB for a unary op
+    assert f(1, A, None, B, 2, 4096, 1e-5, W, 65535, None) == -10
+
+
+def test_host_workspace_bytes(lib):
+    assert tile.tile_host_workspace_bytes("layernorm", 4096, 1) == 2 * 2 * 16384
+    assert tile.tile_host_workspace_bytes("residual_layernorm", 100, 3) == 2 * 3 * 1280
+    assert tile.tile_host_workspace_bytes("softmax", 0, 3) == 0
+    assert tile.tile_host_workspace_bytes(9, 10, 3) == 0

@@ -1,0 +1,63 @@
+"""The benchmark's multi-rank plumbing on CPU: two gloo ranks, barrier and
+max-over-ranks of the timed region, and the whole-job throughput formula
+(replicas: every rank processes the full workload)."""
+
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    d = bench.Dist(world)
+    d.init("gloo")
+    d.barrier()
+    slowest = d.max(10.0 + rank)          # rank 1 is the slow one
+    d.barrier()
+    d.close()
+    q.put((rank, slowest))
+
+
+def test_two_gloo_ranks_take_the_max_time():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=5) for _ in range(world))
+    assert got == {0: 11.0, 1: 11.0}
+
+
+def test_job_throughput_is_weak_scaling():
+    sys.path.insert(0, ROOT)
+    import bench
+    one = bench.job_throughput(1, 3 * 2**30, 10, 5.0)
+    assert one == pytest.approx(3 * 2**30 * 10 / 5e-3 / 1e9)
+    assert bench.job_throughput(4, 3 * 2**30, 10, 5.0) == pytest.approx(4 * one)
+
+
+def test_dist_rejects_mismatched_world(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    with pytest.raises(SystemExit):
+        bench.Dist(4)

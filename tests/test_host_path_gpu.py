@@ -1,0 +1,102 @@
+"""GPU tests of the end-to-end entry point on host buffers: results match the
+oracle and the device entry point, for chunkings from one row per chunk to
+the whole matrix, with pinned and pageable host memory."""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+import tile_compiler_row_gb300 as tile
+from parity import EPS, compare, oracle_of
+
+pytestmark = pytest.mark.gpu
+
+OPS = ("residual_layernorm", "layernorm", "rmsnorm", "softmax")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def device():
+    from tile_compiler_row_gb300 import _build
+    _build.build()
+    torch.cuda.set_device(0)
+    yield
+    assert tile.tile_check_device_status() == 0
+
+
+def _host(a, pinned):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.pin_memory() if pinned else t.clone()
+
+
+def _run_host(op, x, r, chunk_rows, pinned=True, stream=None):
+    rows, width = x.shape
+    ws_bytes = tile.tile_host_workspace_bytes(op, width, chunk_rows)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    hx = _host(x, pinned)
+    hr = _host(r, pinned) if r is not None else None
+    out = torch.full(x.shape, float("nan"))
+    out = out.pin_memory() if pinned else out
+    tile.tile_run_host_f32(op, hx, hr, out, ws, EPS, stream)
+    (stream or torch.cuda.current_stream()).synchronize()
+    return out.numpy().copy()
+
+
+def _run_device(op, x, r):
+    tx = torch.from_numpy(x).cuda()
+    tr = torch.from_numpy(r).cuda() if r is not None else None
+    y = torch.empty_like(tx)
+    tile.run(op, tx, tr, y, EPS)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("rows,width,chunk", [(37, 1537, 1), (37, 1537, 7), (1000, 4096, 125),
+                                              (1000, 4096, 300), (5, 131072, 2), (3, 127, 64)])
+def test_host_path_matches_oracle_and_device_path(op, rows, width, chunk):
+    x = synth.rows_of(3, rows, width, which="x")
+    r = synth.rows_of(3, rows, width, which="r") if op == "residual_layernorm" else None
+    got = _run_host(op, x, r, chunk)
+    compare(got, oracle_of(op, x, r), f"host {op} {rows}x{width} chunk {chunk}")
+    same_plan = tile.tile_describe_plan(op, min(chunk, rows), width)["id"] == \
+        tile.tile_describe_plan(op, rows, width)["id"]
+    if same_plan:
+        assert np.array_equal(got, _run_device(op, x, r))
+
+
+@pytest.mark.parametrize("op", ["residual_layernorm", "softmax"])
+def test_host_path_pageable_memory_and_side_stream(op):
+    x = synth.rows_of(3, 64, 4096, which="x")
+    r = synth.rows_of(3, 64, 4096, which="r") if op == "residual_layernorm" else None
+    s = torch.cuda.Stream()
+    got = _run_host(op, x, r, 9, pinned=False, stream=s)
+    compare(got, oracle_of(op, x, r), f"pageable {op}")
+
+
+def test_host_path_back_to_back_calls_share_the_workspace():
+    """Two calls in a row on one stream through one workspace: the second
+    must not overwrite the first call's chunks before they are copied out."""
+    op = "residual_layernorm"
+    rows, width = 300, 2048
+    x = synth.rows_of(3, rows, width, which="x")
+    r = synth.rows_of(3, rows, width, which="r")
+    x2 = (x[::-1] * np.float32(0.5)).copy()
+    ws = torch.empty(tile.tile_host_workspace_bytes(op, width, 16), dtype=torch.uint8,
+                     device="cuda")
+    outs = []
+    for xi in (x, x2):
+        o = torch.empty(rows, width).pin_memory()
+        tile.tile_run_host_f32(op, _host(xi, True), _host(r, True), o, ws, EPS)
+        outs.append(o)
+    torch.cuda.synchronize()
+    compare(outs[0].numpy(), oracle_of(op, x, r), "first call")
+    compare(outs[1].numpy(), oracle_of(op, x2, r), "second call")
+
+
+def test_host_path_workspace_too_small_raises():
+    x = torch.zeros(4, 4096).pin_memory()
+    ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(tile.TileError) as e:
+        tile.tile_run_host_f32("layernorm", x, None, torch.zeros(4, 4096), ws)
+    assert e.value.status == -10

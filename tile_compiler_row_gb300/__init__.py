@@ -23,7 +23,8 @@ __all__ = [
     "tile_residual_layernorm_f32", "tile_layernorm_f32", "tile_rmsnorm_f32",
     "tile_softmax_f32", "tile_run_plan_f32", "tile_describe_plan", "tile_plan_info",
     "tile_plan_count", "tile_max_width", "tile_status_string",
-    "tile_check_device_status", "tile_last_cuda_error",
+    "tile_check_device_status", "tile_last_cuda_error", "tile_run_host_f32",
+    "tile_host_workspace_bytes",
     "residual_layernorm", "layernorm", "rmsnorm", "softmax", "run",
 ]
 
@@ -89,11 +90,14 @@ def load():
         "tile_max_width": [],
         "tile_check_device_status": [P],
         "tile_last_cuda_error": [],
+        "tile_run_host_f32": [I, P, P, P, I, I, F, P, ctypes.c_size_t, P],
     }
     for name, argtypes in sigs.items():
         fn = getattr(lib, name)
         fn.argtypes = argtypes
         fn.restype = ctypes.c_int
+    lib.tile_host_workspace_bytes.argtypes = [I, I, I]
+    lib.tile_host_workspace_bytes.restype = ctypes.c_size_t
     lib.tile_status_string.argtypes = [I]
     lib.tile_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -181,6 +185,41 @@ def tile_run_plan_f32(op, plan_id, x, residual, out, eps=1e-5, stream=None):
         _same_shape(x, residual, "x/residual")
     _check(load().tile_run_plan_f32(op, plan_id, px, pr, po, rows, width, eps, _stream(stream)),
            "tile_run_plan_f32")
+
+
+def _host_matrix(t, name):
+    """(pointer, rows, width) of a CPU FP32 row-major matrix tensor."""
+    import torch
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a CPU tensor (ideally pinned)")
+    if t.dtype != torch.float32 or t.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D float32 tensor")
+    rows, width = t.shape
+    if rows > 1 and t.stride(0) != width or width > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major with row stride == width")
+    return t.data_ptr(), rows, width
+
+
+def tile_run_host_f32(op, x, residual, out, workspace, eps=1e-5, stream=None):
+    """``op`` on host tensors through the device ``workspace`` (a CUDA tensor)."""
+    op = OPS[op] if isinstance(op, str) else op
+    px, rows, width = _host_matrix(x, "x")
+    po, _, _ = _host_matrix(out, "out")
+    _same_shape(x, out, "x/out")
+    pr = None
+    if residual is not None:
+        pr, _, _ = _host_matrix(residual, "residual")
+        _same_shape(x, residual, "x/residual")
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().tile_run_host_f32(op, px, pr, po, rows, width, eps, workspace.data_ptr(),
+                                    nbytes, _stream(stream)), "tile_run_host_f32")
+
+
+def tile_host_workspace_bytes(op, width, chunk_rows):
+    op = OPS[op] if isinstance(op, str) else op
+    return load().tile_host_workspace_bytes(op, width, chunk_rows)
 
 
 def tile_describe_plan(op, rows, width):

@@ -14,4 +14,13 @@ TILE_DECLARE_OP(layernorm)
 TILE_DECLARE_OP(rmsnorm)
 TILE_DECLARE_OP(softmax)
 #undef TILE_DECLARE_OP
+
+// Check arguments, pick a plan and launch `op` on device buffers (the body of
+// the four compute entry points).  Returns a TILE_* status.
+int run_selected(int op, const float *in, const float *res, float *out, int rows, int width,
+                 float eps, cudaStream_t stream);
+
+// The cudaError_t behind the last TILE_ERR_CUDA on this host thread.
+void set_last_cuda_error(int err);
+int last_cuda_error();
 }  // namespace tile

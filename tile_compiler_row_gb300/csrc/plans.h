@@ -51,9 +51,17 @@
     X(26, 1, 4, 2, 8, 1)                                                      \
     X(27, 1, 8, 1, 16, 1)                                                     \
     X(28, 1, 32, 1, 16, 1)                                                    \
-    X(29, 1, 32, 1, 16, 8)
+    X(29, 1, 32, 1, 16, 8)                                                    \
+    /* deeper stripes: more loads in flight per thread */                     \
+    X(30, 4, 16, 1, 8, 8)                                                     \
+    X(31, 4, 8, 1, 16, 1)                                                     \
+    X(32, 4, 4, 1, 16, 1)                                                     \
+    X(33, 4, 16, 1, 8, 4)                                                     \
+    X(34, 4, 16, 1, 8, 2)                                                     \
+    X(35, 4, 2, 1, 16, 1)                                                     \
+    X(36, 4, 4, 2, 8, 1)
 
-#define TILE_PLAN_COUNT 30
+#define TILE_PLAN_COUNT 37
 
 // Widest row covered by both a V = 4 and a V = 1 plan.
 #define TILE_MAX_WIDTH 131072

@@ -91,8 +91,6 @@ void fill_plan(const PlanDesc &p, int op, int rows, int width, tile_plan_t *out)
     out->grid = rows > 0 ? grid_of(p, rows) : 0;
 }
 
-thread_local int t_last_cuda_error = 0;
-
 bool overlaps(const void *a, const void *b, size_t bytes) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return x < y + bytes && y < x + bytes;
@@ -147,11 +145,22 @@ int launch(int op, int plan_id, const float *in, const float *res, float *out, i
             break;
     }
     if (err != cudaSuccess) {
-        t_last_cuda_error = static_cast<int>(err);
+        tile::set_last_cuda_error(static_cast<int>(err));
         return TILE_ERR_CUDA;
     }
     return TILE_OK;
 }
+
+}  // namespace
+
+namespace tile {
+
+namespace {
+thread_local int t_last_cuda_error = 0;
+}
+
+void set_last_cuda_error(int err) { t_last_cuda_error = err; }
+int last_cuda_error() { return t_last_cuda_error; }
 
 int run_selected(int op, const float *in, const float *res, float *out, int rows, int width,
                  float eps, cudaStream_t stream) {
@@ -164,28 +173,28 @@ int run_selected(int op, const float *in, const float *res, float *out, int rows
     return launch(op, plan, in, res, out, rows, width, eps, stream);
 }
 
-}  // namespace
+}  // namespace tile
 
 extern "C" {
 
 int tile_residual_layernorm_f32(const float *in, const float *residual, float *out, int rows,
                                 int width, float eps, cudaStream_t stream) {
-    return run_selected(TILE_OP_RESIDUAL_LAYERNORM, in, residual, out, rows, width, eps, stream);
+    return tile::run_selected(TILE_OP_RESIDUAL_LAYERNORM, in, residual, out, rows, width, eps, stream);
 }
 
 int tile_layernorm_f32(const float *in, float *out, int rows, int width, float eps,
                        cudaStream_t stream) {
-    return run_selected(TILE_OP_LAYERNORM, in, nullptr, out, rows, width, eps, stream);
+    return tile::run_selected(TILE_OP_LAYERNORM, in, nullptr, out, rows, width, eps, stream);
 }
 
 int tile_rmsnorm_f32(const float *in, float *out, int rows, int width, float eps,
                      cudaStream_t stream) {
-    return run_selected(TILE_OP_RMSNORM, in, nullptr, out, rows, width, eps, stream);
+    return tile::run_selected(TILE_OP_RMSNORM, in, nullptr, out, rows, width, eps, stream);
 }
 
 int tile_softmax_f32(const float *in, float *out, int rows, int width, float eps,
                      cudaStream_t stream) {
-    return run_selected(TILE_OP_SOFTMAX, in, nullptr, out, rows, width, eps, stream);
+    return tile::run_selected(TILE_OP_SOFTMAX, in, nullptr, out, rows, width, eps, stream);
 }
 
 int tile_describe_plan(int op, int rows, int width, tile_plan_t *plan) {
@@ -226,7 +235,7 @@ int tile_run_plan_f32(int op, int plan_id, const float *in, const float *residua
 
 int tile_max_width(void) { return TILE_MAX_WIDTH; }
 
-int tile_last_cuda_error(void) { return t_last_cuda_error; }
+int tile_last_cuda_error(void) { return tile::last_cuda_error(); }
 
 const char *tile_status_string(int status) {
     switch (status) {
@@ -240,6 +249,7 @@ const char *tile_status_string(int status) {
         case TILE_ERR_ALIGN: return "a pointer is not 4-byte aligned";
         case TILE_ERR_PLAN: return "the plan does not exist, cannot cover the width, or needs 16-byte co-aligned pointers";
         case TILE_ERR_DEVICE: return "a kernel recorded an error in the device status word";
+        case TILE_ERR_WORKSPACE: return "the device workspace cannot hold one row chunk twice";
         default: return "unknown status";
     }
 }
@@ -253,7 +263,7 @@ int tile_check_device_status(cudaStream_t stream) {
         v = 0;
         const cudaError_t err = f(&v, stream);
         if (err != cudaSuccess) {
-            t_last_cuda_error = static_cast<int>(err);
+            tile::set_last_cuda_error(static_cast<int>(err));
             return TILE_ERR_CUDA;
         }
         word |= v;

@@ -1,0 +1,115 @@
+"""Measured plan sweep: time every built plan that covers a shape.
+
+The width->plan selector of the library is a table frozen from this sweep
+(measurement picks the mapping, not an analytic score).  For each
+(op, rows, width) every covering float4 plan is timed with CUDA events on
+the current stream: ``--warmup`` calls, then ``--iters`` calls, median of
+the per-call times.  Inputs are uniform random device tensors; only timing
+is recorded here (parity of every plan is covered by the GPU tests).
+
+    python -m tile_compiler_row_gb300.sweep --out sweep.json [--quick]
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import statistics
+import sys
+
+OPS = ("residual_layernorm", "layernorm", "rmsnorm", "softmax")
+BYTES = {"residual_layernorm": 12, "layernorm": 8, "rmsnorm": 8, "softmax": 8}
+
+#: widths of the sweep ladder; ``rows`` fills about 2**26 elements per tensor
+#: (256 MiB, well above L2) so the large-row regime is HBM bound.
+LADDER = (64, 127, 257, 512, 1024, 1537, 2048, 3072, 4096, 6144, 8192, 12288, 16384,
+          32768, 65536, 131072)
+#: the small shapes of the workloads (L2 resident).
+SMALL = ((1, 127), (17, 257), (7, 1537), (64, 4096), (1024, 4096), (128, 8192),
+         (32, 65536))
+
+
+def shapes(quick=False):
+    out = []
+    ladder = LADDER if not quick else (257, 1024, 4096, 8192, 65536)
+    for w in ladder:
+        out.append((max(16, (1 << 26) // w), w))
+    out.extend(SMALL)
+    return out
+
+
+def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream):
+    import torch
+    s = stream.cuda_stream
+    px, pr, py = x.data_ptr(), r.data_ptr(), y.data_ptr()
+
+    def call():
+        st = lib.tile_run_plan_f32(op_code, plan, px, pr, py, rows, width, 1e-5, s)
+        if st != 0:
+            raise RuntimeError(f"plan {plan}: status {st}")
+
+    for _ in range(warmup):
+        call()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
+    evs[0].record(stream)
+    for i in range(iters):
+        call()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(iters)]
+    return statistics.median(per)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--out", default=None)
+    ap.add_argument("--quick", action="store_true")
+    ap.add_argument("--ops", default=",".join(OPS))
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--iters", type=int, default=30)
+    ap.add_argument("--shapes", default=None, help="comma list of ROWSxWIDTH (default: ladder)")
+    args = ap.parse_args(argv)
+
+    import torch
+
+    import tile_compiler_row_gb300 as tile
+    from tile_compiler_row_gb300 import _build
+    _build.build()
+    lib = tile.load()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    results = []
+    todo = shapes(args.quick) if args.shapes is None else \
+        [tuple(int(v) for v in sh.split("x")) for sh in args.shapes.split(",")]
+    for rows, width in todo:
+        n = rows * width
+        g = torch.Generator(device="cuda").manual_seed(rows * 131 + width)
+        x = torch.rand(rows, width, device="cuda", generator=g) * 2 - 1
+        r = torch.rand(rows, width, device="cuda", generator=g) * 2 - 1
+        y = torch.empty_like(x)
+        for op in args.ops.split(","):
+            code = tile.OPS[op]
+            chosen = tile.tile_describe_plan(op, rows, width)["id"]
+            entry = {"op": op, "rows": rows, "width": width, "selected": chosen, "plans": {}}
+            for pid in range(tile.tile_plan_count()):
+                info = tile.tile_plan_info(pid, op, rows, width)
+                if info is None or info["vec"] != 4 or info["grid"] > 0x7FFFFFFF:
+                    continue
+                us = time_plan(lib, code, pid, x, r, y, rows, width, args.warmup, args.iters, stream)
+                entry["plans"][pid] = round(us, 3)
+            best = min(entry["plans"], key=entry["plans"].get)
+            entry["best"] = best
+            entry["best_gbs"] = round(BYTES[op] * n / (entry["plans"][best] * 1e-6) / 1e9, 1)
+            entry["selected_over_best"] = round(entry["plans"][chosen] / entry["plans"][best], 4)
+            results.append(entry)
+            print(json.dumps(entry), flush=True)
+        del x, r, y
+    assert tile.tile_check_device_status() == 0
+    if args.out:
+        with open(args.out, "w") as fh:
+            json.dump(results, fh, indent=1)
+    return results
+
+
+if __name__ == "__main__":
+    sys.exit(0 if main() is not None else 1)
