@@ -137,8 +137,11 @@ int tile_softmax_f32(const float *in, float *out, int rows, int width, float eps
  * memory gives the same results more slowly.  Ownership: the caller owns all
  * buffers and must keep them alive and untouched until `stream` has passed
  * this call (the call returns once everything is enqueued; `stream` is
- * ordered after the last copy).  Results are bitwise equal to the device
- * entry point on the same rows.  `h_residual` is read only by
+ * ordered after the last copy).  Results meet the same tolerance as the
+ * device entry points, and are bitwise equal to them when width is a
+ * multiple of 4 and the chunk and the full matrix get the same plan (chunks
+ * start 256-byte aligned in the workspace, so row start phases can differ
+ * from the full matrix otherwise).  `h_residual` is read only by
  * TILE_OP_RESIDUAL_LAYERNORM.  Errors: as the compute entry points, plus
  * TILE_ERR_NULL for a NULL d_work, TILE_ERR_ALIGN for a misaligned d_work and
  * TILE_ERR_WORKSPACE when not even one row fits twice.  Calls from several

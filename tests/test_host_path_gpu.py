@@ -59,9 +59,12 @@ def test_host_path_matches_oracle_and_device_path(op, rows, width, chunk):
     r = synth.rows_of(3, rows, width, which="r") if op == "residual_layernorm" else None
     got = _run_host(op, x, r, chunk)
     compare(got, oracle_of(op, x, r), f"host {op} {rows}x{width} chunk {chunk}")
+    # Bitwise equality needs the same plan and the same 16-byte phase of every
+    # row start (chunks start 256-byte aligned in the workspace; rows of the
+    # full tensor do only when width is a multiple of 4).
     same_plan = tile.tile_describe_plan(op, min(chunk, rows), width)["id"] == \
         tile.tile_describe_plan(op, rows, width)["id"]
-    if same_plan:
+    if same_plan and width % 4 == 0:
         assert np.array_equal(got, _run_device(op, x, r))
 
 

@@ -37,16 +37,32 @@ int max_width_of(const PlanDesc &p) {
 }
 
 // Selector: for each op, the first entry whose width bound covers the row.
-// Separate tables for 16-byte co-aligned pointers (V = 4 plans) and for the
-// rest (V = 1 plans).
+// The float4 tables (16-byte co-aligned pointers) are frozen from the
+// measured plan sweep on GB300 (sweep.py: every covering plan timed with
+// CUDA events at about 2^26 elements per tensor for each width of a ladder,
+// plus the small workload shapes and 65536 x 4096); each bucket takes the
+// fastest plan, or one within 1 % of it that also wins the neighbouring
+// widths.  Pointers with different 16-byte phases use the scalar plans.
 struct Bucket {
     int max_width;
     int plan;
 };
 
-constexpr Bucket kVec4[] = {
-    {131, 0}, {259, 1}, {515, 2}, {1027, 3}, {2051, 5}, {4099, 8},
-    {8195, 11}, {16387, 13}, {32771, 16}, {65539, 18}, {TILE_MAX_WIDTH, 20},
+constexpr Bucket kVec4ResidualLN[] = {
+    {131, 0}, {259, 1}, {515, 2}, {1027, 4}, {2051, 6}, {3075, 35}, {4099, 7},
+    {8195, 10}, {12291, 31}, {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 20},
+};
+constexpr Bucket kVec4LN[] = {
+    {131, 0}, {259, 1}, {515, 2}, {1027, 4}, {2051, 6}, {4099, 7},
+    {8195, 10}, {16387, 31}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
+};
+constexpr Bucket kVec4RMS[] = {
+    {131, 0}, {259, 2}, {515, 4}, {1027, 6}, {2051, 5}, {3075, 8}, {8195, 10},
+    {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
+};
+constexpr Bucket kVec4Softmax[] = {
+    {131, 0}, {259, 1}, {515, 2}, {1027, 3}, {2051, 6}, {4099, 7},
+    {8195, 10}, {16387, 31}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
 };
 constexpr Bucket kVec1[] = {
     {128, 25}, {1024, 26}, {4096, 27}, {16384, 28}, {TILE_MAX_WIDTH, 29},
@@ -60,9 +76,14 @@ int pick(const Bucket (&table)[N], int width) {
 }
 
 int select_plan(int op, long long rows, int width, bool vec4) {
-    (void)op;
     (void)rows;
-    return vec4 ? pick(kVec4, width) : pick(kVec1, width);
+    if (!vec4) return pick(kVec1, width);
+    switch (op) {
+        case TILE_OP_RESIDUAL_LAYERNORM: return pick(kVec4ResidualLN, width);
+        case TILE_OP_LAYERNORM: return pick(kVec4LN, width);
+        case TILE_OP_RMSNORM: return pick(kVec4RMS, width);
+        default: return pick(kVec4Softmax, width);
+    }
 }
 
 long long grid_of(const PlanDesc &p, long long rows) {
