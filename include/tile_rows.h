@@ -154,6 +154,41 @@ int tile_run_host_f32(int op, const float *h_in, const float *h_residual, float 
  * chunk (0 for invalid arguments).  Host only. */
 size_t tile_host_workspace_bytes(int op, int width, int chunk_rows);
 
+/* Size of the library's own device staging area used by
+ * tile_run_host_static_f32: 64 MiB, held by every GPU that loads the library
+ * until the process exits. */
+#define TILE_STATIC_STAGING_BYTES (64u << 20)
+
+/* tile_run_host_f32 for callers that cannot allocate device memory.  (The
+ * notes this library follows have no counterpart of this call.)
+ *
+ * Some callers cannot call cudaMalloc where they run: code that runs after
+ * an application has fixed its device memory budget, plugin code inside a
+ * framework that owns the device allocator, or latency-critical code where a
+ * device allocation (which can synchronise the device) is not allowed.  This
+ * call allocates nothing: rows are staged through a static device array of
+ * TILE_STATIC_STAGING_BYTES inside the library instead of a caller
+ * workspace.  Arguments, results, errors and ownership are those of
+ * tile_run_host_f32 without d_work/work_bytes.
+ *
+ * Limits: any number of rows (they stream through the area in chunks);
+ * 1 <= width <= tile_max_width() (one row of every tensor, 3 x 4 x 131072
+ * bytes at most, fits the area twice).  A width beyond that maximum returns
+ * TILE_ERR_SHAPE, and TILE_ERR_WORKSPACE would report a row that cannot fit.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, which may load the library's device code) and
+ * creates one event; make that first call before any stream capture.
+ *
+ * Sharing: every call on a device uses the same array, and the array keeps
+ * the last call's contents (nothing in it needs to start at zero: each
+ * chunk is copied in before the kernel reads it).  Calls that overlapped on
+ * the GPU would race on the array, so the library orders each call's work
+ * on the GPU after the previous call's end (an event), whatever stream it
+ * was given; calls on different streams therefore run one after another. */
+int tile_run_host_static_f32(int op, const float *h_in, const float *h_residual, float *h_out,
+                             int rows, int width, float eps, cudaStream_t stream);
+
 /* ---- plans and diagnostics -------------------------------------------- */
 
 /* The plan the library would launch for (op, rows, width) with 16-byte

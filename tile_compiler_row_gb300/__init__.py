@@ -24,7 +24,7 @@ __all__ = [
     "tile_softmax_f32", "tile_run_plan_f32", "tile_describe_plan", "tile_plan_info",
     "tile_plan_count", "tile_max_width", "tile_status_string",
     "tile_check_device_status", "tile_last_cuda_error", "tile_run_host_f32",
-    "tile_host_workspace_bytes",
+    "tile_host_workspace_bytes", "tile_run_host_static_f32",
     "residual_layernorm", "layernorm", "rmsnorm", "softmax", "run",
 ]
 
@@ -91,6 +91,7 @@ def load():
         "tile_check_device_status": [P],
         "tile_last_cuda_error": [],
         "tile_run_host_f32": [I, P, P, P, I, I, F, P, ctypes.c_size_t, P],
+        "tile_run_host_static_f32": [I, P, P, P, I, I, F, P],
     }
     for name, argtypes in sigs.items():
         fn = getattr(lib, name)
@@ -215,6 +216,21 @@ def tile_run_host_f32(op, x, residual, out, workspace, eps=1e-5, stream=None):
     nbytes = workspace.numel() * workspace.element_size()
     _check(load().tile_run_host_f32(op, px, pr, po, rows, width, eps, workspace.data_ptr(),
                                     nbytes, _stream(stream)), "tile_run_host_f32")
+
+
+def tile_run_host_static_f32(op, x, residual, out, eps=1e-5, stream=None):
+    """``op`` on host tensors through the library's static device staging
+    area: for callers that cannot allocate device memory."""
+    op = OPS[op] if isinstance(op, str) else op
+    px, rows, width = _host_matrix(x, "x")
+    po, _, _ = _host_matrix(out, "out")
+    _same_shape(x, out, "x/out")
+    pr = None
+    if residual is not None:
+        pr, _, _ = _host_matrix(residual, "residual")
+        _same_shape(x, residual, "x/residual")
+    _check(load().tile_run_host_static_f32(op, px, pr, po, rows, width, eps, _stream(stream)),
+           "tile_run_host_static_f32")
 
 
 def tile_host_workspace_bytes(op, width, chunk_rows):

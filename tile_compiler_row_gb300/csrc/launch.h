@@ -20,6 +20,10 @@ TILE_DECLARE_OP(softmax)
 int run_selected(int op, const float *in, const float *res, float *out, int rows, int width,
                  float eps, cudaStream_t stream);
 
+// The pipeline of tile_run_host_f32 over a given device workspace.
+int run_host(int op, const float *h_in, const float *h_res, float *h_out, int rows, int width,
+             float eps, void *d_work, size_t work_bytes, cudaStream_t stream);
+
 // The cudaError_t behind the last TILE_ERR_CUDA on this host thread.
 void set_last_cuda_error(int err);
 int last_cuda_error();
