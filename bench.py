@@ -199,9 +199,9 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profile_traffic(op, rows, width):
+def profile_traffic(op, rows, width, plan_id):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the kernel source that is built now (else None)."""
+    the kernel source that is built now and on the same plan (else None)."""
     from tile_compiler_row_gb300 import _build
     path = os.path.join(ROOT, "profiles", f"{op}_{rows}x{width}.md")
     try:
@@ -214,7 +214,9 @@ def profile_traffic(op, rows, width):
         if ":" in line:
             k, v = line.split(":", 1)
             fields[k.strip().strip("`")] = v.strip().strip("`")
-    if fields.get("source_sha256") != _build.source_hash():
+    if fields.get("kernel_sha256") != _build.kernel_hash():
+        return None
+    if fields.get("plan_id") != str(plan_id):
         return None
     try:
         return int(float(fields["dram_bytes_per_launch"]))
@@ -308,7 +310,7 @@ def run_ours(args, dist):
     kernel_ms = statistics.mean(per)
     peak, peak_src = measured_peaks()
     achieved = nbytes / (kernel_ms / 1e3) / 1e9
-    traffic = profile_traffic(op, rows, width)
+    traffic = profile_traffic(op, rows, width, plan["id"])
     line = {
         "metric": METRIC if (op, rows, width) == ("residual_layernorm", 65536, 4096) else
         f"HBM GB/s and µs/call, {op} FP32 {rows}×{width}",

@@ -51,6 +51,17 @@ def source_hash() -> str:
     return h.hexdigest()
 
 
+def kernel_hash() -> str:
+    """SHA-256 of the row kernel's device code and launch code (what an ncu
+    traffic figure was measured on); host-only files do not change it."""
+    h = hashlib.sha256()
+    for name in ("row_kernel.cuh", "ops_inst.cuh"):
+        with open(os.path.join(CSRC, name), "rb") as fh:
+            h.update(name.encode())
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def stale() -> bool:
     if not os.path.exists(LIBRARY):
         return True
