@@ -54,8 +54,16 @@ class Oracle:
         lib.oracle_layernorm.argtypes = [f32p, f64p, L, L, D]
         lib.oracle_rmsnorm.argtypes = [f32p, f64p, L, L, D]
         lib.oracle_softmax.argtypes = [f32p, f64p, L, L]
+        lib.oracle_layernorm_affine.argtypes = [f32p, f32p, f32p, f32p, f64p, L, L, D]
+        lib.oracle_rmsnorm_weighted.argtypes = [f32p, f32p, f64p, L, L, D]
+        lib.oracle_row_sum.argtypes = [f32p, f64p, L, L]
+        lib.oracle_row_minmax.argtypes = [f32p, f64p, f64p, L, L]
+        lib.oracle_sigmoid_pair.argtypes = [f32p, f64p, f64p, L]
+        lib.oracle_gelu_tanh_pair.argtypes = [f32p, f64p, f64p, L]
         for fn in (lib.oracle_residual_layernorm, lib.oracle_layernorm,
-                   lib.oracle_rmsnorm, lib.oracle_softmax):
+                   lib.oracle_rmsnorm, lib.oracle_softmax, lib.oracle_layernorm_affine,
+                   lib.oracle_rmsnorm_weighted, lib.oracle_row_sum, lib.oracle_row_minmax,
+                   lib.oracle_sigmoid_pair, lib.oracle_gelu_tanh_pair):
             fn.restype = None
         self._lib = lib
 
@@ -104,6 +112,75 @@ class Oracle:
             self._lib.oracle_softmax(self._p(x, ctypes.c_float), self._p(y, ctypes.c_double),
                                      x.shape[0], x.shape[1])
         return y
+
+    @staticmethod
+    def _vec(a, n, name):
+        a = np.ascontiguousarray(a, dtype=np.float32).reshape(-1)
+        if a.size != n:
+            raise ValueError(f"{name} must have {n} elements")
+        return a
+
+    def layernorm_affine(self, x, gamma, beta=None, r=None, eps=1e-5):
+        """LayerNorm of x (+ r) times gamma plus beta (r, beta optional)."""
+        x = self._f32(x)
+        rows, width = x.shape
+        g = self._vec(gamma, width, "gamma")
+        b = self._vec(beta, width, "beta") if beta is not None else None
+        rr = self._f32(r) if r is not None else None
+        if rr is not None and rr.shape != x.shape:
+            raise ValueError("x and residual shapes differ")
+        y = np.empty(x.shape, dtype=np.float64)
+        if x.size:
+            f32 = ctypes.c_float
+            self._lib.oracle_layernorm_affine(
+                self._p(x, f32), self._p(rr, f32) if rr is not None else None,
+                self._p(g, f32), self._p(b, f32) if b is not None else None,
+                self._p(y, ctypes.c_double), rows, width, float(eps))
+        return y
+
+    def rmsnorm_weighted(self, x, gamma, eps=1e-5):
+        x = self._f32(x)
+        rows, width = x.shape
+        g = self._vec(gamma, width, "gamma")
+        y = np.empty(x.shape, dtype=np.float64)
+        if x.size:
+            self._lib.oracle_rmsnorm_weighted(self._p(x, ctypes.c_float), self._p(g, ctypes.c_float),
+                                              self._p(y, ctypes.c_double), rows, width, float(eps))
+        return y
+
+    def row_sum(self, x):
+        x = self._f32(x)
+        s = np.empty(x.shape[0], dtype=np.float64)
+        if x.size:
+            self._lib.oracle_row_sum(self._p(x, ctypes.c_float), self._p(s, ctypes.c_double),
+                                     x.shape[0], x.shape[1])
+        return s
+
+    def row_minmax(self, x):
+        x = self._f32(x)
+        mn = np.empty(x.shape[0], dtype=np.float64)
+        mx = np.empty(x.shape[0], dtype=np.float64)
+        if x.size:
+            self._lib.oracle_row_minmax(self._p(x, ctypes.c_float), self._p(mn, ctypes.c_double),
+                                        self._p(mx, ctypes.c_double), x.shape[0], x.shape[1])
+        return mn, mx
+
+    def _pair(self, fn, x):
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        y = np.empty(x.shape, dtype=np.float64)
+        dy = np.empty(x.shape, dtype=np.float64)
+        if x.size:
+            fn(self._p(x, ctypes.c_float), self._p(y, ctypes.c_double),
+               self._p(dy, ctypes.c_double), x.size)
+        return y, dy
+
+    def sigmoid_pair(self, x):
+        """(sigmoid(x), sigmoid'(x)) elementwise, any shape."""
+        return self._pair(self._lib.oracle_sigmoid_pair, x)
+
+    def gelu_tanh_pair(self, x):
+        """(tanh-GELU(x), its derivative) elementwise, any shape."""
+        return self._pair(self._lib.oracle_gelu_tanh_pair, x)
 
     def run(self, op: str, x, r=None, eps=1e-5):
         """Dispatch by library op name."""

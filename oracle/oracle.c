@@ -122,3 +122,125 @@ void oracle_softmax(const float *x, double *y, long rows, long width)
             yi[j] = exp((double)xi[j] - m) / total;
     }
 }
+
+/* ------------------------------------------------------------------------
+ * Further operations named on the pages.
+ *
+ *  - affine LayerNorm: the runner's tolerance table of "Cooperating-program
+ *    packing", section "Predeclared comparison and measurement", lists
+ *    affine LayerNorm; the formula is not printed.  Reading taken: the
+ *    LayerNorm above, then y * gamma[j] + beta[j] (beta optional), with the
+ *    residual added first when one is given.  Weighted RMSNorm likewise:
+ *    x / sqrt(mean(x^2) + eps) * gamma[j].
+ *  - row sum and paired row min/max: the operators "sum" and "paired min/max"
+ *    of "Cooperating-program packing", section "Validation" (sum is also the
+ *    identical-source control of "Immutable input reuse in Metal
+ *    reductions").
+ *  - sigmoid and tanh-approximate GELU, each with its derivative:
+ *    "Multi-output pointwise fusion: evidence and limits", section
+ *    "Measurement definitions and population".  sigmoid(x) = 1/(1+exp(-x)),
+ *    derivative s(1-s).  tanh GELU (Hendrycks and Gimpel 2016):
+ *    g(x) = x/2 (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), derivative
+ *    g'(x) = (1 + tanh(u))/2 + x/2 (1 - tanh(u)^2) sqrt(2/pi) (1 + 3*0.044715 x^2).
+ * ------------------------------------------------------------------------ */
+
+/* y = LayerNorm(x [+ r]) * gamma + beta; r and beta may be NULL. */
+void oracle_layernorm_affine(const float *x, const float *r, const float *gamma,
+                             const float *beta, double *y, long rows, long width, double eps)
+{
+    for (long i = 0; i < rows; ++i) {
+        const float *xi = x + i * width;
+        const float *ri = r ? r + i * width : 0;
+        double *yi = y + i * width;
+
+        double sum = 0.0;
+        for (long j = 0; j < width; ++j)
+            sum += (double)xi[j] + (ri ? (double)ri[j] : 0.0);
+        double mean = sum / (double)width;
+
+        double sq = 0.0;
+        for (long j = 0; j < width; ++j) {
+            double centered = ((double)xi[j] + (ri ? (double)ri[j] : 0.0)) - mean;
+            sq += centered * centered;
+        }
+        double variance = sq / (double)width;
+
+        double denom = sqrt(variance + eps);
+        for (long j = 0; j < width; ++j) {
+            double normed = (((double)xi[j] + (ri ? (double)ri[j] : 0.0)) - mean) / denom;
+            yi[j] = normed * (double)gamma[j] + (beta ? (double)beta[j] : 0.0);
+        }
+    }
+}
+
+/* y = x / sqrt(mean(x^2) + eps) * gamma. */
+void oracle_rmsnorm_weighted(const float *x, const float *gamma, double *y, long rows,
+                             long width, double eps)
+{
+    for (long i = 0; i < rows; ++i) {
+        const float *xi = x + i * width;
+        double *yi = y + i * width;
+
+        double sq = 0.0;
+        for (long j = 0; j < width; ++j)
+            sq += (double)xi[j] * (double)xi[j];
+        double mean_square = sq / (double)width;
+
+        double denom = sqrt(mean_square + eps);
+        for (long j = 0; j < width; ++j)
+            yi[j] = (double)xi[j] / denom * (double)gamma[j];
+    }
+}
+
+/* s[i] = sum_j x[i][j]. */
+void oracle_row_sum(const float *x, double *s, long rows, long width)
+{
+    for (long i = 0; i < rows; ++i) {
+        const float *xi = x + i * width;
+        double sum = 0.0;
+        for (long j = 0; j < width; ++j)
+            sum += (double)xi[j];
+        s[i] = sum;
+    }
+}
+
+/* mn[i] = min_j x[i][j], mx[i] = max_j x[i][j]. */
+void oracle_row_minmax(const float *x, double *mn, double *mx, long rows, long width)
+{
+    for (long i = 0; i < rows; ++i) {
+        const float *xi = x + i * width;
+        double lo = (double)xi[0], hi = (double)xi[0];
+        for (long j = 1; j < width; ++j) {
+            if ((double)xi[j] < lo)
+                lo = (double)xi[j];
+            if ((double)xi[j] > hi)
+                hi = (double)xi[j];
+        }
+        mn[i] = lo;
+        mx[i] = hi;
+    }
+}
+
+/* y = sigmoid(x), dy = sigmoid'(x), elementwise over n values. */
+void oracle_sigmoid_pair(const float *x, double *y, double *dy, long n)
+{
+    for (long k = 0; k < n; ++k) {
+        double s = 1.0 / (1.0 + exp(-(double)x[k]));
+        y[k] = s;
+        dy[k] = s * (1.0 - s);
+    }
+}
+
+/* y = tanh-approximate GELU(x), dy = its derivative, elementwise. */
+void oracle_gelu_tanh_pair(const float *x, double *y, double *dy, long n)
+{
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    const double a = 0.044715;
+    for (long k = 0; k < n; ++k) {
+        double v = (double)x[k];
+        double u = c * (v + a * v * v * v);
+        double t = tanh(u);
+        y[k] = 0.5 * v * (1.0 + t);
+        dy[k] = 0.5 * (1.0 + t) + 0.5 * v * (1.0 - t * t) * c * (1.0 + 3.0 * a * v * v);
+    }
+}

@@ -38,7 +38,8 @@ getcontext().prec = 50
 # ---------------------------------------------------------------------------
 
 def load_golden(path):
-    case = {"x": [], "r": [], "numer": [], "den": [], "expect": [], "atol": 0.0}
+    case = {"x": [], "r": [], "numer": [], "den": [], "expect": [], "atol": 0.0,
+            "min": [], "max": [], "y": [], "dy": []}
     with open(path) as fh:
         for line in fh:
             line = line.split("#", 1)[0].strip()
@@ -53,8 +54,10 @@ def load_golden(path):
                 case["atol"] = float(val)
             elif key in ("x", "r"):
                 case[key].append([float(v) for v in val.split()])
-            elif key in ("numer", "expect"):
+            elif key in ("numer", "expect", "min", "max", "y", "dy"):
                 case[key].append([Fraction(v) for v in val.split()])
+            elif key in ("gamma", "beta"):
+                case[key] = [float(v) for v in val.split()]
             elif key == "den":
                 case[key].append(Fraction(val))
             else:
@@ -62,16 +65,36 @@ def load_golden(path):
     return case
 
 
+def _dec(f):
+    return Decimal(f.numerator) / Decimal(f.denominator)
+
+
+def _exact(rows):
+    return np.array([[float(_dec(f)) for f in row] for row in rows])
+
+
 def golden_expected(case):
     """Expected outputs of a golden case, evaluated to 50 digits."""
-    if case["op"] == "softmax":
-        return np.array([[float(Decimal(f.numerator) / Decimal(f.denominator)) for f in row]
-                         for row in case["expect"]])
+    op = case["op"]
+    if op in ("softmax", "row_sum"):
+        return _exact(case["expect"])
+    if op == "row_minmax":
+        return _exact(case["min"]), _exact(case["max"])
+    if op in ("sigmoid_pair", "gelu_tanh_pair"):
+        return _exact(case["y"]), _exact(case["dy"])
     eps = Decimal(case["eps"])
+    gamma = case.get("gamma")
+    beta = case.get("beta")
     out = []
     for numer, den in zip(case["numer"], case["den"]):
-        root = (Decimal(den.numerator) / Decimal(den.denominator) + eps).sqrt()
-        out.append([float(Decimal(f.numerator) / Decimal(f.denominator) / root) for f in numer])
+        root = (_dec(den) + eps).sqrt()
+        row = []
+        for j, f in enumerate(numer):
+            v = _dec(f) / root
+            if gamma is not None:
+                v = v * Decimal(repr(gamma[j])) + (Decimal(repr(beta[j])) if beta else 0)
+            row.append(float(v))
+        out.append(row)
     return np.array(out)
 
 
@@ -86,14 +109,30 @@ def _run_golden(orc, path):
         return None
     x = np.array(case["x"], dtype=np.float32)
     eps = float(case.get("eps", "1e-5"))
-    if case["op"] == "residual_layernorm":
-        y = orc.residual_layernorm(x, np.array(case["r"], dtype=np.float32), eps)
+    op = case["op"]
+    if op == "residual_layernorm":
+        got = orc.residual_layernorm(x, np.array(case["r"], dtype=np.float32), eps)
+    elif op == "layernorm_affine":
+        got = orc.layernorm_affine(x, case["gamma"], case.get("beta"), eps=eps)
+    elif op == "rmsnorm_weighted":
+        got = orc.rmsnorm_weighted(x, case["gamma"], eps=eps)
+    elif op == "row_sum":
+        got = orc.row_sum(x)[None, :]
+    elif op == "row_minmax":
+        mn, mx = orc.row_minmax(x)
+        got = (mn[None, :], mx[None, :])
+    elif op == "sigmoid_pair":
+        got = tuple(a.reshape(1, -1) for a in orc.sigmoid_pair(x.reshape(-1)))
+    elif op == "gelu_tanh_pair":
+        got = tuple(a.reshape(1, -1) for a in orc.gelu_tanh_pair(x.reshape(-1)))
     else:
-        y = orc.run(case["op"], x, eps=eps)
+        got = orc.run(op, x, eps=eps)
     want = golden_expected(case)
-    tol = 1e-12 + case["atol"] + 1e-12 * np.abs(want)
-    if y.shape != want.shape or not np.all(np.abs(y - want) <= tol):
-        return f"golden {os.path.basename(path)}: got {y.tolist()} want {want.tolist()}"
+    pairs = zip(got, want) if isinstance(want, tuple) else [(got, want)]
+    for g, w in pairs:
+        tol = 1e-12 + case["atol"] + 1e-12 * np.abs(w)
+        if g.shape != w.shape or not np.all(np.abs(g - w) <= tol):
+            return f"golden {os.path.basename(path)}: got {np.asarray(got).tolist()} want {w.tolist()}"
     return None
 
 
@@ -235,13 +274,106 @@ def _pins_torch(orc):
     return fails
 
 
+def _pins_affine(orc):
+    import torch
+    import torch.nn.functional as F
+    fails = []
+    eps = 1e-5
+    x = _seeded(6, 1537, 61)
+    r = _seeded(6, 1537, 62)
+    g = synth.uniform_pm1(63, 1537) * np.float32(2.0)
+    b = synth.uniform_pm1(64, 1537)
+    ones = np.ones(1537, np.float32)
+    if not np.array_equal(orc.layernorm_affine(x, ones, None, eps=eps), orc.layernorm(x, eps)):
+        fails.append("layernorm_affine(gamma=1, no beta) != layernorm")
+    if not np.array_equal(orc.layernorm_affine(x, ones, np.zeros_like(ones), r=r, eps=eps),
+                          orc.residual_layernorm(x, r, eps)):
+        fails.append("layernorm_affine(gamma=1, beta=0, r) != residual_layernorm")
+    two = np.full(1537, 2.0, np.float32)
+    if not _close(orc.layernorm_affine(x, two, ones * np.float32(0.25), eps=eps),
+                  2 * orc.layernorm(x, eps) + 0.25, 1e-14):
+        fails.append("layernorm_affine(gamma=2, beta=1/4) != 2 LN + 1/4")
+    c = torch.from_numpy(x).double() + torch.from_numpy(r).double()
+    want = F.layer_norm(c, (1537,), weight=torch.from_numpy(g).double(),
+                        bias=torch.from_numpy(b).double(), eps=eps).numpy()
+    if not _close(orc.layernorm_affine(x, g, b, r=r, eps=eps), want, 1e-12):
+        fails.append("layernorm_affine differs from torch FP64 layer_norm(weight, bias)")
+    want = F.rms_norm(torch.from_numpy(x).double(), (1537,), weight=torch.from_numpy(g).double(),
+                      eps=eps).numpy()
+    if not _close(orc.rmsnorm_weighted(x, g, eps), want, 1e-12):
+        fails.append("rmsnorm_weighted differs from torch FP64 rms_norm(weight)")
+    if not np.array_equal(orc.rmsnorm_weighted(x, ones, eps), orc.rmsnorm(x, eps)):
+        fails.append("rmsnorm_weighted(gamma=1) != rmsnorm")
+    return fails
+
+
+def _pins_reductions(orc):
+    import math
+    fails = []
+    # integer-valued rows: the FP64 sum is exact, compare with Python integers
+    ints = (np.arange(5 * 999, dtype=np.int64) % 97 - 48).reshape(5, 999)
+    if not np.array_equal(orc.row_sum(ints.astype(np.float32)), ints.sum(axis=1).astype(np.float64)):
+        fails.append("row_sum: integer rows not exact")
+    x = _seeded(7, 4096, 71)
+    fs = np.array([math.fsum(row.astype(np.float64)) for row in x])
+    if not _close(orc.row_sum(x), fs, 1e-10):
+        fails.append("row_sum: differs from math.fsum")
+    if not _close(orc.row_sum(x[:, ::-1]), orc.row_sum(x), 1e-10):
+        fails.append("row_sum: not permutation invariant")
+    mn, mx = orc.row_minmax(x)
+    if not (np.array_equal(mn, x.min(axis=1).astype(np.float64))
+            and np.array_equal(mx, x.max(axis=1).astype(np.float64))):
+        fails.append("row_minmax: differs from numpy min/max")
+    mn2, mx2 = orc.row_minmax(-x)
+    if not (np.array_equal(mn2, -mx) and np.array_equal(mx2, -mn)):
+        fails.append("row_minmax: min(-x) != -max(x)")
+    return fails
+
+
+def _pins_pairs(orc):
+    import torch
+    import torch.nn.functional as F
+    fails = []
+    x = synth.normal(81, 20000, 4.0)
+    y, dy = orc.sigmoid_pair(x)
+    yn, _ = orc.sigmoid_pair(-x)
+    if not _close(y + yn, np.ones_like(y), 1e-15):
+        fails.append("sigmoid: s(x) + s(-x) != 1")
+    tx = torch.from_numpy(x).double().requires_grad_(True)
+    ts = torch.sigmoid(tx)
+    ts.sum().backward()
+    if not (_close(y, ts.detach().numpy(), 1e-15) and _close(dy, tx.grad.numpy(), 1e-15)):
+        fails.append("sigmoid pair differs from torch FP64 sigmoid / autograd")
+    g, dg = orc.gelu_tanh_pair(x)
+    gn, _ = orc.gelu_tanh_pair(-x)
+    if not _close(g - gn, x.astype(np.float64), 1e-12):
+        fails.append("gelu: g(x) - g(-x) != x")
+    tx = torch.from_numpy(x).double().requires_grad_(True)
+    tg = F.gelu(tx, approximate="tanh")
+    tg.sum().backward()
+    if not (_close(g, tg.detach().numpy(), 1e-12) and _close(dg, tx.grad.numpy(), 1e-12)):
+        fails.append("gelu pair differs from torch FP64 gelu(tanh) / autograd")
+    # derivatives against central differences of the value (h = 2^-12)
+    xs = np.linspace(-6, 6, 241).astype(np.float32)
+    h = 2.0 ** -12
+    for name, fn in (("sigmoid", orc.sigmoid_pair), ("gelu", orc.gelu_tanh_pair)):
+        _, d = fn(xs)
+        up, _ = fn((xs.astype(np.float64) + h).astype(np.float32))
+        dn, _ = fn((xs.astype(np.float64) - h).astype(np.float32))
+        fd = (up - dn) / (2 * h)
+        if not _close(d, fd, 1e-6):
+            fails.append(f"{name}: derivative differs from central differences")
+    return fails
+
+
 def check_all(orc):
     fails = []
     for path in golden_cases():
         f = _run_golden(orc, path)
         if f:
             fails.append(f)
-    for group in (_pins_layernorm, _pins_residual, _pins_rmsnorm, _pins_softmax, _pins_torch):
+    for group in (_pins_layernorm, _pins_residual, _pins_rmsnorm, _pins_softmax, _pins_torch,
+                  _pins_affine, _pins_reductions, _pins_pairs):
         try:
             fails.extend(group(orc))
         except Exception as exc:  # a mutant may produce NaN shapes etc.

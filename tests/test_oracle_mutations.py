@@ -34,6 +34,25 @@ MUTATIONS = [
      "total += exp((double)xi[j]);", 0),
     ("softmax-wrong-index", "yi[j] = exp((double)xi[j] - m) / total;",
      "yi[j] = exp((double)xi[0] - m) / total;", 0),
+    ("affine-beta-dropped", "yi[j] = normed * (double)gamma[j] + (beta ? (double)beta[j] : 0.0);",
+     "yi[j] = normed * (double)gamma[j];", 0),
+    ("affine-gamma-beta-swapped",
+     "yi[j] = normed * (double)gamma[j] + (beta ? (double)beta[j] : 0.0);",
+     "yi[j] = normed * (beta ? (double)beta[j] : 1.0) + (double)gamma[j];", 0),
+    ("affine-residual-dropped-from-variance",
+     "double centered = ((double)xi[j] + (ri ? (double)ri[j] : 0.0)) - mean;",
+     "double centered = (double)xi[j] - mean;", 0),
+    ("weighted-rms-gamma-index", "yi[j] = (double)xi[j] / denom * (double)gamma[j];",
+     "yi[j] = (double)xi[j] / denom * (double)gamma[0];", 0),
+    ("row-sum-float-accumulator", "        double sum = 0.0;\n        for (long j = 0; j < width; ++j)\n            sum += (double)xi[j];\n        s[i] = sum;",
+     "        float sum = 0.0f;\n        for (long j = 0; j < width; ++j)\n            sum += xi[j];\n        s[i] = sum;", 0),
+    ("row-sum-skips-last", "        for (long j = 0; j < width; ++j)\n            sum += (double)xi[j];\n        s[i] = sum;",
+     "        for (long j = 0; j + 1 < width; ++j)\n            sum += (double)xi[j];\n        s[i] = sum;", 0),
+    ("minmax-swapped", "        mn[i] = lo;\n        mx[i] = hi;", "        mn[i] = hi;\n        mx[i] = lo;", 0),
+    ("sigmoid-derivative-sign", "dy[k] = s * (1.0 - s);", "dy[k] = s * (1.0 + s);", 0),
+    ("gelu-cubic-coefficient", "const double a = 0.044715;", "const double a = 0.04715;", 0),
+    ("gelu-derivative-missing-3", "(1.0 + 3.0 * a * v * v)", "(1.0 + a * v * v)", 0),
+    ("gelu-derivative-tanh-square", "(1.0 - t * t)", "(1.0 - t)", 0),
 ]
 
 
