@@ -63,11 +63,15 @@ extern "C" {
 #define TILE_ERR_DEVICE      -9  /* a kernel recorded an error on the device  */
 #define TILE_ERR_WORKSPACE  -10  /* device workspace too small for one row    */
 
-/* ---- operation codes (tile_describe_plan, tile_run_plan_f32) ----------- */
+/* ---- operation codes (tile_describe_plan, tile_run_plan_*) ------------- */
 #define TILE_OP_RESIDUAL_LAYERNORM 0
 #define TILE_OP_LAYERNORM          1
 #define TILE_OP_RMSNORM            2
 #define TILE_OP_SOFTMAX            3
+#define TILE_OP_ROW_SUM            4
+#define TILE_OP_ROW_MINMAX         5
+#define TILE_OP_LAYERNORM_AFFINE   6
+#define TILE_OP_RMSNORM_WEIGHTED   7
 
 /* ---- launch paths ------------------------------------------------------ */
 #define TILE_PATH_CTA      0  /* P programs x S warps per CTA, one row each  */
@@ -123,6 +127,66 @@ int tile_rmsnorm_f32(const float *in, float *out, int rows, int width, float eps
  * `eps` is accepted for a uniform signature and ignored. */
 int tile_softmax_f32(const float *in, float *out, int rows, int width, float eps,
                      cudaStream_t stream);
+
+/* ---- more row operations ---------------------------------------------- */
+
+/* Affine LayerNorm: y = LayerNorm(in [+ residual]) * gamma + beta.  The
+ * pages list affine LayerNorm (tolerance atol 1e-5) in "Cooperating-program
+ * packing", "Predeclared comparison and measurement"; the formula is the
+ * LayerNorm above followed by the per-column scale and shift.  residual and
+ * beta may be NULL; gamma, beta: [width] FP32 device vectors (read through
+ * the read-only cache; any 4-byte alignment).  Same contract otherwise. */
+int tile_layernorm_affine_f32(const float *in, const float *residual, const float *gamma,
+                              const float *beta, float *out, int rows, int width, float eps,
+                              cudaStream_t stream);
+
+/* Weighted RMSNorm: y = in / sqrt(mean(in^2) + eps) * gamma, gamma [width]. */
+int tile_rmsnorm_weighted_f32(const float *in, const float *gamma, float *out, int rows,
+                              int width, float eps, cudaStream_t stream);
+
+/* Row sums: sums[i] = sum_j in[i][j], sums: [rows] FP32 on the device.  The
+ * "sum" operator of "Cooperating-program packing", "Validation".  Each
+ * thread and every reduction level keeps a compensated (TwoSum) pair, so the
+ * result is close to the correctly rounded sum even when terms cancel. */
+int tile_row_sum_f32(const float *in, float *sums, int rows, int width, cudaStream_t stream);
+
+/* Paired row min/max in one pass: mins[i] = min_j in[i][j], maxs[i] =
+ * max_j in[i][j] (exact).  The "paired min/max" operator of
+ * "Cooperating-program packing", "Validation".  Inputs must not be NaN. */
+int tile_row_minmax_f32(const float *in, float *mins, float *maxs, int rows, int width,
+                        cudaStream_t stream);
+
+/* Operands of a row operation for tile_run_plan_args_f32.  Unused pointers
+ * are ignored (set them NULL). */
+typedef struct tile_row_args {
+    const float *in;        /* [rows][width]                                    */
+    const float *residual;  /* residual LayerNorm; optional for affine LN       */
+    const float *gamma;     /* affine LN / weighted RMSNorm: [width]            */
+    const float *beta;      /* affine LN: [width] or NULL                       */
+    float *out;             /* [rows][width], or [rows] sums / minima           */
+    float *out2;            /* [rows] maxima (TILE_OP_ROW_MINMAX)               */
+    int rows, width;
+    float eps;              /* normalisers only                                  */
+} tile_row_args_t;
+
+/* Any row operation with the built plan `plan_id` forced (plan sweeps,
+ * per-plan tests).  Errors as tile_run_plan_f32. */
+int tile_run_plan_args_f32(int op, int plan_id, const tile_row_args_t *args, cudaStream_t stream);
+
+/* ---- pointwise value/derivative pairs ---------------------------------- */
+
+/* value[k] = sigmoid(in[k]) and derivative[k] = sigmoid'(in[k]) for k < n,
+ * one read and two writes per element in one kernel ("Multi-output
+ * pointwise fusion: evidence and limits", "Measurement definitions and
+ * population").  Device buffers of n floats, 4-byte aligned; the outputs
+ * must not overlap the input or each other.  n == 0 is a no-op. */
+int tile_sigmoid_pair_f32(const float *in, float *value, float *derivative, long long n,
+                          cudaStream_t stream);
+
+/* The same for tanh-approximate GELU, g(x) = x/2 (1 + tanh(sqrt(2/pi)
+ * (x + 0.044715 x^3))), and its derivative. */
+int tile_gelu_tanh_pair_f32(const float *in, float *value, float *derivative, long long n,
+                            cudaStream_t stream);
 
 /* ---- end to end on host buffers ---------------------------------------- */
 
@@ -203,8 +267,9 @@ int tile_describe_plan(int op, int rows, int width, tile_plan_t *plan);
 int tile_plan_count(void);
 int tile_plan_info(int id, int op, int rows, int width, tile_plan_t *plan);
 
-/* Run `op` with the built plan `plan_id` instead of the selector's choice
- * (used by the measured plan sweep and by tests that check every plan).
+/* Run `op` (one of the first four op codes) with the built plan `plan_id`
+ * instead of the selector's choice (used by the measured plan sweep and by
+ * tests that check every plan; tile_run_plan_args_f32 covers every op).
  * Same contract as the compute entry points; `residual` is used only by
  * TILE_OP_RESIDUAL_LAYERNORM.  Returns TILE_ERR_PLAN if the plan does not
  * exist, cannot cover `width`, or needs 16-byte co-alignment (V = 4) that

@@ -1,6 +1,9 @@
 """Host-only checks of the C ABI: the library loads, exports every function
 declared in include/*.h, and rejects bad arguments before any CUDA call.
-Nothing here launches a kernel, so it runs without a GPU."""
+
+The argument tests pass fake device addresses that every call must reject
+before launching anything.  As a second guard they run only where no GPU is
+visible, so a mistake in a test can never launch a kernel on fake pointers."""
 
 import ctypes
 import glob
@@ -62,10 +65,22 @@ A = 0x10000000      # fake, never dereferenced: every call below fails validatio
 B = 0x20000000
 
 
+def _no_gpu():
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except Exception:
+        return True
+
+
+fake_pointers = pytest.mark.skipif(not _no_gpu(), reason="fake device pointers: CPU-only test")
+
+
 def _resln(lib, x, r, y, rows, width, eps=1e-5):
     return lib.tile_residual_layernorm_f32(x, r, y, rows, width, eps, None)
 
 
+@fake_pointers
 def test_shape_errors(lib):
     assert _resln(lib, A, A, B, -1, 8) == SHAPE
     assert _resln(lib, A, A, B, 4, 0) == SHAPE
@@ -73,11 +88,13 @@ def test_shape_errors(lib):
     assert lib.tile_softmax_f32(A, B, 1, -3, 0.0, None) == SHAPE
 
 
+@fake_pointers
 def test_rows_zero_is_a_noop(lib):
     assert _resln(lib, None, None, None, 0, 8) == OK
     assert lib.tile_softmax_f32(None, None, 0, 8, 0.0, None) == OK
 
 
+@fake_pointers
 def test_null_pointers(lib):
     assert _resln(lib, None, A, B, 2, 8) == NULL
     assert _resln(lib, A, None, B, 2, 8) == NULL
@@ -85,17 +102,20 @@ def test_null_pointers(lib):
     assert lib.tile_layernorm_f32(None, B, 2, 8, 1e-5, None) == NULL
 
 
+@fake_pointers
 def test_eps_checked_for_normalisers_only(lib):
     assert lib.tile_rmsnorm_f32(A, B, 2, 8, -1.0, None) == EPS
     assert lib.tile_layernorm_f32(A, B, 2, 8, float("nan"), None) == EPS
     assert _resln(lib, A, A, B, 2, 8, float("inf")) == EPS
 
 
+@fake_pointers
 def test_alignment(lib):
     assert lib.tile_rmsnorm_f32(A + 2, B, 2, 8, 1e-5, None) == ALIGN
     assert lib.tile_rmsnorm_f32(A, B + 1, 2, 8, 1e-5, None) == ALIGN
 
 
+@fake_pointers
 def test_alias(lib):
     # out overlaps in: [A, A+64) vs [A+32, A+96)
     assert lib.tile_layernorm_f32(A, A + 32, 2, 8, 1e-5, None) == ALIAS
@@ -103,6 +123,7 @@ def test_alias(lib):
     assert lib.tile_softmax_f32(A, A, 1, 1, 0.0, None) == ALIAS
 
 
+@fake_pointers
 def test_run_plan_rejects_bad_plans(lib):
     n = lib.tile_plan_count()
     assert lib.tile_run_plan_f32(0, -1, A, A, B, 2, 8, 1e-5, None) == PLAN
@@ -145,7 +166,7 @@ def test_plan_info_table(lib):
 
 def test_describe_plan_errors(lib):
     plan = tile.TilePlan()
-    assert lib.tile_describe_plan(7, 4, 8, ctypes.byref(plan)) == OP
+    assert lib.tile_describe_plan(8, 4, 8, ctypes.byref(plan)) == OP
     assert lib.tile_describe_plan(0, 4, 0, ctypes.byref(plan)) == SHAPE
     assert lib.tile_describe_plan(0, 4, 8, None) == NULL
 
@@ -157,6 +178,7 @@ def test_binding_rejects_cpu_tensors():
         tile.tile_rmsnorm_f32(x, torch.zeros(2, 8))
 
 
+@fake_pointers
 def test_host_entry_rejects_bad_arguments(lib):
     ws = 1 << 20
     W = 0x30000000                       # fake device workspace, 256-aligned
@@ -178,3 +200,54 @@ def test_host_workspace_bytes(lib):
     assert tile.tile_host_workspace_bytes("residual_layernorm", 100, 3) == 2 * 3 * 1280
     assert tile.tile_host_workspace_bytes("softmax", 0, 3) == 0
     assert tile.tile_host_workspace_bytes(9, 10, 3) == 0
+
+
+@fake_pointers
+def test_new_row_ops_reject_bad_arguments(lib):
+    f = lib.tile_layernorm_affine_f32
+    assert f(A, None, None, None, B, 2, 8, 1e-5, None) == NULL            # gamma required
+    assert f(A, None, A + 64, None, B, 2, 8, -1.0, None) == EPS
+    assert f(A, None, B + 8, None, B, 2, 8, 1e-5, None) == ALIAS          # out overlaps gamma
+    assert f(A, None, A + 64, B + 40, B, 2, 8, 1e-5, None) == ALIAS       # out overlaps beta
+    assert f(A, None, A + 66, None, B, 2, 8, 1e-5, None) == ALIGN
+    assert f(A, None, None, None, B, 0, 8, 1e-5, None) == OK              # rows == 0
+    g = lib.tile_rmsnorm_weighted_f32
+    assert g(A, None, B, 2, 8, 1e-5, None) == NULL
+    assert g(A, A + 64, B, 2, 8, float("nan"), None) == EPS
+    s = lib.tile_row_sum_f32
+    assert s(A, None, 2, 8, None) == NULL
+    assert s(A, A + 4, 2, 8, None) == ALIAS                               # sums inside x
+    assert s(A, B, 2, 0, None) == SHAPE
+    m = lib.tile_row_minmax_f32
+    assert m(A, B, None, 2, 8, None) == NULL
+    assert m(A, B, B + 4, 2, 8, None) == ALIAS                            # mins/maxs overlap
+    assert m(A, B, A + 8, 2, 8, None) == ALIAS                            # maxs inside x
+    assert m(A, B, B + 4096, 0, 8, None) == OK
+
+
+@fake_pointers
+def test_run_plan_args(lib):
+    a = tile.TileRowArgs()
+    a.in_, a.out, a.rows, a.width, a.eps = A, B, 2, 8, 1e-5
+    assert lib.tile_run_plan_args_f32(4, 10**6, ctypes.byref(a), None) == PLAN
+    assert lib.tile_run_plan_args_f32(42, 0, ctypes.byref(a), None) == OP
+    assert lib.tile_run_plan_args_f32(0, 0, None, None) == NULL
+    assert lib.tile_run_plan_args_f32(0, 0, ctypes.byref(a), None) == NULL  # residual missing
+
+
+@fake_pointers
+def test_pair_entry_points_reject_bad_arguments(lib):
+    for f in (lib.tile_sigmoid_pair_f32, lib.tile_gelu_tanh_pair_f32):
+        assert f(A, B, B + 4096, 0, None) == OK
+        assert f(A, B, B + 4096, -1, None) == SHAPE
+        assert f(None, B, B + 4096, 8, None) == NULL
+        assert f(A, A + 4, B, 8, None) == ALIAS
+        assert f(A, B, B + 16, 8, None) == ALIAS
+        assert f(A, B + 2, B + 4096, 8, None) == ALIGN
+
+
+def test_describe_plan_covers_the_new_ops(lib):
+    for op in ("row_sum", "row_minmax", "layernorm_affine", "rmsnorm_weighted"):
+        for w in (1, 127, 4096, 65536, 131072):
+            p = tile.tile_describe_plan(op, 3, w)
+            assert p["max_width"] >= w

@@ -24,12 +24,15 @@ __all__ = [
     "tile_softmax_f32", "tile_run_plan_f32", "tile_describe_plan", "tile_plan_info",
     "tile_plan_count", "tile_max_width", "tile_status_string",
     "tile_check_device_status", "tile_last_cuda_error", "tile_run_host_f32",
-    "tile_host_workspace_bytes", "tile_run_host_static_f32",
+    "tile_host_workspace_bytes", "tile_run_host_static_f32", "tile_layernorm_affine_f32",
+    "tile_rmsnorm_weighted_f32", "tile_row_sum_f32", "tile_row_minmax_f32",
+    "tile_run_plan_args_f32", "tile_sigmoid_pair_f32", "tile_gelu_tanh_pair_f32",
     "residual_layernorm", "layernorm", "rmsnorm", "softmax", "run",
 ]
 
 #: Library operation codes, by name.
-OPS = {"residual_layernorm": 0, "layernorm": 1, "rmsnorm": 2, "softmax": 3}
+OPS = {"residual_layernorm": 0, "layernorm": 1, "rmsnorm": 2, "softmax": 3, "row_sum": 4,
+       "row_minmax": 5, "layernorm_affine": 6, "rmsnorm_weighted": 7}
 
 TILE_OK = 0
 
@@ -58,6 +61,14 @@ class TilePlan(ctypes.Structure):
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class TileRowArgs(ctypes.Structure):
+    _fields_ = [
+        ("in_", ctypes.c_void_p), ("residual", ctypes.c_void_p), ("gamma", ctypes.c_void_p),
+        ("beta", ctypes.c_void_p), ("out", ctypes.c_void_p), ("out2", ctypes.c_void_p),
+        ("rows", ctypes.c_int), ("width", ctypes.c_int), ("eps", ctypes.c_float),
+    ]
 
 
 _lib = None
@@ -92,6 +103,13 @@ def load():
         "tile_last_cuda_error": [],
         "tile_run_host_f32": [I, P, P, P, I, I, F, P, ctypes.c_size_t, P],
         "tile_run_host_static_f32": [I, P, P, P, I, I, F, P],
+        "tile_layernorm_affine_f32": [P, P, P, P, P, I, I, F, P],
+        "tile_rmsnorm_weighted_f32": [P, P, P, I, I, F, P],
+        "tile_row_sum_f32": [P, P, I, I, P],
+        "tile_row_minmax_f32": [P, P, P, I, I, P],
+        "tile_run_plan_args_f32": [I, I, ctypes.POINTER(TileRowArgs), P],
+        "tile_sigmoid_pair_f32": [P, P, P, ctypes.c_longlong, P],
+        "tile_gelu_tanh_pair_f32": [P, P, P, ctypes.c_longlong, P],
     }
     for name, argtypes in sigs.items():
         fn = getattr(lib, name)
@@ -186,6 +204,99 @@ def tile_run_plan_f32(op, plan_id, x, residual, out, eps=1e-5, stream=None):
         _same_shape(x, residual, "x/residual")
     _check(load().tile_run_plan_f32(op, plan_id, px, pr, po, rows, width, eps, _stream(stream)),
            "tile_run_plan_f32")
+
+
+def _vector(t, n, name):
+    """Pointer of a CUDA FP32 contiguous tensor of n elements (None -> NULL)."""
+    import torch
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32:
+        raise ValueError(f"{name} must be a CUDA float32 tensor")
+    if not t.is_contiguous() or t.numel() != n:
+        raise ValueError(f"{name} must be contiguous with {n} elements")
+    return t.data_ptr()
+
+
+def tile_layernorm_affine_f32(x, residual, gamma, beta, out, eps=1e-5, stream=None):
+    """LayerNorm(x [+ residual]) * gamma + beta; residual and beta may be None."""
+    px, rows, width = _matrix(x, "x")
+    po, _, _ = _matrix(out, "out")
+    _same_shape(x, out, "x/out")
+    pr = None
+    if residual is not None:
+        pr, _, _ = _matrix(residual, "residual")
+        _same_shape(x, residual, "x/residual")
+    pg = _vector(gamma, width, "gamma")
+    pb = _vector(beta, width, "beta")
+    _check(load().tile_layernorm_affine_f32(px, pr, pg, pb, po, rows, width, eps, _stream(stream)),
+           "tile_layernorm_affine_f32")
+
+
+def tile_rmsnorm_weighted_f32(x, gamma, out, eps=1e-5, stream=None):
+    px, rows, width = _matrix(x, "x")
+    po, _, _ = _matrix(out, "out")
+    _same_shape(x, out, "x/out")
+    pg = _vector(gamma, width, "gamma")
+    _check(load().tile_rmsnorm_weighted_f32(px, pg, po, rows, width, eps, _stream(stream)),
+           "tile_rmsnorm_weighted_f32")
+
+
+def tile_row_sum_f32(x, sums, stream=None):
+    px, rows, width = _matrix(x, "x")
+    ps = _vector(sums, rows, "sums")
+    _check(load().tile_row_sum_f32(px, ps, rows, width, _stream(stream)), "tile_row_sum_f32")
+
+
+def tile_row_minmax_f32(x, mins, maxs, stream=None):
+    px, rows, width = _matrix(x, "x")
+    pmn = _vector(mins, rows, "mins")
+    pmx = _vector(maxs, rows, "maxs")
+    _check(load().tile_row_minmax_f32(px, pmn, pmx, rows, width, _stream(stream)),
+           "tile_row_minmax_f32")
+
+
+def tile_run_plan_args_f32(op, plan_id, x, out, residual=None, gamma=None, beta=None, out2=None,
+                           eps=1e-5, stream=None):
+    """Any row op with a forced plan (``out``: matrix, or [rows] for row_sum/row_minmax)."""
+    op = OPS[op] if isinstance(op, str) else op
+    px, rows, width = _matrix(x, "x")
+    a = TileRowArgs()
+    a.in_ = px
+    a.residual = _matrix(residual, "residual")[0] if residual is not None else None
+    a.gamma = _vector(gamma, width, "gamma")
+    a.beta = _vector(beta, width, "beta")
+    a.out = out.data_ptr()
+    a.out2 = out2.data_ptr() if out2 is not None else None
+    a.rows, a.width, a.eps = rows, width, eps
+    _check(load().tile_run_plan_args_f32(op, plan_id, ctypes.byref(a), _stream(stream)),
+           "tile_run_plan_args_f32")
+
+
+def _flat(t, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32:
+        raise ValueError(f"{name} must be a CUDA float32 tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr(), t.numel()
+
+
+def _pair_fn(name):
+    def fn(x, value, derivative, stream=None):
+        px, n = _flat(x, "x")
+        pv, nv = _flat(value, "value")
+        pd, nd = _flat(derivative, "derivative")
+        if nv != n or nd != n:
+            raise ValueError("value and derivative must have as many elements as x")
+        _check(getattr(load(), name)(px, pv, pd, n, _stream(stream)), name)
+    fn.__name__ = name
+    fn.__doc__ = f"Calls ``{name}`` (see include/tile_rows.h)."
+    return fn
+
+
+tile_sigmoid_pair_f32 = _pair_fn("tile_sigmoid_pair_f32")
+tile_gelu_tanh_pair_f32 = _pair_fn("tile_gelu_tanh_pair_f32")
 
 
 def _host_matrix(t, name):

@@ -5,15 +5,45 @@
 namespace tile {
 constexpr int kMaxDevices = 64;
 
-#define TILE_DECLARE_OP(name)                                                          \
-    cudaError_t launch_##name(int plan_id, const float *x, const float *r, float *y,   \
-                              long long rows, int width, float eps, cudaStream_t stream); \
+// Arguments of one row-kernel launch.  x, r: [rows][width] inputs (r:
+// residual LayerNorm only).  gamma, beta: optional per-column scale and
+// shift applied after LayerNorm / RMSNorm (NULL = none).  y: [rows][width]
+// output, or [rows] row sums / row minima; y2: [rows] row maxima (min/max).
+// status: the launching op's device error word (filled by the launcher).
+struct RowArgs {
+    const float *x;
+    const float *r;
+    const float *gamma;
+    const float *beta;
+    float *y;
+    float *y2;
+    long long rows;
+    int width;
+    float eps;
+    unsigned int *status;
+};
+
+#define TILE_DECLARE_OP(name)                                                            \
+    cudaError_t launch_##name(int plan_id, RowArgs args, cudaStream_t stream);          \
     cudaError_t status_##name(unsigned int *value, cudaStream_t stream);
 TILE_DECLARE_OP(residual_layernorm)
 TILE_DECLARE_OP(layernorm)
 TILE_DECLARE_OP(rmsnorm)
 TILE_DECLARE_OP(softmax)
+TILE_DECLARE_OP(row_sum)
+TILE_DECLARE_OP(row_minmax)
 #undef TILE_DECLARE_OP
+
+// Pointwise value/derivative pairs (pair_kernel.cu): kind 0 = sigmoid,
+// 1 = tanh-approximate GELU, over n elements.
+enum { PAIR_SIGMOID = 0, PAIR_GELU_TANH = 1 };
+cudaError_t launch_pairs(int kind, const float *x, float *y, float *dy, long long n,
+                         cudaStream_t stream);
+cudaError_t status_pairs(unsigned int *value, cudaStream_t stream);
+
+// Argument checks + launch of a pair kernel (the body of the pair entry points).
+int run_pairs(int kind, const float *in, float *value, float *derivative, long long n,
+              cudaStream_t stream);
 
 // Check arguments, pick a plan and launch `op` on device buffers (the body of
 // the four compute entry points).  Returns a TILE_* status.

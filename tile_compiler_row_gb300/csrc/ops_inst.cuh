@@ -35,11 +35,11 @@ unsigned int *status_address(cudaError_t *err) {
 }
 
 template <int V, int S, int P, int K, int C>
-cudaError_t launch_plan(const float *x, const float *r, float *y, long long rows, int width,
-                        float eps, cudaStream_t stream) {
+cudaError_t launch_plan(RowArgs args, cudaStream_t stream) {
     cudaError_t err = cudaSuccess;
-    unsigned int *status = status_address(&err);
-    if (status == nullptr) return err;
+    args.status = status_address(&err);
+    if (args.status == nullptr) return err;
+    const long long rows = args.rows;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned int>(((rows + P - 1) / P) * C), 1, 1);
     cfg.blockDim = dim3(32 * S * P, 1, 1);
@@ -54,17 +54,14 @@ cudaError_t launch_plan(const float *x, const float *r, float *y, long long rows
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, row_kernel<TILE_INST_OP, V, S, P, K, C>, x, r, y, rows,
-                              width, eps, status);
+    return cudaLaunchKernelEx(&cfg, row_kernel<TILE_INST_OP, V, S, P, K, C>, args);
 }
 }  // namespace
 
-cudaError_t TILE_CAT(launch_, TILE_INST_NAME)(int plan_id, const float *x, const float *r,
-                                              float *y, long long rows, int width, float eps,
-                                              cudaStream_t stream) {
+cudaError_t TILE_CAT(launch_, TILE_INST_NAME)(int plan_id, RowArgs args, cudaStream_t stream) {
     switch (plan_id) {
 #define TILE_CASE(id, V, S, P, K, C) \
-    case id: return launch_plan<V, S, P, K, C>(x, r, y, rows, width, eps, stream);
+    case id: return launch_plan<V, S, P, K, C>(args, stream);
         TILE_PLAN_LIST(TILE_CASE)
 #undef TILE_CASE
         default: return cudaErrorInvalidValue;

@@ -23,9 +23,11 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "launch.h"
+
 namespace tile {
 
-enum { OP_RESLN = 0, OP_LN = 1, OP_RMS = 2, OP_SOFTMAX = 3 };
+enum { OP_RESLN = 0, OP_LN = 1, OP_RMS = 2, OP_SOFTMAX = 3, OP_SUM = 4, OP_MINMAX = 5 };
 
 // Bits of the per-library device error word (read by tile_check_device_status).
 enum { STATUS_BAD_LAUNCH = 1u };
@@ -134,29 +136,86 @@ __device__ __forceinline__ void row_allreduce(float (&v)[N], float *part, float 
     }
 }
 
+// Compensated (error-free) sum of pairs: (s, c) holds s + c with s the FP32
+// sum and c the accumulated rounding errors.  Knuth's TwoSum gives the exact
+// error of one addition (The Art of Computer Programming, vol. 2, 4.2.2);
+// the combine is commutative in its result, so xor butterflies stay uniform.
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+__device__ __forceinline__ void comp_add(float &s, float &c, float v) {
+    float e;
+    two_sum(s, v, s, e);
+    c = __fadd_rn(c, e);
+}
+__device__ __forceinline__ void comp_merge(float &s, float &c, float s2, float c2) {
+    float e;
+    two_sum(s, s2, s, e);
+    c = __fadd_rn(__fadd_rn(c, c2), e);
+}
+
+template <int S, int P, int C>
+__device__ __forceinline__ void row_allreduce_comp(float &s, float &c, float *part, float *cpart,
+                                                   int program, int warp, int lane) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+        comp_merge(s, c, s2, c2);
+    }
+    if constexpr (S > 1) {
+        if (lane == 0) {
+            part[program * S + warp] = s;
+            part[P * S + program * S + warp] = c;
+        }
+        __syncthreads();
+        s = part[program * S];
+        c = part[P * S + program * S];
+#pragma unroll
+        for (int w = 1; w < S; ++w) comp_merge(s, c, part[program * S + w], part[P * S + program * S + w]);
+    }
+    if constexpr (C > 1) {
+        if (threadIdx.x == 0) {
+            cpart[0] = s;
+            cpart[1] = c;
+        }
+        cluster_arrive();
+        cluster_wait();
+        s = load_dsmem(&cpart[0], 0);
+        c = load_dsmem(&cpart[1], 0);
+#pragma unroll
+        for (int q = 1; q < C; ++q) comp_merge(s, c, load_dsmem(&cpart[0], q), load_dsmem(&cpart[1], q));
+    }
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
+
 template <int OP, int V, int S, int P, int K, int C>
-__global__ void __launch_bounds__(32 * S * P)
-    row_kernel(const float *__restrict__ x, const float *__restrict__ r, float *__restrict__ y,
-               long long rows, int width, float eps, unsigned int *status) {
+__global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
     static_assert(V == 1 || V == 4, "V is 1 or 4");
     static_assert(C == 1 || P == 1, "a cluster row has one program per CTA");
     static_assert(32 * S * P <= 1024, "at most 1024 threads per CTA");
     constexpr int W = 32 * S;
-    constexpr int NPH = (OP == OP_RMS) ? 1 : 2;   // reduction phases
-    constexpr float kFill = (OP == OP_SOFTMAX) ? -INFINITY : 0.0f;
+    // Empty stripe slots hold the identity of the first reduction: -inf for
+    // the softmax maximum, NaN for min/max (fmaxf ignores a NaN operand, for
+    // x and for -x alike), 0 for sums.
+    constexpr float kFill = (OP == OP_SOFTMAX) ? -INFINITY : (OP == OP_MINMAX) ? NAN : 0.0f;
+    constexpr bool kRowOutput = (OP == OP_SUM || OP == OP_MINMAX);
 
-    __shared__ float part1[S > 1 ? P * S : 1];
+    __shared__ float part1[S > 1 ? 2 * P * S : 1];
     __shared__ float part2[S > 1 ? 2 * P * S : 1];
     __shared__ float cpart[C > 1 ? 4 : 1];
 
     if (blockDim.x != 32 * S * P) {           // uniform over the grid
-        if (threadIdx.x == 0) atomicOr(status, STATUS_BAD_LAUNCH);
+        if (threadIdx.x == 0) atomicOr(a.status, STATUS_BAD_LAUNCH);
         return;
     }
 
+    const int width = a.width;
     const int tid = threadIdx.x;
     const int program = tid / W;
     const int worker = tid - program * W;
@@ -169,16 +228,16 @@ __global__ void __launch_bounds__(32 * S * P)
         group = cluster_index();
     }
     long long row = group * P + program;
-    const bool active = row < rows;
-    if (!active) row = rows - 1;                  // replay the last row
+    const bool active = row < a.rows;
+    if (!active) row = a.rows - 1;                // replay the last row
 
     const long long base = row * static_cast<long long>(width);
-    const float *xr = x + base;
-    const float *rr = (OP == OP_RESLN) ? r + base : nullptr;
-    float *yr = y + base;
+    const float *xr = a.x + base;
+    const float *rr = (OP == OP_RESLN) ? a.r + base : nullptr;
+    float *yr = kRowOutput ? nullptr : a.y + base;
 
     // Row geometry.  V = 4: h scalars up to the first 16-byte boundary, then
-    // nb float4s, then tl scalars.  All pointers share the 16-byte phase.
+    // nb float4s, then tl scalars.  All row pointers share the 16-byte phase.
     int h = 0, tl = 0, nb;
     if constexpr (V == 4) {
         const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(xr) >> 2) & 3);
@@ -198,16 +257,16 @@ __global__ void __launch_bounds__(32 * S * P)
         const int i = k * (C * W) + gw;
         if (i < nb) {
             if constexpr (V == 4) {
-                float4 a = load4(xr + h + 4 * i);
+                float4 t = load4(xr + h + 4 * i);
                 if constexpr (OP == OP_RESLN) {
                     const float4 b = load4(rr + h + 4 * i);
-                    a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+                    t.x += b.x; t.y += b.y; t.z += b.z; t.w += b.w;
                 }
-                v[k][0] = a.x; v[k][1] = a.y; v[k][2] = a.z; v[k][3] = a.w;
+                v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
             } else {
-                float a = load1(xr + i);
-                if constexpr (OP == OP_RESLN) a += load1(rr + i);
-                v[k][0] = a;
+                float t = load1(xr + i);
+                if constexpr (OP == OP_RESLN) t += load1(rr + i);
+                v[k][0] = t;
             }
         } else {
 #pragma unroll
@@ -232,6 +291,7 @@ __global__ void __launch_bounds__(32 * S * P)
     }
 
     const float n = static_cast<float>(width);
+    float row_out0 = 0.0f, row_out1 = 0.0f;       // per-row results (sum, min/max)
     if constexpr (OP == OP_RESLN || OP == OP_LN) {
         // ---- a2: mean estimate -------------------------------------------
         float s[1] = {hv + tv};
@@ -265,7 +325,7 @@ __global__ void __launch_bounds__(32 * S * P)
         // corrected two-pass: mean = mean0 + mu1, var = E[d^2] - mu1^2
         const float mu1 = q[0] / n;
         const float var = fmaxf(q[1] / n - mu1 * mu1, 0.0f);
-        const float rstd = 1.0f / sqrtf(var + eps);
+        const float rstd = 1.0f / sqrtf(var + a.eps);
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
@@ -280,14 +340,14 @@ __global__ void __launch_bounds__(32 * S * P)
 #pragma unroll
             for (int j = 0; j < V; ++j) s[0] = fmaf(v[k][j], v[k][j], s[0]);
         row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
-        const float rstd = 1.0f / sqrtf(s[0] / n + eps);
+        const float rstd = 1.0f / sqrtf(s[0] / n + a.eps);
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
             for (int j = 0; j < V; ++j) v[k][j] *= rstd;
         hv *= rstd;
         tv *= rstd;
-    } else {
+    } else if constexpr (OP == OP_SOFTMAX) {
         // ---- a2: row maximum (empty slots hold -inf) ---------------------
         float m[1] = {fmaxf(hv, tv)};
 #pragma unroll
@@ -317,28 +377,105 @@ __global__ void __launch_bounds__(32 * S * P)
             for (int j = 0; j < V; ++j) v[k][j] *= inv;
         hv *= inv;
         tv *= inv;
+    } else if constexpr (OP == OP_SUM) {
+        // ---- compensated row sum (empty slots hold 0) --------------------
+        float s = 0.0f, c = 0.0f;
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < V; ++j) comp_add(s, c, v[k][j]);
+        comp_add(s, c, hv);
+        comp_add(s, c, tv);
+        row_allreduce_comp<S, P, C>(s, c, part1, cpart, program, warp, lane);
+        row_out0 = __fadd_rn(s, c);
+    } else {
+        // ---- paired min/max: max(x) and max(-x) in one reduction ---------
+        float m[2] = {fmaxf(hv, tv), fmaxf(-hv, -tv)};
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                m[0] = fmaxf(m[0], v[k][j]);
+                m[1] = fmaxf(m[1], -v[k][j]);
+            }
+        row_allreduce<Max, 2, S, P, C>(m, part1, cpart, program, warp, lane);
+        row_out0 = -m[1];
+        row_out1 = m[0];
     }
-    (void)NPH;
+
+    // Optional per-column scale and shift (affine LayerNorm, weighted
+    // RMSNorm): y = y * gamma[col] + beta[col], loaded through the read-only
+    // cache (every row reuses them).  float4 loads when gamma/beta share the
+    // row's 16-byte phase, scalar loads otherwise.
+    if constexpr (OP == OP_RESLN || OP == OP_LN || OP == OP_RMS) {
+        if (a.gamma != nullptr) {
+            const float *g = a.gamma;
+            const float *b = a.beta;
+            bool gvec = false;
+            if constexpr (V == 4)
+                gvec = ((reinterpret_cast<uintptr_t>(g + h) & 15) == 0) &&
+                       (b == nullptr || (reinterpret_cast<uintptr_t>(b + h) & 15) == 0);
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int i = k * (C * W) + gw;
+                if (i < nb) {
+                    const int col = (V == 4) ? h + 4 * i : i;
+                    float gg[V], bb[V];
+                    bool loaded = false;
+                    if constexpr (V == 4) {
+                        if (gvec) {
+                            const float4 g4 = __ldg(reinterpret_cast<const float4 *>(g + col));
+                            gg[0] = g4.x; gg[1] = g4.y; gg[2] = g4.z; gg[3] = g4.w;
+                            float4 b4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                            if (b != nullptr) b4 = __ldg(reinterpret_cast<const float4 *>(b + col));
+                            bb[0] = b4.x; bb[1] = b4.y; bb[2] = b4.z; bb[3] = b4.w;
+                            loaded = true;
+                        }
+                    }
+                    if (!loaded) {
+#pragma unroll
+                        for (int j = 0; j < V; ++j) {
+                            gg[j] = __ldg(g + col + j);
+                            bb[j] = b != nullptr ? __ldg(b + col + j) : 0.0f;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < V; ++j) v[k][j] = fmaf(v[k][j], gg[j], bb[j]);
+                }
+            }
+            if constexpr (V == 4) {
+                if (has_h) hv = fmaf(hv, __ldg(g + worker), b != nullptr ? __ldg(b + worker) : 0.0f);
+                if (has_t) tv = fmaf(tv, __ldg(g + te), b != nullptr ? __ldg(b + te) : 0.0f);
+            }
+        }
+    }
 
     // Our cluster partials must stay readable until every CTA of the
     // cluster has read them: arrive now, wait after the stores.
     if constexpr (C > 1) cluster_arrive();
 
     // ---- a4: streaming stores, predicated for replayed programs ---------
-    if (active) {
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-            const int i = k * (C * W) + gw;
-            if (i < nb) {
-                if constexpr (V == 4)
-                    store4(yr + h + 4 * i, make_float4(v[k][0], v[k][1], v[k][2], v[k][3]));
-                else
-                    store1(yr + i, v[k][0]);
-            }
+    if constexpr (kRowOutput) {
+        if (active && worker == 0 && rank == 0) {
+            a.y[row] = row_out0;
+            if constexpr (OP == OP_MINMAX) a.y2[row] = row_out1;
         }
-        if constexpr (V == 4) {
-            if (has_h) store1(yr + worker, hv);
-            if (has_t) store1(yr + te, tv);
+    } else {
+        if (active) {
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int i = k * (C * W) + gw;
+                if (i < nb) {
+                    if constexpr (V == 4)
+                        store4(yr + h + 4 * i, make_float4(v[k][0], v[k][1], v[k][2], v[k][3]));
+                    else
+                        store1(yr + i, v[k][0]);
+                }
+            }
+            if constexpr (V == 4) {
+                if (has_h) store1(yr + worker, hv);
+                if (has_t) store1(yr + te, tv);
+            }
         }
     }
     if constexpr (C > 1) cluster_wait();

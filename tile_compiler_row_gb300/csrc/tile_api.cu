@@ -64,6 +64,15 @@ constexpr Bucket kVec4Softmax[] = {
     {131, 0}, {259, 1}, {515, 2}, {1027, 3}, {2051, 6}, {4099, 7},
     {8195, 10}, {16387, 31}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
 };
+// Row sum and min/max: one reduction phase like RMSNorm (until swept).
+constexpr Bucket kVec4RowSum[] = {
+    {131, 0}, {259, 2}, {515, 4}, {1027, 6}, {2051, 5}, {3075, 8}, {8195, 10},
+    {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
+};
+constexpr Bucket kVec4RowMinMax[] = {
+    {131, 0}, {259, 2}, {515, 4}, {1027, 6}, {2051, 5}, {3075, 8}, {8195, 10},
+    {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
+};
 constexpr Bucket kVec1[] = {
     {128, 25}, {1024, 26}, {4096, 27}, {16384, 28}, {TILE_MAX_WIDTH, 29},
 };
@@ -75,13 +84,18 @@ int pick(const Bucket (&table)[N], int width) {
     return -1;
 }
 
-int select_plan(int op, long long rows, int width, bool vec4) {
+int select_plan(int op, long long rows, int width, bool vec4, bool residual) {
     (void)rows;
     if (!vec4) return pick(kVec1, width);
     switch (op) {
         case TILE_OP_RESIDUAL_LAYERNORM: return pick(kVec4ResidualLN, width);
         case TILE_OP_LAYERNORM: return pick(kVec4LN, width);
-        case TILE_OP_RMSNORM: return pick(kVec4RMS, width);
+        case TILE_OP_LAYERNORM_AFFINE:
+            return residual ? pick(kVec4ResidualLN, width) : pick(kVec4LN, width);
+        case TILE_OP_RMSNORM:
+        case TILE_OP_RMSNORM_WEIGHTED: return pick(kVec4RMS, width);
+        case TILE_OP_ROW_SUM: return pick(kVec4RowSum, width);
+        case TILE_OP_ROW_MINMAX: return pick(kVec4RowMinMax, width);
         default: return pick(kVec4Softmax, width);
     }
 }
@@ -107,69 +121,145 @@ void fill_plan(const PlanDesc &p, int op, int rows, int width, tile_plan_t *out)
     out->max_width = max_width_of(p);
     const int part = p.S > 1 ? 3 * p.P * p.S : 0;
     out->smem_bytes = 4 * (part + (p.C > 1 ? 4 : 0));
-    const int phases = op == TILE_OP_RMSNORM ? 1 : 2;
+    const int phases = (op == TILE_OP_RESIDUAL_LAYERNORM || op == TILE_OP_LAYERNORM ||
+                        op == TILE_OP_LAYERNORM_AFFINE || op == TILE_OP_SOFTMAX) ? 2 : 1;
     out->barriers_per_row = (p.S > 1 ? phases : 0) + (p.C > 1 ? phases + 1 : 0);
     out->grid = rows > 0 ? grid_of(p, rows) : 0;
 }
 
-bool overlaps(const void *a, const void *b, size_t bytes) {
+bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes) {
+    if (a == nullptr || b == nullptr) return false;
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-    return x < y + bytes && y < x + bytes;
+    return x < y + bbytes && y < x + abytes;
 }
 
 bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; }
 
-bool coaligned16(const float *in, const float *res, const float *out, bool residual) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(in), c = reinterpret_cast<uintptr_t>(out);
-    if (((a ^ c) & 15u) != 0) return false;
-    if (residual && ((a ^ reinterpret_cast<uintptr_t>(res)) & 15u) != 0) return false;
+bool valid_op(int op) { return op >= TILE_OP_RESIDUAL_LAYERNORM && op <= TILE_OP_RMSNORM_WEIGHTED; }
+
+bool is_normaliser(int op) {
+    return op == TILE_OP_RESIDUAL_LAYERNORM || op == TILE_OP_LAYERNORM || op == TILE_OP_RMSNORM ||
+           op == TILE_OP_LAYERNORM_AFFINE || op == TILE_OP_RMSNORM_WEIGHTED;
+}
+
+bool row_output(int op) { return op == TILE_OP_ROW_SUM || op == TILE_OP_ROW_MINMAX; }
+
+// One call of a row operation with its operands normalised: pointers an op
+// does not use are cleared, so the kernel never sees them.
+struct Call {
+    int op;
+    const float *in, *res, *gamma, *beta;
+    float *out, *out2;
+    int rows, width;
+    float eps;
+};
+
+Call make_call(int op, const tile_row_args_t &a) {
+    Call c{op, a.in, nullptr, nullptr, nullptr, a.out, nullptr, a.rows, a.width, a.eps};
+    if (op == TILE_OP_RESIDUAL_LAYERNORM || op == TILE_OP_LAYERNORM_AFFINE) c.res = a.residual;
+    if (op == TILE_OP_LAYERNORM_AFFINE || op == TILE_OP_RMSNORM_WEIGHTED) c.gamma = a.gamma;
+    if (op == TILE_OP_LAYERNORM_AFFINE) c.beta = a.beta;
+    if (op == TILE_OP_ROW_MINMAX) c.out2 = a.out2;
+    if (!is_normaliser(op)) c.eps = 0.0f;
+    return c;
+}
+
+bool coaligned16(const Call &c) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(c.in);
+    if (!row_output(c.op) && ((a ^ reinterpret_cast<uintptr_t>(c.out)) & 15u) != 0) return false;
+    if (c.res != nullptr && ((a ^ reinterpret_cast<uintptr_t>(c.res)) & 15u) != 0) return false;
     return true;
 }
 
-// Checks shared by every compute entry point.  Returns TILE_OK with *noop set
-// when there is nothing to launch.
-int validate(int op, const float *in, const float *res, const float *out, int rows, int width,
-             float eps, bool *noop) {
+// Checks shared by every row entry point.  Returns TILE_OK with *noop set
+// when there is nothing to launch.  No CUDA call is made.
+int validate(const Call &c, bool *noop) {
     *noop = false;
-    if (op < TILE_OP_RESIDUAL_LAYERNORM || op > TILE_OP_SOFTMAX) return TILE_ERR_OP;
-    if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH) return TILE_ERR_SHAPE;
-    if (op != TILE_OP_SOFTMAX && !(std::isfinite(eps) && eps >= 0.0f)) return TILE_ERR_EPS;
-    if (rows == 0) {
+    if (!valid_op(c.op)) return TILE_ERR_OP;
+    if (c.rows < 0 || c.width < 1 || c.width > TILE_MAX_WIDTH) return TILE_ERR_SHAPE;
+    if (is_normaliser(c.op) && !(std::isfinite(c.eps) && c.eps >= 0.0f)) return TILE_ERR_EPS;
+    if (c.rows == 0) {
         *noop = true;
         return TILE_OK;
     }
-    const bool residual = op == TILE_OP_RESIDUAL_LAYERNORM;
-    if (in == nullptr || out == nullptr || (residual && res == nullptr)) return TILE_ERR_NULL;
-    if (misaligned(in) || misaligned(out) || (residual && misaligned(res))) return TILE_ERR_ALIGN;
-    const size_t bytes = static_cast<size_t>(rows) * static_cast<size_t>(width) * sizeof(float);
-    if (overlaps(out, in, bytes) || (residual && overlaps(out, res, bytes))) return TILE_ERR_ALIAS;
+    if (c.in == nullptr || c.out == nullptr) return TILE_ERR_NULL;
+    if (c.op == TILE_OP_RESIDUAL_LAYERNORM && c.res == nullptr) return TILE_ERR_NULL;
+    if ((c.op == TILE_OP_LAYERNORM_AFFINE || c.op == TILE_OP_RMSNORM_WEIGHTED) && c.gamma == nullptr)
+        return TILE_ERR_NULL;
+    if (c.op == TILE_OP_ROW_MINMAX && c.out2 == nullptr) return TILE_ERR_NULL;
+    for (const void *p : {static_cast<const void *>(c.in), static_cast<const void *>(c.res),
+                          static_cast<const void *>(c.gamma), static_cast<const void *>(c.beta),
+                          static_cast<const void *>(c.out), static_cast<const void *>(c.out2)})
+        if (misaligned(p)) return TILE_ERR_ALIGN;
+    const size_t mat = static_cast<size_t>(c.rows) * static_cast<size_t>(c.width) * sizeof(float);
+    const size_t vec = static_cast<size_t>(c.width) * sizeof(float);
+    const size_t out_bytes = row_output(c.op) ? static_cast<size_t>(c.rows) * sizeof(float) : mat;
+    const size_t out2_bytes = static_cast<size_t>(c.rows) * sizeof(float);
+    if (overlaps(c.out, out_bytes, c.in, mat) || overlaps(c.out, out_bytes, c.res, mat) ||
+        overlaps(c.out, out_bytes, c.gamma, vec) || overlaps(c.out, out_bytes, c.beta, vec) ||
+        overlaps(c.out2, out2_bytes, c.in, mat) || overlaps(c.out2, out2_bytes, c.out, out_bytes))
+        return TILE_ERR_ALIAS;
     return TILE_OK;
 }
 
-int launch(int op, int plan_id, const float *in, const float *res, float *out, int rows,
-           int width, float eps, cudaStream_t stream) {
+int launch(const Call &c, int plan_id, cudaStream_t stream) {
     const PlanDesc &p = kPlans[plan_id];
-    if (grid_of(p, rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
+    if (grid_of(p, c.rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
+    tile::RowArgs a{c.in, c.res, c.gamma, c.beta, c.out, c.out2, c.rows, c.width, c.eps, nullptr};
     cudaError_t err;
-    switch (op) {
-        case TILE_OP_RESIDUAL_LAYERNORM:
-            err = tile::launch_residual_layernorm(plan_id, in, res, out, rows, width, eps, stream);
-            break;
-        case TILE_OP_LAYERNORM:
-            err = tile::launch_layernorm(plan_id, in, nullptr, out, rows, width, eps, stream);
+    switch (c.op) {
+        case TILE_OP_RESIDUAL_LAYERNORM: err = tile::launch_residual_layernorm(plan_id, a, stream); break;
+        case TILE_OP_LAYERNORM: err = tile::launch_layernorm(plan_id, a, stream); break;
+        case TILE_OP_LAYERNORM_AFFINE:
+            err = c.res != nullptr ? tile::launch_residual_layernorm(plan_id, a, stream)
+                                   : tile::launch_layernorm(plan_id, a, stream);
             break;
         case TILE_OP_RMSNORM:
-            err = tile::launch_rmsnorm(plan_id, in, nullptr, out, rows, width, eps, stream);
-            break;
-        default:
-            err = tile::launch_softmax(plan_id, in, nullptr, out, rows, width, eps, stream);
-            break;
+        case TILE_OP_RMSNORM_WEIGHTED: err = tile::launch_rmsnorm(plan_id, a, stream); break;
+        case TILE_OP_ROW_SUM: err = tile::launch_row_sum(plan_id, a, stream); break;
+        case TILE_OP_ROW_MINMAX: err = tile::launch_row_minmax(plan_id, a, stream); break;
+        default: err = tile::launch_softmax(plan_id, a, stream); break;
     }
     if (err != cudaSuccess) {
         tile::set_last_cuda_error(static_cast<int>(err));
         return TILE_ERR_CUDA;
     }
     return TILE_OK;
+}
+
+int run_call(const Call &c, cudaStream_t stream) {
+    bool noop = false;
+    const int st = validate(c, &noop);
+    if (st != TILE_OK || noop) return st;
+    const int plan = select_plan(c.op, c.rows, c.width, coaligned16(c), c.res != nullptr);
+    if (plan < 0) return TILE_ERR_SHAPE;
+    return launch(c, plan, stream);
+}
+
+int run_call_plan(const Call &c, int plan_id, cudaStream_t stream) {
+    bool noop = false;
+    const int st = validate(c, &noop);
+    if (st != TILE_OK) return st;
+    if (plan_id < 0 || plan_id >= TILE_PLAN_COUNT || !covers(kPlans[plan_id], c.width))
+        return TILE_ERR_PLAN;
+    if (noop) return TILE_OK;
+    if (kPlans[plan_id].V == 4 && !coaligned16(c)) return TILE_ERR_PLAN;
+    return launch(c, plan_id, stream);
+}
+
+tile_row_args_t args_of(const float *in, const float *res, const float *gamma, const float *beta,
+                        float *out, float *out2, int rows, int width, float eps) {
+    tile_row_args_t a;
+    a.in = in;
+    a.residual = res;
+    a.gamma = gamma;
+    a.beta = beta;
+    a.out = out;
+    a.out2 = out2;
+    a.rows = rows;
+    a.width = width;
+    a.eps = eps;
+    return a;
 }
 
 }  // namespace
@@ -185,13 +275,26 @@ int last_cuda_error() { return t_last_cuda_error; }
 
 int run_selected(int op, const float *in, const float *res, float *out, int rows, int width,
                  float eps, cudaStream_t stream) {
-    bool noop = false;
-    const int st = validate(op, in, res, out, rows, width, eps, &noop);
-    if (st != TILE_OK || noop) return st;
-    const bool vec4 = coaligned16(in, res, out, op == TILE_OP_RESIDUAL_LAYERNORM);
-    const int plan = select_plan(op, rows, width, vec4);
-    if (plan < 0) return TILE_ERR_SHAPE;
-    return launch(op, plan, in, res, out, rows, width, eps, stream);
+    return run_call(make_call(op, args_of(in, res, nullptr, nullptr, out, nullptr, rows, width, eps)),
+                    stream);
+}
+
+int run_pairs(int kind, const float *in, float *value, float *derivative, long long n,
+              cudaStream_t stream) {
+    if (n < 0) return TILE_ERR_SHAPE;
+    if (n == 0) return TILE_OK;
+    if (in == nullptr || value == nullptr || derivative == nullptr) return TILE_ERR_NULL;
+    if (misaligned(in) || misaligned(value) || misaligned(derivative)) return TILE_ERR_ALIGN;
+    const size_t bytes = static_cast<size_t>(n) * sizeof(float);
+    if (overlaps(value, bytes, in, bytes) || overlaps(derivative, bytes, in, bytes) ||
+        overlaps(value, bytes, derivative, bytes))
+        return TILE_ERR_ALIAS;
+    const cudaError_t err = launch_pairs(kind, in, value, derivative, n, stream);
+    if (err != cudaSuccess) {
+        set_last_cuda_error(static_cast<int>(err));
+        return TILE_ERR_CUDA;
+    }
+    return TILE_OK;
 }
 
 }  // namespace tile
@@ -218,11 +321,52 @@ int tile_softmax_f32(const float *in, float *out, int rows, int width, float eps
     return tile::run_selected(TILE_OP_SOFTMAX, in, nullptr, out, rows, width, eps, stream);
 }
 
+int tile_layernorm_affine_f32(const float *in, const float *residual, const float *gamma,
+                              const float *beta, float *out, int rows, int width, float eps,
+                              cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_LAYERNORM_AFFINE,
+                              args_of(in, residual, gamma, beta, out, nullptr, rows, width, eps)),
+                    stream);
+}
+
+int tile_rmsnorm_weighted_f32(const float *in, const float *gamma, float *out, int rows,
+                              int width, float eps, cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_RMSNORM_WEIGHTED,
+                              args_of(in, nullptr, gamma, nullptr, out, nullptr, rows, width, eps)),
+                    stream);
+}
+
+int tile_row_sum_f32(const float *in, float *sums, int rows, int width, cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_ROW_SUM,
+                              args_of(in, nullptr, nullptr, nullptr, sums, nullptr, rows, width, 0.0f)),
+                    stream);
+}
+
+int tile_row_minmax_f32(const float *in, float *mins, float *maxs, int rows, int width,
+                        cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_ROW_MINMAX,
+                              args_of(in, nullptr, nullptr, nullptr, mins, maxs, rows, width, 0.0f)),
+                    stream);
+}
+
+int tile_run_plan_args_f32(int op, int plan_id, const tile_row_args_t *args, cudaStream_t stream) {
+    if (args == nullptr) return TILE_ERR_NULL;
+    return run_call_plan(make_call(op, *args), plan_id, stream);
+}
+
+int tile_run_plan_f32(int op, int plan_id, const float *in, const float *residual, float *out,
+                      int rows, int width, float eps, cudaStream_t stream) {
+    if (op > TILE_OP_SOFTMAX) return TILE_ERR_OP;
+    return run_call_plan(make_call(op, args_of(in, residual, nullptr, nullptr, out, nullptr, rows,
+                                               width, eps)),
+                         plan_id, stream);
+}
+
 int tile_describe_plan(int op, int rows, int width, tile_plan_t *plan) {
-    if (op < TILE_OP_RESIDUAL_LAYERNORM || op > TILE_OP_SOFTMAX) return TILE_ERR_OP;
+    if (!valid_op(op)) return TILE_ERR_OP;
     if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH) return TILE_ERR_SHAPE;
     if (plan == nullptr) return TILE_ERR_NULL;
-    const int id = select_plan(op, rows, width, true);
+    const int id = select_plan(op, rows, width, true, false);
     if (id < 0) return TILE_ERR_SHAPE;
     fill_plan(kPlans[id], op, rows, width, plan);
     return TILE_OK;
@@ -232,26 +376,12 @@ int tile_plan_count(void) { return TILE_PLAN_COUNT; }
 
 int tile_plan_info(int id, int op, int rows, int width, tile_plan_t *plan) {
     if (id < 0 || id >= TILE_PLAN_COUNT) return TILE_ERR_PLAN;
-    if (op < TILE_OP_RESIDUAL_LAYERNORM || op > TILE_OP_SOFTMAX) return TILE_ERR_OP;
+    if (!valid_op(op)) return TILE_ERR_OP;
     if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH || !covers(kPlans[id], width))
         return TILE_ERR_SHAPE;
     if (plan == nullptr) return TILE_ERR_NULL;
     fill_plan(kPlans[id], op, rows, width, plan);
     return TILE_OK;
-}
-
-int tile_run_plan_f32(int op, int plan_id, const float *in, const float *residual, float *out,
-                      int rows, int width, float eps, cudaStream_t stream) {
-    bool noop = false;
-    const int st = validate(op, in, residual, out, rows, width, eps, &noop);
-    if (st != TILE_OK) return st;
-    if (plan_id < 0 || plan_id >= TILE_PLAN_COUNT || !covers(kPlans[plan_id], width))
-        return TILE_ERR_PLAN;
-    if (noop) return TILE_OK;
-    if (kPlans[plan_id].V == 4 &&
-        !coaligned16(in, residual, out, op == TILE_OP_RESIDUAL_LAYERNORM))
-        return TILE_ERR_PLAN;
-    return launch(op, plan_id, in, residual, out, rows, width, eps, stream);
 }
 
 int tile_max_width(void) { return TILE_MAX_WIDTH; }
@@ -263,11 +393,11 @@ const char *tile_status_string(int status) {
         case TILE_OK: return "ok";
         case TILE_ERR_NULL: return "a required pointer is NULL";
         case TILE_ERR_SHAPE: return "rows < 0, width < 1, width above the maximum, or grid too large";
-        case TILE_ERR_ALIAS: return "out overlaps in or residual";
+        case TILE_ERR_ALIAS: return "an output overlaps an input or the other output";
         case TILE_ERR_EPS: return "eps is negative or not finite";
         case TILE_ERR_CUDA: return "the CUDA runtime reported an error (see tile_last_cuda_error)";
         case TILE_ERR_OP: return "unknown operation code";
-        case TILE_ERR_ALIGN: return "a pointer is not 4-byte aligned";
+        case TILE_ERR_ALIGN: return "a pointer is not 4-byte aligned (workspace: 256-byte)";
         case TILE_ERR_PLAN: return "the plan does not exist, cannot cover the width, or needs 16-byte co-aligned pointers";
         case TILE_ERR_DEVICE: return "a kernel recorded an error in the device status word";
         case TILE_ERR_WORKSPACE: return "the device workspace cannot hold one row chunk twice";
@@ -279,7 +409,7 @@ int tile_check_device_status(cudaStream_t stream) {
     unsigned int word = 0, v = 0;
     cudaError_t (*fetch[])(unsigned int *, cudaStream_t) = {
         tile::status_residual_layernorm, tile::status_layernorm, tile::status_rmsnorm,
-        tile::status_softmax};
+        tile::status_softmax, tile::status_row_sum, tile::status_row_minmax, tile::status_pairs};
     for (auto f : fetch) {
         v = 0;
         const cudaError_t err = f(&v, stream);
@@ -290,6 +420,16 @@ int tile_check_device_status(cudaStream_t stream) {
         word |= v;
     }
     return word ? TILE_ERR_DEVICE : TILE_OK;
+}
+
+int tile_sigmoid_pair_f32(const float *in, float *value, float *derivative, long long n,
+                          cudaStream_t stream) {
+    return tile::run_pairs(tile::PAIR_SIGMOID, in, value, derivative, n, stream);
+}
+
+int tile_gelu_tanh_pair_f32(const float *in, float *value, float *derivative, long long n,
+                            cudaStream_t stream) {
+    return tile::run_pairs(tile::PAIR_GELU_TANH, in, value, derivative, n, stream);
 }
 
 }  // extern "C"

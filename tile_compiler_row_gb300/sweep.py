@@ -18,7 +18,10 @@ import statistics
 import sys
 
 OPS = ("residual_layernorm", "layernorm", "rmsnorm", "softmax")
-BYTES = {"residual_layernorm": 12, "layernorm": 8, "rmsnorm": 8, "softmax": 8}
+MORE_OPS = ("row_sum", "row_minmax", "layernorm_affine", "rmsnorm_weighted")
+#: algorithmic bytes per element (row outputs and gamma/beta are negligible)
+BYTES = {"residual_layernorm": 12, "layernorm": 8, "rmsnorm": 8, "softmax": 8, "row_sum": 4,
+         "row_minmax": 4, "layernorm_affine": 8, "rmsnorm_weighted": 8}
 
 #: widths of the sweep ladder; ``rows`` fills about 2**26 elements per tensor
 #: (256 MiB, well above L2) so the large-row regime is HBM bound.
@@ -38,13 +41,23 @@ def shapes(quick=False):
     return out
 
 
-def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream):
+def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g=None, y2=None):
+    import ctypes
+
     import torch
+
+    import tile_compiler_row_gb300 as tile
     s = stream.cuda_stream
-    px, pr, py = x.data_ptr(), r.data_ptr(), y.data_ptr()
+    a = tile.TileRowArgs()
+    a.in_, a.residual, a.out = x.data_ptr(), r.data_ptr(), y.data_ptr()
+    a.gamma = g.data_ptr() if g is not None else None
+    a.beta = None
+    a.out2 = y2.data_ptr() if y2 is not None else None
+    a.rows, a.width, a.eps = rows, width, 1e-5
+    ref = ctypes.byref(a)
 
     def call():
-        st = lib.tile_run_plan_f32(op_code, plan, px, pr, py, rows, width, 1e-5, s)
+        st = lib.tile_run_plan_args_f32(op_code, plan, ref, s)
         if st != 0:
             raise RuntimeError(f"plan {plan}: status {st}")
 
@@ -83,10 +96,12 @@ def main(argv=None):
         [tuple(int(v) for v in sh.split("x")) for sh in args.shapes.split(",")]
     for rows, width in todo:
         n = rows * width
-        g = torch.Generator(device="cuda").manual_seed(rows * 131 + width)
-        x = torch.rand(rows, width, device="cuda", generator=g) * 2 - 1
-        r = torch.rand(rows, width, device="cuda", generator=g) * 2 - 1
+        gen = torch.Generator(device="cuda").manual_seed(rows * 131 + width)
+        x = torch.rand(rows, width, device="cuda", generator=gen) * 2 - 1
+        r = torch.rand(rows, width, device="cuda", generator=gen) * 2 - 1
         y = torch.empty_like(x)
+        g = torch.rand(width, device="cuda", generator=gen) + 0.5
+        y2 = torch.empty(rows, device="cuda")
         for op in args.ops.split(","):
             code = tile.OPS[op]
             chosen = tile.tile_describe_plan(op, rows, width)["id"]
@@ -95,7 +110,8 @@ def main(argv=None):
                 info = tile.tile_plan_info(pid, op, rows, width)
                 if info is None or info["vec"] != 4 or info["grid"] > 0x7FFFFFFF:
                     continue
-                us = time_plan(lib, code, pid, x, r, y, rows, width, args.warmup, args.iters, stream)
+                us = time_plan(lib, code, pid, x, r, y, rows, width, args.warmup, args.iters, stream,
+                               g=g, y2=y2)
                 entry["plans"][pid] = round(us, 3)
             best = min(entry["plans"], key=entry["plans"].get)
             entry["best"] = best
@@ -103,7 +119,7 @@ def main(argv=None):
             entry["selected_over_best"] = round(entry["plans"][chosen] / entry["plans"][best], 4)
             results.append(entry)
             print(json.dumps(entry), flush=True)
-        del x, r, y
+        del x, r, y, g, y2
     assert tile.tile_check_device_status() == 0
     if args.out:
         with open(args.out, "w") as fh:
