@@ -64,14 +64,19 @@ constexpr Bucket kVec4Softmax[] = {
     {131, 0}, {259, 1}, {515, 2}, {1027, 3}, {2051, 6}, {4099, 7},
     {8195, 10}, {16387, 31}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
 };
-// Row sum and min/max: one reduction phase like RMSNorm (until swept).
-constexpr Bucket kVec4RowSum[] = {
-    {131, 0}, {259, 2}, {515, 4}, {1027, 6}, {2051, 5}, {3075, 8}, {8195, 10},
-    {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
+// Affine LayerNorm (with or without residual), weighted RMSNorm, and the
+// row reductions (sum, min/max), from the same sweep.
+constexpr Bucket kVec4Affine[] = {
+    {131, 0}, {259, 1}, {515, 2}, {1027, 4}, {2051, 6}, {4099, 7},
+    {8195, 10}, {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 20},
 };
-constexpr Bucket kVec4RowMinMax[] = {
-    {131, 0}, {259, 2}, {515, 4}, {1027, 6}, {2051, 5}, {3075, 8}, {8195, 10},
-    {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
+constexpr Bucket kVec4Weighted[] = {
+    {131, 0}, {515, 2}, {1027, 4}, {1540, 6}, {2051, 5}, {4099, 8},
+    {8195, 10}, {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
+};
+constexpr Bucket kVec4RowReduce[] = {
+    {131, 0}, {259, 1}, {515, 2}, {1027, 4}, {2051, 6}, {3075, 35}, {4099, 7},
+    {6147, 32}, {8195, 10}, {16387, 31}, {32771, 34}, {65539, 33}, {TILE_MAX_WIDTH, 30},
 };
 constexpr Bucket kVec1[] = {
     {128, 25}, {1024, 26}, {4096, 27}, {16384, 28}, {TILE_MAX_WIDTH, 29},
@@ -86,16 +91,16 @@ int pick(const Bucket (&table)[N], int width) {
 
 int select_plan(int op, long long rows, int width, bool vec4, bool residual) {
     (void)rows;
+    (void)residual;
     if (!vec4) return pick(kVec1, width);
     switch (op) {
         case TILE_OP_RESIDUAL_LAYERNORM: return pick(kVec4ResidualLN, width);
         case TILE_OP_LAYERNORM: return pick(kVec4LN, width);
-        case TILE_OP_LAYERNORM_AFFINE:
-            return residual ? pick(kVec4ResidualLN, width) : pick(kVec4LN, width);
-        case TILE_OP_RMSNORM:
-        case TILE_OP_RMSNORM_WEIGHTED: return pick(kVec4RMS, width);
-        case TILE_OP_ROW_SUM: return pick(kVec4RowSum, width);
-        case TILE_OP_ROW_MINMAX: return pick(kVec4RowMinMax, width);
+        case TILE_OP_LAYERNORM_AFFINE: return pick(kVec4Affine, width);
+        case TILE_OP_RMSNORM: return pick(kVec4RMS, width);
+        case TILE_OP_RMSNORM_WEIGHTED: return pick(kVec4Weighted, width);
+        case TILE_OP_ROW_SUM:
+        case TILE_OP_ROW_MINMAX: return pick(kVec4RowReduce, width);
         default: return pick(kVec4Softmax, width);
     }
 }

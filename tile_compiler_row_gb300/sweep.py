@@ -41,7 +41,8 @@ def shapes(quick=False):
     return out
 
 
-def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g=None, y2=None):
+def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g=None, y2=None,
+              graph=False):
     import ctypes
 
     import torch
@@ -63,6 +64,25 @@ def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g
 
     for _ in range(warmup):
         call()
+    if graph:
+        # ``iters`` calls captured in one CUDA graph and replayed: the time per
+        # call without host launch overhead (what back-to-back device work sees)
+        cap = torch.cuda.Stream()
+        s = cap.cuda_stream
+        torch.cuda.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=cap):
+            for _ in range(iters):
+                call()
+        cg.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(3):
+            cg.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (3 * iters)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
     evs[0].record(stream)
     for i in range(iters):
@@ -81,6 +101,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--iters", type=int, default=30)
     ap.add_argument("--shapes", default=None, help="comma list of ROWSxWIDTH (default: ladder)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time calls replayed from a CUDA graph (no host launch overhead)")
+    ap.add_argument("--small", action="store_true", help="only the small workload shapes")
     args = ap.parse_args(argv)
 
     import torch
@@ -94,6 +117,8 @@ def main(argv=None):
     results = []
     todo = shapes(args.quick) if args.shapes is None else \
         [tuple(int(v) for v in sh.split("x")) for sh in args.shapes.split(",")]
+    if args.small:
+        todo = list(SMALL)
     for rows, width in todo:
         n = rows * width
         gen = torch.Generator(device="cuda").manual_seed(rows * 131 + width)
@@ -105,13 +130,14 @@ def main(argv=None):
         for op in args.ops.split(","):
             code = tile.OPS[op]
             chosen = tile.tile_describe_plan(op, rows, width)["id"]
-            entry = {"op": op, "rows": rows, "width": width, "selected": chosen, "plans": {}}
+            entry = {"op": op, "rows": rows, "width": width, "selected": chosen, "plans": {},
+                     "timing": "cuda graph replay" if args.graph else "back-to-back launches"}
             for pid in range(tile.tile_plan_count()):
                 info = tile.tile_plan_info(pid, op, rows, width)
                 if info is None or info["vec"] != 4 or info["grid"] > 0x7FFFFFFF:
                     continue
                 us = time_plan(lib, code, pid, x, r, y, rows, width, args.warmup, args.iters, stream,
-                               g=g, y2=y2)
+                               g=g, y2=y2, graph=args.graph)
                 entry["plans"][pid] = round(us, 3)
             best = min(entry["plans"], key=entry["plans"].get)
             entry["best"] = best
