@@ -357,6 +357,26 @@ def run_ours(args, dist):
                            "achieved_gbs": round(b / (k_ms / 1e3) / 1e9, 1),
                            "frac": round(b / (k_ms / 1e3) / 1e9 / peak, 4),
                            "plan_id": tile.tile_describe_plan(name, rows, width)["id"]}
+        # the same residual LayerNorm on BF16 rows (6 bytes per element)
+        xb, rb = x.to(torch.bfloat16), r.to(torch.bfloat16)
+        yb = torch.empty_like(xb)
+
+        def f_bf16():
+            st = lib.tile_residual_layernorm_bf16(xb.data_ptr(), rb.data_ptr(), yb.data_ptr(),
+                                                  rows, width, EPS, s)
+            if st != 0:
+                raise tile.TileError(st, "tile_residual_layernorm_bf16")
+
+        for _ in range(max(3, args.warmup)):
+            f_bf16()
+        per_x, _ = time_calls(f_bf16, max(20, min(args.steps, 200)), stream)
+        k_ms = statistics.mean(per_x)
+        b = 6 * elems
+        extra["residual_layernorm_bf16"] = {
+            "us_per_call": round(k_ms * 1e3, 3), "achieved_gbs": round(b / (k_ms / 1e3) / 1e9, 1),
+            "frac": round(b / (k_ms / 1e3) / 1e9 / peak, 4),
+            "plan_id": tile.tile_describe_plan_ex("residual_layernorm", "bf16", rows, width)["id"]}
+        del xb, rb, yb
         line["other_ops"] = extra
 
     # --- end to end through the C ABI with pinned host buffers -------------

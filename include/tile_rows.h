@@ -62,6 +62,11 @@ extern "C" {
 #define TILE_ERR_PLAN        -8  /* an explicit plan is not one of the built  */
 #define TILE_ERR_DEVICE      -9  /* a kernel recorded an error on the device  */
 #define TILE_ERR_WORKSPACE  -10  /* device workspace too small for one row    */
+#define TILE_ERR_DTYPE      -11  /* unknown element type code                 */
+
+/* ---- element types of row data (tile_row_args_t, tile_*_ex) ------------ */
+#define TILE_DTYPE_F32  0   /* IEEE binary32                                  */
+#define TILE_DTYPE_BF16 1   /* bfloat16: the high 16 bits of a binary32       */
 
 /* ---- operation codes (tile_describe_plan, tile_run_plan_*) ------------- */
 #define TILE_OP_RESIDUAL_LAYERNORM 0
@@ -90,18 +95,20 @@ typedef struct tile_plan {
     int rows, width;        /* the shape the plan was made for                */
     int id;                 /* index in the built plan table                  */
     int path;               /* TILE_PATH_*                                    */
-    int vec;                /* V: 4 = float4 body (+ scalar head/tail), or 1  */
+    int vec;                /* elements per access: a 16-byte vector (4 FP32  */
+                            /* or 8 BF16, + scalar head/tail), or 1           */
     int warps_per_program;  /* S                                              */
     int programs_per_cta;   /* P                                              */
     int chunks;             /* K: V-vectors per worker                        */
     int cluster;            /* C: CTAs per row (1 = no cluster)               */
     int threads;            /* T = 32 * S * P                                 */
     int workers;            /* W = 32 * S                                     */
-    int stripe_floats;      /* K * V registers of row data per thread         */
+    int stripe_floats;      /* K * vec FP32 registers of row data per thread  */
     int max_width;          /* widest row this plan covers                    */
     int smem_bytes;         /* static shared memory per CTA                   */
     int barriers_per_row;   /* CTA or cluster barriers on a row's path        */
     long long grid;         /* CTAs launched for `rows`                       */
+    int dtype;              /* TILE_DTYPE_* the plan was described for        */
 } tile_plan_t;
 
 /* ---- compute entry points --------------------------------------------- */
@@ -159,19 +166,48 @@ int tile_row_minmax_f32(const float *in, float *mins, float *maxs, int rows, int
 /* Operands of a row operation for tile_run_plan_args_f32.  Unused pointers
  * are ignored (set them NULL). */
 typedef struct tile_row_args {
-    const float *in;        /* [rows][width]                                    */
-    const float *residual;  /* residual LayerNorm; optional for affine LN       */
-    const float *gamma;     /* affine LN / weighted RMSNorm: [width]            */
-    const float *beta;      /* affine LN: [width] or NULL                       */
-    float *out;             /* [rows][width], or [rows] sums / minima           */
-    float *out2;            /* [rows] maxima (TILE_OP_ROW_MINMAX)               */
+    const void *in;         /* [rows][width] of `dtype`                         */
+    const void *residual;   /* residual LayerNorm; optional for affine LN       */
+    const float *gamma;     /* affine LN / weighted RMSNorm: [width] FP32       */
+    const float *beta;      /* affine LN: [width] FP32 or NULL                  */
+    void *out;              /* [rows][width] of `dtype`, or [rows] FP32 sums /  */
+                            /* minima                                            */
+    float *out2;            /* [rows] FP32 maxima (TILE_OP_ROW_MINMAX)          */
     int rows, width;
     float eps;              /* normalisers only                                  */
+    int dtype;              /* TILE_DTYPE_F32 or TILE_DTYPE_BF16                */
 } tile_row_args_t;
 
 /* Any row operation with the built plan `plan_id` forced (plan sweeps,
  * per-plan tests).  Errors as tile_run_plan_f32. */
 int tile_run_plan_args_f32(int op, int plan_id, const tile_row_args_t *args, cudaStream_t stream);
+
+/* ---- BF16 rows ----------------------------------------------------------
+ * The row operations on BF16 data (2 bytes per element; the pages cover FP32
+ * only and name low precision as not covered, "Residual LayerNorm
+ * shared-Tile materialization search", "Exact command").  Each element is
+ * widened exactly to FP32, every reduction and map runs in FP32 as for the
+ * FP32 entry points, and outputs are rounded to nearest-even BF16.  gamma,
+ * beta and the row outputs of sum and min/max stay FP32.  Pointers to BF16
+ * data must be 2-byte aligned; 16-byte vectors (8 elements) are used when
+ * in, residual and out share a 16-byte phase.  Everything else is the
+ * contract of the FP32 entry point of the same name. */
+int tile_residual_layernorm_bf16(const void *in, const void *residual, void *out, int rows,
+                                 int width, float eps, cudaStream_t stream);
+int tile_layernorm_bf16(const void *in, void *out, int rows, int width, float eps,
+                        cudaStream_t stream);
+int tile_rmsnorm_bf16(const void *in, void *out, int rows, int width, float eps,
+                      cudaStream_t stream);
+int tile_softmax_bf16(const void *in, void *out, int rows, int width, float eps,
+                      cudaStream_t stream);
+int tile_layernorm_affine_bf16(const void *in, const void *residual, const float *gamma,
+                               const float *beta, void *out, int rows, int width, float eps,
+                               cudaStream_t stream);
+int tile_rmsnorm_weighted_bf16(const void *in, const float *gamma, void *out, int rows,
+                               int width, float eps, cudaStream_t stream);
+int tile_row_sum_bf16(const void *in, float *sums, int rows, int width, cudaStream_t stream);
+int tile_row_minmax_bf16(const void *in, float *mins, float *maxs, int rows, int width,
+                         cudaStream_t stream);
 
 /* ---- pointwise value/derivative pairs ---------------------------------- */
 
@@ -261,11 +297,19 @@ int tile_run_host_static_f32(int op, const float *h_in, const float *h_residual,
  * success only. */
 int tile_describe_plan(int op, int rows, int width, tile_plan_t *plan);
 
+/* tile_describe_plan for an element type (TILE_DTYPE_*); TILE_ERR_DTYPE for
+ * an unknown one. */
+int tile_describe_plan_ex(int op, int dtype, int rows, int width, tile_plan_t *plan);
+
 /* Number of plans built into the library, and plan `id` of that table
  * described for (op, rows, width).  Returns TILE_ERR_PLAN for a bad id and
  * TILE_ERR_SHAPE if the plan cannot cover `width`.  Host only. */
 int tile_plan_count(void);
 int tile_plan_info(int id, int op, int rows, int width, tile_plan_t *plan);
+
+/* tile_plan_info for an element type; TILE_ERR_PLAN also when plan `id` is
+ * not built for that type (BF16 plans whose stripe would pass 64 floats). */
+int tile_plan_info_ex(int id, int op, int dtype, int rows, int width, tile_plan_t *plan);
 
 /* Run `op` (one of the first four op codes) with the built plan `plan_id`
  * instead of the selector's choice (used by the measured plan sweep and by

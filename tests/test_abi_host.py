@@ -251,3 +251,28 @@ def test_describe_plan_covers_the_new_ops(lib):
         for w in (1, 127, 4096, 65536, 131072):
             p = tile.tile_describe_plan(op, 3, w)
             assert p["max_width"] >= w
+
+
+@fake_pointers
+def test_bf16_entry_points_reject_bad_arguments(lib):
+    assert lib.tile_layernorm_bf16(A, B, 2, 0, 1e-5, None) == SHAPE
+    assert lib.tile_layernorm_bf16(A + 1, B, 2, 8, 1e-5, None) == ALIGN     # odd address
+    assert lib.tile_rmsnorm_bf16(A, A + 16, 2, 8, 1e-5, None) == ALIAS      # 2 x 8 x 2 bytes
+    assert lib.tile_residual_layernorm_bf16(A, None, B, 2, 8, 1e-5, None) == NULL
+    assert lib.tile_row_sum_bf16(A, B + 2, 2, 8, None) == ALIGN             # FP32 output
+    a = tile.TileRowArgs()
+    a.in_, a.out, a.rows, a.width, a.eps, a.dtype = A, B, 2, 8, 1e-5, 7
+    assert lib.tile_run_plan_args_f32(1, 0, ctypes.byref(a), None) == -11
+
+
+def test_bf16_plans(lib):
+    for op in ("residual_layernorm", "layernorm", "rmsnorm", "softmax", "row_sum"):
+        for w in (1, 127, 4096, 8192, 65536, 131072):
+            p = tile.tile_describe_plan_ex(op, "bf16", 9, w)
+            assert p["dtype"] == 1 and p["max_width"] >= w
+            assert p["stripe_floats"] <= 64
+    # K = 16 plans are not built for BF16
+    k16 = [pid for pid in range(tile.tile_plan_count())
+           if tile.tile_plan_info(pid, 0, 1, 1)["chunks"] == 16 and
+           tile.tile_plan_info(pid, 0, 1, 1)["vec"] == 4]
+    assert k16 and all(tile.tile_plan_info_ex(pid, 0, "bf16", 1, 1) is None for pid in k16)

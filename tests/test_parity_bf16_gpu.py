@@ -1,0 +1,180 @@
+"""GPU parity of the BF16 row operations against the FP64 oracle.
+
+Inputs are the seeded FP32 workloads rounded to BF16; the oracle receives
+those BF16 values exactly (widened to FP32).  The kernels compute in FP32 and
+round each output to nearest-even BF16, so the bound is the FP32 one plus
+half a BF16 ulp (at most 2^-8 |ref|):
+
+    |y - ref| <= 2e-6 + (2e-5 + 2^-8) |ref|
+
+and, sharper, every output is within one BF16 ulp of round_bf16(ref) and at
+least 99.9 % of them equal it (the FP32 error is far below the BF16 spacing,
+so only outputs next to a rounding boundary may differ)."""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import tile_compiler_row_gb300 as tile
+from parity import ATOL, EPS, RTOL, ref_eps
+
+pytestmark = pytest.mark.gpu
+
+BF16_HALF_ULP_REL = 2.0 ** -8
+
+
+@pytest.fixture(scope="module", autouse=True)
+def device():
+    from tile_compiler_row_gb300 import _build
+    _build.build()
+    torch.cuda.set_device(0)
+    yield
+    assert tile.tile_check_device_status() == 0
+
+
+def _bf16_rows(cfg, rows, width, which="x"):
+    """(bf16 CUDA tensor, its exact FP32 values on the host)."""
+    t = torch.from_numpy(synth.rows_of(cfg, rows, width, which=which)).to(torch.bfloat16)
+    return t, t.float().numpy()
+
+
+def _placed(t, offset=0):
+    buf = torch.empty(t.numel() + 16, dtype=t.dtype, device="cuda")
+    view = buf[offset:offset + t.numel()].view(t.shape)
+    view.copy_(t)
+    return view
+
+
+def _round_bf16(ref):
+    """Round-to-nearest-even BF16 of FP64 values (through FP32)."""
+    b = np.asarray(ref, np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def check_bf16(got_t, ref, atol=ATOL, what=""):
+    got = got_t.float().cpu().numpy().astype(np.float64)
+    assert got.shape == ref.shape, what
+    assert np.all(np.isfinite(got)), what
+    err = np.abs(got - ref)
+    bound = atol + (RTOL + BF16_HALF_ULP_REL) * np.abs(ref)
+    assert np.all(err <= bound), f"{what}: max err {err.max():.3e}"
+    # rounding checks where a relative statement is meaningful (|ref| > 1e-6)
+    big = np.abs(ref) > 1e-6
+    rn = _round_bf16(ref[big])
+    ulp = 2.0 ** (np.floor(np.log2(np.abs(rn))) - 7)
+    assert np.all(np.abs(got[big] - rn) <= ulp), \
+        f"{what}: an output is more than one BF16 ulp from the rounded reference"
+    if big.any():
+        rate = float(np.mean(got[big] == rn))
+        assert rate >= 0.999, f"{what}: only {rate:.4f} correctly rounded"
+
+
+SHAPES = [(1, 127), (17, 257), (7, 1537), (64, 4096), (1024, 4096), (128, 8192), (32, 65536)]
+
+
+@pytest.mark.parametrize("rows,width", SHAPES)
+@pytest.mark.parametrize("op", ["residual_layernorm", "layernorm", "rmsnorm", "softmax"])
+def test_bf16_ops(op, rows, width):
+    cfg = 4 if width in (8192, 65536) and op != "residual_layernorm" else 3
+    x, xf = _bf16_rows(cfg, rows, width)
+    r, rf = _bf16_rows(cfg, rows, width, "r")
+    out = torch.empty(rows, width, dtype=torch.bfloat16, device="cuda")
+    tx = _placed(x)
+    if op == "residual_layernorm":
+        tile.tile_residual_layernorm_bf16(tx, _placed(r), out, EPS)
+        ref = oracle.get().residual_layernorm(xf, rf, ref_eps())
+    else:
+        getattr(tile, f"tile_{op}_bf16")(tx, out, EPS)
+        ref = oracle.get().run(op, xf, eps=ref_eps())
+    check_bf16(out, ref, what=f"bf16 {op} {rows}x{width}")
+
+
+@pytest.mark.parametrize("offset", [1, 3, 5, 7])
+@pytest.mark.parametrize("op", ["residual_layernorm", "layernorm", "rmsnorm", "softmax"])
+def test_bf16_unaligned_rows(op, offset):
+    for rows, width in [(5, 127), (3, 1537), (2, 4099)]:
+        x, xf = _bf16_rows(3, rows, width)
+        r, rf = _bf16_rows(3, rows, width, "r")
+        buf = torch.empty(rows * width + 16, dtype=torch.bfloat16, device="cuda")
+        out = buf[offset:offset + rows * width].view(rows, width)
+        if op == "residual_layernorm":
+            tile.tile_residual_layernorm_bf16(_placed(x, offset), _placed(r, offset), out, EPS)
+            ref = oracle.get().residual_layernorm(xf, rf, ref_eps())
+        else:
+            getattr(tile, f"tile_{op}_bf16")(_placed(x, offset), out, EPS)
+            ref = oracle.get().run(op, xf, eps=ref_eps())
+        check_bf16(out, ref, what=f"bf16 {op} offset {offset} {rows}x{width}")
+        # different phases for input and output: the scalar plans
+        out2 = torch.empty(rows, width, dtype=torch.bfloat16, device="cuda")
+        if op == "residual_layernorm":
+            tile.tile_residual_layernorm_bf16(_placed(x, offset), _placed(r, offset), out2, EPS)
+        else:
+            getattr(tile, f"tile_{op}_bf16")(_placed(x, offset), out2, EPS)
+        check_bf16(out2, ref, what=f"bf16 {op} mixed phases {rows}x{width}")
+
+
+@pytest.mark.parametrize("rows,width", [(7, 1537), (64, 4096), (128, 8192)])
+def test_bf16_affine_and_weighted(rows, width):
+    x, xf = _bf16_rows(3, rows, width)
+    r, rf = _bf16_rows(3, rows, width, "r")
+    g = synth.uniform_pm1(3001, width) * np.float32(2.0)
+    b = synth.uniform_pm1(3002, width)
+    tg, tb = torch.from_numpy(g).cuda(), torch.from_numpy(b).cuda()
+    out = torch.empty(rows, width, dtype=torch.bfloat16, device="cuda")
+    tile.tile_layernorm_affine_bf16(_placed(x), _placed(r), tg, tb, out, EPS)
+    ref = oracle.get().layernorm_affine(xf, g, b, r=rf, eps=ref_eps())
+    check_bf16(out, ref, atol=1e-5, what=f"bf16 affine {rows}x{width}")
+    tile.tile_rmsnorm_weighted_bf16(_placed(x), tg, out, EPS)
+    ref = oracle.get().rmsnorm_weighted(xf, g, eps=ref_eps())
+    check_bf16(out, ref, what=f"bf16 weighted {rows}x{width}")
+
+
+@pytest.mark.parametrize("rows,width", [(17, 257), (64, 4096), (32, 65536), (1000, 1)])
+def test_bf16_row_sum_and_minmax(rows, width):
+    x, xf = _bf16_rows(3, rows, width)
+    sums = torch.empty(rows, device="cuda")
+    tile.tile_row_sum_bf16(_placed(x, 1), sums)
+    ref = oracle.get().row_sum(xf)
+    got = sums.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= ATOL + RTOL * np.abs(ref))
+    mins, maxs = torch.empty(rows, device="cuda"), torch.empty(rows, device="cuda")
+    tile.tile_row_minmax_bf16(_placed(x, 3), mins, maxs)
+    mn, mx = oracle.get().row_minmax(xf)
+    assert np.array_equal(mins.cpu().numpy().astype(np.float64), mn)
+    assert np.array_equal(maxs.cpu().numpy().astype(np.float64), mx)
+
+
+def _bf16_plan_cases():
+    from tile_compiler_row_gb300 import _build
+    _build.build()
+    out = []
+    for pid in range(tile.tile_plan_count()):
+        info = tile.tile_plan_info_ex(pid, 0, "bf16", 1, 1)
+        if info is None:
+            continue
+        maxw = info["max_width"]
+        rows = 3 if maxw > 16384 else 2 * info["programs_per_cta"] + 1
+        for op in ("residual_layernorm", "layernorm", "rmsnorm", "softmax"):
+            out.append((pid, op, rows, sorted({1, 9, min(maxw, 77), maxw})))
+    return out
+
+
+@pytest.mark.parametrize("pid,op,rows,widths", _bf16_plan_cases(),
+                         ids=lambda v: str(v) if not isinstance(v, list) else "w")
+def test_every_bf16_plan(pid, op, rows, widths):
+    for w in widths:
+        x, xf = _bf16_rows(3, rows, w)
+        r, rf = _bf16_rows(3, rows, w, "r")
+        for off in (0, 3):
+            out = _placed(torch.zeros(rows, w, dtype=torch.bfloat16), off)
+            tile.tile_run_plan_args_f32(op, pid, _placed(x, off), out,
+                                        residual=_placed(r, off) if op == "residual_layernorm"
+                                        else None, eps=EPS)
+            ref = (oracle.get().residual_layernorm(xf, rf, ref_eps()) if op == "residual_layernorm"
+                   else oracle.get().run(op, xf, eps=ref_eps()))
+            check_bf16(out, ref, what=f"bf16 plan {pid} {op} w={w} off={off}")

@@ -27,6 +27,9 @@ __all__ = [
     "tile_host_workspace_bytes", "tile_run_host_static_f32", "tile_layernorm_affine_f32",
     "tile_rmsnorm_weighted_f32", "tile_row_sum_f32", "tile_row_minmax_f32",
     "tile_run_plan_args_f32", "tile_sigmoid_pair_f32", "tile_gelu_tanh_pair_f32",
+    "tile_residual_layernorm_bf16", "tile_layernorm_bf16", "tile_rmsnorm_bf16",
+    "tile_softmax_bf16", "tile_layernorm_affine_bf16", "tile_rmsnorm_weighted_bf16",
+    "tile_row_sum_bf16", "tile_row_minmax_bf16", "tile_describe_plan_ex", "tile_plan_info_ex",
     "residual_layernorm", "layernorm", "rmsnorm", "softmax", "run",
 ]
 
@@ -35,6 +38,9 @@ OPS = {"residual_layernorm": 0, "layernorm": 1, "rmsnorm": 2, "softmax": 3, "row
        "row_minmax": 5, "layernorm_affine": 6, "rmsnorm_weighted": 7}
 
 TILE_OK = 0
+
+#: Element type codes (TILE_DTYPE_*).
+DTYPES = {"f32": 0, "bf16": 1}
 
 
 class TileError(RuntimeError):
@@ -57,6 +63,7 @@ class TilePlan(ctypes.Structure):
         ("workers", ctypes.c_int), ("stripe_floats", ctypes.c_int),
         ("max_width", ctypes.c_int), ("smem_bytes", ctypes.c_int),
         ("barriers_per_row", ctypes.c_int), ("grid", ctypes.c_longlong),
+        ("dtype", ctypes.c_int),
     ]
 
     def as_dict(self):
@@ -68,6 +75,7 @@ class TileRowArgs(ctypes.Structure):
         ("in_", ctypes.c_void_p), ("residual", ctypes.c_void_p), ("gamma", ctypes.c_void_p),
         ("beta", ctypes.c_void_p), ("out", ctypes.c_void_p), ("out2", ctypes.c_void_p),
         ("rows", ctypes.c_int), ("width", ctypes.c_int), ("eps", ctypes.c_float),
+        ("dtype", ctypes.c_int),
     ]
 
 
@@ -110,6 +118,16 @@ def load():
         "tile_run_plan_args_f32": [I, I, ctypes.POINTER(TileRowArgs), P],
         "tile_sigmoid_pair_f32": [P, P, P, ctypes.c_longlong, P],
         "tile_gelu_tanh_pair_f32": [P, P, P, ctypes.c_longlong, P],
+        "tile_residual_layernorm_bf16": [P, P, P, I, I, F, P],
+        "tile_layernorm_bf16": [P, P, I, I, F, P],
+        "tile_rmsnorm_bf16": [P, P, I, I, F, P],
+        "tile_softmax_bf16": [P, P, I, I, F, P],
+        "tile_layernorm_affine_bf16": [P, P, P, P, P, I, I, F, P],
+        "tile_rmsnorm_weighted_bf16": [P, P, P, I, I, F, P],
+        "tile_row_sum_bf16": [P, P, I, I, P],
+        "tile_row_minmax_bf16": [P, P, P, I, I, P],
+        "tile_describe_plan_ex": [I, I, I, I, ctypes.POINTER(TilePlan)],
+        "tile_plan_info_ex": [I, I, I, I, I, ctypes.POINTER(TilePlan)],
     }
     for name, argtypes in sigs.items():
         fn = getattr(lib, name)
@@ -136,15 +154,16 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _matrix(t, name):
-    """(pointer, rows, width) of a CUDA FP32 row-major matrix tensor."""
+def _matrix(t, name, dtype="f32"):
+    """(pointer, rows, width) of a CUDA row-major matrix tensor of ``dtype``."""
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
-    if t.dtype != torch.float32:
-        raise ValueError(f"{name} must be float32")
+    want = torch.float32 if dtype == "f32" else torch.bfloat16
+    if t.dtype != want:
+        raise ValueError(f"{name} must be {want}")
     if t.dim() != 2:
         raise ValueError(f"{name} must be 2-D [rows, width]")
     rows, width = t.shape
@@ -258,12 +277,16 @@ def tile_row_minmax_f32(x, mins, maxs, stream=None):
 
 def tile_run_plan_args_f32(op, plan_id, x, out, residual=None, gamma=None, beta=None, out2=None,
                            eps=1e-5, stream=None):
-    """Any row op with a forced plan (``out``: matrix, or [rows] for row_sum/row_minmax)."""
+    """Any row op with a forced plan (``out``: matrix, or [rows] for row_sum/row_minmax).
+    ``x`` may be float32 or bfloat16; the element type follows it."""
+    import torch
     op = OPS[op] if isinstance(op, str) else op
-    px, rows, width = _matrix(x, "x")
+    dt = "bf16" if isinstance(x, torch.Tensor) and x.dtype == torch.bfloat16 else "f32"
+    px, rows, width = _matrix(x, "x", dt)
     a = TileRowArgs()
     a.in_ = px
-    a.residual = _matrix(residual, "residual")[0] if residual is not None else None
+    a.dtype = DTYPES[dt]
+    a.residual = _matrix(residual, "residual", dt)[0] if residual is not None else None
     a.gamma = _vector(gamma, width, "gamma")
     a.beta = _vector(beta, width, "beta")
     a.out = out.data_ptr()
@@ -297,6 +320,67 @@ def _pair_fn(name):
 
 tile_sigmoid_pair_f32 = _pair_fn("tile_sigmoid_pair_f32")
 tile_gelu_tanh_pair_f32 = _pair_fn("tile_gelu_tanh_pair_f32")
+
+
+# ---- BF16 rows ---------------------------------------------------------------
+
+def tile_residual_layernorm_bf16(x, residual, out, eps=1e-5, stream=None):
+    px, rows, width = _matrix(x, "x", "bf16")
+    pr, _, _ = _matrix(residual, "residual", "bf16")
+    po, _, _ = _matrix(out, "out", "bf16")
+    _same_shape(x, residual, "x/residual")
+    _same_shape(x, out, "x/out")
+    _check(load().tile_residual_layernorm_bf16(px, pr, po, rows, width, eps, _stream(stream)),
+           "tile_residual_layernorm_bf16")
+
+
+def _unary_bf16(name):
+    def fn(x, out, eps=1e-5, stream=None):
+        px, rows, width = _matrix(x, "x", "bf16")
+        po, _, _ = _matrix(out, "out", "bf16")
+        _same_shape(x, out, "x/out")
+        _check(getattr(load(), name)(px, po, rows, width, eps, _stream(stream)), name)
+    fn.__name__ = name
+    fn.__doc__ = f"Calls ``{name}`` (see include/tile_rows.h)."
+    return fn
+
+
+tile_layernorm_bf16 = _unary_bf16("tile_layernorm_bf16")
+tile_rmsnorm_bf16 = _unary_bf16("tile_rmsnorm_bf16")
+tile_softmax_bf16 = _unary_bf16("tile_softmax_bf16")
+
+
+def tile_layernorm_affine_bf16(x, residual, gamma, beta, out, eps=1e-5, stream=None):
+    px, rows, width = _matrix(x, "x", "bf16")
+    po, _, _ = _matrix(out, "out", "bf16")
+    _same_shape(x, out, "x/out")
+    pr = None
+    if residual is not None:
+        pr, _, _ = _matrix(residual, "residual", "bf16")
+        _same_shape(x, residual, "x/residual")
+    _check(load().tile_layernorm_affine_bf16(px, pr, _vector(gamma, width, "gamma"),
+                                             _vector(beta, width, "beta"), po, rows, width, eps,
+                                             _stream(stream)), "tile_layernorm_affine_bf16")
+
+
+def tile_rmsnorm_weighted_bf16(x, gamma, out, eps=1e-5, stream=None):
+    px, rows, width = _matrix(x, "x", "bf16")
+    po, _, _ = _matrix(out, "out", "bf16")
+    _same_shape(x, out, "x/out")
+    _check(load().tile_rmsnorm_weighted_bf16(px, _vector(gamma, width, "gamma"), po, rows, width,
+                                             eps, _stream(stream)), "tile_rmsnorm_weighted_bf16")
+
+
+def tile_row_sum_bf16(x, sums, stream=None):
+    px, rows, width = _matrix(x, "x", "bf16")
+    _check(load().tile_row_sum_bf16(px, _vector(sums, rows, "sums"), rows, width, _stream(stream)),
+           "tile_row_sum_bf16")
+
+
+def tile_row_minmax_bf16(x, mins, maxs, stream=None):
+    px, rows, width = _matrix(x, "x", "bf16")
+    _check(load().tile_row_minmax_bf16(px, _vector(mins, rows, "mins"), _vector(maxs, rows, "maxs"),
+                                       rows, width, _stream(stream)), "tile_row_minmax_bf16")
 
 
 def _host_matrix(t, name):
@@ -353,6 +437,27 @@ def tile_describe_plan(op, rows, width):
     op = OPS[op] if isinstance(op, str) else op
     plan = TilePlan()
     _check(load().tile_describe_plan(op, rows, width, ctypes.byref(plan)), "tile_describe_plan")
+    return plan.as_dict()
+
+
+def tile_describe_plan_ex(op, dtype, rows, width):
+    op = OPS[op] if isinstance(op, str) else op
+    dtype = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    plan = TilePlan()
+    _check(load().tile_describe_plan_ex(op, dtype, rows, width, ctypes.byref(plan)),
+           "tile_describe_plan_ex")
+    return plan.as_dict()
+
+
+def tile_plan_info_ex(plan_id, op, dtype, rows, width):
+    """Plan ``plan_id`` for (op, dtype, rows, width), or None if not built / not covering."""
+    op = OPS[op] if isinstance(op, str) else op
+    dtype = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    plan = TilePlan()
+    st = load().tile_plan_info_ex(plan_id, op, dtype, rows, width, ctypes.byref(plan))
+    if st in (-2, -8):
+        return None
+    _check(st, "tile_plan_info_ex")
     return plan.as_dict()
 
 

@@ -5,17 +5,18 @@
 namespace tile {
 constexpr int kMaxDevices = 64;
 
-// Arguments of one row-kernel launch.  x, r: [rows][width] inputs (r:
-// residual LayerNorm only).  gamma, beta: optional per-column scale and
-// shift applied after LayerNorm / RMSNorm (NULL = none).  y: [rows][width]
-// output, or [rows] row sums / row minima; y2: [rows] row maxima (min/max).
+// Arguments of one row-kernel launch.  x, r: [rows][width] inputs of the
+// launch's element type (FP32 or BF16; r: residual LayerNorm only).
+// gamma, beta: optional FP32 per-column scale and shift applied after
+// LayerNorm / RMSNorm (NULL = none).  y: [rows][width] output of the element
+// type, or [rows] FP32 row sums / row minima; y2: [rows] FP32 row maxima.
 // status: the launching op's device error word (filled by the launcher).
 struct RowArgs {
-    const float *x;
-    const float *r;
+    const void *x;
+    const void *r;
     const float *gamma;
     const float *beta;
-    float *y;
+    void *y;
     float *y2;
     long long rows;
     int width;
@@ -32,7 +33,17 @@ TILE_DECLARE_OP(rmsnorm)
 TILE_DECLARE_OP(softmax)
 TILE_DECLARE_OP(row_sum)
 TILE_DECLARE_OP(row_minmax)
+TILE_DECLARE_OP(residual_layernorm_bf16)
+TILE_DECLARE_OP(layernorm_bf16)
+TILE_DECLARE_OP(rmsnorm_bf16)
+TILE_DECLARE_OP(softmax_bf16)
+TILE_DECLARE_OP(row_sum_bf16)
+TILE_DECLARE_OP(row_minmax_bf16)
 #undef TILE_DECLARE_OP
+
+// Largest register stripe (floats per thread) a BF16 plan may use: plans
+// with K * 8 above it are not built for BF16.
+constexpr int kMaxStripeBf16 = 64;
 
 // Pointwise value/derivative pairs (pair_kernel.cu): kind 0 = sigmoid,
 // 1 = tanh-approximate GELU, over n elements.

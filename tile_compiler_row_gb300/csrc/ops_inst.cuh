@@ -1,7 +1,8 @@
-// Instantiates every built plan for one operation and provides its host-side
-// launcher and device error word.  Included once per op by ops_<op>.cu with
-// TILE_INST_OP (tile::OP_*) and TILE_INST_NAME (a C identifier) defined, so
-// the four ops compile as four translation units in parallel.
+// Instantiates every built plan for one operation and element type and
+// provides its host-side launcher and device error word.  Included once per
+// (op, type) by ops_<op>[_bf16].cu with TILE_INST_OP (tile::OP_*),
+// TILE_INST_T (float or __nv_bfloat16) and TILE_INST_NAME (a C identifier)
+// defined, so each compiles as its own translation unit, in parallel.
 #include "row_kernel.cuh"
 #include "plans.h"
 #include "launch.h"
@@ -36,25 +37,33 @@ unsigned int *status_address(cudaError_t *err) {
 
 template <int V, int S, int P, int K, int C>
 cudaError_t launch_plan(RowArgs args, cudaStream_t stream) {
-    cudaError_t err = cudaSuccess;
-    args.status = status_address(&err);
-    if (args.status == nullptr) return err;
-    const long long rows = args.rows;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned int>(((rows + P - 1) / P) * C), 1, 1);
-    cfg.blockDim = dim3(32 * S * P, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    if (C > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = C;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+    constexpr int EV = (V == 4) ? Elem<TILE_INST_T>::kVec : 1;
+    if constexpr (sizeof(TILE_INST_T) == 2 && K * EV > kMaxStripeBf16) {
+        (void)args;
+        (void)stream;
+        return cudaErrorInvalidValue;     // not built: stripe too large for BF16
+    } else {
+        cudaError_t err = cudaSuccess;
+        args.status = status_address(&err);
+        if (args.status == nullptr) return err;
+        const long long rows = args.rows;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned int>(((rows + P - 1) / P) * C), 1, 1);
+        cfg.blockDim = dim3(32 * S * P, 1, 1);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        if (C > 1) {
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = C;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+        }
+        return cudaLaunchKernelEx(&cfg, row_kernel<TILE_INST_OP, TILE_INST_T, V, S, P, K, C>,
+                                  args);
     }
-    return cudaLaunchKernelEx(&cfg, row_kernel<TILE_INST_OP, V, S, P, K, C>, args);
 }
 }  // namespace
 

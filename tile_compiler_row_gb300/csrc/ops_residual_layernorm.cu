@@ -1,4 +1,5 @@
 // residual_layernorm: every built plan (see ops_inst.cuh).
 #define TILE_INST_OP tile::OP_RESLN
+#define TILE_INST_T float
 #define TILE_INST_NAME residual_layernorm
 #include "ops_inst.cuh"

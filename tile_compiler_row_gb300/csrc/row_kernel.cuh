@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <cuda_bf16.h>
 
 #include "launch.h"
 
@@ -33,17 +34,59 @@ enum { OP_RESLN = 0, OP_LN = 1, OP_RMS = 2, OP_SOFTMAX = 3, OP_SUM = 4, OP_MINMA
 enum { STATUS_BAD_LAUNCH = 1u };
 
 // ---------------------------------------------------------------------------
-// memory access: inputs are read once and outputs written once, so both use
-// the streaming cache hint (evict-first).
+// memory access.  Inputs are read once and outputs written once, so both use
+// the streaming cache hint (evict-first).  Elem<T> moves one element or one
+// 16-byte vector (4 FP32 or 8 BF16 values) between memory and FP32
+// registers; BF16 widens exactly and narrows with round-to-nearest-even.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float4 load4(const float *p) {
-    return __ldcs(reinterpret_cast<const float4 *>(p));
-}
-__device__ __forceinline__ float load1(const float *p) { return __ldcs(p); }
-__device__ __forceinline__ void store4(float *p, float4 v) {
-    __stcs(reinterpret_cast<float4 *>(p), v);
-}
-__device__ __forceinline__ void store1(float *p, float v) { __stcs(p, v); }
+template <class T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+    static constexpr int kVec = 4;
+    __device__ static void load_vec(const float *p, float (&v)[4]) {
+        const float4 t = __ldcs(reinterpret_cast<const float4 *>(p));
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    }
+    __device__ static void store_vec(float *p, const float (&v)[4]) {
+        __stcs(reinterpret_cast<float4 *>(p), make_float4(v[0], v[1], v[2], v[3]));
+    }
+    __device__ static float load(const float *p) { return __ldcs(p); }
+    __device__ static void store(float *p, float v) { __stcs(p, v); }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+    __device__ static float widen(unsigned int bits16) { return __uint_as_float(bits16 << 16); }
+    __device__ static unsigned int narrow(float v) {
+        return static_cast<unsigned int>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
+    }
+    __device__ static void load_vec(const __nv_bfloat16 *p, float (&v)[8]) {
+        const uint4 t = __ldcs(reinterpret_cast<const uint4 *>(p));
+        const unsigned int w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = widen(w[i] & 0xffffu);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    __device__ static void store_vec(__nv_bfloat16 *p, const float (&v)[8]) {
+        uint4 t;
+        t.x = narrow(v[0]) | (narrow(v[1]) << 16);
+        t.y = narrow(v[2]) | (narrow(v[3]) << 16);
+        t.z = narrow(v[4]) | (narrow(v[5]) << 16);
+        t.w = narrow(v[6]) | (narrow(v[7]) << 16);
+        __stcs(reinterpret_cast<uint4 *>(p), t);
+    }
+    __device__ static float load(const __nv_bfloat16 *p) {
+        return widen(__ldcs(reinterpret_cast<const unsigned short *>(p)));
+    }
+    __device__ static void store(__nv_bfloat16 *p, float v) {
+        __stcs(reinterpret_cast<unsigned short *>(p), static_cast<unsigned short>(narrow(v)));
+    }
+};
 
 // ---------------------------------------------------------------------------
 // cluster primitives (inline PTX)
@@ -194,9 +237,11 @@ __device__ __forceinline__ void row_allreduce_comp(float &s, float &c, float *pa
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int OP, int V, int S, int P, int K, int C>
+template <int OP, class T, int V, int S, int P, int K, int C>
 __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
-    static_assert(V == 1 || V == 4, "V is 1 or 4");
+    static_assert(V == 1 || V == 4, "V is 1 (scalar) or 4 (16-byte vectors)");
+    // elements per access: one 16-byte vector (4 FP32 or 8 BF16), or one
+    constexpr int EV = (V == 4) ? Elem<T>::kVec : 1;
     static_assert(C == 1 || P == 1, "a cluster row has one program per CTA");
     static_assert(32 * S * P <= 1024, "at most 1024 threads per CTA");
     constexpr int W = 32 * S;
@@ -232,45 +277,48 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
     if (!active) row = a.rows - 1;                // replay the last row
 
     const long long base = row * static_cast<long long>(width);
-    const float *xr = a.x + base;
-    const float *rr = (OP == OP_RESLN) ? a.r + base : nullptr;
-    float *yr = kRowOutput ? nullptr : a.y + base;
+    const T *xr = static_cast<const T *>(a.x) + base;
+    const T *rr = (OP == OP_RESLN) ? static_cast<const T *>(a.r) + base : nullptr;
+    T *yr = kRowOutput ? nullptr : static_cast<T *>(a.y) + base;
 
     // Row geometry.  V = 4: h scalars up to the first 16-byte boundary, then
-    // nb float4s, then tl scalars.  All row pointers share the 16-byte phase.
+    // nb vectors of EV elements, then tl scalars.  All row pointers share the
+    // 16-byte phase.
     int h = 0, tl = 0, nb;
     if constexpr (V == 4) {
-        const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(xr) >> 2) & 3);
-        h = (4 - mis) & 3;
+        const int mis =
+            static_cast<int>((reinterpret_cast<uintptr_t>(xr) / sizeof(T)) & (EV - 1));
+        h = (EV - mis) & (EV - 1);
         if (h > width) h = width;
-        nb = (width - h) >> 2;
-        tl = width - h - (nb << 2);
+        nb = (width - h) / EV;
+        tl = width - h - nb * EV;
     } else {
         nb = width;
     }
     const int gw = rank * W + worker;
 
     // ---- a1: load the row once into the register stripe ----------------
-    float v[K][V];
+    float v[K][EV];
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         const int i = k * (C * W) + gw;
         if (i < nb) {
             if constexpr (V == 4) {
-                float4 t = load4(xr + h + 4 * i);
+                Elem<T>::load_vec(xr + h + EV * i, v[k]);
                 if constexpr (OP == OP_RESLN) {
-                    const float4 b = load4(rr + h + 4 * i);
-                    t.x += b.x; t.y += b.y; t.z += b.z; t.w += b.w;
+                    float b[EV];
+                    Elem<T>::load_vec(rr + h + EV * i, b);
+#pragma unroll
+                    for (int j = 0; j < EV; ++j) v[k][j] += b[j];
                 }
-                v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
             } else {
-                float t = load1(xr + i);
-                if constexpr (OP == OP_RESLN) t += load1(rr + i);
+                float t = Elem<T>::load(xr + i);
+                if constexpr (OP == OP_RESLN) t += Elem<T>::load(rr + i);
                 v[k][0] = t;
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < V; ++j) v[k][j] = kFill;
+            for (int j = 0; j < EV; ++j) v[k][j] = kFill;
         }
     }
     bool has_h = false, has_t = false;
@@ -279,14 +327,14 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
     if constexpr (V == 4) {
         has_h = (rank == 0) && (worker < h);
         has_t = (rank == 0) && (worker < tl);
-        te = h + 4 * nb + worker;
+        te = h + EV * nb + worker;
         if (has_h) {
-            hv = load1(xr + worker);
-            if constexpr (OP == OP_RESLN) hv += load1(rr + worker);
+            hv = Elem<T>::load(xr + worker);
+            if constexpr (OP == OP_RESLN) hv += Elem<T>::load(rr + worker);
         }
         if (has_t) {
-            tv = load1(xr + te);
-            if constexpr (OP == OP_RESLN) tv += load1(rr + te);
+            tv = Elem<T>::load(xr + te);
+            if constexpr (OP == OP_RESLN) tv += Elem<T>::load(rr + te);
         }
     }
 
@@ -299,7 +347,7 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
         for (int k = 0; k < K; ++k) {
             float t = v[k][0];
 #pragma unroll
-            for (int j = 1; j < V; ++j) t += v[k][j];
+            for (int j = 1; j < EV; ++j) t += v[k][j];
             s[0] += t;
         }
         row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
@@ -310,7 +358,7 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
         for (int k = 0; k < K; ++k) {
             const bool ok = k * (C * W) + gw < nb;
 #pragma unroll
-            for (int j = 0; j < V; ++j) {
+            for (int j = 0; j < EV; ++j) {
                 const float d = ok ? v[k][j] - mean0 : 0.0f;
                 v[k][j] = d;
                 q[0] += d;
@@ -329,7 +377,7 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
-            for (int j = 0; j < V; ++j) v[k][j] = (v[k][j] - mu1) * rstd;
+            for (int j = 0; j < EV; ++j) v[k][j] = (v[k][j] - mu1) * rstd;
         hv = (hv - mu1) * rstd;
         tv = (tv - mu1) * rstd;
     } else if constexpr (OP == OP_RMS) {
@@ -338,13 +386,13 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
-            for (int j = 0; j < V; ++j) s[0] = fmaf(v[k][j], v[k][j], s[0]);
+            for (int j = 0; j < EV; ++j) s[0] = fmaf(v[k][j], v[k][j], s[0]);
         row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
         const float rstd = 1.0f / sqrtf(s[0] / n + a.eps);
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
-            for (int j = 0; j < V; ++j) v[k][j] *= rstd;
+            for (int j = 0; j < EV; ++j) v[k][j] *= rstd;
         hv *= rstd;
         tv *= rstd;
     } else if constexpr (OP == OP_SOFTMAX) {
@@ -353,7 +401,7 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
-            for (int j = 0; j < V; ++j) m[0] = fmaxf(m[0], v[k][j]);
+            for (int j = 0; j < EV; ++j) m[0] = fmaxf(m[0], v[k][j]);
         row_allreduce<Max, 1, S, P, C>(m, part1, cpart, program, warp, lane);
         const float mx = m[0];
         // ---- a3: exponentiate in place (exp(-inf) = 0), reduce the sum ---
@@ -361,7 +409,7 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
-            for (int j = 0; j < V; ++j) {
+            for (int j = 0; j < EV; ++j) {
                 const float e = expf(v[k][j] - mx);
                 v[k][j] = e;
                 s[0] += e;
@@ -374,7 +422,7 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
-            for (int j = 0; j < V; ++j) v[k][j] *= inv;
+            for (int j = 0; j < EV; ++j) v[k][j] *= inv;
         hv *= inv;
         tv *= inv;
     } else if constexpr (OP == OP_SUM) {
@@ -383,7 +431,7 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
-            for (int j = 0; j < V; ++j) comp_add(s, c, v[k][j]);
+            for (int j = 0; j < EV; ++j) comp_add(s, c, v[k][j]);
         comp_add(s, c, hv);
         comp_add(s, c, tv);
         row_allreduce_comp<S, P, C>(s, c, part1, cpart, program, warp, lane);
@@ -394,7 +442,7 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
-            for (int j = 0; j < V; ++j) {
+            for (int j = 0; j < EV; ++j) {
                 m[0] = fmaxf(m[0], v[k][j]);
                 m[1] = fmaxf(m[1], -v[k][j]);
             }
@@ -419,28 +467,35 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
             for (int k = 0; k < K; ++k) {
                 const int i = k * (C * W) + gw;
                 if (i < nb) {
-                    const int col = (V == 4) ? h + 4 * i : i;
-                    float gg[V], bb[V];
+                    const int col = (V == 4) ? h + EV * i : i;
+                    float gg[EV], bb[EV];
                     bool loaded = false;
                     if constexpr (V == 4) {
                         if (gvec) {
-                            const float4 g4 = __ldg(reinterpret_cast<const float4 *>(g + col));
-                            gg[0] = g4.x; gg[1] = g4.y; gg[2] = g4.z; gg[3] = g4.w;
-                            float4 b4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                            if (b != nullptr) b4 = __ldg(reinterpret_cast<const float4 *>(b + col));
-                            bb[0] = b4.x; bb[1] = b4.y; bb[2] = b4.z; bb[3] = b4.w;
+#pragma unroll
+                            for (int q = 0; q < EV / 4; ++q) {
+                                const float4 g4 =
+                                    __ldg(reinterpret_cast<const float4 *>(g + col) + q);
+                                gg[4 * q] = g4.x; gg[4 * q + 1] = g4.y;
+                                gg[4 * q + 2] = g4.z; gg[4 * q + 3] = g4.w;
+                                float4 b4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                                if (b != nullptr)
+                                    b4 = __ldg(reinterpret_cast<const float4 *>(b + col) + q);
+                                bb[4 * q] = b4.x; bb[4 * q + 1] = b4.y;
+                                bb[4 * q + 2] = b4.z; bb[4 * q + 3] = b4.w;
+                            }
                             loaded = true;
                         }
                     }
                     if (!loaded) {
 #pragma unroll
-                        for (int j = 0; j < V; ++j) {
+                        for (int j = 0; j < EV; ++j) {
                             gg[j] = __ldg(g + col + j);
                             bb[j] = b != nullptr ? __ldg(b + col + j) : 0.0f;
                         }
                     }
 #pragma unroll
-                    for (int j = 0; j < V; ++j) v[k][j] = fmaf(v[k][j], gg[j], bb[j]);
+                    for (int j = 0; j < EV; ++j) v[k][j] = fmaf(v[k][j], gg[j], bb[j]);
                 }
             }
             if constexpr (V == 4) {
@@ -457,7 +512,7 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
     // ---- a4: streaming stores, predicated for replayed programs ---------
     if constexpr (kRowOutput) {
         if (active && worker == 0 && rank == 0) {
-            a.y[row] = row_out0;
+            static_cast<float *>(a.y)[row] = row_out0;
             if constexpr (OP == OP_MINMAX) a.y2[row] = row_out1;
         }
     } else {
@@ -467,14 +522,14 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
                 const int i = k * (C * W) + gw;
                 if (i < nb) {
                     if constexpr (V == 4)
-                        store4(yr + h + 4 * i, make_float4(v[k][0], v[k][1], v[k][2], v[k][3]));
+                        Elem<T>::store_vec(yr + h + EV * i, v[k]);
                     else
-                        store1(yr + i, v[k][0]);
+                        Elem<T>::store(yr + i, v[k][0]);
                 }
             }
             if constexpr (V == 4) {
-                if (has_h) store1(yr + worker, hv);
-                if (has_t) store1(yr + te, tv);
+                if (has_h) Elem<T>::store(yr + worker, hv);
+                if (has_t) Elem<T>::store(yr + te, tv);
             }
         }
     }

@@ -26,13 +26,26 @@ constexpr long long capacity(const PlanDesc &p) {
     return static_cast<long long>(p.K) * 32 * p.S * p.C;
 }
 
-bool covers(const PlanDesc &p, int width) {
-    if (width < 1) return false;
-    return p.V == 4 ? (width / 4) <= capacity(p) : width <= capacity(p);
+// Elements per access of a plan for an element type: a 16-byte vector
+// (4 FP32 or 8 BF16) for V = 4 plans, one element for V = 1 plans.
+int elems_per_vec(const PlanDesc &p, int dtype) {
+    return p.V == 4 ? (dtype == TILE_DTYPE_BF16 ? 8 : 4) : 1;
 }
 
-int max_width_of(const PlanDesc &p) {
-    const long long w = p.V == 4 ? capacity(p) * 4 + 3 : capacity(p);
+// BF16 plans whose stripe would exceed the register budget are not built.
+bool built(const PlanDesc &p, int dtype) {
+    return dtype != TILE_DTYPE_BF16 || p.K * elems_per_vec(p, dtype) <= tile::kMaxStripeBf16;
+}
+
+bool covers(const PlanDesc &p, int width, int dtype = TILE_DTYPE_F32) {
+    if (width < 1 || !built(p, dtype)) return false;
+    const int ev = elems_per_vec(p, dtype);
+    return (width / ev) <= capacity(p);
+}
+
+int max_width_of(const PlanDesc &p, int dtype = TILE_DTYPE_F32) {
+    const int ev = elems_per_vec(p, dtype);
+    const long long w = capacity(p) * ev + (ev - 1);
     return w > TILE_MAX_WIDTH ? TILE_MAX_WIDTH : static_cast<int>(w);
 }
 
@@ -89,10 +102,24 @@ int pick(const Bucket (&table)[N], int width) {
     return -1;
 }
 
-int select_plan(int op, long long rows, int width, bool vec4, bool residual) {
+const Bucket *table_of(int op, int *n);
+
+// BF16 rows move half the bytes of FP32 rows of the same width: a BF16 row
+// takes the FP32 bucket of the same row bytes, then the first plan from there
+// on that is built for BF16 and covers the width.
+int select_plan(int op, long long rows, int width, bool vec4, int dtype) {
     (void)rows;
-    (void)residual;
     if (!vec4) return pick(kVec1, width);
+    if (dtype == TILE_DTYPE_BF16) {
+        int n = 0;
+        const Bucket *t = table_of(op, &n);
+        const int equiv = (width + 1) / 2;
+        int i = 0;
+        while (i < n && equiv > t[i].max_width) ++i;
+        for (; i < n; ++i)
+            if (covers(kPlans[t[i].plan], width, dtype)) return t[i].plan;
+        return -1;
+    }
     switch (op) {
         case TILE_OP_RESIDUAL_LAYERNORM: return pick(kVec4ResidualLN, width);
         case TILE_OP_LAYERNORM: return pick(kVec4LN, width);
@@ -105,25 +132,45 @@ int select_plan(int op, long long rows, int width, bool vec4, bool residual) {
     }
 }
 
+const Bucket *table_of(int op, int *n) {
+#define TILE_TABLE(t) \
+    do {                                   \
+        *n = sizeof(t) / sizeof(t[0]);     \
+        return t;                          \
+    } while (0)
+    switch (op) {
+        case TILE_OP_RESIDUAL_LAYERNORM: TILE_TABLE(kVec4ResidualLN);
+        case TILE_OP_LAYERNORM: TILE_TABLE(kVec4LN);
+        case TILE_OP_LAYERNORM_AFFINE: TILE_TABLE(kVec4Affine);
+        case TILE_OP_RMSNORM: TILE_TABLE(kVec4RMS);
+        case TILE_OP_RMSNORM_WEIGHTED: TILE_TABLE(kVec4Weighted);
+        case TILE_OP_ROW_SUM:
+        case TILE_OP_ROW_MINMAX: TILE_TABLE(kVec4RowReduce);
+        default: TILE_TABLE(kVec4Softmax);
+    }
+#undef TILE_TABLE
+}
+
 long long grid_of(const PlanDesc &p, long long rows) {
     return ((rows + p.P - 1) / p.P) * p.C;
 }
 
-void fill_plan(const PlanDesc &p, int op, int rows, int width, tile_plan_t *out) {
+void fill_plan(const PlanDesc &p, int op, int dtype, int rows, int width, tile_plan_t *out) {
     out->op = op;
     out->rows = rows;
     out->width = width;
     out->id = p.id;
     out->path = p.C > 1 ? TILE_PATH_CLUSTER : TILE_PATH_CTA;
-    out->vec = p.V;
+    out->vec = elems_per_vec(p, dtype);
     out->warps_per_program = p.S;
     out->programs_per_cta = p.P;
     out->chunks = p.K;
     out->cluster = p.C;
     out->threads = 32 * p.S * p.P;
     out->workers = 32 * p.S;
-    out->stripe_floats = p.K * p.V;
-    out->max_width = max_width_of(p);
+    out->stripe_floats = p.K * elems_per_vec(p, dtype);
+    out->max_width = max_width_of(p, dtype);
+    out->dtype = dtype;
     const int part = p.S > 1 ? 3 * p.P * p.S : 0;
     out->smem_bytes = 4 * (part + (p.C > 1 ? 4 : 0));
     const int phases = (op == TILE_OP_RESIDUAL_LAYERNORM || op == TILE_OP_LAYERNORM ||
@@ -153,14 +200,17 @@ bool row_output(int op) { return op == TILE_OP_ROW_SUM || op == TILE_OP_ROW_MINM
 // does not use are cleared, so the kernel never sees them.
 struct Call {
     int op;
-    const float *in, *res, *gamma, *beta;
-    float *out, *out2;
+    int dtype;
+    const void *in, *res;
+    const float *gamma, *beta;
+    void *out;
+    float *out2;
     int rows, width;
     float eps;
 };
 
 Call make_call(int op, const tile_row_args_t &a) {
-    Call c{op, a.in, nullptr, nullptr, nullptr, a.out, nullptr, a.rows, a.width, a.eps};
+    Call c{op, a.dtype, a.in, nullptr, nullptr, nullptr, a.out, nullptr, a.rows, a.width, a.eps};
     if (op == TILE_OP_RESIDUAL_LAYERNORM || op == TILE_OP_LAYERNORM_AFFINE) c.res = a.residual;
     if (op == TILE_OP_LAYERNORM_AFFINE || op == TILE_OP_RMSNORM_WEIGHTED) c.gamma = a.gamma;
     if (op == TILE_OP_LAYERNORM_AFFINE) c.beta = a.beta;
@@ -178,9 +228,16 @@ bool coaligned16(const Call &c) {
 
 // Checks shared by every row entry point.  Returns TILE_OK with *noop set
 // when there is nothing to launch.  No CUDA call is made.
+size_t elem_size(int dtype) { return dtype == TILE_DTYPE_BF16 ? 2 : 4; }
+
+bool misaligned_to(const void *p, size_t bytes) {
+    return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) != 0;
+}
+
 int validate(const Call &c, bool *noop) {
     *noop = false;
     if (!valid_op(c.op)) return TILE_ERR_OP;
+    if (c.dtype != TILE_DTYPE_F32 && c.dtype != TILE_DTYPE_BF16) return TILE_ERR_DTYPE;
     if (c.rows < 0 || c.width < 1 || c.width > TILE_MAX_WIDTH) return TILE_ERR_SHAPE;
     if (is_normaliser(c.op) && !(std::isfinite(c.eps) && c.eps >= 0.0f)) return TILE_ERR_EPS;
     if (c.rows == 0) {
@@ -192,11 +249,14 @@ int validate(const Call &c, bool *noop) {
     if ((c.op == TILE_OP_LAYERNORM_AFFINE || c.op == TILE_OP_RMSNORM_WEIGHTED) && c.gamma == nullptr)
         return TILE_ERR_NULL;
     if (c.op == TILE_OP_ROW_MINMAX && c.out2 == nullptr) return TILE_ERR_NULL;
-    for (const void *p : {static_cast<const void *>(c.in), static_cast<const void *>(c.res),
-                          static_cast<const void *>(c.gamma), static_cast<const void *>(c.beta),
-                          static_cast<const void *>(c.out), static_cast<const void *>(c.out2)})
+    const size_t es = elem_size(c.dtype);
+    if (misaligned_to(c.in, es) || misaligned_to(c.res, es) ||
+        misaligned_to(c.out, row_output(c.op) ? sizeof(float) : es))
+        return TILE_ERR_ALIGN;
+    for (const void *p : {static_cast<const void *>(c.gamma), static_cast<const void *>(c.beta),
+                          static_cast<const void *>(c.out2)})
         if (misaligned(p)) return TILE_ERR_ALIGN;
-    const size_t mat = static_cast<size_t>(c.rows) * static_cast<size_t>(c.width) * sizeof(float);
+    const size_t mat = static_cast<size_t>(c.rows) * static_cast<size_t>(c.width) * es;
     const size_t vec = static_cast<size_t>(c.width) * sizeof(float);
     const size_t out_bytes = row_output(c.op) ? static_cast<size_t>(c.rows) * sizeof(float) : mat;
     const size_t out2_bytes = static_cast<size_t>(c.rows) * sizeof(float);
@@ -211,19 +271,42 @@ int launch(const Call &c, int plan_id, cudaStream_t stream) {
     const PlanDesc &p = kPlans[plan_id];
     if (grid_of(p, c.rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
     tile::RowArgs a{c.in, c.res, c.gamma, c.beta, c.out, c.out2, c.rows, c.width, c.eps, nullptr};
+    const bool bf = c.dtype == TILE_DTYPE_BF16;
     cudaError_t err;
     switch (c.op) {
-        case TILE_OP_RESIDUAL_LAYERNORM: err = tile::launch_residual_layernorm(plan_id, a, stream); break;
-        case TILE_OP_LAYERNORM: err = tile::launch_layernorm(plan_id, a, stream); break;
+        case TILE_OP_RESIDUAL_LAYERNORM:
+            err = bf ? tile::launch_residual_layernorm_bf16(plan_id, a, stream)
+                     : tile::launch_residual_layernorm(plan_id, a, stream);
+            break;
+        case TILE_OP_LAYERNORM:
+            err = bf ? tile::launch_layernorm_bf16(plan_id, a, stream)
+                     : tile::launch_layernorm(plan_id, a, stream);
+            break;
         case TILE_OP_LAYERNORM_AFFINE:
-            err = c.res != nullptr ? tile::launch_residual_layernorm(plan_id, a, stream)
-                                   : tile::launch_layernorm(plan_id, a, stream);
+            if (c.res != nullptr)
+                err = bf ? tile::launch_residual_layernorm_bf16(plan_id, a, stream)
+                         : tile::launch_residual_layernorm(plan_id, a, stream);
+            else
+                err = bf ? tile::launch_layernorm_bf16(plan_id, a, stream)
+                         : tile::launch_layernorm(plan_id, a, stream);
             break;
         case TILE_OP_RMSNORM:
-        case TILE_OP_RMSNORM_WEIGHTED: err = tile::launch_rmsnorm(plan_id, a, stream); break;
-        case TILE_OP_ROW_SUM: err = tile::launch_row_sum(plan_id, a, stream); break;
-        case TILE_OP_ROW_MINMAX: err = tile::launch_row_minmax(plan_id, a, stream); break;
-        default: err = tile::launch_softmax(plan_id, a, stream); break;
+        case TILE_OP_RMSNORM_WEIGHTED:
+            err = bf ? tile::launch_rmsnorm_bf16(plan_id, a, stream)
+                     : tile::launch_rmsnorm(plan_id, a, stream);
+            break;
+        case TILE_OP_ROW_SUM:
+            err = bf ? tile::launch_row_sum_bf16(plan_id, a, stream)
+                     : tile::launch_row_sum(plan_id, a, stream);
+            break;
+        case TILE_OP_ROW_MINMAX:
+            err = bf ? tile::launch_row_minmax_bf16(plan_id, a, stream)
+                     : tile::launch_row_minmax(plan_id, a, stream);
+            break;
+        default:
+            err = bf ? tile::launch_softmax_bf16(plan_id, a, stream)
+                     : tile::launch_softmax(plan_id, a, stream);
+            break;
     }
     if (err != cudaSuccess) {
         tile::set_last_cuda_error(static_cast<int>(err));
@@ -236,7 +319,7 @@ int run_call(const Call &c, cudaStream_t stream) {
     bool noop = false;
     const int st = validate(c, &noop);
     if (st != TILE_OK || noop) return st;
-    const int plan = select_plan(c.op, c.rows, c.width, coaligned16(c), c.res != nullptr);
+    const int plan = select_plan(c.op, c.rows, c.width, coaligned16(c), c.dtype);
     if (plan < 0) return TILE_ERR_SHAPE;
     return launch(c, plan, stream);
 }
@@ -245,16 +328,18 @@ int run_call_plan(const Call &c, int plan_id, cudaStream_t stream) {
     bool noop = false;
     const int st = validate(c, &noop);
     if (st != TILE_OK) return st;
-    if (plan_id < 0 || plan_id >= TILE_PLAN_COUNT || !covers(kPlans[plan_id], c.width))
+    if (plan_id < 0 || plan_id >= TILE_PLAN_COUNT || !covers(kPlans[plan_id], c.width, c.dtype))
         return TILE_ERR_PLAN;
     if (noop) return TILE_OK;
     if (kPlans[plan_id].V == 4 && !coaligned16(c)) return TILE_ERR_PLAN;
     return launch(c, plan_id, stream);
 }
 
-tile_row_args_t args_of(const float *in, const float *res, const float *gamma, const float *beta,
-                        float *out, float *out2, int rows, int width, float eps) {
+tile_row_args_t args_of(const void *in, const void *res, const float *gamma, const float *beta,
+                        void *out, float *out2, int rows, int width, float eps,
+                        int dtype = TILE_DTYPE_F32) {
     tile_row_args_t a;
+    a.dtype = dtype;
     a.in = in;
     a.residual = res;
     a.gamma = gamma;
@@ -354,6 +439,70 @@ int tile_row_minmax_f32(const float *in, float *mins, float *maxs, int rows, int
                     stream);
 }
 
+int tile_residual_layernorm_bf16(const void *in, const void *residual, void *out, int rows,
+                                 int width, float eps, cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_RESIDUAL_LAYERNORM,
+                              args_of(in, residual, nullptr, nullptr, out, nullptr, rows, width,
+                                      eps, TILE_DTYPE_BF16)),
+                    stream);
+}
+
+int tile_layernorm_bf16(const void *in, void *out, int rows, int width, float eps,
+                        cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_LAYERNORM, args_of(in, nullptr, nullptr, nullptr, out,
+                                                         nullptr, rows, width, eps,
+                                                         TILE_DTYPE_BF16)),
+                    stream);
+}
+
+int tile_rmsnorm_bf16(const void *in, void *out, int rows, int width, float eps,
+                      cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_RMSNORM, args_of(in, nullptr, nullptr, nullptr, out,
+                                                       nullptr, rows, width, eps,
+                                                       TILE_DTYPE_BF16)),
+                    stream);
+}
+
+int tile_softmax_bf16(const void *in, void *out, int rows, int width, float eps,
+                      cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_SOFTMAX, args_of(in, nullptr, nullptr, nullptr, out,
+                                                       nullptr, rows, width, eps,
+                                                       TILE_DTYPE_BF16)),
+                    stream);
+}
+
+int tile_layernorm_affine_bf16(const void *in, const void *residual, const float *gamma,
+                               const float *beta, void *out, int rows, int width, float eps,
+                               cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_LAYERNORM_AFFINE,
+                              args_of(in, residual, gamma, beta, out, nullptr, rows, width, eps,
+                                      TILE_DTYPE_BF16)),
+                    stream);
+}
+
+int tile_rmsnorm_weighted_bf16(const void *in, const float *gamma, void *out, int rows,
+                               int width, float eps, cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_RMSNORM_WEIGHTED,
+                              args_of(in, nullptr, gamma, nullptr, out, nullptr, rows, width, eps,
+                                      TILE_DTYPE_BF16)),
+                    stream);
+}
+
+int tile_row_sum_bf16(const void *in, float *sums, int rows, int width, cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_ROW_SUM, args_of(in, nullptr, nullptr, nullptr, sums,
+                                                       nullptr, rows, width, 0.0f,
+                                                       TILE_DTYPE_BF16)),
+                    stream);
+}
+
+int tile_row_minmax_bf16(const void *in, float *mins, float *maxs, int rows, int width,
+                         cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_ROW_MINMAX, args_of(in, nullptr, nullptr, nullptr, mins,
+                                                          maxs, rows, width, 0.0f,
+                                                          TILE_DTYPE_BF16)),
+                    stream);
+}
+
 int tile_run_plan_args_f32(int op, int plan_id, const tile_row_args_t *args, cudaStream_t stream) {
     if (args == nullptr) return TILE_ERR_NULL;
     return run_call_plan(make_call(op, *args), plan_id, stream);
@@ -367,26 +516,37 @@ int tile_run_plan_f32(int op, int plan_id, const float *in, const float *residua
                          plan_id, stream);
 }
 
-int tile_describe_plan(int op, int rows, int width, tile_plan_t *plan) {
+int tile_describe_plan_ex(int op, int dtype, int rows, int width, tile_plan_t *plan) {
     if (!valid_op(op)) return TILE_ERR_OP;
+    if (dtype != TILE_DTYPE_F32 && dtype != TILE_DTYPE_BF16) return TILE_ERR_DTYPE;
     if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH) return TILE_ERR_SHAPE;
     if (plan == nullptr) return TILE_ERR_NULL;
-    const int id = select_plan(op, rows, width, true, false);
+    const int id = select_plan(op, rows, width, true, dtype);
     if (id < 0) return TILE_ERR_SHAPE;
-    fill_plan(kPlans[id], op, rows, width, plan);
+    fill_plan(kPlans[id], op, dtype, rows, width, plan);
     return TILE_OK;
+}
+
+int tile_describe_plan(int op, int rows, int width, tile_plan_t *plan) {
+    return tile_describe_plan_ex(op, TILE_DTYPE_F32, rows, width, plan);
 }
 
 int tile_plan_count(void) { return TILE_PLAN_COUNT; }
 
-int tile_plan_info(int id, int op, int rows, int width, tile_plan_t *plan) {
+int tile_plan_info_ex(int id, int op, int dtype, int rows, int width, tile_plan_t *plan) {
     if (id < 0 || id >= TILE_PLAN_COUNT) return TILE_ERR_PLAN;
     if (!valid_op(op)) return TILE_ERR_OP;
-    if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH || !covers(kPlans[id], width))
+    if (dtype != TILE_DTYPE_F32 && dtype != TILE_DTYPE_BF16) return TILE_ERR_DTYPE;
+    if (!built(kPlans[id], dtype)) return TILE_ERR_PLAN;
+    if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH || !covers(kPlans[id], width, dtype))
         return TILE_ERR_SHAPE;
     if (plan == nullptr) return TILE_ERR_NULL;
-    fill_plan(kPlans[id], op, rows, width, plan);
+    fill_plan(kPlans[id], op, dtype, rows, width, plan);
     return TILE_OK;
+}
+
+int tile_plan_info(int id, int op, int rows, int width, tile_plan_t *plan) {
+    return tile_plan_info_ex(id, op, TILE_DTYPE_F32, rows, width, plan);
 }
 
 int tile_max_width(void) { return TILE_MAX_WIDTH; }
@@ -406,6 +566,7 @@ const char *tile_status_string(int status) {
         case TILE_ERR_PLAN: return "the plan does not exist, cannot cover the width, or needs 16-byte co-aligned pointers";
         case TILE_ERR_DEVICE: return "a kernel recorded an error in the device status word";
         case TILE_ERR_WORKSPACE: return "the device workspace cannot hold one row chunk twice";
+        case TILE_ERR_DTYPE: return "unknown element type code";
         default: return "unknown status";
     }
 }
@@ -414,7 +575,10 @@ int tile_check_device_status(cudaStream_t stream) {
     unsigned int word = 0, v = 0;
     cudaError_t (*fetch[])(unsigned int *, cudaStream_t) = {
         tile::status_residual_layernorm, tile::status_layernorm, tile::status_rmsnorm,
-        tile::status_softmax, tile::status_row_sum, tile::status_row_minmax, tile::status_pairs};
+        tile::status_softmax, tile::status_row_sum, tile::status_row_minmax,
+        tile::status_residual_layernorm_bf16, tile::status_layernorm_bf16,
+        tile::status_rmsnorm_bf16, tile::status_softmax_bf16, tile::status_row_sum_bf16,
+        tile::status_row_minmax_bf16, tile::status_pairs};
     for (auto f : fetch) {
         v = 0;
         const cudaError_t err = f(&v, stream);
