@@ -60,6 +60,13 @@ class Oracle:
         lib.oracle_row_minmax.argtypes = [f32p, f64p, f64p, L, L]
         lib.oracle_sigmoid_pair.argtypes = [f32p, f64p, f64p, L]
         lib.oracle_gelu_tanh_pair.argtypes = [f32p, f64p, f64p, L]
+        lib.oracle_layernorm_backward.argtypes = [f32p, f32p, f32p, f64p, L, L, D]
+        lib.oracle_rmsnorm_backward.argtypes = [f32p, f32p, f32p, f64p, L, L, D]
+        lib.oracle_softmax_backward.argtypes = [f32p, f32p, f64p, L, L]
+        lib.oracle_norm_param_grad.argtypes = [f32p, f32p, f64p, f64p, L, L, D, ctypes.c_int]
+        for fn in (lib.oracle_layernorm_backward, lib.oracle_rmsnorm_backward,
+                   lib.oracle_softmax_backward, lib.oracle_norm_param_grad):
+            fn.restype = None
         for fn in (lib.oracle_residual_layernorm, lib.oracle_layernorm,
                    lib.oracle_rmsnorm, lib.oracle_softmax, lib.oracle_layernorm_affine,
                    lib.oracle_rmsnorm_weighted, lib.oracle_row_sum, lib.oracle_row_minmax,
@@ -181,6 +188,48 @@ class Oracle:
     def gelu_tanh_pair(self, x):
         """(tanh-GELU(x), its derivative) elementwise, any shape."""
         return self._pair(self._lib.oracle_gelu_tanh_pair, x)
+
+    def layernorm_backward(self, x, dy, gamma=None, eps=1e-5):
+        """dx of LayerNorm(x) * gamma (gamma optional) for upstream gradient dy."""
+        return self._backward(self._lib.oracle_layernorm_backward, x, dy, gamma, eps)
+
+    def rmsnorm_backward(self, x, dy, gamma=None, eps=1e-5):
+        return self._backward(self._lib.oracle_rmsnorm_backward, x, dy, gamma, eps)
+
+    def _backward(self, fn, x, dy, gamma, eps):
+        x, dy = self._f32(x), self._f32(dy)
+        if x.shape != dy.shape:
+            raise ValueError("x and dy shapes differ")
+        g = self._vec(gamma, x.shape[1], "gamma") if gamma is not None else None
+        out = np.empty(x.shape, dtype=np.float64)
+        if x.size:
+            fn(self._p(x, ctypes.c_float), self._p(g, ctypes.c_float) if g is not None else None,
+               self._p(dy, ctypes.c_float), self._p(out, ctypes.c_double), x.shape[0], x.shape[1],
+               float(eps))
+        return out
+
+    def softmax_backward(self, y, dy):
+        """dx of softmax given its output y and upstream gradient dy."""
+        y, dy = self._f32(y), self._f32(dy)
+        if y.shape != dy.shape:
+            raise ValueError("y and dy shapes differ")
+        out = np.empty(y.shape, dtype=np.float64)
+        if y.size:
+            self._lib.oracle_softmax_backward(self._p(y, ctypes.c_float), self._p(dy, ctypes.c_float),
+                                              self._p(out, ctypes.c_double), y.shape[0], y.shape[1])
+        return out
+
+    def norm_param_grad(self, x, dy, eps=1e-5, rms=False):
+        """(dgamma, dbeta) summed over rows (dbeta None for RMSNorm)."""
+        x, dy = self._f32(x), self._f32(dy)
+        width = x.shape[1]
+        dg = np.empty(width, dtype=np.float64)
+        db = None if rms else np.empty(width, dtype=np.float64)
+        self._lib.oracle_norm_param_grad(
+            self._p(x, ctypes.c_float), self._p(dy, ctypes.c_float), self._p(dg, ctypes.c_double),
+            self._p(db, ctypes.c_double) if db is not None else None, x.shape[0], width,
+            float(eps), int(bool(rms)))
+        return dg, db
 
     def run(self, op: str, x, r=None, eps=1e-5):
         """Dispatch by library op name."""

@@ -244,3 +244,124 @@ void oracle_gelu_tanh_pair(const float *x, double *y, double *dy, long n)
         dy[k] = 0.5 * (1.0 + t) + 0.5 * v * (1.0 - t * t) * c * (1.0 + 3.0 * a * v * v);
     }
 }
+
+/* ------------------------------------------------------------------------
+ * Backward passes (gradients with respect to the inputs and the per-column
+ * parameters).  The pages do not cover backward normalisation ("Residual
+ * LayerNorm shared-Tile materialization search", last paragraph); these are
+ * the chain rule applied to the forward definitions above, with
+ * xhat = (x - mean) * rstd (LayerNorm) or x * rstd (RMSNorm),
+ * rstd = 1/sqrt(var + eps) or 1/sqrt(mean(x^2) + eps), and g = dy * gamma
+ * (gamma = 1 when NULL):
+ *   LayerNorm:  dx = rstd * (g - mean(g) - xhat * mean(g * xhat))
+ *   RMSNorm:    dx = rstd * (g - xhat * mean(g * xhat))
+ *   softmax:    dx = y * (dy - sum(dy * y))        (from the forward output y)
+ *   parameters: dgamma[j] = sum_rows dy * xhat,  dbeta[j] = sum_rows dy.
+ * ------------------------------------------------------------------------ */
+
+/* dx of y = LayerNorm(x) * gamma (+ beta); gamma may be NULL. */
+void oracle_layernorm_backward(const float *x, const float *gamma, const float *dy, double *dx,
+                               long rows, long width, double eps)
+{
+    for (long i = 0; i < rows; ++i) {
+        const float *xi = x + i * width;
+        const float *di = dy + i * width;
+        double *out = dx + i * width;
+
+        double sum = 0.0;
+        for (long j = 0; j < width; ++j)
+            sum += (double)xi[j];
+        double mean = sum / (double)width;
+        double sq = 0.0;
+        for (long j = 0; j < width; ++j)
+            sq += ((double)xi[j] - mean) * ((double)xi[j] - mean);
+        double rstd = 1.0 / sqrt(sq / (double)width + eps);
+
+        double sum_g = 0.0, sum_gx = 0.0;
+        for (long j = 0; j < width; ++j) {
+            double g = (double)di[j] * (gamma ? (double)gamma[j] : 1.0);
+            double xhat = ((double)xi[j] - mean) * rstd;
+            sum_g += g;
+            sum_gx += g * xhat;
+        }
+        double mean_g = sum_g / (double)width;
+        double mean_gx = sum_gx / (double)width;
+        for (long j = 0; j < width; ++j) {
+            double g = (double)di[j] * (gamma ? (double)gamma[j] : 1.0);
+            double xhat = ((double)xi[j] - mean) * rstd;
+            out[j] = rstd * (g - mean_g - xhat * mean_gx);
+        }
+    }
+}
+
+/* dx of y = RMSNorm(x) * gamma; gamma may be NULL. */
+void oracle_rmsnorm_backward(const float *x, const float *gamma, const float *dy, double *dx,
+                             long rows, long width, double eps)
+{
+    for (long i = 0; i < rows; ++i) {
+        const float *xi = x + i * width;
+        const float *di = dy + i * width;
+        double *out = dx + i * width;
+
+        double sq = 0.0;
+        for (long j = 0; j < width; ++j)
+            sq += (double)xi[j] * (double)xi[j];
+        double rstd = 1.0 / sqrt(sq / (double)width + eps);
+
+        double sum_gx = 0.0;
+        for (long j = 0; j < width; ++j)
+            sum_gx += (double)di[j] * (gamma ? (double)gamma[j] : 1.0) * ((double)xi[j] * rstd);
+        double mean_gx = sum_gx / (double)width;
+        for (long j = 0; j < width; ++j) {
+            double g = (double)di[j] * (gamma ? (double)gamma[j] : 1.0);
+            out[j] = rstd * (g - (double)xi[j] * rstd * mean_gx);
+        }
+    }
+}
+
+/* dx of y = softmax(x), given y and dy. */
+void oracle_softmax_backward(const float *y, const float *dy, double *dx, long rows, long width)
+{
+    for (long i = 0; i < rows; ++i) {
+        const float *yi = y + i * width;
+        const float *di = dy + i * width;
+        double *out = dx + i * width;
+
+        double dot = 0.0;
+        for (long j = 0; j < width; ++j)
+            dot += (double)di[j] * (double)yi[j];
+        for (long j = 0; j < width; ++j)
+            out[j] = (double)yi[j] * ((double)di[j] - dot);
+    }
+}
+
+/* dgamma[j] = sum_i dy[i][j] * xhat[i][j]; dbeta[j] = sum_i dy[i][j] (LayerNorm;
+ * dbeta may be NULL).  rms != 0 uses the RMSNorm xhat = x * rstd instead. */
+void oracle_norm_param_grad(const float *x, const float *dy, double *dgamma, double *dbeta,
+                            long rows, long width, double eps, int rms)
+{
+    for (long j = 0; j < width; ++j) {
+        dgamma[j] = 0.0;
+        if (dbeta)
+            dbeta[j] = 0.0;
+    }
+    for (long i = 0; i < rows; ++i) {
+        const float *xi = x + i * width;
+        const float *di = dy + i * width;
+        double mean = 0.0;
+        if (!rms) {
+            for (long j = 0; j < width; ++j)
+                mean += (double)xi[j];
+            mean /= (double)width;
+        }
+        double sq = 0.0;
+        for (long j = 0; j < width; ++j)
+            sq += ((double)xi[j] - mean) * ((double)xi[j] - mean);
+        double rstd = 1.0 / sqrt(sq / (double)width + eps);
+        for (long j = 0; j < width; ++j) {
+            dgamma[j] += (double)di[j] * (((double)xi[j] - mean) * rstd);
+            if (dbeta)
+                dbeta[j] += (double)di[j];
+        }
+    }
+}

@@ -52,8 +52,8 @@ def load_golden(path):
                 case["eps"] = val
             elif key == "atol":
                 case["atol"] = float(val)
-            elif key in ("x", "r"):
-                case[key].append([float(v) for v in val.split()])
+            elif key in ("x", "r", "upstream", "fwd"):
+                case.setdefault(key, []).append([float(v) for v in val.split()])
             elif key in ("numer", "expect", "min", "max", "y", "dy"):
                 case[key].append([Fraction(v) for v in val.split()])
             elif key in ("gamma", "beta"):
@@ -76,7 +76,7 @@ def _exact(rows):
 def golden_expected(case):
     """Expected outputs of a golden case, evaluated to 50 digits."""
     op = case["op"]
-    if op in ("softmax", "row_sum"):
+    if op in ("softmax", "row_sum", "softmax_backward"):
         return _exact(case["expect"])
     if op == "row_minmax":
         return _exact(case["min"]), _exact(case["max"])
@@ -107,10 +107,17 @@ def _run_golden(orc, path):
     case = load_golden(path)
     if "op" not in case:
         return None
-    x = np.array(case["x"], dtype=np.float32)
+    x = np.array(case["x"], dtype=np.float32) if case["x"] else None
     eps = float(case.get("eps", "1e-5"))
     op = case["op"]
-    if op == "residual_layernorm":
+    if op == "layernorm_backward":
+        got = orc.layernorm_backward(x, np.array(case["upstream"], np.float32), eps=eps)
+    elif op == "rmsnorm_backward":
+        got = orc.rmsnorm_backward(x, np.array(case["upstream"], np.float32), eps=eps)
+    elif op == "softmax_backward":
+        got = orc.softmax_backward(np.array(case["fwd"], np.float32),
+                                   np.array(case["upstream"], np.float32))
+    elif op == "residual_layernorm":
         got = orc.residual_layernorm(x, np.array(case["r"], dtype=np.float32), eps)
     elif op == "layernorm_affine":
         got = orc.layernorm_affine(x, case["gamma"], case.get("beta"), eps=eps)
@@ -366,6 +373,75 @@ def _pins_pairs(orc):
     return fails
 
 
+def _pins_backward(orc):
+    """Backward passes against torch autograd in FP64 (library special case),
+    directional finite differences of the forward oracle, and invariants."""
+    import torch
+    import torch.nn.functional as F
+    fails = []
+    eps = 1e-5
+    rows, width = 6, 257
+    x = _seeded(rows, width, 91)
+    dy = _seeded(rows, width, 92)
+    g = synth.uniform_pm1(93, width) + np.float32(1.5)
+    for name, fwd, bwd in (
+            ("layernorm", lambda t, w: F.layer_norm(t, (width,), weight=w, eps=eps),
+             orc.layernorm_backward),
+            ("rmsnorm", lambda t, w: F.rms_norm(t, (width,), weight=w, eps=eps),
+             orc.rmsnorm_backward)):
+        for gamma in (None, g):
+            tx = torch.from_numpy(x).double().requires_grad_(True)
+            tw = torch.from_numpy(gamma).double() if gamma is not None else None
+            fwd(tx, tw).backward(torch.from_numpy(dy).double())
+            if not _close(bwd(x, dy, gamma, eps), tx.grad.numpy(), 1e-12):
+                fails.append(f"{name} backward differs from torch autograd (gamma={gamma is not None})")
+    ty = torch.from_numpy(x).double().requires_grad_(True)
+    sm = torch.softmax(ty, dim=1)
+    sm.backward(torch.from_numpy(dy).double())
+    y32 = sm.detach().numpy().astype(np.float32)
+    # the oracle takes the FP32 output; compare with autograd at that y
+    tyy = torch.from_numpy(y32).double()
+    want = (tyy * (torch.from_numpy(dy).double() - (torch.from_numpy(dy).double() * tyy)
+                   .sum(dim=1, keepdim=True))).numpy()
+    if not _close(orc.softmax_backward(y32, dy), want, 1e-14):
+        fails.append("softmax backward differs from y*(dy - sum(dy*y))")
+    if not _close(orc.softmax_backward(sm.detach().numpy().astype(np.float32), dy),
+                  ty.grad.numpy(), 1e-6):
+        fails.append("softmax backward differs from torch autograd")
+    # directional finite differences of the forward oracle: <dy, dF/dx v> = <dx, v>
+    v = _seeded(rows, width, 94)
+    h = 2.0 ** -10
+    for name, f, bwd in (("layernorm", orc.layernorm, orc.layernorm_backward),
+                         ("rmsnorm", orc.rmsnorm, orc.rmsnorm_backward)):
+        xp = (x.astype(np.float64) + h * v).astype(np.float32)
+        xm = (x.astype(np.float64) - h * v).astype(np.float32)
+        dirv = (xp.astype(np.float64) - xm.astype(np.float64)) / 2.0   # exact step taken
+        lhs = np.sum(dy * (f(xp, eps) - f(xm, eps)), axis=1)
+        rhs = np.sum(bwd(x, dy, None, eps) * 2.0 * dirv, axis=1)
+        if not _close(lhs, rhs, 1e-5 * np.abs(rhs).max() + 1e-9):
+            fails.append(f"{name} backward differs from central differences")
+    # invariants: LayerNorm is shift invariant, so rows of dx sum to 0;
+    # softmax rows of dx sum to 0 as well
+    if not np.all(np.abs(orc.layernorm_backward(x, dy, g, eps).sum(axis=1)) <= 1e-10):
+        fails.append("layernorm backward rows do not sum to 0")
+    if not np.all(np.abs(orc.softmax_backward(y32, dy).sum(axis=1)) <= 1e-6):
+        fails.append("softmax backward rows do not sum to 0")
+    # parameter gradients against autograd
+    tx = torch.from_numpy(x).double()
+    tw = torch.from_numpy(g).double().requires_grad_(True)
+    tb = torch.zeros(width, dtype=torch.float64, requires_grad=True)
+    F.layer_norm(tx, (width,), weight=tw, bias=tb, eps=eps).backward(torch.from_numpy(dy).double())
+    dg, db = orc.norm_param_grad(x, dy, eps)
+    if not (_close(dg, tw.grad.numpy(), 1e-12) and _close(db, tb.grad.numpy(), 1e-12)):
+        fails.append("layernorm parameter gradients differ from torch autograd")
+    tw = torch.from_numpy(g).double().requires_grad_(True)
+    F.rms_norm(tx, (width,), weight=tw, eps=eps).backward(torch.from_numpy(dy).double())
+    dg, db = orc.norm_param_grad(x, dy, eps, rms=True)
+    if db is not None or not _close(dg, tw.grad.numpy(), 1e-12):
+        fails.append("rmsnorm parameter gradient differs from torch autograd")
+    return fails
+
+
 def check_all(orc):
     fails = []
     for path in golden_cases():
@@ -373,7 +449,7 @@ def check_all(orc):
         if f:
             fails.append(f)
     for group in (_pins_layernorm, _pins_residual, _pins_rmsnorm, _pins_softmax, _pins_torch,
-                  _pins_affine, _pins_reductions, _pins_pairs):
+                  _pins_affine, _pins_reductions, _pins_pairs, _pins_backward):
         try:
             fails.extend(group(orc))
         except Exception as exc:  # a mutant may produce NaN shapes etc.

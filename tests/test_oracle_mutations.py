@@ -53,6 +53,18 @@ MUTATIONS = [
     ("gelu-cubic-coefficient", "const double a = 0.044715;", "const double a = 0.04715;", 0),
     ("gelu-derivative-missing-3", "(1.0 + 3.0 * a * v * v)", "(1.0 + a * v * v)", 0),
     ("gelu-derivative-tanh-square", "(1.0 - t * t)", "(1.0 - t)", 0),
+    ("ln-backward-mean-g-dropped", "out[j] = rstd * (g - mean_g - xhat * mean_gx);",
+     "out[j] = rstd * (g - xhat * mean_gx);", 0),
+    ("ln-backward-sign", "out[j] = rstd * (g - mean_g - xhat * mean_gx);",
+     "out[j] = rstd * (g - mean_g + xhat * mean_gx);", 0),
+    ("ln-backward-gamma-ignored", "double g = (double)di[j] * (gamma ? (double)gamma[j] : 1.0);\n            double xhat = ((double)xi[j] - mean) * rstd;\n            out[j]",
+     "double g = (double)di[j];\n            double xhat = ((double)xi[j] - mean) * rstd;\n            out[j]", 0),
+    ("rms-backward-rstd-dropped", "out[j] = rstd * (g - (double)xi[j] * rstd * mean_gx);",
+     "out[j] = rstd * (g - (double)xi[j] * mean_gx);", 0),
+    ("softmax-backward-sign", "out[j] = (double)yi[j] * ((double)di[j] - dot);",
+     "out[j] = (double)yi[j] * ((double)di[j] + dot);", 0),
+    ("param-grad-dbeta", "dbeta[j] += (double)di[j];", "dbeta[j] += (double)di[j] * (double)xi[j];", 0),
+    ("param-grad-rms-centred", "        if (!rms) {", "        if (1) {", 0),
 ]
 
 
