@@ -7,9 +7,10 @@ half a BF16 ulp (at most 2^-8 |ref|):
 
     |y - ref| <= 2e-6 + (2e-5 + 2^-8) |ref|
 
-and, sharper, every output is within one BF16 ulp of round_bf16(ref) and at
-least 99.9 % of them equal it (the FP32 error is far below the BF16 spacing,
-so only outputs next to a rounding boundary may differ)."""
+and, sharper, every output with |ref| > 1e-2 is within one BF16 ulp of
+round_bf16(ref) and at least 99.9 % of them equal it (there the FP32 error is
+far below the BF16 spacing, so only outputs next to a rounding boundary may
+differ)."""
 
 from __future__ import annotations
 
@@ -63,8 +64,10 @@ def check_bf16(got_t, ref, atol=ATOL, what=""):
     err = np.abs(got - ref)
     bound = atol + (RTOL + BF16_HALF_ULP_REL) * np.abs(ref)
     assert np.all(err <= bound), f"{what}: max err {err.max():.3e}"
-    # rounding checks where a relative statement is meaningful (|ref| > 1e-6)
-    big = np.abs(ref) > 1e-6
+    # Rounding checks where the BF16 spacing dwarfs the FP32 error (|ref| >
+    # 1e-2: half a BF16 ulp is >= 2e-5 there, the FP32 error about 2e-7);
+    # for smaller outputs the FP32 error can reach a BF16 ulp of the output.
+    big = np.abs(ref) > 1e-2
     rn = _round_bf16(ref[big])
     ulp = 2.0 ** (np.floor(np.log2(np.abs(rn))) - 7)
     assert np.all(np.abs(got[big] - rn) <= ulp), \

@@ -55,6 +55,7 @@ def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g
     a.beta = None
     a.out2 = y2.data_ptr() if y2 is not None else None
     a.rows, a.width, a.eps = rows, width, 1e-5
+    a.dtype = 1 if x.dtype == torch.bfloat16 else 0
     ref = ctypes.byref(a)
 
     def call():
@@ -104,6 +105,7 @@ def main(argv=None):
     ap.add_argument("--graph", action="store_true",
                     help="time calls replayed from a CUDA graph (no host launch overhead)")
     ap.add_argument("--small", action="store_true", help="only the small workload shapes")
+    ap.add_argument("--dtype", default="f32", choices=("f32", "bf16"))
     args = ap.parse_args(argv)
 
     import torch
@@ -124,16 +126,19 @@ def main(argv=None):
         gen = torch.Generator(device="cuda").manual_seed(rows * 131 + width)
         x = torch.rand(rows, width, device="cuda", generator=gen) * 2 - 1
         r = torch.rand(rows, width, device="cuda", generator=gen) * 2 - 1
+        if args.dtype == "bf16":
+            x, r = x.to(torch.bfloat16), r.to(torch.bfloat16)
         y = torch.empty_like(x)
         g = torch.rand(width, device="cuda", generator=gen) + 0.5
         y2 = torch.empty(rows, device="cuda")
         for op in args.ops.split(","):
             code = tile.OPS[op]
-            chosen = tile.tile_describe_plan(op, rows, width)["id"]
+            chosen = tile.tile_describe_plan_ex(op, args.dtype, rows, width)["id"]
             entry = {"op": op, "rows": rows, "width": width, "selected": chosen, "plans": {},
+                     "dtype": args.dtype,
                      "timing": "cuda graph replay" if args.graph else "back-to-back launches"}
             for pid in range(tile.tile_plan_count()):
-                info = tile.tile_plan_info(pid, op, rows, width)
+                info = tile.tile_plan_info_ex(pid, op, args.dtype, rows, width)
                 if info is None or info["vec"] != 4 or info["grid"] > 0x7FFFFFFF:
                     continue
                 us = time_plan(lib, code, pid, x, r, y, rows, width, args.warmup, args.iters, stream,
@@ -141,7 +146,8 @@ def main(argv=None):
                 entry["plans"][pid] = round(us, 3)
             best = min(entry["plans"], key=entry["plans"].get)
             entry["best"] = best
-            entry["best_gbs"] = round(BYTES[op] * n / (entry["plans"][best] * 1e-6) / 1e9, 1)
+            scale = 0.5 if args.dtype == "bf16" else 1.0      # 2-byte elements
+            entry["best_gbs"] = round(scale * BYTES[op] * n / (entry["plans"][best] * 1e-6) / 1e9, 1)
             entry["selected_over_best"] = round(entry["plans"][chosen] / entry["plans"][best], 4)
             results.append(entry)
             print(json.dumps(entry), flush=True)
