@@ -209,6 +209,51 @@ int tile_row_sum_bf16(const void *in, float *sums, int rows, int width, cudaStre
 int tile_row_minmax_bf16(const void *in, float *mins, float *maxs, int rows, int width,
                          cudaStream_t stream);
 
+/* ---- backward passes ---------------------------------------------------
+ * Input gradients of LayerNorm, RMSNorm and softmax, FP32.  The pages do
+ * not cover backward normalisation ("Residual LayerNorm shared-Tile
+ * materialization search", last paragraph); these are the chain rule of the
+ * forward maps above:
+ *   LayerNorm  dx = rstd (g - mean(g) - xhat mean(g xhat)),  xhat = (x - mean) rstd
+ *   RMSNorm    dx = rstd (g - xhat mean(g xhat)),            xhat = x rstd
+ *   softmax    dx = y (dy - sum(dy y))
+ * with g = dy * gamma (gamma = 1 when NULL).  `in` is the forward input
+ * (x, or x + residual for residual LayerNorm); the statistics are recomputed
+ * from it exactly as the forward kernels compute them.  Each row of in and
+ * dy is read once into registers, dx written once.  If row_stats is not
+ * NULL, (mean, rstd) of every row is written to row_stats[2*i], [2*i+1]
+ * (mean 0 for RMSNorm) for tile_norm_param_grad_f32.  dx and row_stats must
+ * not overlap any input.  Other rules as the forward entry points. */
+int tile_layernorm_backward_f32(const float *in, const float *gamma, const float *dy, float *dx,
+                                float *row_stats, int rows, int width, float eps,
+                                cudaStream_t stream);
+int tile_rmsnorm_backward_f32(const float *in, const float *gamma, const float *dy, float *dx,
+                              float *row_stats, int rows, int width, float eps,
+                              cudaStream_t stream);
+/* y: the forward softmax output. */
+int tile_softmax_backward_f32(const float *y, const float *dy, float *dx, int rows, int width,
+                              cudaStream_t stream);
+
+/* A backward call with the built plan `plan_id` forced (op: TILE_OP_LAYERNORM,
+ * TILE_OP_RMSNORM or TILE_OP_SOFTMAX).  TILE_ERR_PLAN if the plan is not built
+ * for backward (two stripes of at most 32 floats), cannot cover the width, or
+ * needs co-aligned pointers. */
+int tile_run_backward_plan_f32(int op, int plan_id, const float *in, const float *gamma,
+                               const float *dy, float *dx, float *row_stats, int rows, int width,
+                               float eps, cudaStream_t stream);
+
+/* Parameter gradients, summed over rows:
+ *   dgamma[j] = sum_i dy[i][j] (in[i][j] - mean_i) rstd_i,  dbeta[j] = sum_i dy[i][j]
+ * from the row statistics a backward call wrote (RMSNorm: mean 0, pass
+ * dbeta = NULL).  Deterministic: rows are split into fixed blocks whose
+ * column partials (compensated sums) go to the caller's device `workspace`
+ * of at least tile_norm_param_grad_workspace_bytes(rows, width) bytes,
+ * then are summed in block order.  rows == 0 writes zeros. */
+size_t tile_norm_param_grad_workspace_bytes(int rows, int width);
+int tile_norm_param_grad_f32(const float *in, const float *dy, const float *row_stats,
+                             float *dgamma, float *dbeta, int rows, int width, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
 /* ---- pointwise value/derivative pairs ---------------------------------- */
 
 /* value[k] = sigmoid(in[k]) and derivative[k] = sigmoid'(in[k]) for k < n,

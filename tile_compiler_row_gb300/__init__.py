@@ -30,6 +30,9 @@ __all__ = [
     "tile_residual_layernorm_bf16", "tile_layernorm_bf16", "tile_rmsnorm_bf16",
     "tile_softmax_bf16", "tile_layernorm_affine_bf16", "tile_rmsnorm_weighted_bf16",
     "tile_row_sum_bf16", "tile_row_minmax_bf16", "tile_describe_plan_ex", "tile_plan_info_ex",
+    "tile_layernorm_backward_f32", "tile_rmsnorm_backward_f32", "tile_softmax_backward_f32",
+    "tile_run_backward_plan_f32", "tile_norm_param_grad_workspace_bytes",
+    "tile_norm_param_grad_f32",
     "residual_layernorm", "layernorm", "rmsnorm", "softmax", "run",
 ]
 
@@ -127,12 +130,19 @@ def load():
         "tile_row_sum_bf16": [P, P, I, I, P],
         "tile_row_minmax_bf16": [P, P, P, I, I, P],
         "tile_describe_plan_ex": [I, I, I, I, ctypes.POINTER(TilePlan)],
+        "tile_layernorm_backward_f32": [P, P, P, P, P, I, I, F, P],
+        "tile_rmsnorm_backward_f32": [P, P, P, P, P, I, I, F, P],
+        "tile_softmax_backward_f32": [P, P, P, I, I, P],
+        "tile_run_backward_plan_f32": [I, I, P, P, P, P, P, I, I, F, P],
+        "tile_norm_param_grad_f32": [P, P, P, P, P, I, I, P, ctypes.c_size_t, P],
         "tile_plan_info_ex": [I, I, I, I, I, ctypes.POINTER(TilePlan)],
     }
     for name, argtypes in sigs.items():
         fn = getattr(lib, name)
         fn.argtypes = argtypes
         fn.restype = ctypes.c_int
+    lib.tile_norm_param_grad_workspace_bytes.argtypes = [I, I]
+    lib.tile_norm_param_grad_workspace_bytes.restype = ctypes.c_size_t
     lib.tile_host_workspace_bytes.argtypes = [I, I, I]
     lib.tile_host_workspace_bytes.restype = ctypes.c_size_t
     lib.tile_status_string.argtypes = [I]
@@ -320,6 +330,64 @@ def _pair_fn(name):
 
 tile_sigmoid_pair_f32 = _pair_fn("tile_sigmoid_pair_f32")
 tile_gelu_tanh_pair_f32 = _pair_fn("tile_gelu_tanh_pair_f32")
+
+
+# ---- backward passes ----------------------------------------------------------
+
+def _bwd(name):
+    def fn(x, gamma, dy, dx, row_stats=None, eps=1e-5, stream=None):
+        px, rows, width = _matrix(x, "x")
+        pd, _, _ = _matrix(dy, "dy")
+        po, _, _ = _matrix(dx, "dx")
+        _same_shape(x, dy, "x/dy")
+        _same_shape(x, dx, "x/dx")
+        ps = _vector(row_stats, 2 * rows, "row_stats") if row_stats is not None else None
+        _check(getattr(load(), name)(px, _vector(gamma, width, "gamma"), pd, po, ps, rows, width,
+                                     eps, _stream(stream)), name)
+    fn.__name__ = name
+    fn.__doc__ = f"Calls ``{name}`` (see include/tile_rows.h)."
+    return fn
+
+
+tile_layernorm_backward_f32 = _bwd("tile_layernorm_backward_f32")
+tile_rmsnorm_backward_f32 = _bwd("tile_rmsnorm_backward_f32")
+
+
+def tile_softmax_backward_f32(y, dy, dx, stream=None):
+    py, rows, width = _matrix(y, "y")
+    pd, _, _ = _matrix(dy, "dy")
+    po, _, _ = _matrix(dx, "dx")
+    _same_shape(y, dy, "y/dy")
+    _same_shape(y, dx, "y/dx")
+    _check(load().tile_softmax_backward_f32(py, pd, po, rows, width, _stream(stream)),
+           "tile_softmax_backward_f32")
+
+
+def tile_run_backward_plan_f32(op, plan_id, x, gamma, dy, dx, row_stats=None, eps=1e-5,
+                               stream=None):
+    op = OPS[op] if isinstance(op, str) else op
+    px, rows, width = _matrix(x, "x")
+    pd, _, _ = _matrix(dy, "dy")
+    po, _, _ = _matrix(dx, "dx")
+    ps = _vector(row_stats, 2 * rows, "row_stats") if row_stats is not None else None
+    _check(load().tile_run_backward_plan_f32(op, plan_id, px, _vector(gamma, width, "gamma"), pd,
+                                             po, ps, rows, width, eps, _stream(stream)),
+           "tile_run_backward_plan_f32")
+
+
+def tile_norm_param_grad_workspace_bytes(rows, width):
+    return load().tile_norm_param_grad_workspace_bytes(rows, width)
+
+
+def tile_norm_param_grad_f32(x, dy, row_stats, dgamma, dbeta, workspace, stream=None):
+    px, rows, width = _matrix(x, "x")
+    pd, _, _ = _matrix(dy, "dy")
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    _check(load().tile_norm_param_grad_f32(
+        px, pd, _vector(row_stats, 2 * rows, "row_stats"), _vector(dgamma, width, "dgamma"),
+        _vector(dbeta, width, "dbeta"), rows, width, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "tile_norm_param_grad_f32")
 
 
 # ---- BF16 rows ---------------------------------------------------------------

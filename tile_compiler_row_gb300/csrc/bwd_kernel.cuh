@@ -1,0 +1,246 @@
+// Backward row kernels: input gradients of LayerNorm, RMSNorm and softmax.
+//
+// Same mapping as the forward row kernel (P row programs of W = 32*S workers
+// per CTA, or one row over a cluster of C CTAs), with two register stripes:
+// the forward input (or softmax output) and the upstream gradient dy, each
+// read from global memory once.  Row statistics are recomputed from the
+// input with the forward kernel's corrected two-pass form; every reduction
+// level combines in a fixed order, so a plan is bitwise deterministic.
+//
+//   LayerNorm:  xhat = (x - mean) rstd,  g = dy * gamma
+//               dx = rstd (g - mean(g) - xhat mean(g xhat))
+//   RMSNorm:    xhat = x rstd,  dx = rstd (g - xhat mean(g xhat))
+//   softmax:    dx = y (dy - sum(dy y))
+//
+// Optionally (stats != NULL, LayerNorm / RMSNorm) the row statistics are
+// written to stats[row] = (mean, rstd) (mean 0 for RMSNorm) for the
+// parameter-gradient kernel (param_grad.cu).
+#pragma once
+
+#include "row_kernel.cuh"
+
+namespace tile {
+
+enum { BWD_LN = BWD_LN_OP, BWD_RMS = BWD_RMS_OP, BWD_SOFTMAX = BWD_SOFTMAX_OP };
+
+template <int OP, int V, int S, int P, int K, int C>
+__global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
+    static_assert(V == 1 || V == 4, "V is 1 (scalar) or 4 (float4)");
+    static_assert(C == 1 || P == 1, "a cluster row has one program per CTA");
+    constexpr int W = 32 * S;
+    constexpr int EV = V;                         // FP32: 4 per 16-byte vector
+
+    __shared__ float part1[S > 1 ? 2 * P * S : 1];
+    __shared__ float part2[S > 1 ? 2 * P * S : 1];
+    __shared__ float part3[S > 1 ? 2 * P * S : 1];
+    __shared__ float cpart[C > 1 ? 5 : 1];
+
+    if (blockDim.x != 32 * S * P) {
+        if (threadIdx.x == 0) atomicOr(a.status, STATUS_BAD_LAUNCH);
+        return;
+    }
+    const int width = a.width;
+    const int tid = threadIdx.x;
+    const int program = tid / W;
+    const int worker = tid - program * W;
+    const int warp = worker >> 5;
+    const int lane = tid & 31;
+    int rank = 0;
+    long long group = blockIdx.x;
+    if constexpr (C > 1) {
+        rank = static_cast<int>(cluster_rank());
+        group = cluster_index();
+    }
+    long long row = group * P + program;
+    const bool active = row < a.rows;
+    if (!active) row = a.rows - 1;                // replay the last row
+
+    const long long base = row * static_cast<long long>(width);
+    const float *xr = a.x + base;
+    const float *dr = a.dy + base;
+    float *outr = a.dx + base;
+
+    int h = 0, tl = 0, nb;
+    if constexpr (V == 4) {
+        const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(xr) >> 2) & 3);
+        h = (4 - mis) & 3;
+        if (h > width) h = width;
+        nb = (width - h) >> 2;
+        tl = width - h - (nb << 2);
+    } else {
+        nb = width;
+    }
+    const int gw = rank * W + worker;
+
+    // ---- load both stripes once ---------------------------------------
+    float v[K][EV], u[K][EV];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int i = k * (C * W) + gw;
+        if (i < nb) {
+            if constexpr (V == 4) {
+                Elem<float>::load_vec(xr + h + 4 * i, v[k]);
+                Elem<float>::load_vec(dr + h + 4 * i, u[k]);
+            } else {
+                v[k][0] = Elem<float>::load(xr + i);
+                u[k][0] = Elem<float>::load(dr + i);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < EV; ++j) {
+                v[k][j] = 0.0f;
+                u[k][j] = 0.0f;
+            }
+        }
+    }
+    bool has_h = false, has_t = false;
+    float hv = 0.0f, tv = 0.0f, hu = 0.0f, tu = 0.0f;
+    int te = 0;
+    if constexpr (V == 4) {
+        has_h = (rank == 0) && (worker < h);
+        has_t = (rank == 0) && (worker < tl);
+        te = h + 4 * nb + worker;
+        if (has_h) {
+            hv = Elem<float>::load(xr + worker);
+            hu = Elem<float>::load(dr + worker);
+        }
+        if (has_t) {
+            tv = Elem<float>::load(xr + te);
+            tu = Elem<float>::load(dr + te);
+        }
+    }
+
+    const float n = static_cast<float>(width);
+    const float *gam = a.gamma;
+    auto col_of = [&](int i) { return (V == 4) ? h + 4 * i : i; };
+
+    if constexpr (OP == BWD_SOFTMAX) {
+        // ---- sum(dy * y), then dx = y (dy - sum) -------------------------
+        float s[1] = {fmaf(hu, hv, tu * tv)};
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < EV; ++j) s[0] = fmaf(u[k][j], v[k][j], s[0]);
+        row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
+        const float dot = s[0];
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < EV; ++j) v[k][j] = v[k][j] * (u[k][j] - dot);
+        hv = hv * (hu - dot);
+        tv = tv * (tu - dot);
+    } else {
+        // ---- statistics of the input row -> rstd and xhat in place -------
+        float rstd, mean = 0.0f;
+        if constexpr (OP == BWD_LN) {
+            float s[1] = {hv + tv};
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int j = 0; j < EV; ++j) s[0] += v[k][j];
+            row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
+            const float mean0 = s[0] / n;
+            float q[2] = {0.0f, 0.0f};
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const bool ok = k * (C * W) + gw < nb;
+#pragma unroll
+                for (int j = 0; j < EV; ++j) {
+                    const float d = ok ? v[k][j] - mean0 : 0.0f;
+                    v[k][j] = d;
+                    q[0] += d;
+                    q[1] = fmaf(d, d, q[1]);
+                }
+            }
+            hv = has_h ? hv - mean0 : 0.0f;
+            tv = has_t ? tv - mean0 : 0.0f;
+            q[0] += hv + tv;
+            q[1] = fmaf(hv, hv, fmaf(tv, tv, q[1]));
+            row_allreduce<Sum, 2, S, P, C>(q, part2, cpart + 1, program, warp, lane);
+            const float mu1 = q[0] / n;
+            const float var = fmaxf(q[1] / n - mu1 * mu1, 0.0f);
+            rstd = 1.0f / sqrtf(var + a.eps);
+            mean = mean0 + mu1;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const bool ok = k * (C * W) + gw < nb;
+#pragma unroll
+                for (int j = 0; j < EV; ++j) v[k][j] = ok ? (v[k][j] - mu1) * rstd : 0.0f;
+            }
+            hv = has_h ? (hv - mu1) * rstd : 0.0f;
+            tv = has_t ? (tv - mu1) * rstd : 0.0f;
+        } else {
+            float s[1] = {fmaf(hv, hv, tv * tv)};
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int j = 0; j < EV; ++j) s[0] = fmaf(v[k][j], v[k][j], s[0]);
+            row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
+            rstd = 1.0f / sqrtf(s[0] / n + a.eps);
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int j = 0; j < EV; ++j) v[k][j] *= rstd;
+            hv *= rstd;
+            tv *= rstd;
+        }
+
+        if (a.stats != nullptr && active && worker == 0 && rank == 0) {
+            a.stats[2 * row] = mean;
+            a.stats[2 * row + 1] = rstd;
+        }
+
+        // ---- g = dy * gamma in place; reduce (sum g, sum g xhat) ---------
+        if (gam != nullptr) {
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int i = k * (C * W) + gw;
+                if (i < nb) {
+#pragma unroll
+                    for (int j = 0; j < EV; ++j) u[k][j] *= __ldg(gam + col_of(i) + j);
+                }
+            }
+            if (has_h) hu *= __ldg(gam + worker);
+            if (has_t) tu *= __ldg(gam + te);
+        }
+        float q[2] = {hu + tu, fmaf(hu, hv, tu * tv)};
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < EV; ++j) {
+                q[0] += u[k][j];
+                q[1] = fmaf(u[k][j], v[k][j], q[1]);
+            }
+        row_allreduce<Sum, 2, S, P, C>(q, part3, cpart + 3, program, warp, lane);
+        const float mean_g = (OP == BWD_LN) ? q[0] / n : 0.0f;
+        const float mean_gx = q[1] / n;
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < EV; ++j)
+                v[k][j] = rstd * (u[k][j] - mean_g - v[k][j] * mean_gx);
+        hv = rstd * (hu - mean_g - hv * mean_gx);
+        tv = rstd * (tu - mean_g - tv * mean_gx);
+    }
+
+    if constexpr (C > 1) cluster_arrive();
+    if (active) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int i = k * (C * W) + gw;
+            if (i < nb) {
+                if constexpr (V == 4)
+                    Elem<float>::store_vec(outr + h + 4 * i, v[k]);
+                else
+                    Elem<float>::store(outr + i, v[k][0]);
+            }
+        }
+        if constexpr (V == 4) {
+            if (has_h) Elem<float>::store(outr + worker, hv);
+            if (has_t) Elem<float>::store(outr + te, tv);
+        }
+    }
+    if constexpr (C > 1) cluster_wait();
+}
+
+}  // namespace tile

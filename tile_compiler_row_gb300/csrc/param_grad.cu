@@ -1,0 +1,174 @@
+// Parameter gradients of LayerNorm / RMSNorm: column sums over all rows,
+//   dgamma[j] = sum_i dy[i][j] * (x[i][j] - mean_i) * rstd_i
+//   dbeta[j]  = sum_i dy[i][j]
+// with (mean_i, rstd_i) the row statistics the backward kernel wrote
+// (mean 0 for RMSNorm).
+//
+// Stage 1 splits the rows into nblk fixed blocks; a thread owns 4 adjacent
+// columns (one float4 when rows are 16-byte aligned, else 4 scalars) and
+// accumulates compensated (TwoSum) sums over its block's rows, four rows in
+// flight.  Block partials go to the caller's workspace [nblk][2][width].
+// Stage 2 sums the nblk partials of each column in block order.  The
+// partition depends only on (rows, width), so results are bitwise
+// reproducible.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "launch.h"
+#include "row_kernel.cuh"
+
+namespace tile {
+namespace {
+
+__device__ unsigned int g_status;   // device error word of the parameter kernels
+constexpr int kThreads = 256;
+constexpr int kRowsInFlight = 4;
+
+__global__ void __launch_bounds__(kThreads)
+    param_partial_kernel(const float *__restrict__ x, const float *__restrict__ dy,
+                         const float *__restrict__ stats, float *__restrict__ ws, long long rows,
+                         int width, int rows_per_block, int vec, int with_beta,
+                         unsigned int *status) {
+    if (blockDim.x != kThreads) {
+        if (threadIdx.x == 0) atomicOr(status, 1u);
+        return;
+    }
+    const int c0 = (blockIdx.x * kThreads + threadIdx.x) * 4;   // first owned column
+    if (c0 >= width) return;
+    const long long r0 = static_cast<long long>(blockIdx.y) * rows_per_block;
+    long long r1 = r0 + rows_per_block;
+    if (r1 > rows) r1 = rows;
+    const int ncol = width - c0 < 4 ? width - c0 : 4;
+
+    float sg[4] = {0, 0, 0, 0}, cg[4] = {0, 0, 0, 0};
+    float sb[4] = {0, 0, 0, 0}, cb[4] = {0, 0, 0, 0};
+    for (long long r = r0; r < r1; r += kRowsInFlight) {
+        float xv[kRowsInFlight][4], dv[kRowsInFlight][4], mu[kRowsInFlight], rs[kRowsInFlight];
+#pragma unroll
+        for (int q = 0; q < kRowsInFlight; ++q) {
+            const long long rr = r + q;
+            if (rr < r1) {
+                const float *xr = x + rr * width + c0;
+                const float *dr = dy + rr * width + c0;
+                if (vec) {
+                    Elem<float>::load_vec(xr, xv[q]);
+                    Elem<float>::load_vec(dr, dv[q]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        xv[q][j] = j < ncol ? Elem<float>::load(xr + j) : 0.0f;
+                        dv[q][j] = j < ncol ? Elem<float>::load(dr + j) : 0.0f;
+                    }
+                }
+                mu[q] = __ldg(stats + 2 * rr);
+                rs[q] = __ldg(stats + 2 * rr + 1);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    xv[q][j] = 0.0f;
+                    dv[q][j] = 0.0f;
+                }
+                mu[q] = 0.0f;
+                rs[q] = 0.0f;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kRowsInFlight; ++q)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                comp_add(sg[j], cg[j], dv[q][j] * ((xv[q][j] - mu[q]) * rs[q]));
+                comp_add(sb[j], cb[j], dv[q][j]);
+            }
+    }
+    float *wg = ws + static_cast<long long>(blockIdx.y) * 2 * width + c0;
+    float *wb = wg + width;
+    for (int j = 0; j < ncol; ++j) {
+        wg[j] = __fadd_rn(sg[j], cg[j]);
+        if (with_beta) wb[j] = __fadd_rn(sb[j], cb[j]);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    param_final_kernel(const float *__restrict__ ws, int nblk, int width,
+                       float *__restrict__ dgamma, float *__restrict__ dbeta,
+                       unsigned int *status) {
+    if (blockDim.x != kThreads) {
+        if (threadIdx.x == 0) atomicOr(status, 1u);
+        return;
+    }
+    const int c = blockIdx.x * kThreads + threadIdx.x;
+    if (c >= width) return;
+    float sg = 0.0f, cg = 0.0f, sb = 0.0f, cb = 0.0f;
+    for (int b = 0; b < nblk; ++b) {
+        comp_add(sg, cg, ws[static_cast<long long>(b) * 2 * width + c]);
+        if (dbeta != nullptr) comp_add(sb, cb, ws[static_cast<long long>(b) * 2 * width + width + c]);
+    }
+    dgamma[c] = __fadd_rn(sg, cg);
+    if (dbeta != nullptr) dbeta[c] = __fadd_rn(sb, cb);
+}
+
+unsigned int *status_address(cudaError_t *err) {
+    static std::atomic<unsigned int *> cache[kMaxDevices];
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    unsigned int *p = cache[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        *err = cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_status);
+        if (*err != cudaSuccess) return nullptr;
+        cache[dev].store(p, std::memory_order_release);
+    }
+    return p;
+}
+
+}  // namespace
+
+int param_blocks(long long rows) {
+    long long nblk = (rows + 31) / 32;
+    if (nblk > 512) nblk = 512;
+    if (nblk < 1) nblk = 1;
+    return static_cast<int>(nblk);
+}
+
+cudaError_t launch_param_grad(const float *x, const float *dy, const float *stats, float *dgamma,
+                              float *dbeta, long long rows, int width, float *ws,
+                              cudaStream_t stream) {
+    cudaError_t err = cudaSuccess;
+    unsigned int *status = status_address(&err);
+    if (status == nullptr) return err;
+    const int nblk = param_blocks(rows);
+    const int rows_per_block = static_cast<int>((rows + nblk - 1) / nblk);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(x), b = reinterpret_cast<uintptr_t>(dy);
+    const int vec = (width % 4 == 0) && (a % 16 == 0) && (b % 16 == 0);
+    const dim3 grid1((width + 4 * kThreads - 1) / (4 * kThreads), nblk, 1);
+    param_partial_kernel<<<grid1, kThreads, 0, stream>>>(x, dy, stats, ws, rows, width,
+                                                         rows_per_block, vec, dbeta != nullptr,
+                                                         status);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const dim3 grid2((width + kThreads - 1) / kThreads, 1, 1);
+    param_final_kernel<<<grid2, kThreads, 0, stream>>>(ws, nblk, width, dgamma, dbeta, status);
+    return cudaGetLastError();
+}
+
+cudaError_t status_param_grad(unsigned int *value, cudaStream_t stream) {
+    cudaError_t err = cudaMemcpyFromSymbolAsync(value, g_status, sizeof(unsigned int), 0,
+                                                cudaMemcpyDeviceToHost, stream);
+    if (err != cudaSuccess) return err;
+    err = cudaStreamSynchronize(stream);
+    if (err != cudaSuccess) return err;
+    if (*value == 0) return cudaSuccess;
+    const unsigned int zero = 0;
+    err = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(unsigned int), 0,
+                                  cudaMemcpyHostToDevice, stream);
+    if (err != cudaSuccess) return err;
+    return cudaStreamSynchronize(stream);
+}
+
+}  // namespace tile

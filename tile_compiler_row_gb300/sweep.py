@@ -139,7 +139,7 @@ def main(argv=None):
                      "timing": "cuda graph replay" if args.graph else "back-to-back launches"}
             for pid in range(tile.tile_plan_count()):
                 info = tile.tile_plan_info_ex(pid, op, args.dtype, rows, width)
-                if info is None or info["vec"] != 4 or info["grid"] > 0x7FFFFFFF:
+                if info is None or info["vec"] == 1 or info["grid"] > 0x7FFFFFFF:
                     continue
                 us = time_plan(lib, code, pid, x, r, y, rows, width, args.warmup, args.iters, stream,
                                g=g, y2=y2, graph=args.graph)
