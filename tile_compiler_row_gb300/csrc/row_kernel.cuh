@@ -63,21 +63,27 @@ struct Elem<__nv_bfloat16> {
     __device__ static unsigned int narrow(float v) {
         return static_cast<unsigned int>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
     }
+    // Two values per 32-bit word: the low half is the element at the lower
+    // address; widening is a shift, narrowing one paired conversion.
+    __device__ static unsigned int narrow2(float lo, float hi) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const unsigned int *>(&h);
+    }
     __device__ static void load_vec(const __nv_bfloat16 *p, float (&v)[8]) {
         const uint4 t = __ldcs(reinterpret_cast<const uint4 *>(p));
         const unsigned int w[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            v[2 * i] = widen(w[i] & 0xffffu);
+            v[2 * i] = __uint_as_float(w[i] << 16);
             v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
         }
     }
     __device__ static void store_vec(__nv_bfloat16 *p, const float (&v)[8]) {
         uint4 t;
-        t.x = narrow(v[0]) | (narrow(v[1]) << 16);
-        t.y = narrow(v[2]) | (narrow(v[3]) << 16);
-        t.z = narrow(v[4]) | (narrow(v[5]) << 16);
-        t.w = narrow(v[6]) | (narrow(v[7]) << 16);
+        t.x = narrow2(v[0], v[1]);
+        t.y = narrow2(v[2], v[3]);
+        t.z = narrow2(v[4], v[5]);
+        t.w = narrow2(v[6], v[7]);
         __stcs(reinterpret_cast<uint4 *>(p), t);
     }
     __device__ static float load(const __nv_bfloat16 *p) {
@@ -127,6 +133,30 @@ struct Sum {
 struct Max {
     __device__ static float apply(float a, float b) { return fmaxf(a, b); }
 };
+
+// Combine per-vector-lane accumulators in a fixed pairwise order.
+template <int N>
+__device__ __forceinline__ float lane_total(const float (&a)[N]) {
+    if constexpr (N == 1) {
+        return a[0];
+    } else {
+        float t[N / 2];
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) t[i] = a[2 * i] + a[2 * i + 1];
+        return lane_total(t);
+    }
+}
+template <int N>
+__device__ __forceinline__ float lane_max(const float (&a)[N]) {
+    if constexpr (N == 1) {
+        return a[0];
+    } else {
+        float t[N / 2];
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) t[i] = fmaxf(a[2 * i], a[2 * i + 1]);
+        return lane_max(t);
+    }
+}
 
 // xor butterfly: every lane ends with the same value (IEEE + and max are
 // commutative, so lane i and lane i^o compute the same pair).
@@ -341,19 +371,21 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
     const float n = static_cast<float>(width);
     float row_out0 = 0.0f, row_out1 = 0.0f;       // per-row results (sum, min/max)
     if constexpr (OP == OP_RESLN || OP == OP_LN) {
-        // ---- a2: mean estimate -------------------------------------------
-        float s[1] = {hv + tv};
+        // ---- a2: mean estimate (one accumulator per vector lane) ----------
+        float acc[EV];
 #pragma unroll
-        for (int k = 0; k < K; ++k) {
-            float t = v[k][0];
+        for (int j = 0; j < EV; ++j) acc[j] = 0.0f;
 #pragma unroll
-            for (int j = 1; j < EV; ++j) t += v[k][j];
-            s[0] += t;
-        }
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < EV; ++j) acc[j] += v[k][j];
+        float s[1] = {lane_total(acc) + (hv + tv)};
         row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
         const float mean0 = s[0] / n;
         // ---- a3: centre in place; reduce (sum d, sum d^2) -----------------
-        float q[2] = {0.0f, 0.0f};
+        float a1[EV], a2[EV];
+#pragma unroll
+        for (int j = 0; j < EV; ++j) a1[j] = a2[j] = 0.0f;
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             const bool ok = k * (C * W) + gw < nb;
@@ -361,14 +393,13 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
             for (int j = 0; j < EV; ++j) {
                 const float d = ok ? v[k][j] - mean0 : 0.0f;
                 v[k][j] = d;
-                q[0] += d;
-                q[1] = fmaf(d, d, q[1]);
+                a1[j] += d;
+                a2[j] = fmaf(d, d, a2[j]);
             }
         }
         hv = has_h ? hv - mean0 : 0.0f;
         tv = has_t ? tv - mean0 : 0.0f;
-        q[0] += hv + tv;
-        q[1] = fmaf(hv, hv, fmaf(tv, tv, q[1]));
+        float q[2] = {lane_total(a1) + (hv + tv), fmaf(hv, hv, fmaf(tv, tv, lane_total(a2)))};
         row_allreduce<Sum, 2, S, P, C>(q, part2, cpart + 1, program, warp, lane);
         // corrected two-pass: mean = mean0 + mu1, var = E[d^2] - mu1^2
         const float mu1 = q[0] / n;
@@ -382,11 +413,14 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
         tv = (tv - mu1) * rstd;
     } else if constexpr (OP == OP_RMS) {
         // ---- a2: mean square ---------------------------------------------
-        float s[1] = {fmaf(hv, hv, tv * tv)};
+        float acc[EV];
+#pragma unroll
+        for (int j = 0; j < EV; ++j) acc[j] = 0.0f;
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
-            for (int j = 0; j < EV; ++j) s[0] = fmaf(v[k][j], v[k][j], s[0]);
+            for (int j = 0; j < EV; ++j) acc[j] = fmaf(v[k][j], v[k][j], acc[j]);
+        float s[1] = {fmaf(hv, hv, fmaf(tv, tv, lane_total(acc)))};
         row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
         const float rstd = 1.0f / sqrtf(s[0] / n + a.eps);
 #pragma unroll
@@ -397,26 +431,31 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
         tv *= rstd;
     } else if constexpr (OP == OP_SOFTMAX) {
         // ---- a2: row maximum (empty slots hold -inf) ---------------------
-        float m[1] = {fmaxf(hv, tv)};
+        float mj[EV];
+#pragma unroll
+        for (int j = 0; j < EV; ++j) mj[j] = kFill;
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
-            for (int j = 0; j < EV; ++j) m[0] = fmaxf(m[0], v[k][j]);
+            for (int j = 0; j < EV; ++j) mj[j] = fmaxf(mj[j], v[k][j]);
+        float m[1] = {fmaxf(lane_max(mj), fmaxf(hv, tv))};
         row_allreduce<Max, 1, S, P, C>(m, part1, cpart, program, warp, lane);
         const float mx = m[0];
         // ---- a3: exponentiate in place (exp(-inf) = 0), reduce the sum ---
-        float s[1] = {0.0f};
+        float acc[EV];
+#pragma unroll
+        for (int j = 0; j < EV; ++j) acc[j] = 0.0f;
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
             for (int j = 0; j < EV; ++j) {
                 const float e = expf(v[k][j] - mx);
                 v[k][j] = e;
-                s[0] += e;
+                acc[j] += e;
             }
         hv = expf(hv - mx);
         tv = expf(tv - mx);
-        s[0] += hv + tv;
+        float s[1] = {lane_total(acc) + (hv + tv)};
         row_allreduce<Sum, 1, S, P, C>(s, part2, cpart + 1, program, warp, lane);
         const float inv = 1.0f / s[0];
 #pragma unroll
@@ -438,14 +477,17 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
         row_out0 = __fadd_rn(s, c);
     } else {
         // ---- paired min/max: max(x) and max(-x) in one reduction ---------
-        float m[2] = {fmaxf(hv, tv), fmaxf(-hv, -tv)};
+        float hi[EV], lo[EV];
+#pragma unroll
+        for (int j = 0; j < EV; ++j) hi[j] = lo[j] = kFill;
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
             for (int j = 0; j < EV; ++j) {
-                m[0] = fmaxf(m[0], v[k][j]);
-                m[1] = fmaxf(m[1], -v[k][j]);
+                hi[j] = fmaxf(hi[j], v[k][j]);
+                lo[j] = fmaxf(lo[j], -v[k][j]);
             }
+        float m[2] = {fmaxf(lane_max(hi), fmaxf(hv, tv)), fmaxf(lane_max(lo), fmaxf(-hv, -tv))};
         row_allreduce<Max, 2, S, P, C>(m, part1, cpart, program, warp, lane);
         row_out0 = -m[1];
         row_out1 = m[0];
