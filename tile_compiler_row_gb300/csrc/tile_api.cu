@@ -91,6 +91,35 @@ constexpr Bucket kVec4RowReduce[] = {
     {131, 0}, {259, 1}, {515, 2}, {1027, 4}, {2051, 6}, {3075, 35}, {4099, 7},
     {6147, 32}, {8195, 10}, {16387, 31}, {32771, 34}, {65539, 33}, {TILE_MAX_WIDTH, 30},
 };
+// Small problems (rows * width <= kSmallElems, L2 resident): the few
+// buckets where the CUDA-graph sweep of the small workload shapes picked a
+// different plan than the large-row sweep; other widths use the tables above.
+constexpr long long kSmallElems = 1LL << 22;
+constexpr Bucket kSmallResidualLN[] = {{32771, -1}, {65539, 33}};
+constexpr Bucket kSmallLN[] = {{131, -1}, {259, 2}, {4099, -1}, {8195, 32}, {32771, -1}, {65539, 33}};
+constexpr Bucket kSmallRMS[] = {{1027, -1}, {2051, 6}, {3075, -1}, {4099, 7}, {32771, -1}, {65539, 33}};
+constexpr Bucket kSmallSoftmax[] = {{32771, -1}, {65539, 33}};
+
+// BF16 rows (16-byte vectors of 8 values), from the BF16 sweep.  The row
+// reductions and weighted RMSNorm use the RMSNorm table, affine LayerNorm
+// the LayerNorm table.
+constexpr Bucket kBf16ResidualLN[] = {
+    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {4103, 6}, {8199, 8},
+    {16391, 10}, {32775, 13}, {65543, 17}, {TILE_MAX_WIDTH, 33},
+};
+constexpr Bucket kBf16LN[] = {
+    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {4103, 6}, {8199, 8},
+    {16391, 10}, {32775, 14}, {65543, 17}, {TILE_MAX_WIDTH, 19},
+};
+constexpr Bucket kBf16RMS[] = {
+    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {4103, 6}, {8199, 8},
+    {16391, 11}, {32775, 13}, {65543, 17}, {TILE_MAX_WIDTH, 19},
+};
+constexpr Bucket kBf16Softmax[] = {
+    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {4103, 6}, {8199, 8},
+    {16391, 10}, {32775, 15}, {65543, 16}, {TILE_MAX_WIDTH, 18},
+};
+
 constexpr Bucket kVec1[] = {
     {128, 25}, {1024, 26}, {4096, 27}, {16384, 28}, {TILE_MAX_WIDTH, 29},
 };
@@ -102,23 +131,29 @@ int pick(const Bucket (&table)[N], int width) {
     return -1;
 }
 
-const Bucket *table_of(int op, int *n);
-
-// BF16 rows move half the bytes of FP32 rows of the same width: a BF16 row
-// takes the FP32 bucket of the same row bytes, then the first plan from there
-// on that is built for BF16 and covers the width.
 int select_plan(int op, long long rows, int width, bool vec4, int dtype) {
-    (void)rows;
     if (!vec4) return pick(kVec1, width);
     if (dtype == TILE_DTYPE_BF16) {
-        int n = 0;
-        const Bucket *t = table_of(op, &n);
-        const int equiv = (width + 1) / 2;
-        int i = 0;
-        while (i < n && equiv > t[i].max_width) ++i;
-        for (; i < n; ++i)
-            if (covers(kPlans[t[i].plan], width, dtype)) return t[i].plan;
-        return -1;
+        int id;
+        switch (op) {
+            case TILE_OP_RESIDUAL_LAYERNORM: id = pick(kBf16ResidualLN, width); break;
+            case TILE_OP_LAYERNORM:
+            case TILE_OP_LAYERNORM_AFFINE: id = pick(kBf16LN, width); break;
+            case TILE_OP_SOFTMAX: id = pick(kBf16Softmax, width); break;
+            default: id = pick(kBf16RMS, width); break;
+        }
+        return (id >= 0 && covers(kPlans[id], width, dtype)) ? id : -1;
+    }
+    if (rows * static_cast<long long>(width) <= kSmallElems) {
+        int id = -1;
+        switch (op) {
+            case TILE_OP_RESIDUAL_LAYERNORM: id = pick(kSmallResidualLN, width); break;
+            case TILE_OP_LAYERNORM: id = pick(kSmallLN, width); break;
+            case TILE_OP_RMSNORM: id = pick(kSmallRMS, width); break;
+            case TILE_OP_SOFTMAX: id = pick(kSmallSoftmax, width); break;
+            default: break;
+        }
+        if (id >= 0) return id;
     }
     switch (op) {
         case TILE_OP_RESIDUAL_LAYERNORM: return pick(kVec4ResidualLN, width);
@@ -130,25 +165,6 @@ int select_plan(int op, long long rows, int width, bool vec4, int dtype) {
         case TILE_OP_ROW_MINMAX: return pick(kVec4RowReduce, width);
         default: return pick(kVec4Softmax, width);
     }
-}
-
-const Bucket *table_of(int op, int *n) {
-#define TILE_TABLE(t) \
-    do {                                   \
-        *n = sizeof(t) / sizeof(t[0]);     \
-        return t;                          \
-    } while (0)
-    switch (op) {
-        case TILE_OP_RESIDUAL_LAYERNORM: TILE_TABLE(kVec4ResidualLN);
-        case TILE_OP_LAYERNORM: TILE_TABLE(kVec4LN);
-        case TILE_OP_LAYERNORM_AFFINE: TILE_TABLE(kVec4Affine);
-        case TILE_OP_RMSNORM: TILE_TABLE(kVec4RMS);
-        case TILE_OP_RMSNORM_WEIGHTED: TILE_TABLE(kVec4Weighted);
-        case TILE_OP_ROW_SUM:
-        case TILE_OP_ROW_MINMAX: TILE_TABLE(kVec4RowReduce);
-        default: TILE_TABLE(kVec4Softmax);
-    }
-#undef TILE_TABLE
 }
 
 long long grid_of(const PlanDesc &p, long long rows) {
