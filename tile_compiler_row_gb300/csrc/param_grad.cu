@@ -8,9 +8,9 @@
 // columns (one float4 when rows are 16-byte aligned, else 4 scalars) and
 // accumulates compensated (TwoSum) sums over its block's rows, four rows in
 // flight.  Block partials go to the caller's workspace [nblk][2][width].
-// Stage 2 sums the nblk partials of each column in block order.  The
-// partition depends only on (rows, width), so results are bitwise
-// reproducible.
+// Stage 2 sums the nblk partials of each column in a fixed order (eight
+// interleaved warp slices, then the slices in warp order).  The partition
+// depends only on (rows, width), so results are bitwise reproducible.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -90,23 +90,46 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// Stage 2: a CTA owns 32 columns; warp w sums row blocks w, w+8, w+16, ...
+// (coalesced 128-byte reads), then warp 0 combines the 8 warp partials in
+// warp order.
 __global__ void __launch_bounds__(kThreads)
     param_final_kernel(const float *__restrict__ ws, int nblk, int width,
                        float *__restrict__ dgamma, float *__restrict__ dbeta,
                        unsigned int *status) {
+    constexpr int kWarps = kThreads / 32;
+    __shared__ float part[4][kWarps][32];
     if (blockDim.x != kThreads) {
         if (threadIdx.x == 0) atomicOr(status, 1u);
         return;
     }
-    const int c = blockIdx.x * kThreads + threadIdx.x;
-    if (c >= width) return;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int c = blockIdx.x * 32 + lane;
     float sg = 0.0f, cg = 0.0f, sb = 0.0f, cb = 0.0f;
-    for (int b = 0; b < nblk; ++b) {
-        comp_add(sg, cg, ws[static_cast<long long>(b) * 2 * width + c]);
-        if (dbeta != nullptr) comp_add(sb, cb, ws[static_cast<long long>(b) * 2 * width + width + c]);
+    if (c < width) {
+        for (int b = warp; b < nblk; b += kWarps) {
+            comp_add(sg, cg, ws[static_cast<long long>(b) * 2 * width + c]);
+            if (dbeta != nullptr)
+                comp_add(sb, cb, ws[static_cast<long long>(b) * 2 * width + width + c]);
+        }
     }
-    dgamma[c] = __fadd_rn(sg, cg);
-    if (dbeta != nullptr) dbeta[c] = __fadd_rn(sb, cb);
+    part[0][warp][lane] = sg;
+    part[1][warp][lane] = cg;
+    part[2][warp][lane] = sb;
+    part[3][warp][lane] = cb;
+    __syncthreads();
+    if (warp == 0 && c < width) {
+        float tg = part[0][0][lane], ug = part[1][0][lane];
+        float tb = part[2][0][lane], ub = part[3][0][lane];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) {
+            comp_merge(tg, ug, part[0][w][lane], part[1][w][lane]);
+            comp_merge(tb, ub, part[2][w][lane], part[3][w][lane]);
+        }
+        dgamma[c] = __fadd_rn(tg, ug);
+        if (dbeta != nullptr) dbeta[c] = __fadd_rn(tb, ub);
+    }
 }
 
 unsigned int *status_address(cudaError_t *err) {
@@ -152,7 +175,7 @@ cudaError_t launch_param_grad(const float *x, const float *dy, const float *stat
                                                          status);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    const dim3 grid2((width + kThreads - 1) / kThreads, 1, 1);
+    const dim3 grid2((width + 31) / 32, 1, 1);
     param_final_kernel<<<grid2, kThreads, 0, stream>>>(ws, nblk, width, dgamma, dbeta, status);
     return cudaGetLastError();
 }
