@@ -82,6 +82,11 @@ extern "C" {
 #define TILE_PATH_CTA      0  /* P programs x S warps per CTA, one row each  */
 #define TILE_PATH_CLUSTER  1  /* one row split over a cluster of C CTAs,     */
                               /* partials exchanged through DSMEM            */
+#define TILE_PATH_STAGED   2  /* persistent CTAs; whole rows copied into a   */
+                              /* ring of shared-memory stages by the bulk-   */
+                              /* copy engine (mbarrier completion), several  */
+                              /* rows in flight per CTA; 16-byte aligned     */
+                              /* rows of whole vectors; normalisers, softmax */
 
 /*
  * A launch plan: how rows map onto the GPU.  Worker w of program p in a CTA
@@ -107,7 +112,8 @@ typedef struct tile_plan {
     int max_width;          /* widest row this plan covers                    */
     int smem_bytes;         /* static shared memory per CTA                   */
     int barriers_per_row;   /* CTA or cluster barriers on a row's path        */
-    long long grid;         /* CTAs launched for `rows`                       */
+    long long grid;         /* CTAs launched for `rows` (0 for staged plans:  */
+                            /* persistent, min(rows, SMs x resident CTAs))    */
     int dtype;              /* TILE_DTYPE_* the plan was described for        */
 } tile_plan_t;
 

@@ -154,7 +154,12 @@ def test_plan_info_table(lib):
     seen_vec1 = False
     for pid in range(n):
         info = tile.tile_plan_info(pid, 0, 3, 1)
-        assert info is not None and info["id"] == pid
+        if info is None:                               # staged: whole vectors only
+            info = tile.tile_plan_info(pid, 0, 3, 4)
+            assert info is not None and info["path"] == 2 and info["id"] == pid
+            assert tile.tile_plan_info(pid, 0, 3, 6) is None
+            continue
+        assert info["id"] == pid
         assert tile.tile_plan_info(pid, 0, 3, info["max_width"]) is not None
         if info["max_width"] < tile.tile_max_width():
             assert tile.tile_plan_info(pid, 0, 3, info["max_width"] + 1) is None
@@ -273,6 +278,6 @@ def test_bf16_plans(lib):
             assert p["stripe_floats"] <= 64
     # K = 16 plans are not built for BF16
     k16 = [pid for pid in range(tile.tile_plan_count())
-           if tile.tile_plan_info(pid, 0, 1, 1)["chunks"] == 16 and
-           tile.tile_plan_info(pid, 0, 1, 1)["vec"] == 4]
+           if tile.tile_plan_info(pid, 0, 1, 4)["chunks"] == 16 and
+           tile.tile_plan_info(pid, 0, 1, 4)["vec"] == 4]
     assert k16 and all(tile.tile_plan_info_ex(pid, 0, "bf16", 1, 1) is None for pid in k16)

@@ -141,7 +141,7 @@ def _bwd_plan_cases():
     out = []
     for pid in range(tile.tile_plan_count()):
         info = tile.tile_plan_info(pid, 0, 1, 1)
-        if info["chunks"] * info["vec"] > 32:
+        if info is None or info["chunks"] * info["vec"] > 32:
             continue
         maxw = info["max_width"]
         rows = 3 if maxw > 16384 else 2 * info["programs_per_cta"] + 1

@@ -1,0 +1,118 @@
+"""GPU parity of the shared-memory-staged plans (bulk row copies into a ring
+of shared-memory stages, persistent CTAs) against the FP64 oracle.
+
+Row counts are chosen so every CTA walks several times round its ring of
+stages (stage reuse, barrier phase flips).  Bounds as for the register
+plans: 2e-6 + 2e-5 |ref| (affine LayerNorm atol 1e-5), BF16 outputs plus
+half a BF16 ulp.  The staged plans need 16-byte aligned rows of whole
+vectors; anything else is rejected with TILE_ERR_PLAN."""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import tile_compiler_row_gb300 as tile
+from parity import ATOL, EPS, RTOL, ref_eps
+
+pytestmark = pytest.mark.gpu
+
+BF16_HALF_ULP_REL = 2.0 ** -8
+
+
+@pytest.fixture(scope="module", autouse=True)
+def device():
+    from tile_compiler_row_gb300 import _build
+    _build.build()
+    torch.cuda.set_device(0)
+    yield
+    assert tile.tile_check_device_status() == 0
+
+
+def _staged_plans():
+    from tile_compiler_row_gb300 import _build
+    _build.build()
+    out = []
+    for pid in range(tile.tile_plan_count()):
+        info = tile.tile_plan_info(pid, 0, 1, 8)
+        if info is not None and info["path"] == 2:
+            out.append(pid)
+    return out
+
+
+STAGED = _staged_plans()
+OPS = ("residual_layernorm", "layernorm", "rmsnorm", "softmax", "layernorm_affine",
+       "rmsnorm_weighted")
+
+
+def _reference(op, x, r, g, b):
+    orc = oracle.get()
+    if op == "residual_layernorm":
+        return orc.residual_layernorm(x, r, ref_eps())
+    if op == "layernorm_affine":
+        return orc.layernorm_affine(x, g, b, r=r, eps=ref_eps())
+    if op == "rmsnorm_weighted":
+        return orc.rmsnorm_weighted(x, g, eps=ref_eps())
+    return orc.run(op, x, eps=ref_eps())
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("pid", STAGED)
+def test_staged_plan(pid, op, dtype):
+    info = tile.tile_plan_info_ex(pid, 0, dtype, 1, 8)
+    assert info is not None and info["path"] == 2
+    ev = info["vec"]
+    cap = info["max_width"]
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    for width in sorted({ev, 256, cap // 2, cap}):
+        rows = 20000 if width <= 512 else 3000
+        x = torch.from_numpy(synth.rows_of(3, rows, width, which="x")).to(tdt)
+        r = torch.from_numpy(synth.rows_of(3, rows, width, which="r")).to(tdt)
+        xf, rf = x.float().numpy(), r.float().numpy()
+        g = synth.uniform_pm1(3001, width) * np.float32(2.0)
+        b = synth.uniform_pm1(3002, width)
+        with_res = op in ("residual_layernorm", "layernorm_affine")
+        out = torch.full((rows, width), float("nan"), dtype=tdt, device="cuda")
+        tile.tile_run_plan_args_f32(
+            op, pid, x.cuda(), out, residual=r.cuda() if with_res else None,
+            gamma=torch.from_numpy(g).cuda() if op in ("layernorm_affine", "rmsnorm_weighted")
+            else None,
+            beta=torch.from_numpy(b).cuda() if op == "layernorm_affine" else None, eps=EPS)
+        ref = _reference(op, xf, rf if with_res else None, g, b)
+        got = out.float().cpu().numpy().astype(np.float64)
+        atol = 1e-5 if op == "layernorm_affine" else ATOL
+        rtol = RTOL + (BF16_HALF_ULP_REL if dtype == "bf16" else 0.0)
+        err = np.abs(got - ref)
+        bad = ~(err <= atol + rtol * np.abs(ref))
+        assert not bad.any(), (f"staged plan {pid} {op} {dtype} {rows}x{width}: "
+                               f"{int(bad.sum())} beyond the bound, max err {np.nanmax(err):.3e}")
+    assert tile.tile_check_device_status() == 0
+
+
+def test_staged_plans_reject_unaligned_rows_and_partial_vectors():
+    pid = STAGED[0]
+    x = torch.zeros(4 * 256 + 8, device="cuda")
+    out = torch.zeros(4 * 256 + 8, device="cuda")
+    with pytest.raises(tile.TileError) as e:            # rows not 16-byte aligned
+        tile.tile_run_plan_args_f32("rmsnorm", pid, x[1:1 + 1024].view(4, 256),
+                                    out[1:1 + 1024].view(4, 256))
+    assert e.value.status == -8
+    with pytest.raises(tile.TileError) as e:            # width not whole vectors
+        tile.tile_run_plan_args_f32("rmsnorm", pid, x[:4 * 254].view(4, 254),
+                                    out[:4 * 254].view(4, 254))
+    assert e.value.status == -8
+    assert tile.tile_plan_info(pid, "rmsnorm", 4, 254) is None
+
+
+def test_staged_results_are_deterministic():
+    pid = STAGED[-1]
+    x = torch.from_numpy(synth.rows_of(3, 5000, 1024, which="x")).cuda()
+    a = torch.empty_like(x)
+    b = torch.empty_like(x)
+    tile.tile_run_plan_args_f32("layernorm", pid, x, a, eps=EPS)
+    tile.tile_run_plan_args_f32("layernorm", pid, x, b, eps=EPS)
+    assert torch.equal(a, b)

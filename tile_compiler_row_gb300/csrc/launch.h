@@ -5,6 +5,9 @@
 namespace tile {
 constexpr int kMaxDevices = 64;
 
+// Row-kernel operations (template argument OP of the row kernels).
+enum { OP_RESLN = 0, OP_LN = 1, OP_RMS = 2, OP_SOFTMAX = 3, OP_SUM = 4, OP_MINMAX = 5 };
+
 // Arguments of one row-kernel launch.  x, r: [rows][width] inputs of the
 // launch's element type (FP32 or BF16; r: residual LayerNorm only).
 // gamma, beta: optional FP32 per-column scale and shift applied after
@@ -39,6 +42,12 @@ struct BwdArgs {
     float eps;
     unsigned int *status;
 };
+
+// Shared-memory-staged row kernel (staged.cu): kernel_op is OP_RESLN, OP_LN,
+// OP_RMS or OP_SOFTMAX; plan_id one of TILE_STAGED_LIST.
+cudaError_t launch_staged(int kernel_op, bool bf16, int plan_id, RowArgs args,
+                          cudaStream_t stream);
+cudaError_t status_staged(unsigned int *value, cudaStream_t stream);
 
 // Backward kernel ops (bwd_kernel.cuh).
 enum { BWD_LN_OP = 0, BWD_RMS_OP = 1, BWD_SOFTMAX_OP = 2 };

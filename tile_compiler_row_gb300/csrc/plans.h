@@ -63,5 +63,16 @@
 
 #define TILE_PLAN_COUNT 37
 
+// Shared-memory-staged plans (staged_kernel.cuh): X(id, S, K), one row per
+// CTA iteration (P = 1, C = 1), 16-byte vectors, persistent grid.  Their ids
+// follow the register plans.
+#define TILE_STAGED_LIST(X) \
+    X(37, 4, 4)             \
+    X(38, 4, 8)             \
+    X(39, 8, 4)             \
+    X(40, 8, 8)
+
+#define TILE_STAGED_COUNT 4
+
 // Widest row covered by both a V = 4 and a V = 1 plan.
 #define TILE_MAX_WIDTH 131072

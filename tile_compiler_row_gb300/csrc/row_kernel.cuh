@@ -28,8 +28,6 @@
 
 namespace tile {
 
-enum { OP_RESLN = 0, OP_LN = 1, OP_RMS = 2, OP_SOFTMAX = 3, OP_SUM = 4, OP_MINMAX = 5 };
-
 // Bits of the per-library device error word (read by tile_check_device_status).
 enum { STATUS_BAD_LAUNCH = 1u };
 

@@ -1,0 +1,322 @@
+// Shared-memory-staged row kernel: persistent CTAs, rows copied into a ring
+// of shared-memory stages by the bulk-copy engine, several rows in flight.
+//
+// The register kernel holds a row's bytes in flight in registers, so a BF16
+// row (2 bytes of DRAM data per 4-byte FP32 register) keeps half as many
+// bytes in flight per SM as an FP32 row.  Here thread 0 issues
+// cp.async.bulk copies of whole rows (x, and the residual) into `nst`
+// shared-memory stages, each completing on its own mbarrier
+// (expect_tx / complete_tx), so up to nst rows per CTA are in flight
+// independently of registers.  Every thread waits on the stage's barrier,
+// reads its elements into an FP32 register stripe, and the row is then
+// reduced and written exactly as in the register kernel (same corrected
+// two-pass LayerNorm, same per-lane accumulators and fixed combine order).
+// The stage is refilled with the CTA's row nst steps ahead as soon as every
+// thread has passed the first reduction barrier of the row (all its stage
+// reads are done by then; the stage reads are volatile so they cannot be
+// repeated after the barrier).
+//
+// Preconditions (checked on the host): rows are 16-byte aligned and a
+// multiple of 16 bytes long (width * sizeof(T) % 16 == 0, bases 16-byte
+// aligned), K * W * EV >= width, S >= 2.
+//
+// Waits are bounded: a wait that does not complete within kWaitSpins polls
+// sets STATUS_WAIT_TIMEOUT in the op's device status word and a CTA-wide
+// abort flag; from then on no thread of the CTA waits and no copy is issued
+// (the CTA's outputs are then invalid, which the status word reports), so no
+// wait can hang the GPU.
+#pragma once
+
+#include "row_kernel.cuh"
+
+namespace tile {
+
+enum { STATUS_WAIT_TIMEOUT = 2u };
+constexpr int kMaxStages = 8;
+constexpr unsigned int kWaitSpins = 1u << 20;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned int count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, unsigned int bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned int parity) {
+    unsigned int ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bulk copy global -> this CTA's shared memory, completing `bytes` on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, unsigned int bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// One 16-byte shared-memory read that the compiler may neither drop nor
+// repeat (the stage is rewritten by the copy engine after the barrier).
+__device__ __forceinline__ uint4 lds128(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_addr(p))
+                 : "memory");
+    return v;
+}
+
+template <class T>
+__device__ __forceinline__ void widen_vec(uint4 t, float (&v)[16 / sizeof(T)]) {
+    if constexpr (sizeof(T) == 4) {
+        v[0] = __uint_as_float(t.x);
+        v[1] = __uint_as_float(t.y);
+        v[2] = __uint_as_float(t.z);
+        v[3] = __uint_as_float(t.w);
+    } else {
+        const unsigned int w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+}
+
+template <int OP, class T, int S, int K>
+__global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int nst) {
+    static_assert(S >= 2, "the stage refill relies on the first CTA barrier");
+    static_assert(OP == OP_RESLN || OP == OP_LN || OP == OP_RMS || OP == OP_SOFTMAX,
+                  "normalisers and softmax");
+    constexpr int W = 32 * S;
+    constexpr int EV = 16 / sizeof(T);
+    constexpr int NIN = (OP == OP_RESLN) ? 2 : 1;
+    constexpr float kFill = (OP == OP_SOFTMAX) ? -INFINITY : 0.0f;
+
+    extern __shared__ __align__(128) unsigned char stage_mem[];
+    __shared__ __align__(8) uint64_t full[kMaxStages];
+    __shared__ float part1[2][2 * S];              // double-buffered by row parity
+    __shared__ float part2[2][2 * S];
+    __shared__ int abort_flag;
+
+    if (blockDim.x != W || nst < 1 || nst > kMaxStages) {
+        if (threadIdx.x == 0) atomicOr(a.status, STATUS_BAD_LAUNCH);
+        return;
+    }
+    const int width = a.width;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const long long rows = a.rows;
+    const long long G = gridDim.x;
+    const unsigned int row_bytes = static_cast<unsigned int>(width) * sizeof(T);
+    const size_t stage_bytes = static_cast<size_t>(row_bytes) * NIN;
+    const int nb = width / EV;                      // vectors per row (no head or tail)
+    const T *xg = static_cast<const T *>(a.x);
+    const T *rg = static_cast<const T *>(a.r);
+    T *yg = static_cast<T *>(a.y);
+
+    auto issue = [&](int s, long long row) {
+        unsigned char *dst = stage_mem + s * stage_bytes;
+        mbar_expect_tx(&full[s], static_cast<unsigned int>(stage_bytes));
+        bulk_load(dst, xg + row * width, row_bytes, &full[s]);
+        if constexpr (NIN == 2) bulk_load(dst + row_bytes, rg + row * width, row_bytes, &full[s]);
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < nst; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+        abort_flag = 0;
+    }
+    __syncthreads();
+    volatile int *abort_seen = &abort_flag;
+    bool aborted = false;
+    if (tid == 0) {
+        for (int s = 0; s < nst; ++s) {
+            const long long row = blockIdx.x + s * G;
+            if (row < rows) issue(s, row);
+        }
+    }
+
+    const float n = static_cast<float>(width);
+    for (long long it = 0;; ++it) {
+        const long long row = blockIdx.x + it * G;
+        if (row >= rows) break;                     // uniform over the CTA
+        const int s = static_cast<int>(it % nst);
+        const unsigned int parity = static_cast<unsigned int>((it / nst) & 1);
+        const int pb = static_cast<int>(it & 1);
+        if (!aborted && *abort_seen) aborted = true;
+        if (!aborted) {
+            unsigned int spins = 0;
+            while (!mbar_try_wait(&full[s], parity)) {
+                if (++spins == kWaitSpins || *abort_seen) {
+                    atomicOr(a.status, STATUS_WAIT_TIMEOUT);
+                    *abort_seen = 1;
+                    aborted = true;
+                    break;
+                }
+            }
+        }
+
+        // ---- stage -> FP32 register stripe ---------------------------------
+        const unsigned char *sx = stage_mem + s * stage_bytes;
+        float v[K][EV];
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int i = k * W + tid;
+            if (i < nb) {
+                widen_vec<T>(lds128(sx + static_cast<size_t>(i) * 16), v[k]);
+                if constexpr (OP == OP_RESLN) {
+                    float b[EV];
+                    widen_vec<T>(lds128(sx + row_bytes + static_cast<size_t>(i) * 16), b);
+#pragma unroll
+                    for (int j = 0; j < EV; ++j) v[k][j] += b[j];
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < EV; ++j) v[k][j] = kFill;
+            }
+        }
+
+        // ---- first reduction; after its barrier the stage is free --------
+        float mean0 = 0.0f, rstd = 0.0f, mx = 0.0f;
+        {
+            float acc[EV];
+#pragma unroll
+            for (int j = 0; j < EV; ++j) acc[j] = kFill;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int j = 0; j < EV; ++j) {
+                    if constexpr (OP == OP_RMS)
+                        acc[j] = fmaf(v[k][j], v[k][j], acc[j]);
+                    else if constexpr (OP == OP_SOFTMAX)
+                        acc[j] = fmaxf(acc[j], v[k][j]);
+                    else
+                        acc[j] += v[k][j];
+                }
+            float r1[1];
+            if constexpr (OP == OP_SOFTMAX) {
+                r1[0] = lane_max(acc);
+                row_allreduce<Max, 1, S, 1, 1>(r1, part1[pb], nullptr, 0, warp, lane);
+                mx = r1[0];
+            } else {
+                r1[0] = lane_total(acc);
+                row_allreduce<Sum, 1, S, 1, 1>(r1, part1[pb], nullptr, 0, warp, lane);
+                if constexpr (OP == OP_RMS)
+                    rstd = 1.0f / sqrtf(r1[0] / n + a.eps);
+                else
+                    mean0 = r1[0] / n;
+            }
+        }
+        if (tid == 0 && !aborted && !*abort_seen) {
+            const long long next = row + static_cast<long long>(nst) * G;
+            if (next < rows) {
+                fence_proxy_async();
+                issue(s, next);
+            }
+        }
+
+        // ---- remaining phases, in registers --------------------------------
+        if constexpr (OP == OP_RESLN || OP == OP_LN) {
+            float a1[EV], a2[EV];
+#pragma unroll
+            for (int j = 0; j < EV; ++j) a1[j] = a2[j] = 0.0f;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const bool ok = k * W + tid < nb;
+#pragma unroll
+                for (int j = 0; j < EV; ++j) {
+                    const float d = ok ? v[k][j] - mean0 : 0.0f;
+                    v[k][j] = d;
+                    a1[j] += d;
+                    a2[j] = fmaf(d, d, a2[j]);
+                }
+            }
+            float q[2] = {lane_total(a1), lane_total(a2)};
+            row_allreduce<Sum, 2, S, 1, 1>(q, part2[pb], nullptr, 0, warp, lane);
+            const float mu1 = q[0] / n;
+            const float var = fmaxf(q[1] / n - mu1 * mu1, 0.0f);
+            rstd = 1.0f / sqrtf(var + a.eps);
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int j = 0; j < EV; ++j) v[k][j] = (v[k][j] - mu1) * rstd;
+        } else if constexpr (OP == OP_RMS) {
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int j = 0; j < EV; ++j) v[k][j] *= rstd;
+        } else {
+            float acc[EV];
+#pragma unroll
+            for (int j = 0; j < EV; ++j) acc[j] = 0.0f;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int j = 0; j < EV; ++j) {
+                    const float e = expf(v[k][j] - mx);
+                    v[k][j] = e;
+                    acc[j] += e;
+                }
+            float r2[1] = {lane_total(acc)};
+            row_allreduce<Sum, 1, S, 1, 1>(r2, part2[pb], nullptr, 0, warp, lane);
+            const float inv = 1.0f / r2[0];
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int j = 0; j < EV; ++j) v[k][j] *= inv;
+        }
+
+        // optional per-column scale and shift (gamma/beta FP32, 16-byte aligned)
+        if constexpr (OP == OP_RESLN || OP == OP_LN || OP == OP_RMS) {
+            if (a.gamma != nullptr) {
+#pragma unroll
+                for (int k = 0; k < K; ++k) {
+                    const int i = k * W + tid;
+                    if (i < nb) {
+#pragma unroll
+                        for (int q = 0; q < EV / 4; ++q) {
+                            const float4 g4 =
+                                __ldg(reinterpret_cast<const float4 *>(a.gamma + EV * i) + q);
+                            float4 b4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                            if (a.beta != nullptr)
+                                b4 = __ldg(reinterpret_cast<const float4 *>(a.beta + EV * i) + q);
+                            v[k][4 * q] = fmaf(v[k][4 * q], g4.x, b4.x);
+                            v[k][4 * q + 1] = fmaf(v[k][4 * q + 1], g4.y, b4.y);
+                            v[k][4 * q + 2] = fmaf(v[k][4 * q + 2], g4.z, b4.z);
+                            v[k][4 * q + 3] = fmaf(v[k][4 * q + 3], g4.w, b4.w);
+                        }
+                    }
+                }
+            }
+        }
+
+        // ---- streaming stores ----------------------------------------------
+        T *yr = yg + row * width;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int i = k * W + tid;
+            if (i < nb) Elem<T>::store_vec(yr + EV * i, v[k]);
+        }
+    }
+}
+
+}  // namespace tile

@@ -13,12 +13,18 @@ namespace {
 
 struct PlanDesc {
     int id, V, S, P, K, C;
+    bool staged;   // shared-memory-staged persistent kernel (staged_kernel.cuh)
 };
 
-constexpr PlanDesc kPlans[TILE_PLAN_COUNT] = {
-#define TILE_ROW(id, V, S, P, K, C) {id, V, S, P, K, C},
+constexpr int kAllPlans = TILE_PLAN_COUNT + TILE_STAGED_COUNT;
+
+constexpr PlanDesc kPlans[kAllPlans] = {
+#define TILE_ROW(id, V, S, P, K, C) {id, V, S, P, K, C, false},
     TILE_PLAN_LIST(TILE_ROW)
 #undef TILE_ROW
+#define TILE_STAGED_ROW(id, S, K) {id, 4, S, 1, K, 1, true},
+    TILE_STAGED_LIST(TILE_STAGED_ROW)
+#undef TILE_STAGED_ROW
 };
 
 // Vector slots a plan's workers own for one row.
@@ -40,12 +46,18 @@ bool built(const PlanDesc &p, int dtype) {
 bool covers(const PlanDesc &p, int width, int dtype = TILE_DTYPE_F32) {
     if (width < 1 || !built(p, dtype)) return false;
     const int ev = elems_per_vec(p, dtype);
+    if (p.staged)   // whole 16-byte vectors only: no head or tail
+        return width % ev == 0 && width / ev <= capacity(p);
     return (width / ev) <= capacity(p);
 }
 
+// A staged plan copies whole rows with the bulk-copy engine: every row
+// pointer (and gamma/beta) must be 16-byte aligned.
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 int max_width_of(const PlanDesc &p, int dtype = TILE_DTYPE_F32) {
     const int ev = elems_per_vec(p, dtype);
-    const long long w = capacity(p) * ev + (ev - 1);
+    const long long w = capacity(p) * ev + (p.staged ? 0 : ev - 1);
     return w > TILE_MAX_WIDTH ? TILE_MAX_WIDTH : static_cast<int>(w);
 }
 
@@ -176,7 +188,7 @@ void fill_plan(const PlanDesc &p, int op, int dtype, int rows, int width, tile_p
     out->rows = rows;
     out->width = width;
     out->id = p.id;
-    out->path = p.C > 1 ? TILE_PATH_CLUSTER : TILE_PATH_CTA;
+    out->path = p.staged ? TILE_PATH_STAGED : p.C > 1 ? TILE_PATH_CLUSTER : TILE_PATH_CTA;
     out->vec = elems_per_vec(p, dtype);
     out->warps_per_program = p.S;
     out->programs_per_cta = p.P;
@@ -189,10 +201,20 @@ void fill_plan(const PlanDesc &p, int op, int dtype, int rows, int width, tile_p
     out->dtype = dtype;
     const int part = p.S > 1 ? 3 * p.P * p.S : 0;
     out->smem_bytes = 4 * (part + (p.C > 1 ? 4 : 0));
+    if (p.staged) {
+        // the launcher's stage count: about 100 KB of staged rows, 1..8 stages
+        const int nin = (op == TILE_OP_RESIDUAL_LAYERNORM) ? 2 : 1;
+        const long long stage = static_cast<long long>(width) *
+                                (dtype == TILE_DTYPE_BF16 ? 2 : 4) * nin;
+        long long nst = (100LL << 10) / stage;
+        nst = nst > 8 ? 8 : nst < 1 ? 1 : nst;
+        out->smem_bytes = static_cast<int>(stage * nst) + 4 * 8 * p.S + 80;
+    }
     const int phases = (op == TILE_OP_RESIDUAL_LAYERNORM || op == TILE_OP_LAYERNORM ||
                         op == TILE_OP_LAYERNORM_AFFINE || op == TILE_OP_SOFTMAX) ? 2 : 1;
     out->barriers_per_row = (p.S > 1 ? phases : 0) + (p.C > 1 ? phases + 1 : 0);
     out->grid = rows > 0 ? grid_of(p, rows) : 0;
+    if (p.staged) out->grid = 0;   // persistent: min(rows, SMs x resident CTAs), device dependent
 }
 
 bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes) {
@@ -283,12 +305,42 @@ int validate(const Call &c, bool *noop) {
     return TILE_OK;
 }
 
+int kernel_op_of(const Call &c) {
+    switch (c.op) {
+        case TILE_OP_RESIDUAL_LAYERNORM: return tile::OP_RESLN;
+        case TILE_OP_LAYERNORM: return tile::OP_LN;
+        case TILE_OP_LAYERNORM_AFFINE: return c.res != nullptr ? tile::OP_RESLN : tile::OP_LN;
+        case TILE_OP_RMSNORM:
+        case TILE_OP_RMSNORM_WEIGHTED: return tile::OP_RMS;
+        case TILE_OP_SOFTMAX: return tile::OP_SOFTMAX;
+        case TILE_OP_ROW_SUM: return tile::OP_SUM;
+        default: return tile::OP_MINMAX;
+    }
+}
+
+// Staged plans serve the normalisers and softmax, with every pointer
+// 16-byte aligned.
+bool staged_ok(const Call &c) {
+    const int k = kernel_op_of(c);
+    if (k == tile::OP_SUM || k == tile::OP_MINMAX) return false;
+    return aligned16(c.in) && aligned16(c.out) && (c.res == nullptr || aligned16(c.res)) &&
+           (c.gamma == nullptr || aligned16(c.gamma)) && (c.beta == nullptr || aligned16(c.beta));
+}
+
 int launch(const Call &c, int plan_id, cudaStream_t stream) {
     const PlanDesc &p = kPlans[plan_id];
     if (grid_of(p, c.rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
     tile::RowArgs a{c.in, c.res, c.gamma, c.beta, c.out, c.out2, c.rows, c.width, c.eps, nullptr};
     const bool bf = c.dtype == TILE_DTYPE_BF16;
     cudaError_t err;
+    if (p.staged) {
+        err = tile::launch_staged(kernel_op_of(c), bf, plan_id, a, stream);
+        if (err != cudaSuccess) {
+            tile::set_last_cuda_error(static_cast<int>(err));
+            return TILE_ERR_CUDA;
+        }
+        return TILE_OK;
+    }
     switch (c.op) {
         case TILE_OP_RESIDUAL_LAYERNORM:
             err = bf ? tile::launch_residual_layernorm_bf16(plan_id, a, stream)
@@ -344,10 +396,11 @@ int run_call_plan(const Call &c, int plan_id, cudaStream_t stream) {
     bool noop = false;
     const int st = validate(c, &noop);
     if (st != TILE_OK) return st;
-    if (plan_id < 0 || plan_id >= TILE_PLAN_COUNT || !covers(kPlans[plan_id], c.width, c.dtype))
+    if (plan_id < 0 || plan_id >= kAllPlans || !covers(kPlans[plan_id], c.width, c.dtype))
         return TILE_ERR_PLAN;
     if (noop) return TILE_OK;
     if (kPlans[plan_id].V == 4 && !coaligned16(c)) return TILE_ERR_PLAN;
+    if (kPlans[plan_id].staged && !staged_ok(c)) return TILE_ERR_PLAN;
     return launch(c, plan_id, stream);
 }
 
@@ -389,7 +442,7 @@ int run_backward(int op, int plan_id, const float *x, const float *gamma, const 
         return TILE_ERR_OP;
     if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH) return TILE_ERR_SHAPE;
     if (op != TILE_OP_SOFTMAX && !(std::isfinite(eps) && eps >= 0.0f)) return TILE_ERR_EPS;
-    if (plan_id >= TILE_PLAN_COUNT) return TILE_ERR_PLAN;
+    if (plan_id >= TILE_PLAN_COUNT) return TILE_ERR_PLAN;   // register plans only
     if (plan_id >= 0 && (!built_backward(kPlans[plan_id]) || !covers(kPlans[plan_id], width)))
         return TILE_ERR_PLAN;
     if (rows == 0) return TILE_OK;
@@ -604,10 +657,10 @@ int tile_describe_plan(int op, int rows, int width, tile_plan_t *plan) {
     return tile_describe_plan_ex(op, TILE_DTYPE_F32, rows, width, plan);
 }
 
-int tile_plan_count(void) { return TILE_PLAN_COUNT; }
+int tile_plan_count(void) { return kAllPlans; }
 
 int tile_plan_info_ex(int id, int op, int dtype, int rows, int width, tile_plan_t *plan) {
-    if (id < 0 || id >= TILE_PLAN_COUNT) return TILE_ERR_PLAN;
+    if (id < 0 || id >= kAllPlans) return TILE_ERR_PLAN;
     if (!valid_op(op)) return TILE_ERR_OP;
     if (dtype != TILE_DTYPE_F32 && dtype != TILE_DTYPE_BF16) return TILE_ERR_DTYPE;
     if (!built(kPlans[id], dtype)) return TILE_ERR_PLAN;
@@ -652,7 +705,7 @@ int tile_check_device_status(cudaStream_t stream) {
         tile::status_residual_layernorm_bf16, tile::status_layernorm_bf16,
         tile::status_rmsnorm_bf16, tile::status_softmax_bf16, tile::status_row_sum_bf16,
         tile::status_row_minmax_bf16, tile::status_pairs, tile::status_backward,
-        tile::status_param_grad};
+        tile::status_param_grad, tile::status_staged};
     for (auto f : fetch) {
         v = 0;
         const cudaError_t err = f(&v, stream);
