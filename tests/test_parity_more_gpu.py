@@ -113,18 +113,20 @@ def test_affine_with_unaligned_rows_and_vectors(x_off, g_off):
 
 
 def test_affine_with_unit_gamma_matches_the_plain_ops_bitwise():
+    """gamma = 1, beta = 0 on the same plan gives the plain op's bits."""
     x = synth.rows_of(3, 33, 4096, which="x")
     ones = np.ones(4096, np.float32)
     zeros = np.zeros(4096, np.float32)
     tx = _placed(x)
-    a = _out((33, 4096))
-    b = _out((33, 4096))
-    tile.tile_layernorm_affine_f32(tx, None, _placed(ones), _placed(zeros), a, EPS)
-    tile.tile_layernorm_f32(tx, b, EPS)
-    assert torch.equal(a, b)
-    tile.tile_rmsnorm_weighted_f32(tx, _placed(ones), a, EPS)
-    tile.tile_rmsnorm_f32(tx, b, EPS)
-    assert torch.equal(a, b)
+    for plain, affine in (("layernorm", "layernorm_affine"), ("rmsnorm", "rmsnorm_weighted")):
+        pid = tile.tile_describe_plan(plain, 33, 4096)["id"]
+        a = _out((33, 4096))
+        b = _out((33, 4096))
+        tile.tile_run_plan_args_f32(affine, pid, tx, a, gamma=_placed(ones),
+                                    beta=_placed(zeros) if affine == "layernorm_affine" else None,
+                                    eps=EPS)
+        tile.tile_run_plan_args_f32(plain, pid, tx, b, eps=EPS)
+        assert torch.equal(a, b)
 
 
 # ---------------------------------------------------------------------------

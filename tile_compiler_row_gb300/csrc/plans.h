@@ -63,16 +63,22 @@
 
 #define TILE_PLAN_COUNT 37
 
-// Shared-memory-staged plans (staged_kernel.cuh): X(id, S, K), one row per
-// CTA iteration (P = 1, C = 1), 16-byte vectors, persistent grid.  Their ids
-// follow the register plans.
+// Shared-memory-staged plans (staged_kernel.cuh): X(id, S, K, KB), one row
+// per CTA iteration (P = 1, C = 1), 16-byte vectors, persistent grid; KB is
+// the shared memory a CTA gives to its ring of stages (between 1 and 8 rows,
+// so a smaller budget means more CTAs, and warps, per SM).  Their ids follow
+// the register plans.
 #define TILE_STAGED_LIST(X) \
-    X(37, 4, 4)             \
-    X(38, 4, 8)             \
-    X(39, 8, 4)             \
-    X(40, 8, 8)
+    X(37, 4, 4, 100)        \
+    X(38, 4, 8, 100)        \
+    X(39, 8, 4, 100)        \
+    X(40, 8, 8, 100)        \
+    X(41, 4, 4, 48)         \
+    X(42, 4, 8, 48)         \
+    X(43, 2, 8, 32)         \
+    X(44, 4, 4, 32)
 
-#define TILE_STAGED_COUNT 4
+#define TILE_STAGED_COUNT 8
 
 // Widest row covered by both a V = 4 and a V = 1 plan.
 #define TILE_MAX_WIDTH 131072

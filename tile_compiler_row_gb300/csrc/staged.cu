@@ -44,7 +44,7 @@ int sm_count(cudaError_t *err) {
     return v;
 }
 
-template <int OP, class T, int S, int K>
+template <int OP, class T, int S, int K, int KB>
 cudaError_t launch_one(RowArgs a, cudaStream_t stream) {
     constexpr int EV = 16 / sizeof(T);
     if constexpr (K * EV > 64) {
@@ -60,8 +60,8 @@ cudaError_t launch_one(RowArgs a, cudaStream_t stream) {
         auto kernel = row_staged_kernel<OP, T, S, K>;
         const int nin = (OP == OP_RESLN) ? 2 : 1;
         const size_t stage = static_cast<size_t>(a.width) * sizeof(T) * nin;
-        // stages for about two CTAs per SM: ~100 KB of staged rows per CTA
-        int nst = static_cast<int>((100u << 10) / stage);
+        // as many stages as fit the plan's budget of KB kilobytes, 1 to 8
+        int nst = static_cast<int>((static_cast<size_t>(KB) << 10) / stage);
         if (nst > kMaxStages) nst = kMaxStages;
         if (nst < 1) nst = 1;
         const size_t dyn = stage * nst;
@@ -82,8 +82,8 @@ cudaError_t launch_one(RowArgs a, cudaStream_t stream) {
 template <int OP, class T>
 cudaError_t launch_op(int staged_id, RowArgs a, cudaStream_t stream) {
     switch (staged_id) {
-#define TILE_CASE(id, S, K) \
-    case id: return launch_one<OP, T, S, K>(a, stream);
+#define TILE_CASE(id, S, K, KB) \
+    case id: return launch_one<OP, T, S, K, KB>(a, stream);
         TILE_STAGED_LIST(TILE_CASE)
 #undef TILE_CASE
         default: return cudaErrorInvalidValue;

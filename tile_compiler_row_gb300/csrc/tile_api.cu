@@ -14,15 +14,16 @@ namespace {
 struct PlanDesc {
     int id, V, S, P, K, C;
     bool staged;   // shared-memory-staged persistent kernel (staged_kernel.cuh)
+    int stage_kb;  // staged plans: shared memory budget of the ring of stages
 };
 
 constexpr int kAllPlans = TILE_PLAN_COUNT + TILE_STAGED_COUNT;
 
 constexpr PlanDesc kPlans[kAllPlans] = {
-#define TILE_ROW(id, V, S, P, K, C) {id, V, S, P, K, C, false},
+#define TILE_ROW(id, V, S, P, K, C) {id, V, S, P, K, C, false, 0},
     TILE_PLAN_LIST(TILE_ROW)
 #undef TILE_ROW
-#define TILE_STAGED_ROW(id, S, K) {id, 4, S, 1, K, 1, true},
+#define TILE_STAGED_ROW(id, S, K, KB) {id, 4, S, 1, K, 1, true, KB},
     TILE_STAGED_LIST(TILE_STAGED_ROW)
 #undef TILE_STAGED_ROW
 };
@@ -202,11 +203,11 @@ void fill_plan(const PlanDesc &p, int op, int dtype, int rows, int width, tile_p
     const int part = p.S > 1 ? 3 * p.P * p.S : 0;
     out->smem_bytes = 4 * (part + (p.C > 1 ? 4 : 0));
     if (p.staged) {
-        // the launcher's stage count: about 100 KB of staged rows, 1..8 stages
+        // the launcher's stage count: the plan's budget, 1..8 stages
         const int nin = (op == TILE_OP_RESIDUAL_LAYERNORM) ? 2 : 1;
         const long long stage = static_cast<long long>(width) *
                                 (dtype == TILE_DTYPE_BF16 ? 2 : 4) * nin;
-        long long nst = (100LL << 10) / stage;
+        long long nst = (static_cast<long long>(p.stage_kb) << 10) / stage;
         nst = nst > 8 ? 8 : nst < 1 ? 1 : nst;
         out->smem_bytes = static_cast<int>(stage * nst) + 4 * 8 * p.S + 80;
     }
