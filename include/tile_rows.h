@@ -285,7 +285,9 @@ int tile_gelu_tanh_pair_f32(const float *in, float *value, float *derivative, lo
  * `stream` runs the kernels; two internal non-blocking streams per device,
  * created on first use, run the copies).  Host buffers should be pinned
  * (cudaHostAlloc / cudaHostRegister) for the copies to overlap; pageable
- * memory gives the same results more slowly.  Ownership: the caller owns all
+ * memory gives the same results more slowly.  When h_out is pinned the
+ * kernels store the results straight into it through its device address
+ * (NVLink-C2C on Grace systems) and no device->host copies are made.  Ownership: the caller owns all
  * buffers and must keep them alive and untouched until `stream` has passed
  * this call (the call returns once everything is enqueued; `stream` is
  * ordered after the last copy).  Results meet the same tolerance as the

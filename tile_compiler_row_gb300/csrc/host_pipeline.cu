@@ -10,6 +10,11 @@
 // b = c % 2.  Each wait is issued after the record it must see (chunks are
 // enqueued in order), so chunk c+2 reuses buffer b only once chunk c's
 // kernel has consumed the inputs and chunk c's output has left the device.
+//
+// When the output buffer is pinned host memory the device can address (over
+// NVLink-C2C on Grace systems), the kernels store each chunk's results
+// straight into it and the device->host copies are skipped: the copy
+// engines then carry only the inputs, which is what bounds the pipeline.
 #include "../../include/tile_rows.h"
 
 #include <cmath>
@@ -107,6 +112,17 @@ int run_host(int op, const float *h_in, const float *h_res, float *h_out, int ro
         return TILE_ERR_CUDA;
     }
 
+    // Pinned, device-addressable output: the kernels write it directly.
+    float *out_dev = nullptr;
+    {
+        cudaPointerAttributes attr;
+        if (cudaPointerGetAttributes(&attr, h_out) == cudaSuccess &&
+            attr.type == cudaMemoryTypeHost && attr.devicePointer != nullptr)
+            out_dev = static_cast<float *>(attr.devicePointer);
+        else
+            (void)cudaGetLastError();   // clear a non-sticky error of the query
+    }
+
     const size_t buf = round_up(static_cast<size_t>(chunk) * width * sizeof(float));
     char *base = static_cast<char *>(d_work);
     float *dx[2], *dr[2], *dy[2];
@@ -145,6 +161,12 @@ int run_host(int op, const float *h_in, const float *h_res, float *h_out, int ro
         TILE_TRY(cudaEventRecord(q.h2d_ev[b], q.h2d));
 
         TILE_TRY(cudaStreamWaitEvent(stream, q.h2d_ev[b], 0));
+        if (out_dev != nullptr) {
+            const int st = run_selected(op, dx[b], dr[b], out_dev + off, n, width, eps, stream);
+            if (st != TILE_OK) return st;
+            TILE_TRY(cudaEventRecord(q.compute_ev[b], stream));
+            continue;
+        }
         if (c >= 2) TILE_TRY(cudaStreamWaitEvent(stream, q.d2h_ev[b], 0));
         const int st = run_selected(op, dx[b], dr[b], dy[b], n, width, eps, stream);
         if (st != TILE_OK) return st;
