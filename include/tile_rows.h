@@ -279,9 +279,11 @@ int tile_gelu_tanh_pair_f32(const float *in, float *value, float *derivative, lo
 
 /* Run `op` on HOST buffers h_in[, h_residual] -> h_out ([rows][width] FP32
  * each).  Rows stream through the caller's device workspace `d_work`
- * (`work_bytes` bytes, 256-byte aligned) in chunks, double-buffered: the
- * host->device copy of one chunk, the kernel on the previous chunk and the
- * device->host copy of the one before overlap on three streams (the caller's
+ * (`work_bytes` bytes, 256-byte aligned) in chunks of about rows/16 rows (at
+ * least 1 MiB of a tensor, at most what fits twice in the workspace), held in
+ * a ring of 2 to 4 workspace buffers (as many as fit): the host->device copy
+ * of one chunk, the kernel on an earlier chunk and the device->host copy of
+ * one before that overlap on three streams (the caller's
  * `stream` runs the kernels; two internal non-blocking streams per device,
  * created on first use, run the copies).  Host buffers should be pinned
  * (cudaHostAlloc / cudaHostRegister) for the copies to overlap; pageable
@@ -306,6 +308,17 @@ int tile_run_host_f32(int op, const float *h_in, const float *h_residual, float 
 /* Workspace bytes tile_run_host_f32 needs to move `chunk_rows` rows per
  * chunk (0 for invalid arguments).  Host only. */
 size_t tile_host_workspace_bytes(int op, int width, int chunk_rows);
+
+/* The schedule tile_run_host_f32 uses for these arguments: rows per chunk
+ * (the last chunk may be shorter) and the number of workspace buffers in the
+ * ring.  `direct_output` != 0 describes a call whose h_out is pinned and
+ * device-addressable (results stored straight into it), 0 one whose results
+ * are copied out.  Host only: no CUDA call.  Returns TILE_OK, TILE_ERR_OP,
+ * TILE_ERR_SHAPE (rows < 1 or width outside 1..tile_max_width()),
+ * TILE_ERR_NULL for a NULL output pointer, or TILE_ERR_WORKSPACE as
+ * tile_run_host_f32 would. */
+int tile_host_schedule(int op, int rows, int width, size_t work_bytes, int direct_output,
+                       int *chunk_rows, int *slots);
 
 /* Size of the library's own device staging area used by
  * tile_run_host_static_f32: 64 MiB, held by every GPU that loads the library

@@ -207,6 +207,39 @@ def test_host_workspace_bytes(lib):
     assert tile.tile_host_workspace_bytes(9, 10, 3) == 0
 
 
+@pytest.mark.parametrize("op", ["residual_layernorm", "layernorm", "rmsnorm", "softmax"])
+@pytest.mark.parametrize("rows,width", [(1, 1), (3, 127), (37, 1537), (65536, 4096),
+                                        (20000, 257), (5, 131072)])
+@pytest.mark.parametrize("ws_rows", [1, 7, 1 << 20])
+@pytest.mark.parametrize("direct", [False, True])
+def test_host_schedule_fits_the_workspace(lib, op, rows, width, ws_rows, direct):
+    """The host pipeline's chunking: every slot of the ring fits the
+    workspace, chunks never exceed the rows, there are 2 to 4 slots, and a
+    roomy workspace gives about 16 chunks of at least 1 MiB each."""
+    ws = tile.tile_host_workspace_bytes(op, width, min(ws_rows, rows))
+    chunk, slots = tile.tile_host_schedule(op, rows, width, ws, direct_output=direct)
+    row_bytes = 4 * width
+    per_slot = (2 if op == "residual_layernorm" else 1) + (0 if direct else 1)
+    buf = -(-chunk * row_bytes // 256) * 256
+    assert 1 <= chunk <= rows and 2 <= slots <= 4
+    assert slots * per_slot * buf <= ws
+    nchunks = -(-rows // chunk)
+    if nchunks >= 2:
+        assert slots <= nchunks
+    if ws_rows >= rows:
+        assert chunk == min(rows, max(-(-rows // 16), -(-(1 << 20) // row_bytes)))
+
+
+def test_host_schedule_rejects_bad_arguments(lib):
+    c, k = ctypes.c_int(), ctypes.c_int()
+    f = lib.tile_host_schedule
+    assert f(7, 4, 8, 1 << 20, 1, ctypes.byref(c), ctypes.byref(k)) == -6
+    assert f(1, 0, 8, 1 << 20, 1, ctypes.byref(c), ctypes.byref(k)) == SHAPE
+    assert f(1, 4, 0, 1 << 20, 1, ctypes.byref(c), ctypes.byref(k)) == SHAPE
+    assert f(1, 4, 8, 1 << 20, 1, None, ctypes.byref(k)) == NULL
+    assert f(1, 4, 4096, 65535, 1, ctypes.byref(c), ctypes.byref(k)) == -10
+
+
 @fake_pointers
 def test_new_row_ops_reject_bad_arguments(lib):
     f = lib.tile_layernorm_affine_f32

@@ -61,3 +61,23 @@ def test_dist_rejects_mismatched_world(monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     with pytest.raises(SystemExit):
         bench.Dist(4)
+
+
+@pytest.mark.parametrize("op", ["residual_layernorm", "rmsnorm", "softmax"])
+@pytest.mark.parametrize("threads", [1, 3, 8, 40])
+def test_cpu_baseline_row_blocks_cover_every_row_once(op, threads):
+    """The all-core CPU baseline splits rows into contiguous blocks; together
+    they must equal one oracle call over all rows, bit for bit."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    import synth
+    rows, width = 37, 96
+    x = synth.rows_of(3, rows, width, which="x")
+    r = synth.rows_of(3, rows, width, which="r") if op == "residual_layernorm" else None
+    orc = oracle.get()
+    eps = oracle.kernel_eps(bench.EPS)
+    parts = bench.oracle_rows(orc, op, x, r, eps, threads)
+    assert len(parts) == min(threads, rows)
+    assert np.array_equal(np.concatenate(parts), orc.run(op, x, r, eps))

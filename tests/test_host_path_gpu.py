@@ -62,10 +62,29 @@ def test_host_path_matches_oracle_and_device_path(op, rows, width, chunk):
     # Bitwise equality needs the same plan and the same 16-byte phase of every
     # row start (chunks start 256-byte aligned in the workspace; rows of the
     # full tensor do only when width is a multiple of 4).
-    same_plan = tile.tile_describe_plan(op, min(chunk, rows), width)["id"] == \
-        tile.tile_describe_plan(op, rows, width)["id"]
+    used, _ = tile.tile_host_schedule(op, rows, width,
+                                      tile.tile_host_workspace_bytes(op, width, chunk))
+    full = tile.tile_describe_plan(op, rows, width)["id"]
+    sizes = {used, rows - (rows - 1) // used * used}
+    same_plan = all(tile.tile_describe_plan(op, n, width)["id"] == full for n in sizes)
     if same_plan and width % 4 == 0:
         assert np.array_equal(got, _run_device(op, x, r))
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("rows,width", [(20000, 257), (9001, 1024)])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_path_ring_of_four_slots(op, rows, width, pinned):
+    """Workspace for the whole matrix: about 16 chunks cycle through a ring
+    of four slots (each slot reused four times), with results stored
+    directly (pinned) or copied out (pageable)."""
+    ws = tile.tile_host_workspace_bytes(op, width, rows)
+    chunk, slots = tile.tile_host_schedule(op, rows, width, ws, direct_output=pinned)
+    assert slots == 4 and -(-rows // chunk) >= 12
+    x = synth.rows_of(3, rows, width, which="x")
+    r = synth.rows_of(3, rows, width, which="r") if op == "residual_layernorm" else None
+    got = _run_host(op, x, r, rows, pinned=pinned)
+    compare(got, oracle_of(op, x, r), f"ring {op} {rows}x{width} pinned={pinned}")
 
 
 @pytest.mark.parametrize("op", ["residual_layernorm", "softmax"])

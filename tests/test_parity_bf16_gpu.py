@@ -186,9 +186,9 @@ def test_every_bf16_plan(pid, op, rows, widths):
 @pytest.mark.parametrize("op", ["residual_layernorm", "layernorm", "softmax"])
 @pytest.mark.parametrize("rows,width", [(2048, 4096), (1024, 8192), (512, 16384)])
 def test_bf16_selected_staged_plans(op, rows, width):
-    """Large BF16 rows of whole vectors select a shared-memory-staged plan;
-    the same rows one element off the 16-byte phase fall back to a register
-    plan.  Both must meet the bound."""
+    """Large BF16 rows of whole vectors select a shared-memory-staged plan
+    where it measured faster; the same rows one element off the 16-byte phase
+    fall back to a register plan.  Both must meet the bound."""
     x, xf = _bf16_rows(3, rows, width)
     r, rf = _bf16_rows(3, rows, width, "r")
     ref = (oracle.get().residual_layernorm(xf, rf, ref_eps()) if op == "residual_layernorm"
@@ -201,4 +201,6 @@ def test_bf16_selected_staged_plans(op, rows, width):
         else:
             getattr(tile, f"tile_{op}_bf16")(_placed(x, off), out, EPS)
         check_bf16(out, ref, what=f"bf16 {op} {rows}x{width} offset {off}")
-    assert tile.tile_describe_plan_ex(op, "bf16", rows, width)["path"] == 2
+    # The sweep found the staged kernel faster only for these BF16 shapes.
+    staged = not ((op == "layernorm" and width <= 8192) or (op == "softmax" and width <= 4096))
+    assert (tile.tile_describe_plan_ex(op, "bf16", rows, width)["path"] == 2) == staged

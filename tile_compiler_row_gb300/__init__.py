@@ -24,7 +24,7 @@ __all__ = [
     "tile_softmax_f32", "tile_run_plan_f32", "tile_describe_plan", "tile_plan_info",
     "tile_plan_count", "tile_max_width", "tile_status_string",
     "tile_check_device_status", "tile_last_cuda_error", "tile_run_host_f32",
-    "tile_host_workspace_bytes", "tile_run_host_static_f32", "tile_layernorm_affine_f32",
+    "tile_host_workspace_bytes", "tile_host_schedule", "tile_run_host_static_f32", "tile_layernorm_affine_f32",
     "tile_rmsnorm_weighted_f32", "tile_row_sum_f32", "tile_row_minmax_f32",
     "tile_run_plan_args_f32", "tile_sigmoid_pair_f32", "tile_gelu_tanh_pair_f32",
     "tile_residual_layernorm_bf16", "tile_layernorm_bf16", "tile_rmsnorm_bf16",
@@ -113,6 +113,8 @@ def load():
         "tile_check_device_status": [P],
         "tile_last_cuda_error": [],
         "tile_run_host_f32": [I, P, P, P, I, I, F, P, ctypes.c_size_t, P],
+        "tile_host_schedule": [I, I, I, ctypes.c_size_t, I, ctypes.POINTER(ctypes.c_int),
+                               ctypes.POINTER(ctypes.c_int)],
         "tile_run_host_static_f32": [I, P, P, P, I, I, F, P],
         "tile_layernorm_affine_f32": [P, P, P, P, P, I, I, F, P],
         "tile_rmsnorm_weighted_f32": [P, P, P, I, I, F, P],
@@ -499,6 +501,17 @@ def tile_run_host_static_f32(op, x, residual, out, eps=1e-5, stream=None):
 def tile_host_workspace_bytes(op, width, chunk_rows):
     op = OPS[op] if isinstance(op, str) else op
     return load().tile_host_workspace_bytes(op, width, chunk_rows)
+
+
+def tile_host_schedule(op, rows, width, work_bytes, direct_output=True):
+    """(chunk rows, ring slots) that tile_run_host_f32 uses for these
+    arguments; `direct_output` describes a pinned output buffer."""
+    op = OPS[op] if isinstance(op, str) else op
+    chunk, slots = ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().tile_host_schedule(op, rows, width, work_bytes, int(bool(direct_output)),
+                                     ctypes.byref(chunk), ctypes.byref(slots)),
+           "tile_host_schedule")
+    return chunk.value, slots.value
 
 
 def tile_describe_plan(op, rows, width):

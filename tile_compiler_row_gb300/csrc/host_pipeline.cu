@@ -1,15 +1,17 @@
-// End-to-end entry point on host buffers: rows stream through a
-// double-buffered device workspace in chunks, and three streams overlap the
-// host->device copy of chunk c+1, the kernel on chunk c and the
-// device->host copy of chunk c-1.
+// End-to-end entry point on host buffers: rows stream through a ring of
+// device buffers ("slots") carved from the caller's workspace, in chunks,
+// and three streams overlap the host->device copy of chunk c+1, the kernel
+// on chunk c and the device->host copy of chunk c-1.
 //
 //   h2d stream:      wait compute[b] -> copy in (x, r) -> record h2d[b]
 //   caller stream:   wait h2d[b], wait d2h[b] -> kernel -> record compute[b]
 //   d2h stream:      wait compute[b] -> copy out y -> record d2h[b]
 //
-// b = c % 2.  Each wait is issued after the record it must see (chunks are
-// enqueued in order), so chunk c+2 reuses buffer b only once chunk c's
+// b = c % slots.  Each wait is issued after the record it must see (chunks
+// are enqueued in order), so chunk c+slots reuses slot b only once chunk c's
 // kernel has consumed the inputs and chunk c's output has left the device.
+// More than two slots let the copies in run ahead of a kernel that is slow
+// to finish (one that writes its results over the host link).
 //
 // When the output buffer is pinned host memory the device can address (over
 // NVLink-C2C on Grace systems), the kernels store each chunk's results
@@ -26,17 +28,23 @@
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr int kMaxSlots = 4;
+// A chunk is about 1/16 of the rows (the tail after the last copy in is one
+// chunk's kernel) but at least 1 MiB of each input (per-chunk overheads).
+constexpr long long kStages = 16;
+constexpr size_t kMinChunkBytes = size_t(1) << 20;
 
 size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
-int tensors_of(int op) { return op == TILE_OP_RESIDUAL_LAYERNORM ? 3 : 2; }
+int inputs_of(int op) { return op == TILE_OP_RESIDUAL_LAYERNORM ? 2 : 1; }
+int tensors_of(int op) { return inputs_of(op) + 1; }
 
 // Internal streams and events, created once per device.
 struct DeviceQueues {
     bool ready = false;
     cudaStream_t h2d = nullptr, d2h = nullptr;
     cudaEvent_t start = nullptr, done = nullptr;
-    cudaEvent_t h2d_ev[2] = {}, compute_ev[2] = {}, d2h_ev[2] = {};
+    cudaEvent_t h2d_ev[kMaxSlots] = {}, compute_ev[kMaxSlots] = {}, d2h_ev[kMaxSlots] = {};
     std::mutex mu;
 };
 
@@ -49,7 +57,7 @@ cudaError_t ensure_queues(DeviceQueues &q) {
     const unsigned flags = cudaEventDisableTiming;
     if (err == cudaSuccess) err = cudaEventCreateWithFlags(&q.start, flags);
     if (err == cudaSuccess) err = cudaEventCreateWithFlags(&q.done, flags);
-    for (int b = 0; b < 2 && err == cudaSuccess; ++b) {
+    for (int b = 0; b < kMaxSlots && err == cudaSuccess; ++b) {
         err = cudaEventCreateWithFlags(&q.h2d_ev[b], flags);
         if (err == cudaSuccess) err = cudaEventCreateWithFlags(&q.compute_ev[b], flags);
         if (err == cudaSuccess) err = cudaEventCreateWithFlags(&q.d2h_ev[b], flags);
@@ -67,16 +75,38 @@ bool overlaps(const void *a, const void *b, size_t bytes) {
 
 namespace tile {
 
-// Rows per chunk for a workspace of `work_bytes`: as many as fit twice
-// (double buffering), at most ceil(rows/8) so the pipeline has stages to
-// overlap, and at least 1 (0 if not even one row fits).
-long long host_chunk_rows(int op, int rows, int width, size_t work_bytes) {
+// Rows per chunk when a slot holds `tensors` row blocks: as many as fit in
+// two slots, at most about rows/16 (but not below 1 MiB of one tensor) so the
+// pipeline has stages to overlap, and at least 1 (0 if not even one row fits
+// twice).
+long long host_chunk_rows(int tensors, int rows, int width, size_t work_bytes) {
     const size_t row_bytes = static_cast<size_t>(width) * sizeof(float);
-    const size_t per_buffer = work_bytes / (2 * static_cast<size_t>(tensors_of(op)));
+    const size_t per_buffer = work_bytes / (2 * static_cast<size_t>(tensors));
     long long fit = static_cast<long long>((per_buffer / kAlign * kAlign) / row_bytes);
-    const long long stage = (static_cast<long long>(rows) + 7) / 8;
+    long long stage = (static_cast<long long>(rows) + kStages - 1) / kStages;
+    const long long min_rows = static_cast<long long>((kMinChunkBytes + row_bytes - 1) / row_bytes);
+    if (stage < min_rows) stage = min_rows;
+    if (stage > rows) stage = rows;
     if (fit > stage) fit = stage;
     return fit;
+}
+
+// Chunk rows and ring slots for a workspace of `work_bytes`.  Slots hold
+// the inputs, plus the output unless it is stored directly; `slots` is as
+// many as fit (2 to kMaxSlots, never more than there are chunks, but at
+// least 2, which host_chunk_rows guarantees fit).
+void schedule(int op, int rows, int width, size_t work_bytes, bool direct, long long *chunk,
+              int *slots) {
+    const int per_slot = inputs_of(op) + (direct ? 0 : 1);
+    const long long c = host_chunk_rows(per_slot, rows, width, work_bytes);
+    *chunk = c;
+    *slots = 0;
+    if (c < 1) return;
+    const size_t buf = round_up(static_cast<size_t>(c) * width * sizeof(float));
+    const long long nchunks = (rows + c - 1) / c;
+    long long fit = static_cast<long long>(work_bytes / (per_slot * buf));
+    if (fit > nchunks) fit = nchunks;
+    *slots = fit < 2 ? 2 : (fit > kMaxSlots ? kMaxSlots : static_cast<int>(fit));
 }
 
 // The pipeline over caller-provided workspace (also used by the entry point
@@ -94,8 +124,10 @@ int run_host(int op, const float *h_in, const float *h_res, float *h_out, int ro
     const size_t total = static_cast<size_t>(rows) * static_cast<size_t>(width) * sizeof(float);
     if (overlaps(h_out, h_in, total) || (residual && overlaps(h_out, h_res, total)))
         return TILE_ERR_ALIAS;
-    const long long chunk = host_chunk_rows(op, rows, width, work_bytes);
-    if (chunk < 1) return TILE_ERR_WORKSPACE;
+    // Checked on the host before any CUDA call: one row of every tensor must
+    // fit twice (whether or not the output later turns out to be stored
+    // directly).
+    if (host_chunk_rows(tensors_of(op), rows, width, work_bytes) < 1) return TILE_ERR_WORKSPACE;
 
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -123,14 +155,20 @@ int run_host(int op, const float *h_in, const float *h_res, float *h_out, int ro
             (void)cudaGetLastError();   // clear a non-sticky error of the query
     }
 
+    long long chunk = 0;
+    int slots = 0;
+    schedule(op, rows, width, work_bytes, out_dev != nullptr, &chunk, &slots);
+    const int per_slot = inputs_of(op) + (out_dev != nullptr ? 0 : 1);
     const size_t buf = round_up(static_cast<size_t>(chunk) * width * sizeof(float));
+    const long long nchunks = (rows + chunk - 1) / chunk;
     char *base = static_cast<char *>(d_work);
-    float *dx[2], *dr[2], *dy[2];
-    for (int b = 0; b < 2; ++b) {
-        char *p = base + static_cast<size_t>(b) * tensors_of(op) * buf;
+    float *dx[kMaxSlots], *dr[kMaxSlots], *dy[kMaxSlots];
+    for (int b = 0; b < slots; ++b) {
+        char *p = base + static_cast<size_t>(b) * per_slot * buf;
         dx[b] = reinterpret_cast<float *>(p);
         dr[b] = residual ? reinterpret_cast<float *>(p + buf) : nullptr;
-        dy[b] = reinterpret_cast<float *>(p + (residual ? 2 : 1) * buf);
+        dy[b] = out_dev != nullptr ? nullptr
+                                   : reinterpret_cast<float *>(p + (residual ? 2 : 1) * buf);
     }
 
     // Everything enqueued here runs after the work already on `stream`.
@@ -147,14 +185,13 @@ int run_host(int op, const float *h_in, const float *h_res, float *h_out, int ro
     TILE_TRY(cudaStreamWaitEvent(q.h2d, q.start, 0));
     TILE_TRY(cudaStreamWaitEvent(q.d2h, q.start, 0));
 
-    const long long nchunks = (rows + chunk - 1) / chunk;
     for (long long c = 0; c < nchunks; ++c) {
-        const int b = static_cast<int>(c & 1);
+        const int b = static_cast<int>(c % slots);
         const long long r0 = c * chunk;
         const int n = static_cast<int>(rows - r0 < chunk ? rows - r0 : chunk);
         const size_t off = static_cast<size_t>(r0) * width;
         const size_t bytes = static_cast<size_t>(n) * width * sizeof(float);
-        if (c >= 2) TILE_TRY(cudaStreamWaitEvent(q.h2d, q.compute_ev[b], 0));
+        if (c >= slots) TILE_TRY(cudaStreamWaitEvent(q.h2d, q.compute_ev[b], 0));
         TILE_TRY(cudaMemcpyAsync(dx[b], h_in + off, bytes, cudaMemcpyHostToDevice, q.h2d));
         if (residual)
             TILE_TRY(cudaMemcpyAsync(dr[b], h_res + off, bytes, cudaMemcpyHostToDevice, q.h2d));
@@ -167,7 +204,7 @@ int run_host(int op, const float *h_in, const float *h_res, float *h_out, int ro
             TILE_TRY(cudaEventRecord(q.compute_ev[b], stream));
             continue;
         }
-        if (c >= 2) TILE_TRY(cudaStreamWaitEvent(stream, q.d2h_ev[b], 0));
+        if (c >= slots) TILE_TRY(cudaStreamWaitEvent(stream, q.d2h_ev[b], 0));
         const int st = run_selected(op, dx[b], dr[b], dy[b], n, width, eps, stream);
         if (st != TILE_OK) return st;
         TILE_TRY(cudaEventRecord(q.compute_ev[b], stream));
@@ -189,6 +226,21 @@ int run_host(int op, const float *h_in, const float *h_res, float *h_out, int ro
 }  // namespace tile
 
 extern "C" {
+
+int tile_host_schedule(int op, int rows, int width, size_t work_bytes, int direct_output,
+                       int *chunk_rows, int *slots) {
+    if (op < TILE_OP_RESIDUAL_LAYERNORM || op > TILE_OP_SOFTMAX) return TILE_ERR_OP;
+    if (rows < 1 || width < 1 || width > tile_max_width()) return TILE_ERR_SHAPE;
+    if (chunk_rows == nullptr || slots == nullptr) return TILE_ERR_NULL;
+    if (tile::host_chunk_rows(tensors_of(op), rows, width, work_bytes) < 1)
+        return TILE_ERR_WORKSPACE;
+    long long c = 0;
+    int k = 0;
+    tile::schedule(op, rows, width, work_bytes, direct_output != 0, &c, &k);
+    *chunk_rows = static_cast<int>(c);
+    *slots = k;
+    return TILE_OK;
+}
 
 size_t tile_host_workspace_bytes(int op, int width, int chunk_rows) {
     if (op < TILE_OP_RESIDUAL_LAYERNORM || op > TILE_OP_SOFTMAX || width < 1 || chunk_rows < 1)

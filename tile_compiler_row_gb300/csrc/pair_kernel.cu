@@ -6,8 +6,7 @@
 // fused element grid.  Here one streaming kernel per function reads x once
 // and writes both outputs: float4 accesses when the three pointers share a
 // 16-byte phase (scalar head and tail around the aligned body), scalar
-// accesses otherwise; a grid-stride loop with four vectors in flight per
-// thread.
+// accesses otherwise; each thread has four vectors in flight.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -140,18 +139,6 @@ unsigned int *status_address(cudaError_t *err) {
     return p;
 }
 
-int sm_count() {
-    static std::atomic<int> cache[kMaxDevices];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
-    int v = cache[dev].load(std::memory_order_relaxed);
-    if (v == 0) {
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) v = 148;
-        cache[dev].store(v, std::memory_order_relaxed);
-    }
-    return v;
-}
-
 }  // namespace
 
 cudaError_t launch_pairs(int kind, const float *x, float *y, float *dy, long long n,
@@ -162,11 +149,13 @@ cudaError_t launch_pairs(int kind, const float *x, float *y, float *dy, long lon
     const uintptr_t px = reinterpret_cast<uintptr_t>(x);
     const int vec = ((px ^ reinterpret_cast<uintptr_t>(y)) & 15) == 0 &&
                     ((px ^ reinterpret_cast<uintptr_t>(dy)) & 15) == 0;
-    // Enough CTAs for 8 per SM, fewer for small n (each thread handles at
-    // least kUnroll vectors when there is that much work).
+    // One pass: every thread handles kUnroll vectors once (a grid over the
+    // whole array streamed faster on GB300 than a persistent grid of a few
+    // CTAs per SM walking it); the grid-stride loop only covers arrays past
+    // the grid-size limit.
     const long long per_block = static_cast<long long>(kThreads) * (vec ? 4 : 1) * kUnroll;
     long long blocks = (n + per_block - 1) / per_block;
-    const long long cap = static_cast<long long>(sm_count()) * 8;
+    const long long cap = 0x7fffffffLL;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     if (kind == PAIR_SIGMOID)
