@@ -374,7 +374,9 @@ int tile_plan_count(void);
 int tile_plan_info(int id, int op, int rows, int width, tile_plan_t *plan);
 
 /* tile_plan_info for an element type; TILE_ERR_PLAN also when plan `id` is
- * not built for that type (BF16 plans whose stripe would pass 64 floats). */
+ * not built for that type (BF16 plans whose stripe would pass 64 floats), or
+ * is a shared-memory-staged plan and `op` a row reduction (sum, min/max),
+ * which only the register plans implement. */
 int tile_plan_info_ex(int id, int op, int dtype, int rows, int width, tile_plan_t *plan);
 
 /* Run `op` (one of the first four op codes) with the built plan `plan_id`

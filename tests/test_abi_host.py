@@ -314,3 +314,13 @@ def test_bf16_plans(lib):
            if tile.tile_plan_info(pid, 0, 1, 4)["chunks"] == 16 and
            tile.tile_plan_info(pid, 0, 1, 4)["vec"] == 4]
     assert k16 and all(tile.tile_plan_info_ex(pid, 0, "bf16", 1, 1) is None for pid in k16)
+
+
+def test_staged_plans_have_no_row_reductions(lib):
+    staged = [pid for pid in range(tile.tile_plan_count())
+              if (tile.tile_plan_info(pid, "layernorm", 8, 4096) or {}).get("path") == 2]
+    assert staged
+    for pid in staged:
+        for op in ("row_sum", "row_minmax"):
+            assert tile.tile_plan_info(pid, op, 8, 4096) is None
+            assert tile.tile_plan_info_ex(pid, op, "bf16", 8, 4096) is None

@@ -183,8 +183,9 @@ def test_every_bf16_plan(pid, op, rows, widths):
             check_bf16(out, ref, what=f"bf16 plan {pid} {op} w={w} off={off}")
 
 
-@pytest.mark.parametrize("op", ["residual_layernorm", "layernorm", "softmax"])
-@pytest.mark.parametrize("rows,width", [(2048, 4096), (1024, 8192), (512, 16384)])
+@pytest.mark.parametrize("op", ["residual_layernorm", "layernorm", "rmsnorm", "softmax"])
+@pytest.mark.parametrize("rows,width", [(2048, 4096), (1024, 8192), (1024, 12288),
+                                        (512, 16384)])
 def test_bf16_selected_staged_plans(op, rows, width):
     """Large BF16 rows of whole vectors select a shared-memory-staged plan
     where it measured faster; the same rows one element off the 16-byte phase
@@ -202,5 +203,6 @@ def test_bf16_selected_staged_plans(op, rows, width):
             getattr(tile, f"tile_{op}_bf16")(_placed(x, off), out, EPS)
         check_bf16(out, ref, what=f"bf16 {op} {rows}x{width} offset {off}")
     # The sweep found the staged kernel faster only for these BF16 shapes.
-    staged = not ((op == "layernorm" and width <= 8192) or (op == "softmax" and width <= 4096))
+    staged = (op == "residual_layernorm" or (op == "layernorm" and width == 16384)
+              or (op == "rmsnorm" and width == 12288))
     assert (tile.tile_describe_plan_ex(op, "bf16", rows, width)["path"] == 2) == staged

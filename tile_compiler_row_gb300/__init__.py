@@ -531,7 +531,8 @@ def tile_describe_plan_ex(op, dtype, rows, width):
 
 
 def tile_plan_info_ex(plan_id, op, dtype, rows, width):
-    """Plan ``plan_id`` for (op, dtype, rows, width), or None if not built / not covering."""
+    """Plan ``plan_id`` for (op, dtype, rows, width), or None if not built, not
+    covering, or without a variant for ``op``."""
     op = OPS[op] if isinstance(op, str) else op
     dtype = DTYPES[dtype] if isinstance(dtype, str) else dtype
     plan = TilePlan()
@@ -543,11 +544,12 @@ def tile_plan_info_ex(plan_id, op, dtype, rows, width):
 
 
 def tile_plan_info(plan_id, op, rows, width):
-    """The built plan ``plan_id`` for (op, rows, width), or None if it cannot cover ``width``."""
+    """The built plan ``plan_id`` for (op, rows, width), or None if it cannot
+    cover ``width`` or has no variant for ``op``."""
     op = OPS[op] if isinstance(op, str) else op
     plan = TilePlan()
     st = load().tile_plan_info(plan_id, op, rows, width, ctypes.byref(plan))
-    if st == -2:
+    if st in (-2, -8):
         return None
     _check(st, "tile_plan_info")
     return plan.as_dict()

@@ -30,9 +30,9 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
     constexpr int W = 32 * S;
     constexpr int EV = V;                         // FP32: 4 per 16-byte vector
 
+    // Reduction partials, one buffer per round: [N][P*S] floats (N = 2, 4).
     __shared__ float part1[S > 1 ? 2 * P * S : 1];
-    __shared__ float part2[S > 1 ? 2 * P * S : 1];
-    __shared__ float part3[S > 1 ? 2 * P * S : 1];
+    __shared__ float part2[S > 1 ? 4 * P * S : 1];
     __shared__ float cpart[C > 1 ? 5 : 1];
 
     if (blockDim.x != 32 * S * P) {
@@ -130,8 +130,25 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
         hv = hv * (hu - dot);
         tv = tv * (tu - dot);
     } else {
-        // ---- statistics of the input row -> rstd and xhat in place -------
-        float rstd, mean = 0.0f;
+        // ---- g = dy * gamma in place ---------------------------------------
+        if (gam != nullptr) {
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int i = k * (C * W) + gw;
+                if (i < nb) {
+#pragma unroll
+                    for (int j = 0; j < EV; ++j) u[k][j] *= __ldg(gam + col_of(i) + j);
+                }
+            }
+            if (has_h) hu *= __ldg(gam + worker);
+            if (has_t) tu *= __ldg(gam + te);
+        }
+        // ---- row statistics and the two gradient sums, xhat in place ------
+        // The gradient sums need no extra reduction round: with d = x - m0
+        // (LayerNorm) sum(g xhat) = rstd (sum(g d) - mu1 sum(g)), and for
+        // RMSNorm sum(g xhat) = rstd sum(g x), so they are reduced together
+        // with the statistics they depend on.
+        float rstd, mean = 0.0f, mean_g = 0.0f, mean_gx;
         if constexpr (OP == BWD_LN) {
             float s[1] = {hv + tv};
 #pragma unroll
@@ -140,7 +157,7 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
                 for (int j = 0; j < EV; ++j) s[0] += v[k][j];
             row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
             const float mean0 = s[0] / n;
-            float q[2] = {0.0f, 0.0f};
+            float q[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const bool ok = k * (C * W) + gw < nb;
@@ -150,17 +167,23 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
                     v[k][j] = d;
                     q[0] += d;
                     q[1] = fmaf(d, d, q[1]);
+                    q[2] += u[k][j];
+                    q[3] = fmaf(u[k][j], d, q[3]);
                 }
             }
             hv = has_h ? hv - mean0 : 0.0f;
             tv = has_t ? tv - mean0 : 0.0f;
             q[0] += hv + tv;
             q[1] = fmaf(hv, hv, fmaf(tv, tv, q[1]));
-            row_allreduce<Sum, 2, S, P, C>(q, part2, cpart + 1, program, warp, lane);
+            q[2] += hu + tu;
+            q[3] = fmaf(hu, hv, fmaf(tu, tv, q[3]));
+            row_allreduce<Sum, 4, S, P, C>(q, part2, cpart + 1, program, warp, lane);
             const float mu1 = q[0] / n;
             const float var = fmaxf(q[1] / n - mu1 * mu1, 0.0f);
             rstd = 1.0f / sqrtf(var + a.eps);
             mean = mean0 + mu1;
+            mean_g = q[2] / n;
+            mean_gx = rstd * fmaf(-mu1, q[2], q[3]) / n;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const bool ok = k * (C * W) + gw < nb;
@@ -170,13 +193,17 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
             hv = has_h ? (hv - mu1) * rstd : 0.0f;
             tv = has_t ? (tv - mu1) * rstd : 0.0f;
         } else {
-            float s[1] = {fmaf(hv, hv, tv * tv)};
+            float q[2] = {fmaf(hv, hv, tv * tv), fmaf(hu, hv, tu * tv)};
 #pragma unroll
             for (int k = 0; k < K; ++k)
 #pragma unroll
-                for (int j = 0; j < EV; ++j) s[0] = fmaf(v[k][j], v[k][j], s[0]);
-            row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
-            rstd = 1.0f / sqrtf(s[0] / n + a.eps);
+                for (int j = 0; j < EV; ++j) {
+                    q[0] = fmaf(v[k][j], v[k][j], q[0]);
+                    q[1] = fmaf(u[k][j], v[k][j], q[1]);
+                }
+            row_allreduce<Sum, 2, S, P, C>(q, part1, cpart, program, warp, lane);
+            rstd = 1.0f / sqrtf(q[0] / n + a.eps);
+            mean_gx = rstd * q[1] / n;
 #pragma unroll
             for (int k = 0; k < K; ++k)
 #pragma unroll
@@ -190,30 +217,7 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
             a.stats[2 * row + 1] = rstd;
         }
 
-        // ---- g = dy * gamma in place; reduce (sum g, sum g xhat) ---------
-        if (gam != nullptr) {
-#pragma unroll
-            for (int k = 0; k < K; ++k) {
-                const int i = k * (C * W) + gw;
-                if (i < nb) {
-#pragma unroll
-                    for (int j = 0; j < EV; ++j) u[k][j] *= __ldg(gam + col_of(i) + j);
-                }
-            }
-            if (has_h) hu *= __ldg(gam + worker);
-            if (has_t) tu *= __ldg(gam + te);
-        }
-        float q[2] = {hu + tu, fmaf(hu, hv, tu * tv)};
-#pragma unroll
-        for (int k = 0; k < K; ++k)
-#pragma unroll
-            for (int j = 0; j < EV; ++j) {
-                q[0] += u[k][j];
-                q[1] = fmaf(u[k][j], v[k][j], q[1]);
-            }
-        row_allreduce<Sum, 2, S, P, C>(q, part3, cpart + 3, program, warp, lane);
-        const float mean_g = (OP == BWD_LN) ? q[0] / n : 0.0f;
-        const float mean_gx = q[1] / n;
+        // ---- dx = rstd (g - mean(g) - xhat mean(g xhat)) --------------------
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll

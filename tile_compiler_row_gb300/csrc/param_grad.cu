@@ -10,7 +10,9 @@
 // flight.  Block partials go to the caller's workspace [nblk][2][width].
 // Stage 2 sums the nblk partials of each column in a fixed order (eight
 // interleaved warp slices, then the slices in warp order).  The partition
-// depends only on (rows, width), so results are bitwise reproducible.
+// depends only on (rows, width) and the device (its SM count and the
+// kernel's resident CTAs per SM), so results are bitwise reproducible on a
+// device.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -159,17 +161,56 @@ int param_blocks(long long rows) {
     return static_cast<int>(nblk);
 }
 
+namespace {
+
+// CTA slots of stage 1 on this device (SMs x resident CTAs), cached.
+int partial_slots() {
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        int sms = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, param_partial_kernel,
+                                                          kThreads, 0) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        v = sms * per_sm;
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// Row blocks for stage 1: at most param_blocks(rows) (what the workspace
+// holds), lowered so the grid (column tiles x row blocks) fills whole waves
+// of the device's CTA slots when it spans more than one wave: a last wave
+// half full leaves half the SMs idle for its duration.
+int balanced_blocks(long long rows, int col_tiles) {
+    const int nmax = param_blocks(rows);
+    const long long slots = partial_slots();
+    const long long total = static_cast<long long>(col_tiles) * nmax;
+    if (slots <= 0 || total <= slots) return nmax;
+    const long long waves = total / slots;
+    const long long n = waves * slots / col_tiles;
+    return n >= 1 && n <= nmax ? static_cast<int>(n) : nmax;
+}
+
+}  // namespace
+
 cudaError_t launch_param_grad(const float *x, const float *dy, const float *stats, float *dgamma,
                               float *dbeta, long long rows, int width, float *ws,
                               cudaStream_t stream) {
     cudaError_t err = cudaSuccess;
     unsigned int *status = status_address(&err);
     if (status == nullptr) return err;
-    const int nblk = param_blocks(rows);
+    const int col_tiles = (width + 4 * kThreads - 1) / (4 * kThreads);
+    const int nblk = balanced_blocks(rows, col_tiles);
     const int rows_per_block = static_cast<int>((rows + nblk - 1) / nblk);
     const uintptr_t a = reinterpret_cast<uintptr_t>(x), b = reinterpret_cast<uintptr_t>(dy);
     const int vec = (width % 4 == 0) && (a % 16 == 0) && (b % 16 == 0);
-    const dim3 grid1((width + 4 * kThreads - 1) / (4 * kThreads), nblk, 1);
+    const dim3 grid1(col_tiles, nblk, 1);
     param_partial_kernel<<<grid1, kThreads, 0, stream>>>(x, dy, stats, ws, rows, width,
                                                          rows_per_block, vec, dbeta != nullptr,
                                                          status);

@@ -59,9 +59,13 @@
     X(33, 4, 16, 1, 8, 4)                                                     \
     X(34, 4, 16, 1, 8, 2)                                                     \
     X(35, 4, 2, 1, 16, 1)                                                     \
-    X(36, 4, 4, 2, 8, 1)
+    X(36, 4, 4, 2, 8, 1)                                                      \
+    /* fewer workers, deeper stripes (packed BF16 rows of 2048-4096) */       \
+    X(37, 4, 2, 1, 8, 1)                                                      \
+    X(38, 4, 2, 2, 8, 1)                                                      \
+    X(39, 4, 1, 4, 8, 1)
 
-#define TILE_PLAN_COUNT 37
+#define TILE_PLAN_COUNT 40
 
 // Shared-memory-staged plans (staged_kernel.cuh): X(id, S, K, KB), one row
 // per CTA iteration (P = 1, C = 1), 16-byte vectors, persistent grid; KB is
@@ -69,14 +73,14 @@
 // so a smaller budget means more CTAs, and warps, per SM).  Their ids follow
 // the register plans.
 #define TILE_STAGED_LIST(X) \
-    X(37, 4, 4, 100)        \
-    X(38, 4, 8, 100)        \
-    X(39, 8, 4, 100)        \
-    X(40, 8, 8, 100)        \
-    X(41, 4, 4, 48)         \
-    X(42, 4, 8, 48)         \
-    X(43, 2, 8, 32)         \
-    X(44, 4, 4, 32)
+    X(40, 4, 4, 100)        \
+    X(41, 4, 8, 100)        \
+    X(42, 8, 4, 100)        \
+    X(43, 8, 8, 100)        \
+    X(44, 4, 4, 48)         \
+    X(45, 4, 8, 48)         \
+    X(46, 2, 8, 32)         \
+    X(47, 4, 4, 32)
 
 #define TILE_STAGED_COUNT 8
 

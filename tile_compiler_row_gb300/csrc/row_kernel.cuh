@@ -92,6 +92,25 @@ struct Elem<__nv_bfloat16> {
     }
 };
 
+// exp(t), t <= 0 or -inf, for the softmax numerators.  FP32 rows call expf.
+// BF16 rows, whose outputs keep 8 significant bits, use the identity
+// e^t = 2^(t log2 e) with the hardware base-2 exponential (PTX
+// ex2.approx.ftz.f32, relative error about 2^-22; ex2(-inf) = +0): rounding
+// t log2 e adds a relative error of at most |t| ln(2) 2^-24, about 1e-6 at
+// t = -20, where e^t is already below 1e-8; both stay far inside half a
+// BF16 ulp (2^-9).  It takes a fraction of expf's instructions, which
+// matters because BF16 rows carry twice the elements per byte.
+template <class T>
+__device__ __forceinline__ float softmax_exp(float t) {
+    if constexpr (sizeof(T) == 2) {
+        float r;
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t * 1.4426950408889634f));
+        return r;
+    } else {
+        return expf(t);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // cluster primitives (inline PTX)
 // ---------------------------------------------------------------------------
@@ -447,12 +466,12 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
         for (int k = 0; k < K; ++k)
 #pragma unroll
             for (int j = 0; j < EV; ++j) {
-                const float e = expf(v[k][j] - mx);
+                const float e = softmax_exp<T>(v[k][j] - mx);
                 v[k][j] = e;
                 acc[j] += e;
             }
-        hv = expf(hv - mx);
-        tv = expf(tv - mx);
+        hv = softmax_exp<T>(hv - mx);
+        tv = softmax_exp<T>(tv - mx);
         float s[1] = {lane_total(acc) + (hv + tv)};
         row_allreduce<Sum, 1, S, P, C>(s, part2, cpart + 1, program, warp, lane);
         const float inv = 1.0f / s[0];

@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int
             for (int k = 0; k < K; ++k)
 #pragma unroll
                 for (int j = 0; j < EV; ++j) {
-                    const float e = expf(v[k][j] - mx);
+                    const float e = softmax_exp<T>(v[k][j] - mx);
                     v[k][j] = e;
                     acc[j] += e;
                 }

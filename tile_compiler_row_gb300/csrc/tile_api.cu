@@ -75,7 +75,7 @@ struct Bucket {
 };
 
 constexpr Bucket kVec4ResidualLN[] = {
-    {131, 0}, {259, 1}, {515, 2}, {1027, 4}, {2051, 6}, {3075, 35}, {4099, 7},
+    {131, 0}, {259, 1}, {515, 39}, {1027, 4}, {1540, 37}, {2051, 6}, {3075, 35}, {4099, 7},
     {8195, 10}, {12291, 31}, {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 20},
 };
 constexpr Bucket kVec4LN[] = {
@@ -83,7 +83,7 @@ constexpr Bucket kVec4LN[] = {
     {8195, 10}, {16387, 31}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
 };
 constexpr Bucket kVec4RMS[] = {
-    {131, 0}, {259, 2}, {515, 4}, {1027, 6}, {2051, 5}, {3075, 8}, {8195, 10},
+    {131, 0}, {259, 2}, {515, 39}, {1027, 6}, {1540, 35}, {2051, 5}, {3075, 8}, {8195, 10},
     {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
 };
 constexpr Bucket kVec4Softmax[] = {
@@ -93,7 +93,7 @@ constexpr Bucket kVec4Softmax[] = {
 // Affine LayerNorm (with or without residual), weighted RMSNorm, and the
 // row reductions (sum, min/max), from the same sweep.
 constexpr Bucket kVec4Affine[] = {
-    {131, 0}, {259, 1}, {515, 2}, {1027, 4}, {2051, 6}, {4099, 7},
+    {131, 0}, {259, 1}, {515, 39}, {1540, 37}, {2051, 6}, {4099, 7},
     {8195, 10}, {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 20},
 };
 constexpr Bucket kVec4Weighted[] = {
@@ -101,7 +101,7 @@ constexpr Bucket kVec4Weighted[] = {
     {8195, 10}, {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
 };
 constexpr Bucket kVec4RowReduce[] = {
-    {131, 0}, {259, 1}, {515, 2}, {1027, 4}, {2051, 6}, {3075, 35}, {4099, 7},
+    {131, 0}, {259, 1}, {515, 2}, {1027, 39}, {1540, 37}, {2051, 6}, {3075, 35}, {4099, 7},
     {6147, 32}, {8195, 10}, {16387, 31}, {32771, 34}, {65539, 33}, {TILE_MAX_WIDTH, 30},
 };
 // Small problems (rows * width <= kSmallElems, L2 resident): the few
@@ -113,33 +113,38 @@ constexpr Bucket kSmallLN[] = {{131, -1}, {259, 2}, {4099, -1}, {8195, 32}, {327
 constexpr Bucket kSmallRMS[] = {{1027, -1}, {2051, 6}, {3075, -1}, {4099, 7}, {32771, -1}, {65539, 33}};
 constexpr Bucket kSmallSoftmax[] = {{32771, -1}, {65539, 33}};
 
-// BF16 rows (16-byte vectors of 8 values), from the BF16 sweep.  The row
-// reductions and weighted RMSNorm use the RMSNorm table, affine LayerNorm
-// the LayerNorm table.
+// BF16 rows (16-byte vectors of 8 values), from the BF16 sweep.  Weighted
+// RMSNorm uses the RMSNorm table, affine LayerNorm the LayerNorm table.
 constexpr Bucket kBf16ResidualLN[] = {
     {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {4103, 6}, {8199, 8},
     {16391, 10}, {32775, 13}, {65543, 17}, {TILE_MAX_WIDTH, 33},
 };
 constexpr Bucket kBf16LN[] = {
-    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {4103, 6}, {8199, 8},
+    {263, 0}, {519, 1}, {1031, 2}, {1543, 39}, {2055, 4}, {4103, 6}, {8199, 8},
     {16391, 10}, {32775, 14}, {65543, 17}, {TILE_MAX_WIDTH, 19},
 };
 constexpr Bucket kBf16RMS[] = {
-    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {4103, 6}, {8199, 8},
+    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {3079, 37}, {4103, 6}, {6151, 7}, {8199, 8},
     {16391, 11}, {32775, 13}, {65543, 17}, {TILE_MAX_WIDTH, 19},
 };
 constexpr Bucket kBf16Softmax[] = {
-    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {4103, 6}, {8199, 8},
+    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {4103, 6}, {8199, 7},
     {16391, 10}, {32775, 15}, {65543, 16}, {TILE_MAX_WIDTH, 18},
+};
+constexpr Bucket kBf16RowReduce[] = {
+    {263, 0}, {519, 1}, {1031, 2}, {1543, 39}, {2055, 4}, {4103, 37}, {8199, 7},
+    {16391, 10}, {32775, 15}, {65543, 17}, {TILE_MAX_WIDTH, 19},
 };
 
 // BF16 rows of whole 16-byte vectors on 16-byte aligned pointers, more than
 // kSmallElems elements: the widths where a shared-memory-staged plan beat
 // every register plan in the BF16 sweep (residual LayerNorm 65536x4096:
-// 269 us vs 322 us; 4096x16384: 67 us vs 125 us).  -1: use the table above.
-constexpr Bucket kStagedBf16ResidualLN[] = {{1024, -1}, {2048, 43}, {8192, 42}, {16384, 40}};
-constexpr Bucket kStagedBf16LN[] = {{8192, -1}, {16384, 40}};
-constexpr Bucket kStagedBf16Softmax[] = {{4096, -1}, {8192, 42}, {16384, 40}};
+// 269 us vs 322 us; 4096x16384: 66 us vs 125 us).  -1: use the table above.
+// (BF16 softmax, with its base-2 exponential, is fastest on register plans.)
+constexpr Bucket kStagedBf16ResidualLN[] = {{1024, -1}, {2048, 46}, {3072, 44}, {4096, 45},
+                                            {6144, 42}, {8192, 45}, {16384, 43}};
+constexpr Bucket kStagedBf16LN[] = {{4096, -1}, {6144, 45}, {8192, -1}, {16384, 43}};
+constexpr Bucket kStagedBf16RMS[] = {{8192, -1}, {12288, 43}};
 
 constexpr Bucket kVec1[] = {
     {128, 25}, {1024, 26}, {4096, 27}, {16384, 28}, {TILE_MAX_WIDTH, 29},
@@ -161,7 +166,7 @@ int select_plan(int op, long long rows, int width, bool vec4, int dtype,
             switch (op) {
                 case TILE_OP_RESIDUAL_LAYERNORM: sid = pick(kStagedBf16ResidualLN, width); break;
                 case TILE_OP_LAYERNORM: sid = pick(kStagedBf16LN, width); break;
-                case TILE_OP_SOFTMAX: sid = pick(kStagedBf16Softmax, width); break;
+                case TILE_OP_RMSNORM: sid = pick(kStagedBf16RMS, width); break;
                 default: break;
             }
             if (sid >= 0 && covers(kPlans[sid], width, dtype)) return sid;
@@ -172,6 +177,8 @@ int select_plan(int op, long long rows, int width, bool vec4, int dtype,
             case TILE_OP_LAYERNORM:
             case TILE_OP_LAYERNORM_AFFINE: id = pick(kBf16LN, width); break;
             case TILE_OP_SOFTMAX: id = pick(kBf16Softmax, width); break;
+            case TILE_OP_ROW_SUM:
+            case TILE_OP_ROW_MINMAX: id = pick(kBf16RowReduce, width); break;
             default: id = pick(kBf16RMS, width); break;
         }
         return (id >= 0 && covers(kPlans[id], width, dtype)) ? id : -1;
@@ -684,6 +691,9 @@ int tile_plan_info_ex(int id, int op, int dtype, int rows, int width, tile_plan_
     if (!valid_op(op)) return TILE_ERR_OP;
     if (dtype != TILE_DTYPE_F32 && dtype != TILE_DTYPE_BF16) return TILE_ERR_DTYPE;
     if (!built(kPlans[id], dtype)) return TILE_ERR_PLAN;
+    // the staged kernel has no row-reduction (sum, min/max) variant
+    if (kPlans[id].staged && (op == TILE_OP_ROW_SUM || op == TILE_OP_ROW_MINMAX))
+        return TILE_ERR_PLAN;
     if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH || !covers(kPlans[id], width, dtype))
         return TILE_ERR_SHAPE;
     if (plan == nullptr) return TILE_ERR_NULL;

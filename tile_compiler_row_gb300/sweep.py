@@ -42,7 +42,10 @@ def shapes(quick=False):
 
 
 def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g=None, y2=None,
-              graph=False):
+              graph=False, cutoff=None):
+    """Median microseconds per call of ``plan``.  With ``cutoff`` (µs), a plan
+    whose first call after one warm-up already takes longer is not timed
+    further: that single call's time is returned."""
     import ctypes
 
     import torch
@@ -63,6 +66,16 @@ def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g
         if st != 0:
             raise RuntimeError(f"plan {plan}: status {st}")
 
+    if cutoff is not None and not graph:
+        call()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        first = e0.elapsed_time(e1) * 1e3
+        if first > cutoff:
+            return first
     for _ in range(warmup):
         call()
     if graph:
@@ -141,8 +154,10 @@ def main(argv=None):
                 info = tile.tile_plan_info_ex(pid, op, args.dtype, rows, width)
                 if info is None or info["vec"] == 1 or info["grid"] > 0x7FFFFFFF:
                     continue
+                best_so_far = min(entry["plans"].values(), default=None)
                 us = time_plan(lib, code, pid, x, r, y, rows, width, args.warmup, args.iters, stream,
-                               g=g, y2=y2, graph=args.graph)
+                               g=g, y2=y2, graph=args.graph,
+                               cutoff=None if best_so_far is None else 3.0 * best_so_far)
                 entry["plans"][pid] = round(us, 3)
             best = min(entry["plans"], key=entry["plans"].get)
             entry["best"] = best
