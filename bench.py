@@ -411,6 +411,15 @@ def run_ours(args, dist):
                                f"in a ring of {slots} device slots, copies in overlapped with "
                                "kernels that store straight into the pinned output"}
         ref = torch.empty_like(x)
+        # The link alone on this machine, for context: a plain host->device
+        # copy of one pinned input tensor.  The pipeline's floor is its
+        # host->device bytes at this rate.
+        for _ in range(2):
+            ref.copy_(xp, non_blocking=True)
+        _, link_ms = time_calls(lambda: ref.copy_(xp, non_blocking=True), 5, stream)
+        link_gbs = elems * 4 * 5 / (link_ms * 1e-3) / 1e9
+        line["e2e"]["link_h2d_gbs"] = round(link_gbs, 1)
+        line["e2e"]["link_floor_ms"] = round(h2d / (link_gbs * 1e9) * 1e3, 3)
         call_op(op, ref, args.plan)
         torch.cuda.synchronize()
         if not torch.equal(yp[:64].cuda(), ref[:64]):

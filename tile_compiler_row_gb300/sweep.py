@@ -32,11 +32,13 @@ SMALL = ((1, 127), (17, 257), (7, 1537), (64, 4096), (1024, 4096), (128, 8192),
          (32, 65536))
 
 
-def shapes(quick=False):
+def shapes(quick=False, elems_log2=26):
+    """The ladder at about 2**elems_log2 elements per tensor (256 MiB of FP32
+    at 26, of BF16 at 27: twice the 129 MB L2), then the small shapes."""
     out = []
     ladder = LADDER if not quick else (257, 1024, 4096, 8192, 65536)
     for w in ladder:
-        out.append((max(16, (1 << 26) // w), w))
+        out.append((max(16, (1 << elems_log2) // w), w))
     out.extend(SMALL)
     return out
 
@@ -130,7 +132,7 @@ def main(argv=None):
     torch.cuda.set_device(0)
     stream = torch.cuda.current_stream()
     results = []
-    todo = shapes(args.quick) if args.shapes is None else \
+    todo = shapes(args.quick, 27 if args.dtype == "bf16" else 26) if args.shapes is None else \
         [tuple(int(v) for v in sh.split("x")) for sh in args.shapes.split(",")]
     if args.small:
         todo = list(SMALL)
