@@ -276,6 +276,12 @@ int tile_gelu_tanh_pair_f32(const float *in, float *value, float *derivative, lo
                             cudaStream_t stream);
 
 /* ---- end to end on host buffers ---------------------------------------- */
+/* The notes time single calls in two phases, GPU time and end to end with
+ * the host's part included ("Immutable input reuse in Metal reductions",
+ * "Fixed-width GPU and dispatch results"); on a GPU whose inputs start in
+ * host memory the end-to-end phase also moves the rows across the host
+ * link, which these entry points pipeline.  The notes have no interface of
+ * this kind: its arguments and schedule are this library's own. */
 
 /* Run `op` on HOST buffers h_in[, h_residual] -> h_out ([rows][width] FP32
  * each).  Rows stream through the caller's device workspace `d_work`

@@ -128,7 +128,7 @@ constexpr Bucket kBf16RMS[] = {
     {16391, 11}, {32775, 13}, {65543, 17}, {TILE_MAX_WIDTH, 19},
 };
 constexpr Bucket kBf16Softmax[] = {
-    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {4103, 6}, {8199, 7},
+    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {3079, 37}, {4103, 6}, {8199, 7},
     {16391, 10}, {32775, 15}, {65543, 16}, {TILE_MAX_WIDTH, 18},
 };
 constexpr Bucket kBf16RowReduce[] = {
@@ -143,7 +143,8 @@ constexpr Bucket kBf16RowReduce[] = {
 // (BF16 softmax, with its base-2 exponential, is fastest on register plans.)
 constexpr Bucket kStagedBf16ResidualLN[] = {{1024, -1}, {2048, 46}, {3072, 44}, {4096, 45},
                                             {6144, 42}, {8192, 45}, {16384, 43}};
-constexpr Bucket kStagedBf16LN[] = {{4096, -1}, {6144, 45}, {8192, -1}, {16384, 43}};
+constexpr Bucket kStagedBf16LN[] = {{2048, -1}, {3072, 47}, {4096, -1}, {6144, 45},
+                                    {8192, -1}, {16384, 43}};
 constexpr Bucket kStagedBf16RMS[] = {{8192, -1}, {12288, 43}};
 
 constexpr Bucket kVec1[] = {
