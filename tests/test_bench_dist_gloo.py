@@ -81,3 +81,40 @@ def test_cpu_baseline_row_blocks_cover_every_row_once(op, threads):
     parts = bench.oracle_rows(orc, op, x, r, eps, threads)
     assert len(parts) == min(threads, rows)
     assert np.array_equal(np.concatenate(parts), orc.run(op, x, r, eps))
+
+
+def _bench(args, env_extra=None):
+    import json
+    import subprocess
+    env = dict(os.environ)
+    env.update(env_extra or {})
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                       capture_output=True, text=True, env=env, timeout=300, cwd=ROOT)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    return [json.loads(l) for l in lines]
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference`: the FP64 oracle on the host cores, one
+    JSON line with the headline's metric and unit, no GPU work."""
+    sys.path.insert(0, ROOT)
+    import bench
+    out = _bench(["--impl", "reference", "--steps", "3", "--warmup", "3", "--rows", "2048",
+                  "--width", "512"])
+    assert len(out) == 1
+    d = out[0]
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["value"] > 0 and d["steps"] == 3 and d["warmup"] == 3
+    assert d["higher_is_better"] is True and d["gpu_launches"] == 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    out = _bench(["--impl", "reference", "--gpus", "2", "--steps", "3", "--warmup", "3",
+                  "--rows", "256", "--width", "256"],
+                 {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert out == []
