@@ -206,3 +206,22 @@ def test_bf16_selected_staged_plans(op, rows, width):
     staged = (op == "residual_layernorm" or (op == "layernorm" and width >= 12288)
               or (op == "rmsnorm" and width == 12288))
     assert (tile.tile_describe_plan_ex(op, "bf16", rows, width)["path"] == 2) == staged
+
+
+@pytest.mark.parametrize("op", ["layernorm", "residual_layernorm"])
+@pytest.mark.parametrize("rows,width", [(4, 257), (2048, 4096), (512, 16384)])
+def test_bf16_constant_rows_normalise_to_zero(op, rows, width):
+    """Constant rows (the closed form gives LayerNorm output 0) on register
+    and staged plans: every output within the absolute bound of 0."""
+    vals = torch.tensor([0.1, 3.140625, -7.5, 1000.0, -20000.0], dtype=torch.float32)
+    x = vals[torch.arange(rows) % len(vals)][:, None].expand(rows, width).contiguous()
+    x = x.to(torch.bfloat16).cuda()
+    y = torch.full_like(x, float("nan"))
+    if op == "residual_layernorm":
+        r = torch.zeros_like(x)
+        tile.tile_residual_layernorm_bf16(x, r, y, EPS)
+    else:
+        tile.tile_layernorm_bf16(x, y, EPS)
+    torch.cuda.synchronize()
+    got = y.float().cpu().numpy()
+    assert np.all(np.abs(got) <= ATOL), f"{op} {rows}x{width}: max |y| {np.abs(got).max():.3e}"

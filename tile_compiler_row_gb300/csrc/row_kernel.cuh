@@ -111,6 +111,22 @@ __device__ __forceinline__ float softmax_exp(float t) {
     }
 }
 
+// LayerNorm output map of a centred value d (centred on the mean estimate,
+// with mu1 the remaining mean offset): (d - mu1) rstd.  FP32 rows use that
+// form, which is exactly 0 for a constant row (every d equals mu1).  BF16
+// rows, whose kernels are bound by instruction issue and whose outputs keep
+// 8 significant bits, use one FMA, d rstd + (-mu1 rstd): it differs from the
+// two-step form by at most the rounding of mu1 rstd (mu1 is the rounding
+// error of the mean estimate, so about 2^-24 |mean| rstd), and a constant
+// row gives |y| of that order instead of an exact 0.
+template <class T>
+__device__ __forceinline__ float ln_out(float d, float mu1, float rstd) {
+    if constexpr (sizeof(T) == 2)
+        return fmaf(d, rstd, -mu1 * rstd);
+    else
+        return (d - mu1) * rstd;
+}
+
 // ---------------------------------------------------------------------------
 // cluster primitives (inline PTX)
 // ---------------------------------------------------------------------------
@@ -425,9 +441,9 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
-            for (int j = 0; j < EV; ++j) v[k][j] = (v[k][j] - mu1) * rstd;
-        hv = (hv - mu1) * rstd;
-        tv = (tv - mu1) * rstd;
+            for (int j = 0; j < EV; ++j) v[k][j] = ln_out<T>(v[k][j], mu1, rstd);
+        hv = ln_out<T>(hv, mu1, rstd);
+        tv = ln_out<T>(tv, mu1, rstd);
     } else if constexpr (OP == OP_RMS) {
         // ---- a2: mean square ---------------------------------------------
         float acc[EV];

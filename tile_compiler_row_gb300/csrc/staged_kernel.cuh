@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int
 #pragma unroll
             for (int k = 0; k < K; ++k)
 #pragma unroll
-                for (int j = 0; j < EV; ++j) v[k][j] = (v[k][j] - mu1) * rstd;
+                for (int j = 0; j < EV; ++j) v[k][j] = ln_out<T>(v[k][j], mu1, rstd);
         } else if constexpr (OP == OP_RMS) {
 #pragma unroll
             for (int k = 0; k < K; ++k)
