@@ -203,7 +203,7 @@ def test_bf16_selected_staged_plans(op, rows, width):
             getattr(tile, f"tile_{op}_bf16")(_placed(x, off), out, EPS)
         check_bf16(out, ref, what=f"bf16 {op} {rows}x{width} offset {off}")
     # The sweep found the staged kernel faster only for these BF16 shapes.
-    staged = (op == "residual_layernorm" or (op == "layernorm" and width >= 12288)
+    staged = (op == "residual_layernorm" or (op == "layernorm" and width >= 8192)
               or (op == "rmsnorm" and width == 12288))
     assert (tile.tile_describe_plan_ex(op, "bf16", rows, width)["path"] == 2) == staged
 

@@ -128,6 +128,109 @@ __device__ __forceinline__ float ln_out(float d, float mu1, float rstd) {
 }
 
 // ---------------------------------------------------------------------------
+// Lane-wise arithmetic on a vector of EV FP32 lanes.  With PK (BF16 rows,
+// whose kernels are bound by instruction issue) two lanes go through one
+// packed instruction (PTX add / mul / fma .rn.f32x2, sm_100 and later); each
+// lane is rounded exactly as by the scalar instruction, so the results are
+// the same bit for bit with half the arithmetic instructions.  Without PK
+// (FP32 rows, bound by DRAM) the scalar loop is kept.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void add_x2(float &a0, float &a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb;\n\tmov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
+        "add.rn.f32x2 ra, ra, rb;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void mul_x2(float &a0, float &a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb;\n\tmov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
+        "mul.rn.f32x2 ra, ra, rb;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
+}
+// (a0, a1) = (b0 * c0 + a0, b1 * c1 + a1), fused
+__device__ __forceinline__ void fma_x2(float &a0, float &a1, float b0, float b1, float c0,
+                                       float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\tmov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
+        "mov.b64 rc, {%4, %5};\n\tfma.rn.f32x2 ra, rb, rc, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// a[j] += b[j]
+template <bool PK, int EV>
+__device__ __forceinline__ void vadd(float (&a)[EV], const float (&b)[EV]) {
+    if constexpr (PK && EV % 2 == 0) {
+#pragma unroll
+        for (int j = 0; j < EV; j += 2) add_x2(a[j], a[j + 1], b[j], b[j + 1]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < EV; ++j) a[j] += b[j];
+    }
+}
+// a[j] += c
+template <bool PK, int EV>
+__device__ __forceinline__ void vadd_c(float (&a)[EV], float c) {
+    if constexpr (PK && EV % 2 == 0) {
+#pragma unroll
+        for (int j = 0; j < EV; j += 2) add_x2(a[j], a[j + 1], c, c);
+    } else {
+#pragma unroll
+        for (int j = 0; j < EV; ++j) a[j] += c;
+    }
+}
+// a[j] *= c
+template <bool PK, int EV>
+__device__ __forceinline__ void vmul_c(float (&a)[EV], float c) {
+    if constexpr (PK && EV % 2 == 0) {
+#pragma unroll
+        for (int j = 0; j < EV; j += 2) mul_x2(a[j], a[j + 1], c, c);
+    } else {
+#pragma unroll
+        for (int j = 0; j < EV; ++j) a[j] *= c;
+    }
+}
+// acc[j] = fma(d[j], d[j], acc[j])
+template <bool PK, int EV>
+__device__ __forceinline__ void vsq_acc(float (&acc)[EV], const float (&d)[EV]) {
+    if constexpr (PK && EV % 2 == 0) {
+#pragma unroll
+        for (int j = 0; j < EV; j += 2) fma_x2(acc[j], acc[j + 1], d[j], d[j + 1], d[j], d[j + 1]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < EV; ++j) acc[j] = fmaf(d[j], d[j], acc[j]);
+    }
+}
+// a[j] = fma(a[j], b, c)
+template <bool PK, int EV>
+__device__ __forceinline__ void vfma_c(float (&a)[EV], float b, float c) {
+    if constexpr (PK && EV % 2 == 0) {
+#pragma unroll
+        for (int j = 0; j < EV; j += 2) {
+            float c0 = c, c1 = c;
+            fma_x2(c0, c1, a[j], a[j + 1], b, b);
+            a[j] = c0;
+            a[j + 1] = c1;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < EV; ++j) a[j] = fmaf(a[j], b, c);
+    }
+}
+// a[j] = fma(a[j], b[j], c[j])
+template <bool PK, int EV>
+__device__ __forceinline__ void vfma(float (&a)[EV], const float (&b)[EV], const float (&c)[EV]) {
+    if constexpr (PK && EV % 2 == 0) {
+#pragma unroll
+        for (int j = 0; j < EV; j += 2) {
+            float c0 = c[j], c1 = c[j + 1];
+            fma_x2(c0, c1, a[j], a[j + 1], b[j], b[j + 1]);
+            a[j] = c0;
+            a[j + 1] = c1;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < EV; ++j) a[j] = fmaf(a[j], b[j], c[j]);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // cluster primitives (inline PTX)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -313,6 +416,13 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
     // x and for -x alike), 0 for sums.
     constexpr float kFill = (OP == OP_SOFTMAX) ? -INFINITY : (OP == OP_MINMAX) ? NAN : 0.0f;
     constexpr bool kRowOutput = (OP == OP_SUM || OP == OP_MINMAX);
+    // BF16 LayerNorm rows of 16-byte vectors, the op with the most lane
+    // arithmetic: packed pairs (BF16 LayerNorm 166 -> 159 us at 65536x4096),
+    // except in 1024-thread CTAs, whose 64-register cap the paired operands
+    // (aligned register pairs) would push into spills.  BF16 RMSNorm and
+    // softmax measured no gain at 4096 columns and a loss at 12288-16384.
+    constexpr bool PK = sizeof(T) == 2 && V == 4 && 32 * S * P <= 512 &&
+                        (OP == OP_LN || OP == OP_RESLN);
 
     __shared__ float part1[S > 1 ? 2 * P * S : 1];
     __shared__ float part2[S > 1 ? 2 * P * S : 1];
@@ -371,8 +481,7 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
                 if constexpr (OP == OP_RESLN) {
                     float b[EV];
                     Elem<T>::load_vec(rr + h + EV * i, b);
-#pragma unroll
-                    for (int j = 0; j < EV; ++j) v[k][j] += b[j];
+                    vadd<PK, EV>(v[k], b);
                 }
             } else {
                 float t = Elem<T>::load(xr + i);
@@ -409,9 +518,7 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
 #pragma unroll
         for (int j = 0; j < EV; ++j) acc[j] = 0.0f;
 #pragma unroll
-        for (int k = 0; k < K; ++k)
-#pragma unroll
-            for (int j = 0; j < EV; ++j) acc[j] += v[k][j];
+        for (int k = 0; k < K; ++k) vadd<PK, EV>(acc, v[k]);
         float s[1] = {lane_total(acc) + (hv + tv)};
         row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
         const float mean0 = s[0] / n;
@@ -422,12 +529,24 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             const bool ok = k * (C * W) + gw < nb;
+            if constexpr (PK) {
+                // d = v + (-mean0) is v - mean0 exactly; empty slots give 0
+                if (ok) {
+                    vadd_c<PK, EV>(v[k], -mean0);
+                    vadd<PK, EV>(a1, v[k]);
+                    vsq_acc<PK, EV>(a2, v[k]);
+                } else {
 #pragma unroll
-            for (int j = 0; j < EV; ++j) {
-                const float d = ok ? v[k][j] - mean0 : 0.0f;
-                v[k][j] = d;
-                a1[j] += d;
-                a2[j] = fmaf(d, d, a2[j]);
+                    for (int j = 0; j < EV; ++j) v[k][j] = 0.0f;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < EV; ++j) {
+                    const float d = ok ? v[k][j] - mean0 : 0.0f;
+                    v[k][j] = d;
+                    a1[j] += d;
+                    a2[j] = fmaf(d, d, a2[j]);
+                }
             }
         }
         hv = has_h ? hv - mean0 : 0.0f;
@@ -438,10 +557,16 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
         const float mu1 = q[0] / n;
         const float var = fmaxf(q[1] / n - mu1 * mu1, 0.0f);
         const float rstd = 1.0f / sqrtf(var + a.eps);
+        if constexpr (PK) {
+            const float nb_shift = -mu1 * rstd;      // ln_out<T>: one FMA per lane
 #pragma unroll
-        for (int k = 0; k < K; ++k)
+            for (int k = 0; k < K; ++k) vfma_c<PK, EV>(v[k], rstd, nb_shift);
+        } else {
 #pragma unroll
-            for (int j = 0; j < EV; ++j) v[k][j] = ln_out<T>(v[k][j], mu1, rstd);
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int j = 0; j < EV; ++j) v[k][j] = ln_out<T>(v[k][j], mu1, rstd);
+        }
         hv = ln_out<T>(hv, mu1, rstd);
         tv = ln_out<T>(tv, mu1, rstd);
     } else if constexpr (OP == OP_RMS) {
@@ -450,16 +575,12 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
 #pragma unroll
         for (int j = 0; j < EV; ++j) acc[j] = 0.0f;
 #pragma unroll
-        for (int k = 0; k < K; ++k)
-#pragma unroll
-            for (int j = 0; j < EV; ++j) acc[j] = fmaf(v[k][j], v[k][j], acc[j]);
+        for (int k = 0; k < K; ++k) vsq_acc<PK, EV>(acc, v[k]);
         float s[1] = {fmaf(hv, hv, fmaf(tv, tv, lane_total(acc)))};
         row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
         const float rstd = 1.0f / sqrtf(s[0] / n + a.eps);
 #pragma unroll
-        for (int k = 0; k < K; ++k)
-#pragma unroll
-            for (int j = 0; j < EV; ++j) v[k][j] *= rstd;
+        for (int k = 0; k < K; ++k) vmul_c<PK, EV>(v[k], rstd);
         hv *= rstd;
         tv *= rstd;
     } else if constexpr (OP == OP_SOFTMAX) {
@@ -479,22 +600,28 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
 #pragma unroll
         for (int j = 0; j < EV; ++j) acc[j] = 0.0f;
 #pragma unroll
-        for (int k = 0; k < K; ++k)
+        for (int k = 0; k < K; ++k) {
+            if constexpr (PK) {
+                vadd_c<PK, EV>(v[k], -mx);                      // v - mx, exactly
 #pragma unroll
-            for (int j = 0; j < EV; ++j) {
-                const float e = softmax_exp<T>(v[k][j] - mx);
-                v[k][j] = e;
-                acc[j] += e;
+                for (int j = 0; j < EV; ++j) v[k][j] = softmax_exp<T>(v[k][j]);
+                vadd<PK, EV>(acc, v[k]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < EV; ++j) {
+                    const float e = softmax_exp<T>(v[k][j] - mx);
+                    v[k][j] = e;
+                    acc[j] += e;
+                }
             }
+        }
         hv = softmax_exp<T>(hv - mx);
         tv = softmax_exp<T>(tv - mx);
         float s[1] = {lane_total(acc) + (hv + tv)};
         row_allreduce<Sum, 1, S, P, C>(s, part2, cpart + 1, program, warp, lane);
         const float inv = 1.0f / s[0];
 #pragma unroll
-        for (int k = 0; k < K; ++k)
-#pragma unroll
-            for (int j = 0; j < EV; ++j) v[k][j] *= inv;
+        for (int k = 0; k < K; ++k) vmul_c<PK, EV>(v[k], inv);
         hv *= inv;
         tv *= inv;
     } else if constexpr (OP == OP_SUM) {
@@ -569,8 +696,7 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
                             bb[j] = b != nullptr ? __ldg(b + col + j) : 0.0f;
                         }
                     }
-#pragma unroll
-                    for (int j = 0; j < EV; ++j) v[k][j] = fmaf(v[k][j], gg[j], bb[j]);
+                    vfma<PK, EV>(v[k], gg, bb);
                 }
             }
             if constexpr (V == 4) {

@@ -143,8 +143,7 @@ constexpr Bucket kBf16RowReduce[] = {
 // (BF16 softmax, with its base-2 exponential, is fastest on register plans.)
 constexpr Bucket kStagedBf16ResidualLN[] = {{1024, -1}, {2048, 46}, {3072, 44}, {4096, 45},
                                             {6144, 42}, {8192, 45}, {16384, 43}};
-constexpr Bucket kStagedBf16LN[] = {{2048, -1}, {3072, 47}, {4096, -1}, {6144, 45},
-                                    {8192, -1}, {16384, 43}};
+constexpr Bucket kStagedBf16LN[] = {{4096, -1}, {6144, 45}, {8192, 42}, {16384, 43}};
 constexpr Bucket kStagedBf16RMS[] = {{8192, -1}, {12288, 43}};
 
 constexpr Bucket kVec1[] = {
