@@ -109,10 +109,9 @@ __global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int
     constexpr int EV = 16 / sizeof(T);
     constexpr int NIN = (OP == OP_RESLN) ? 2 : 1;
     constexpr float kFill = (OP == OP_SOFTMAX) ? -INFINITY : 0.0f;
-    // Lane arithmetic stays scalar here: packed pairs (which need aligned
-    // register pairs) raised the BF16 kernels' registers from 96 to 112 and
-    // made BF16 residual LayerNorm 9 % slower at 65536x4096.
-    constexpr bool PK = false;
+    // Lane arithmetic stays scalar here: packed f32x2 pairs (as the register
+    // kernel uses for BF16 LayerNorm) raised these kernels' registers from 96
+    // to 112 and made BF16 residual LayerNorm 9 % slower at 65536x4096.
 
     extern __shared__ __align__(128) unsigned char stage_mem[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
@@ -190,7 +189,8 @@ __global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int
                 if constexpr (OP == OP_RESLN) {
                     float b[EV];
                     widen_vec<T>(lds128(sx + row_bytes + static_cast<size_t>(i) * 16), b);
-                    vadd<PK, EV>(v[k], b);
+#pragma unroll
+                    for (int j = 0; j < EV; ++j) v[k][j] += b[j];
                 }
             } else {
 #pragma unroll
@@ -205,16 +205,16 @@ __global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int
 #pragma unroll
             for (int j = 0; j < EV; ++j) acc[j] = kFill;
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
-                if constexpr (OP == OP_RMS) {
-                    vsq_acc<PK, EV>(acc, v[k]);
-                } else if constexpr (OP == OP_SOFTMAX) {
+            for (int k = 0; k < K; ++k)
 #pragma unroll
-                    for (int j = 0; j < EV; ++j) acc[j] = fmaxf(acc[j], v[k][j]);
-                } else {
-                    vadd<PK, EV>(acc, v[k]);
+                for (int j = 0; j < EV; ++j) {
+                    if constexpr (OP == OP_RMS)
+                        acc[j] = fmaf(v[k][j], v[k][j], acc[j]);
+                    else if constexpr (OP == OP_SOFTMAX)
+                        acc[j] = fmaxf(acc[j], v[k][j]);
+                    else
+                        acc[j] += v[k][j];
                 }
-            }
             float r1[1];
             if constexpr (OP == OP_SOFTMAX) {
                 r1[0] = lane_max(acc);
@@ -245,24 +245,12 @@ __global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const bool ok = k * W + tid < nb;
-                if constexpr (PK) {
-                    // d = v + (-mean0) is v - mean0 exactly; empty slots give 0
-                    if (ok) {
-                        vadd_c<PK, EV>(v[k], -mean0);
-                        vadd<PK, EV>(a1, v[k]);
-                        vsq_acc<PK, EV>(a2, v[k]);
-                    } else {
 #pragma unroll
-                        for (int j = 0; j < EV; ++j) v[k][j] = 0.0f;
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < EV; ++j) {
-                        const float d = ok ? v[k][j] - mean0 : 0.0f;
-                        v[k][j] = d;
-                        a1[j] += d;
-                        a2[j] = fmaf(d, d, a2[j]);
-                    }
+                for (int j = 0; j < EV; ++j) {
+                    const float d = ok ? v[k][j] - mean0 : 0.0f;
+                    v[k][j] = d;
+                    a1[j] += d;
+                    a2[j] = fmaf(d, d, a2[j]);
                 }
             }
             float q[2] = {lane_total(a1), lane_total(a2)};
@@ -270,44 +258,34 @@ __global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int
             const float mu1 = q[0] / n;
             const float var = fmaxf(q[1] / n - mu1 * mu1, 0.0f);
             rstd = 1.0f / sqrtf(var + a.eps);
-            if constexpr (PK) {
-                const float nb_shift = -mu1 * rstd;      // ln_out<T>: one FMA per lane
 #pragma unroll
-                for (int k = 0; k < K; ++k) vfma_c<PK, EV>(v[k], rstd, nb_shift);
-            } else {
+            for (int k = 0; k < K; ++k)
 #pragma unroll
-                for (int k = 0; k < K; ++k)
-#pragma unroll
-                    for (int j = 0; j < EV; ++j) v[k][j] = ln_out<T>(v[k][j], mu1, rstd);
-            }
+                for (int j = 0; j < EV; ++j) v[k][j] = ln_out<T>(v[k][j], mu1, rstd);
         } else if constexpr (OP == OP_RMS) {
 #pragma unroll
-            for (int k = 0; k < K; ++k) vmul_c<PK, EV>(v[k], rstd);
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int j = 0; j < EV; ++j) v[k][j] *= rstd;
         } else {
             float acc[EV];
 #pragma unroll
             for (int j = 0; j < EV; ++j) acc[j] = 0.0f;
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
-                if constexpr (PK) {
-                    vadd_c<PK, EV>(v[k], -mx);                  // v - mx, exactly
+            for (int k = 0; k < K; ++k)
 #pragma unroll
-                    for (int j = 0; j < EV; ++j) v[k][j] = softmax_exp<T>(v[k][j]);
-                    vadd<PK, EV>(acc, v[k]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < EV; ++j) {
-                        const float e = softmax_exp<T>(v[k][j] - mx);
-                        v[k][j] = e;
-                        acc[j] += e;
-                    }
+                for (int j = 0; j < EV; ++j) {
+                    const float e = softmax_exp<T>(v[k][j] - mx);
+                    v[k][j] = e;
+                    acc[j] += e;
                 }
-            }
             float r2[1] = {lane_total(acc)};
             row_allreduce<Sum, 1, S, 1, 1>(r2, part2[pb], nullptr, 0, warp, lane);
             const float inv = 1.0f / r2[0];
 #pragma unroll
-            for (int k = 0; k < K; ++k) vmul_c<PK, EV>(v[k], inv);
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int j = 0; j < EV; ++j) v[k][j] *= inv;
         }
 
         // optional per-column scale and shift (gamma/beta FP32, 16-byte aligned)
@@ -317,7 +295,6 @@ __global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int
                 for (int k = 0; k < K; ++k) {
                     const int i = k * W + tid;
                     if (i < nb) {
-                        float gg[EV], bb[EV];
 #pragma unroll
                         for (int q = 0; q < EV / 4; ++q) {
                             const float4 g4 =
@@ -325,12 +302,11 @@ __global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int
                             float4 b4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                             if (a.beta != nullptr)
                                 b4 = __ldg(reinterpret_cast<const float4 *>(a.beta + EV * i) + q);
-                            gg[4 * q] = g4.x; gg[4 * q + 1] = g4.y;
-                            gg[4 * q + 2] = g4.z; gg[4 * q + 3] = g4.w;
-                            bb[4 * q] = b4.x; bb[4 * q + 1] = b4.y;
-                            bb[4 * q + 2] = b4.z; bb[4 * q + 3] = b4.w;
+                            v[k][4 * q] = fmaf(v[k][4 * q], g4.x, b4.x);
+                            v[k][4 * q + 1] = fmaf(v[k][4 * q + 1], g4.y, b4.y);
+                            v[k][4 * q + 2] = fmaf(v[k][4 * q + 2], g4.z, b4.z);
+                            v[k][4 * q + 3] = fmaf(v[k][4 * q + 3], g4.w, b4.w);
                         }
-                        vfma<PK, EV>(v[k], gg, bb);
                     }
                 }
             }
