@@ -127,6 +127,30 @@ __device__ __forceinline__ float ln_out(float d, float mu1, float rstd) {
         return (d - mu1) * rstd;
 }
 
+// v[j] += the 16-byte vector `t` of element type T (4 FP32 or 8 BF16 lanes,
+// the lower address in the lower half of each word).  BF16 lanes use the
+// mixed-precision add (PTX add.rn.f32.bf16, sm_100 and later): the BF16
+// operand is widened exactly inside the instruction, so each lane is
+// round(v + x) as after an explicit widening, one instruction instead of two.
+template <class T>
+__device__ __forceinline__ void add_raw_vec(float (&v)[16 / sizeof(T)], uint4 t) {
+    if constexpr (sizeof(T) == 4) {
+        v[0] += __uint_as_float(t.x);
+        v[1] += __uint_as_float(t.y);
+        v[2] += __uint_as_float(t.z);
+        v[3] += __uint_as_float(t.w);
+    } else {
+        const unsigned int w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+                "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+                : "+f"(v[2 * i]), "+f"(v[2 * i + 1])
+                : "r"(w[i]));
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Lane-wise arithmetic on a vector of EV FP32 lanes.  With PK (BF16 rows,
 // whose kernels are bound by instruction issue) two lanes go through one
@@ -479,9 +503,13 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
             if constexpr (V == 4) {
                 Elem<T>::load_vec(xr + h + EV * i, v[k]);
                 if constexpr (OP == OP_RESLN) {
-                    float b[EV];
-                    Elem<T>::load_vec(rr + h + EV * i, b);
-                    vadd<PK, EV>(v[k], b);
+                    if constexpr (sizeof(T) == 2) {
+                        add_raw_vec<T>(v[k], __ldcs(reinterpret_cast<const uint4 *>(rr + h + EV * i)));
+                    } else {
+                        float b[EV];
+                        Elem<T>::load_vec(rr + h + EV * i, b);
+                        vadd<PK, EV>(v[k], b);
+                    }
                 }
             } else {
                 float t = Elem<T>::load(xr + i);

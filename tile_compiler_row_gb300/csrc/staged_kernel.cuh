@@ -186,12 +186,8 @@ __global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int
             const int i = k * W + tid;
             if (i < nb) {
                 widen_vec<T>(lds128(sx + static_cast<size_t>(i) * 16), v[k]);
-                if constexpr (OP == OP_RESLN) {
-                    float b[EV];
-                    widen_vec<T>(lds128(sx + row_bytes + static_cast<size_t>(i) * 16), b);
-#pragma unroll
-                    for (int j = 0; j < EV; ++j) v[k][j] += b[j];
-                }
+                if constexpr (OP == OP_RESLN)
+                    add_raw_vec<T>(v[k], lds128(sx + row_bytes + static_cast<size_t>(i) * 16));
             } else {
 #pragma unroll
                 for (int j = 0; j < EV; ++j) v[k][j] = kFill;
