@@ -370,7 +370,10 @@ int tile_run_host_static_f32(int op, const float *h_in, const float *h_residual,
 int tile_describe_plan(int op, int rows, int width, tile_plan_t *plan);
 
 /* tile_describe_plan for an element type (TILE_DTYPE_*); TILE_ERR_DTYPE for
- * an unknown one. */
+ * an unknown one.  For BF16 the answer may be a shared-memory-staged plan
+ * (path TILE_PATH_STAGED), which a call takes only when every pointer is
+ * 16-byte aligned and width is a multiple of 8 (whole 16-byte rows); other
+ * calls of that shape take the register plan of the same width. */
 int tile_describe_plan_ex(int op, int dtype, int rows, int width, tile_plan_t *plan);
 
 /* Number of plans built into the library, and plan `id` of that table
