@@ -67,6 +67,7 @@ extern "C" {
 /* ---- element types of row data (tile_row_args_t, tile_*_ex) ------------ */
 #define TILE_DTYPE_F32  0   /* IEEE binary32                                  */
 #define TILE_DTYPE_BF16 1   /* bfloat16: the high 16 bits of a binary32       */
+#define TILE_DTYPE_F16  2   /* IEEE binary16                                  */
 
 /* ---- operation codes (tile_describe_plan, tile_run_plan_*) ------------- */
 #define TILE_OP_RESIDUAL_LAYERNORM 0
@@ -101,7 +102,7 @@ typedef struct tile_plan {
     int id;                 /* index in the built plan table                  */
     int path;               /* TILE_PATH_*                                    */
     int vec;                /* elements per access: a 16-byte vector (4 FP32  */
-                            /* or 8 BF16, + scalar head/tail), or 1           */
+                            /* or 8 BF16/FP16, + scalar head/tail), or 1      */
     int warps_per_program;  /* S                                              */
     int programs_per_cta;   /* P                                              */
     int chunks;             /* K: V-vectors per worker                        */
@@ -181,7 +182,7 @@ typedef struct tile_row_args {
     float *out2;            /* [rows] FP32 maxima (TILE_OP_ROW_MINMAX)          */
     int rows, width;
     float eps;              /* normalisers only                                  */
-    int dtype;              /* TILE_DTYPE_F32 or TILE_DTYPE_BF16                */
+    int dtype;              /* TILE_DTYPE_F32, TILE_DTYPE_BF16 or TILE_DTYPE_F16 */
 } tile_row_args_t;
 
 /* Any row operation with the built plan `plan_id` forced (plan sweeps,
@@ -214,6 +215,31 @@ int tile_rmsnorm_weighted_bf16(const void *in, const float *gamma, void *out, in
 int tile_row_sum_bf16(const void *in, float *sums, int rows, int width, cudaStream_t stream);
 int tile_row_minmax_bf16(const void *in, float *mins, float *maxs, int rows, int width,
                          cudaStream_t stream);
+
+/* ---- FP16 rows ----------------------------------------------------------
+ * The same row operations on IEEE binary16 data (the "FP16 I/O" of low
+ * precision the pages name as not covered, same section as above): each
+ * element is widened exactly to FP32, every reduction and map runs in FP32,
+ * outputs are rounded to nearest-even binary16 (an output beyond 65504
+ * becomes +-inf, as a binary16 rounding does; normalised rows stay far below
+ * it).  Layout, alignment, vectors, plans and errors as the BF16 entry
+ * points; gamma, beta and the row outputs of sum and min/max stay FP32. */
+int tile_residual_layernorm_f16(const void *in, const void *residual, void *out, int rows,
+                                int width, float eps, cudaStream_t stream);
+int tile_layernorm_f16(const void *in, void *out, int rows, int width, float eps,
+                       cudaStream_t stream);
+int tile_rmsnorm_f16(const void *in, void *out, int rows, int width, float eps,
+                     cudaStream_t stream);
+int tile_softmax_f16(const void *in, void *out, int rows, int width, float eps,
+                     cudaStream_t stream);
+int tile_layernorm_affine_f16(const void *in, const void *residual, const float *gamma,
+                              const float *beta, void *out, int rows, int width, float eps,
+                              cudaStream_t stream);
+int tile_rmsnorm_weighted_f16(const void *in, const float *gamma, void *out, int rows,
+                              int width, float eps, cudaStream_t stream);
+int tile_row_sum_f16(const void *in, float *sums, int rows, int width, cudaStream_t stream);
+int tile_row_minmax_f16(const void *in, float *mins, float *maxs, int rows, int width,
+                        cudaStream_t stream);
 
 /* ---- backward passes ---------------------------------------------------
  * Input gradients of LayerNorm, RMSNorm and softmax, FP32.  The pages do
@@ -370,7 +396,7 @@ int tile_run_host_static_f32(int op, const float *h_in, const float *h_residual,
 int tile_describe_plan(int op, int rows, int width, tile_plan_t *plan);
 
 /* tile_describe_plan for an element type (TILE_DTYPE_*); TILE_ERR_DTYPE for
- * an unknown one.  For BF16 the answer may be a shared-memory-staged plan
+ * an unknown one.  For BF16 and FP16 the answer may be a shared-memory-staged plan
  * (path TILE_PATH_STAGED), which a call takes only when every pointer is
  * 16-byte aligned and width is a multiple of 8 (whole 16-byte rows); other
  * calls of that shape take the register plan of the same width. */
@@ -383,7 +409,7 @@ int tile_plan_count(void);
 int tile_plan_info(int id, int op, int rows, int width, tile_plan_t *plan);
 
 /* tile_plan_info for an element type; TILE_ERR_PLAN also when plan `id` is
- * not built for that type (BF16 plans whose stripe would pass 64 floats), or
+ * not built for that type (BF16 / FP16 plans whose stripe would pass 64 floats), or
  * is a shared-memory-staged plan and `op` a row reduction (sum, min/max),
  * which only the register plans implement. */
 int tile_plan_info_ex(int id, int op, int dtype, int rows, int width, tile_plan_t *plan);

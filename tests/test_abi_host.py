@@ -324,3 +324,32 @@ def test_staged_plans_have_no_row_reductions(lib):
         for op in ("row_sum", "row_minmax"):
             assert tile.tile_plan_info(pid, op, 8, 4096) is None
             assert tile.tile_plan_info_ex(pid, op, "bf16", 8, 4096) is None
+
+
+@fake_pointers
+def test_f16_entry_points_reject_bad_arguments(lib):
+    assert lib.tile_layernorm_f16(A, B, 2, 0, 1e-5, None) == SHAPE
+    assert lib.tile_layernorm_f16(A + 1, B, 2, 8, 1e-5, None) == ALIGN      # odd address
+    assert lib.tile_softmax_f16(A, A + 16, 2, 8, 1e-5, None) == ALIAS       # 2 x 8 x 2 bytes
+    assert lib.tile_residual_layernorm_f16(A, None, B, 2, 8, 1e-5, None) == NULL
+    assert lib.tile_layernorm_affine_f16(A, None, None, None, B, 2, 8, 1e-5, None) == NULL
+    assert lib.tile_row_minmax_f16(A, B + 2, B + 64, 2, 8, None) == ALIGN    # FP32 outputs
+    assert lib.tile_rmsnorm_f16(A, B, 2, 8, -1.0, None) == EPS
+
+
+def test_f16_plans_are_the_bf16_plans(lib):
+    """FP16 rows have the BF16 geometry (2-byte elements, 8 per vector) and
+    share its selector tables."""
+    for op in ("residual_layernorm", "layernorm", "rmsnorm", "softmax", "row_sum",
+               "row_minmax", "layernorm_affine", "rmsnorm_weighted"):
+        for rows, w in ((9, 1), (9, 127), (65536, 4096), (4096, 8192), (1024, 16384),
+                        (64, 65536), (9, 131072)):
+            a = tile.tile_describe_plan_ex(op, "f16", rows, w)
+            b = tile.tile_describe_plan_ex(op, "bf16", rows, w)
+            assert a["dtype"] == 2
+            assert {k: v for k, v in a.items() if k != "dtype"} == \
+                {k: v for k, v in b.items() if k != "dtype"}
+    for pid in range(tile.tile_plan_count()):
+        a = tile.tile_plan_info_ex(pid, "layernorm", "f16", 4, 1024)
+        b = tile.tile_plan_info_ex(pid, "layernorm", "bf16", 4, 1024)
+        assert (a is None) == (b is None)

@@ -3,8 +3,8 @@ of shared-memory stages, persistent CTAs) against the FP64 oracle.
 
 Row counts are chosen so every CTA walks several times round its ring of
 stages (stage reuse, barrier phase flips).  Bounds as for the register
-plans: 2e-6 + 2e-5 |ref| (affine LayerNorm atol 1e-5), BF16 outputs plus
-half a BF16 ulp.  The staged plans need 16-byte aligned rows of whole
+plans: 2e-6 + 2e-5 |ref| (affine LayerNorm atol 1e-5), BF16 and FP16
+outputs plus half an ulp of their type.  The staged plans need 16-byte aligned rows of whole
 vectors; anything else is rejected with TILE_ERR_PLAN."""
 
 from __future__ import annotations
@@ -20,7 +20,7 @@ from parity import ATOL, EPS, RTOL, ref_eps
 
 pytestmark = pytest.mark.gpu
 
-BF16_HALF_ULP_REL = 2.0 ** -8
+HALF_ULP_REL = {"f32": 0.0, "bf16": 2.0 ** -8, "f16": 2.0 ** -11}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -59,7 +59,7 @@ def _reference(op, x, r, g, b):
     return orc.run(op, x, eps=ref_eps())
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("pid", STAGED)
 def test_staged_plan(pid, op, dtype):
@@ -67,7 +67,7 @@ def test_staged_plan(pid, op, dtype):
     assert info is not None and info["path"] == 2
     ev = info["vec"]
     cap = info["max_width"]
-    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
     for width in sorted({ev, 256, cap // 2, cap}):
         rows = 20000 if width <= 512 else 3000
         x = torch.from_numpy(synth.rows_of(3, rows, width, which="x")).to(tdt)
@@ -85,7 +85,7 @@ def test_staged_plan(pid, op, dtype):
         ref = _reference(op, xf, rf if with_res else None, g, b)
         got = out.float().cpu().numpy().astype(np.float64)
         atol = 1e-5 if op == "layernorm_affine" else ATOL
-        rtol = RTOL + (BF16_HALF_ULP_REL if dtype == "bf16" else 0.0)
+        rtol = RTOL + HALF_ULP_REL[dtype]
         err = np.abs(got - ref)
         bad = ~(err <= atol + rtol * np.abs(ref))
         assert not bad.any(), (f"staged plan {pid} {op} {dtype} {rows}x{width}: "

@@ -29,7 +29,10 @@ __all__ = [
     "tile_run_plan_args_f32", "tile_sigmoid_pair_f32", "tile_gelu_tanh_pair_f32",
     "tile_residual_layernorm_bf16", "tile_layernorm_bf16", "tile_rmsnorm_bf16",
     "tile_softmax_bf16", "tile_layernorm_affine_bf16", "tile_rmsnorm_weighted_bf16",
-    "tile_row_sum_bf16", "tile_row_minmax_bf16", "tile_describe_plan_ex", "tile_plan_info_ex",
+    "tile_row_sum_bf16", "tile_row_minmax_bf16", "tile_residual_layernorm_f16",
+    "tile_layernorm_f16", "tile_rmsnorm_f16", "tile_softmax_f16", "tile_layernorm_affine_f16",
+    "tile_rmsnorm_weighted_f16", "tile_row_sum_f16", "tile_row_minmax_f16",
+    "tile_describe_plan_ex", "tile_plan_info_ex",
     "tile_layernorm_backward_f32", "tile_rmsnorm_backward_f32", "tile_softmax_backward_f32",
     "tile_run_backward_plan_f32", "tile_norm_param_grad_workspace_bytes",
     "tile_norm_param_grad_f32",
@@ -43,7 +46,7 @@ OPS = {"residual_layernorm": 0, "layernorm": 1, "rmsnorm": 2, "softmax": 3, "row
 TILE_OK = 0
 
 #: Element type codes (TILE_DTYPE_*).
-DTYPES = {"f32": 0, "bf16": 1}
+DTYPES = {"f32": 0, "bf16": 1, "f16": 2}
 
 
 class TileError(RuntimeError):
@@ -131,6 +134,14 @@ def load():
         "tile_rmsnorm_weighted_bf16": [P, P, P, I, I, F, P],
         "tile_row_sum_bf16": [P, P, I, I, P],
         "tile_row_minmax_bf16": [P, P, P, I, I, P],
+        "tile_residual_layernorm_f16": [P, P, P, I, I, F, P],
+        "tile_layernorm_f16": [P, P, I, I, F, P],
+        "tile_rmsnorm_f16": [P, P, I, I, F, P],
+        "tile_softmax_f16": [P, P, I, I, F, P],
+        "tile_layernorm_affine_f16": [P, P, P, P, P, I, I, F, P],
+        "tile_rmsnorm_weighted_f16": [P, P, P, I, I, F, P],
+        "tile_row_sum_f16": [P, P, I, I, P],
+        "tile_row_minmax_f16": [P, P, P, I, I, P],
         "tile_describe_plan_ex": [I, I, I, I, ctypes.POINTER(TilePlan)],
         "tile_layernorm_backward_f32": [P, P, P, P, P, I, I, F, P],
         "tile_rmsnorm_backward_f32": [P, P, P, P, P, I, I, F, P],
@@ -173,7 +184,7 @@ def _matrix(t, name, dtype="f32"):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
-    want = torch.float32 if dtype == "f32" else torch.bfloat16
+    want = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
     if t.dtype != want:
         raise ValueError(f"{name} must be {want}")
     if t.dim() != 2:
@@ -290,10 +301,11 @@ def tile_row_minmax_f32(x, mins, maxs, stream=None):
 def tile_run_plan_args_f32(op, plan_id, x, out, residual=None, gamma=None, beta=None, out2=None,
                            eps=1e-5, stream=None):
     """Any row op with a forced plan (``out``: matrix, or [rows] for row_sum/row_minmax).
-    ``x`` may be float32 or bfloat16; the element type follows it."""
+    ``x`` may be float32, bfloat16 or float16; the element type follows it."""
     import torch
     op = OPS[op] if isinstance(op, str) else op
-    dt = "bf16" if isinstance(x, torch.Tensor) and x.dtype == torch.bfloat16 else "f32"
+    dt = {torch.bfloat16: "bf16", torch.float16: "f16"}.get(
+        x.dtype if isinstance(x, torch.Tensor) else None, "f32")
     px, rows, width = _matrix(x, "x", dt)
     a = TileRowArgs()
     a.in_ = px
@@ -451,6 +463,65 @@ def tile_row_minmax_bf16(x, mins, maxs, stream=None):
     px, rows, width = _matrix(x, "x", "bf16")
     _check(load().tile_row_minmax_bf16(px, _vector(mins, rows, "mins"), _vector(maxs, rows, "maxs"),
                                        rows, width, _stream(stream)), "tile_row_minmax_bf16")
+
+
+def tile_residual_layernorm_f16(x, residual, out, eps=1e-5, stream=None):
+    px, rows, width = _matrix(x, "x", "f16")
+    pr, _, _ = _matrix(residual, "residual", "f16")
+    po, _, _ = _matrix(out, "out", "f16")
+    _same_shape(x, residual, "x/residual")
+    _same_shape(x, out, "x/out")
+    _check(load().tile_residual_layernorm_f16(px, pr, po, rows, width, eps, _stream(stream)),
+           "tile_residual_layernorm_f16")
+
+
+def _unary_f16(name):
+    def fn(x, out, eps=1e-5, stream=None):
+        px, rows, width = _matrix(x, "x", "f16")
+        po, _, _ = _matrix(out, "out", "f16")
+        _same_shape(x, out, "x/out")
+        _check(getattr(load(), name)(px, po, rows, width, eps, _stream(stream)), name)
+    fn.__name__ = name
+    fn.__doc__ = f"Calls ``{name}`` (see include/tile_rows.h)."
+    return fn
+
+
+tile_layernorm_f16 = _unary_f16("tile_layernorm_f16")
+tile_rmsnorm_f16 = _unary_f16("tile_rmsnorm_f16")
+tile_softmax_f16 = _unary_f16("tile_softmax_f16")
+
+
+def tile_layernorm_affine_f16(x, residual, gamma, beta, out, eps=1e-5, stream=None):
+    px, rows, width = _matrix(x, "x", "f16")
+    po, _, _ = _matrix(out, "out", "f16")
+    _same_shape(x, out, "x/out")
+    pr = None
+    if residual is not None:
+        pr, _, _ = _matrix(residual, "residual", "f16")
+        _same_shape(x, residual, "x/residual")
+    _check(load().tile_layernorm_affine_f16(px, pr, _vector(gamma, width, "gamma"),
+                                             _vector(beta, width, "beta"), po, rows, width, eps,
+                                             _stream(stream)), "tile_layernorm_affine_f16")
+
+
+def tile_rmsnorm_weighted_f16(x, gamma, out, eps=1e-5, stream=None):
+    px, rows, width = _matrix(x, "x", "f16")
+    po, _, _ = _matrix(out, "out", "f16")
+    _same_shape(x, out, "x/out")
+    _check(load().tile_rmsnorm_weighted_f16(px, _vector(gamma, width, "gamma"), po, rows, width,
+                                             eps, _stream(stream)), "tile_rmsnorm_weighted_f16")
+
+
+def tile_row_sum_f16(x, sums, stream=None):
+    px, rows, width = _matrix(x, "x", "f16")
+    _check(load().tile_row_sum_f16(px, _vector(sums, rows, "sums"), rows, width, _stream(stream)),
+           "tile_row_sum_f16")
+
+
+def tile_row_minmax_f16(x, mins, maxs, stream=None):
+    px, rows, width = _matrix(x, "x", "f16")
+    _check(load().tile_row_minmax_f16(px, _vector(mins, rows, "mins"), _vector(maxs, rows, "maxs"),
+                                       rows, width, _stream(stream)), "tile_row_minmax_f16")
 
 
 def _host_matrix(t, name):

@@ -9,7 +9,7 @@ constexpr int kMaxDevices = 64;
 enum { OP_RESLN = 0, OP_LN = 1, OP_RMS = 2, OP_SOFTMAX = 3, OP_SUM = 4, OP_MINMAX = 5 };
 
 // Arguments of one row-kernel launch.  x, r: [rows][width] inputs of the
-// launch's element type (FP32 or BF16; r: residual LayerNorm only).
+// launch's element type (FP32, BF16 or FP16; r: residual LayerNorm only).
 // gamma, beta: optional FP32 per-column scale and shift applied after
 // LayerNorm / RMSNorm (NULL = none).  y: [rows][width] output of the element
 // type, or [rows] FP32 row sums / row minima; y2: [rows] FP32 row maxima.
@@ -44,8 +44,11 @@ struct BwdArgs {
 };
 
 // Shared-memory-staged row kernel (staged.cu): kernel_op is OP_RESLN, OP_LN,
-// OP_RMS or OP_SOFTMAX; plan_id one of TILE_STAGED_LIST.
-cudaError_t launch_staged(int kernel_op, bool bf16, int plan_id, RowArgs args,
+// OP_RMS or OP_SOFTMAX; elem the element type (ELEM_F32, ELEM_BF16,
+// ELEM_F16, the values of the ABI's TILE_DTYPE_*); plan_id one of
+// TILE_STAGED_LIST.
+enum { ELEM_F32 = 0, ELEM_BF16 = 1, ELEM_F16 = 2 };
+cudaError_t launch_staged(int kernel_op, int elem, int plan_id, RowArgs args,
                           cudaStream_t stream);
 cudaError_t status_staged(unsigned int *value, cudaStream_t stream);
 
@@ -81,10 +84,16 @@ TILE_DECLARE_OP(rmsnorm_bf16)
 TILE_DECLARE_OP(softmax_bf16)
 TILE_DECLARE_OP(row_sum_bf16)
 TILE_DECLARE_OP(row_minmax_bf16)
+TILE_DECLARE_OP(residual_layernorm_f16)
+TILE_DECLARE_OP(layernorm_f16)
+TILE_DECLARE_OP(rmsnorm_f16)
+TILE_DECLARE_OP(softmax_f16)
+TILE_DECLARE_OP(row_sum_f16)
+TILE_DECLARE_OP(row_minmax_f16)
 #undef TILE_DECLARE_OP
 
-// Largest register stripe (floats per thread) a BF16 plan may use: plans
-// with K * 8 above it are not built for BF16.
+// Largest register stripe (floats per thread) a plan on 2-byte elements
+// (BF16, FP16) may use: plans with K * 8 above it are not built for them.
 constexpr int kMaxStripeBf16 = 64;
 
 // Pointwise value/derivative pairs (pair_kernel.cu): kind 0 = sigmoid,

@@ -1,7 +1,7 @@
 // Instantiates every built plan for one operation and element type and
 // provides its host-side launcher and device error word.  Included once per
-// (op, type) by ops_<op>[_bf16].cu with TILE_INST_OP (tile::OP_*),
-// TILE_INST_T (float or __nv_bfloat16) and TILE_INST_NAME (a C identifier)
+// (op, type) by ops_<op>[_bf16|_f16].cu with TILE_INST_OP (tile::OP_*),
+// TILE_INST_T (float, __nv_bfloat16 or __half) and TILE_INST_NAME (a C identifier)
 // defined, so each compiles as its own translation unit, in parallel.
 #include "row_kernel.cuh"
 #include "plans.h"

@@ -1,0 +1,5 @@
+// row_minmax on FP16 rows (FP32 arithmetic): every built plan (see ops_inst.cuh).
+#define TILE_INST_OP tile::OP_MINMAX
+#define TILE_INST_T __half
+#define TILE_INST_NAME row_minmax_f16
+#include "ops_inst.cuh"

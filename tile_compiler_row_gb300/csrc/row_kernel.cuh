@@ -22,7 +22,9 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <type_traits>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "launch.h"
 
@@ -92,14 +94,54 @@ struct Elem<__nv_bfloat16> {
     }
 };
 
+template <>
+struct Elem<__half> {
+    static constexpr int kVec = 8;
+    // Two values per 32-bit word (lower address in the low half); widening
+    // is exact, narrowing one paired round-to-nearest-even conversion.
+    __device__ static float2 widen2(unsigned int w) {
+        return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+    }
+    __device__ static unsigned int narrow2(float lo, float hi) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const unsigned int *>(&h);
+    }
+    __device__ static void load_vec(const __half *p, float (&v)[8]) {
+        const uint4 t = __ldcs(reinterpret_cast<const uint4 *>(p));
+        const unsigned int w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = widen2(w[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+    __device__ static void store_vec(__half *p, const float (&v)[8]) {
+        uint4 t;
+        t.x = narrow2(v[0], v[1]);
+        t.y = narrow2(v[2], v[3]);
+        t.z = narrow2(v[4], v[5]);
+        t.w = narrow2(v[6], v[7]);
+        __stcs(reinterpret_cast<uint4 *>(p), t);
+    }
+    __device__ static float load(const __half *p) {
+        return __half2float(__ushort_as_half(__ldcs(reinterpret_cast<const unsigned short *>(p))));
+    }
+    __device__ static void store(__half *p, float v) {
+        __stcs(reinterpret_cast<unsigned short *>(p), __half_as_ushort(__float2half_rn(v)));
+    }
+};
+
 // exp(t), t <= 0 or -inf, for the softmax numerators.  FP32 rows call expf.
-// BF16 rows, whose outputs keep 8 significant bits, use the identity
+// 2-byte rows (BF16, FP16), whose outputs keep 8 or 11 significant bits,
+// use the identity
 // e^t = 2^(t log2 e) with the hardware base-2 exponential (PTX
 // ex2.approx.ftz.f32, relative error about 2^-22; ex2(-inf) = +0): rounding
 // t log2 e adds a relative error of at most |t| ln(2) 2^-24, about 1e-6 at
-// t = -20, where e^t is already below 1e-8; both stay far inside half a
-// BF16 ulp (2^-9).  It takes a fraction of expf's instructions, which
-// matters because BF16 rows carry twice the elements per byte.
+// t = -20, where e^t is already below 1e-8; both stay far inside half an
+// ulp of the output (2^-9 BF16, 2^-12 FP16).  It takes a fraction of expf's
+// instructions, which matters because 2-byte rows carry twice the elements
+// per byte.
 template <class T>
 __device__ __forceinline__ float softmax_exp(float t) {
     if constexpr (sizeof(T) == 2) {
@@ -113,9 +155,10 @@ __device__ __forceinline__ float softmax_exp(float t) {
 
 // LayerNorm output map of a centred value d (centred on the mean estimate,
 // with mu1 the remaining mean offset): (d - mu1) rstd.  FP32 rows use that
-// form, which is exactly 0 for a constant row (every d equals mu1).  BF16
-// rows, whose kernels are bound by instruction issue and whose outputs keep
-// 8 significant bits, use one FMA, d rstd + (-mu1 rstd): it differs from the
+// form, which is exactly 0 for a constant row (every d equals mu1).  2-byte
+// rows (BF16, FP16), whose kernels are bound by instruction issue and whose
+// outputs keep 8 or 11 significant bits, use one FMA, d rstd + (-mu1 rstd):
+// it differs from the
 // two-step form by at most the rounding of mu1 rstd (mu1 is the rounding
 // error of the mean estimate, so about 2^-24 |mean| rstd), and a constant
 // row gives |y| of that order instead of an exact 0.
@@ -127,11 +170,12 @@ __device__ __forceinline__ float ln_out(float d, float mu1, float rstd) {
         return (d - mu1) * rstd;
 }
 
-// v[j] += the 16-byte vector `t` of element type T (4 FP32 or 8 BF16 lanes,
-// the lower address in the lower half of each word).  BF16 lanes use the
-// mixed-precision add (PTX add.rn.f32.bf16, sm_100 and later): the BF16
-// operand is widened exactly inside the instruction, so each lane is
-// round(v + x) as after an explicit widening, one instruction instead of two.
+// v[j] += the 16-byte vector `t` of element type T (4 FP32 or 8 BF16 / FP16
+// lanes, the lower address in the lower half of each word).  2-byte lanes
+// use the mixed-precision add (PTX add.rn.f32.bf16 / add.rn.f32.f16, sm_100
+// and later): the 2-byte operand is widened exactly inside the instruction,
+// so each lane is round(v + x) as after an explicit widening, one
+// instruction instead of two.
 template <class T>
 __device__ __forceinline__ void add_raw_vec(float (&v)[16 / sizeof(T)], uint4 t) {
     if constexpr (sizeof(T) == 4) {
@@ -143,10 +187,16 @@ __device__ __forceinline__ void add_raw_vec(float (&v)[16 / sizeof(T)], uint4 t)
         const unsigned int w[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-                "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
-                : "+f"(v[2 * i]), "+f"(v[2 * i + 1])
-                : "r"(w[i]));
+            if constexpr (std::is_same<T, __half>::value)
+                asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+                    "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+                    : "+f"(v[2 * i]), "+f"(v[2 * i + 1])
+                    : "r"(w[i]));
+            else
+                asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+                    "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+                    : "+f"(v[2 * i]), "+f"(v[2 * i + 1])
+                    : "r"(w[i]));
         }
     }
 }

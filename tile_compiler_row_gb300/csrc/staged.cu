@@ -103,9 +103,13 @@ cudaError_t launch_type(int op, int staged_id, RowArgs a, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_staged(int kernel_op, bool bf16, int plan_id, RowArgs a, cudaStream_t stream) {
-    return bf16 ? launch_type<__nv_bfloat16>(kernel_op, plan_id, a, stream)
-                : launch_type<float>(kernel_op, plan_id, a, stream);
+cudaError_t launch_staged(int kernel_op, int elem, int plan_id, RowArgs a, cudaStream_t stream) {
+    switch (elem) {
+        case ELEM_F32: return launch_type<float>(kernel_op, plan_id, a, stream);
+        case ELEM_BF16: return launch_type<__nv_bfloat16>(kernel_op, plan_id, a, stream);
+        case ELEM_F16: return launch_type<__half>(kernel_op, plan_id, a, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t status_staged(unsigned int *value, cudaStream_t stream) {

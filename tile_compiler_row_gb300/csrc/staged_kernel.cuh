@@ -90,6 +90,14 @@ __device__ __forceinline__ void widen_vec(uint4 t, float (&v)[16 / sizeof(T)]) {
         v[1] = __uint_as_float(t.y);
         v[2] = __uint_as_float(t.z);
         v[3] = __uint_as_float(t.w);
+    } else if constexpr (std::is_same<T, __half>::value) {
+        const unsigned int w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = Elem<__half>::widen2(w[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
     } else {
         const unsigned int w[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll

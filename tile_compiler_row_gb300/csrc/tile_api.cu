@@ -34,14 +34,17 @@ constexpr long long capacity(const PlanDesc &p) {
 }
 
 // Elements per access of a plan for an element type: a 16-byte vector
-// (4 FP32 or 8 BF16) for V = 4 plans, one element for V = 1 plans.
+// (4 FP32 or 8 BF16 / FP16) for V = 4 plans, one element for V = 1 plans.
+bool two_byte(int dtype) { return dtype == TILE_DTYPE_BF16 || dtype == TILE_DTYPE_F16; }
+bool valid_dtype(int dtype) { return dtype == TILE_DTYPE_F32 || two_byte(dtype); }
+
 int elems_per_vec(const PlanDesc &p, int dtype) {
-    return p.V == 4 ? (dtype == TILE_DTYPE_BF16 ? 8 : 4) : 1;
+    return p.V == 4 ? (two_byte(dtype) ? 8 : 4) : 1;
 }
 
-// BF16 plans whose stripe would exceed the register budget are not built.
+// 2-byte plans whose stripe would exceed the register budget are not built.
 bool built(const PlanDesc &p, int dtype) {
-    return dtype != TILE_DTYPE_BF16 || p.K * elems_per_vec(p, dtype) <= tile::kMaxStripeBf16;
+    return !two_byte(dtype) || p.K * elems_per_vec(p, dtype) <= tile::kMaxStripeBf16;
 }
 
 bool covers(const PlanDesc &p, int width, int dtype = TILE_DTYPE_F32) {
@@ -160,7 +163,7 @@ int pick(const Bucket (&table)[N], int width) {
 int select_plan(int op, long long rows, int width, bool vec4, int dtype,
                 bool staged_eligible = false) {
     if (!vec4) return pick(kVec1, width);
-    if (dtype == TILE_DTYPE_BF16) {
+    if (two_byte(dtype)) {     // FP16 rows share the BF16 tables (same geometry)
         if (staged_eligible && rows * static_cast<long long>(width) > kSmallElems) {
             int sid = -1;
             switch (op) {
@@ -232,7 +235,7 @@ void fill_plan(const PlanDesc &p, int op, int dtype, int rows, int width, tile_p
         // the launcher's stage count: the plan's budget, 1..8 stages
         const int nin = (op == TILE_OP_RESIDUAL_LAYERNORM) ? 2 : 1;
         const long long stage = static_cast<long long>(width) *
-                                (dtype == TILE_DTYPE_BF16 ? 2 : 4) * nin;
+                                (two_byte(dtype) ? 2 : 4) * nin;
         long long nst = (static_cast<long long>(p.stage_kb) << 10) / stage;
         nst = nst > 8 ? 8 : nst < 1 ? 1 : nst;
         out->smem_bytes = static_cast<int>(stage * nst) + 4 * 8 * p.S + 80;
@@ -293,7 +296,7 @@ bool coaligned16(const Call &c) {
 
 // Checks shared by every row entry point.  Returns TILE_OK with *noop set
 // when there is nothing to launch.  No CUDA call is made.
-size_t elem_size(int dtype) { return dtype == TILE_DTYPE_BF16 ? 2 : 4; }
+size_t elem_size(int dtype) { return two_byte(dtype) ? 2 : 4; }
 
 bool misaligned_to(const void *p, size_t bytes) {
     return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) != 0;
@@ -302,7 +305,7 @@ bool misaligned_to(const void *p, size_t bytes) {
 int validate(const Call &c, bool *noop) {
     *noop = false;
     if (!valid_op(c.op)) return TILE_ERR_OP;
-    if (c.dtype != TILE_DTYPE_F32 && c.dtype != TILE_DTYPE_BF16) return TILE_ERR_DTYPE;
+    if (!valid_dtype(c.dtype)) return TILE_ERR_DTYPE;
     if (c.rows < 0 || c.width < 1 || c.width > TILE_MAX_WIDTH) return TILE_ERR_SHAPE;
     if (is_normaliser(c.op) && !(std::isfinite(c.eps) && c.eps >= 0.0f)) return TILE_ERR_EPS;
     if (c.rows == 0) {
@@ -358,50 +361,40 @@ int launch(const Call &c, int plan_id, cudaStream_t stream) {
     const PlanDesc &p = kPlans[plan_id];
     if (grid_of(p, c.rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
     tile::RowArgs a{c.in, c.res, c.gamma, c.beta, c.out, c.out2, c.rows, c.width, c.eps, nullptr};
-    const bool bf = c.dtype == TILE_DTYPE_BF16;
     cudaError_t err;
     if (p.staged) {
-        err = tile::launch_staged(kernel_op_of(c), bf, plan_id, a, stream);
+        err = tile::launch_staged(kernel_op_of(c), c.dtype, plan_id, a, stream);
         if (err != cudaSuccess) {
             tile::set_last_cuda_error(static_cast<int>(err));
             return TILE_ERR_CUDA;
         }
         return TILE_OK;
     }
-    switch (c.op) {
-        case TILE_OP_RESIDUAL_LAYERNORM:
-            err = bf ? tile::launch_residual_layernorm_bf16(plan_id, a, stream)
-                     : tile::launch_residual_layernorm(plan_id, a, stream);
-            break;
-        case TILE_OP_LAYERNORM:
-            err = bf ? tile::launch_layernorm_bf16(plan_id, a, stream)
-                     : tile::launch_layernorm(plan_id, a, stream);
-            break;
-        case TILE_OP_LAYERNORM_AFFINE:
-            if (c.res != nullptr)
-                err = bf ? tile::launch_residual_layernorm_bf16(plan_id, a, stream)
-                         : tile::launch_residual_layernorm(plan_id, a, stream);
-            else
-                err = bf ? tile::launch_layernorm_bf16(plan_id, a, stream)
-                         : tile::launch_layernorm(plan_id, a, stream);
-            break;
-        case TILE_OP_RMSNORM:
-        case TILE_OP_RMSNORM_WEIGHTED:
-            err = bf ? tile::launch_rmsnorm_bf16(plan_id, a, stream)
-                     : tile::launch_rmsnorm(plan_id, a, stream);
-            break;
-        case TILE_OP_ROW_SUM:
-            err = bf ? tile::launch_row_sum_bf16(plan_id, a, stream)
-                     : tile::launch_row_sum(plan_id, a, stream);
-            break;
-        case TILE_OP_ROW_MINMAX:
-            err = bf ? tile::launch_row_minmax_bf16(plan_id, a, stream)
-                     : tile::launch_row_minmax(plan_id, a, stream);
-            break;
-        default:
-            err = bf ? tile::launch_softmax_bf16(plan_id, a, stream)
-                     : tile::launch_softmax(plan_id, a, stream);
-            break;
+    // the launcher of each row-kernel op, per element type
+    using Launch = cudaError_t (*)(int, tile::RowArgs, cudaStream_t);
+    struct Launchers {
+        Launch resln, ln, rms, softmax, sum, minmax;
+    };
+    static const Launchers kF32 = {tile::launch_residual_layernorm, tile::launch_layernorm,
+                                   tile::launch_rmsnorm, tile::launch_softmax,
+                                   tile::launch_row_sum, tile::launch_row_minmax};
+    static const Launchers kBf16 = {tile::launch_residual_layernorm_bf16,
+                                    tile::launch_layernorm_bf16, tile::launch_rmsnorm_bf16,
+                                    tile::launch_softmax_bf16, tile::launch_row_sum_bf16,
+                                    tile::launch_row_minmax_bf16};
+    static const Launchers kF16 = {tile::launch_residual_layernorm_f16,
+                                   tile::launch_layernorm_f16, tile::launch_rmsnorm_f16,
+                                   tile::launch_softmax_f16, tile::launch_row_sum_f16,
+                                   tile::launch_row_minmax_f16};
+    const Launchers &L =
+        c.dtype == TILE_DTYPE_BF16 ? kBf16 : c.dtype == TILE_DTYPE_F16 ? kF16 : kF32;
+    switch (kernel_op_of(c)) {
+        case tile::OP_RESLN: err = L.resln(plan_id, a, stream); break;
+        case tile::OP_LN: err = L.ln(plan_id, a, stream); break;
+        case tile::OP_RMS: err = L.rms(plan_id, a, stream); break;
+        case tile::OP_SUM: err = L.sum(plan_id, a, stream); break;
+        case tile::OP_MINMAX: err = L.minmax(plan_id, a, stream); break;
+        default: err = L.softmax(plan_id, a, stream); break;
     }
     if (err != cudaSuccess) {
         tile::set_last_cuda_error(static_cast<int>(err));
@@ -656,6 +649,70 @@ int tile_row_minmax_bf16(const void *in, float *mins, float *maxs, int rows, int
                     stream);
 }
 
+int tile_residual_layernorm_f16(const void *in, const void *residual, void *out, int rows,
+                                 int width, float eps, cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_RESIDUAL_LAYERNORM,
+                              args_of(in, residual, nullptr, nullptr, out, nullptr, rows, width,
+                                      eps, TILE_DTYPE_F16)),
+                    stream);
+}
+
+int tile_layernorm_f16(const void *in, void *out, int rows, int width, float eps,
+                        cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_LAYERNORM, args_of(in, nullptr, nullptr, nullptr, out,
+                                                         nullptr, rows, width, eps,
+                                                         TILE_DTYPE_F16)),
+                    stream);
+}
+
+int tile_rmsnorm_f16(const void *in, void *out, int rows, int width, float eps,
+                      cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_RMSNORM, args_of(in, nullptr, nullptr, nullptr, out,
+                                                       nullptr, rows, width, eps,
+                                                       TILE_DTYPE_F16)),
+                    stream);
+}
+
+int tile_softmax_f16(const void *in, void *out, int rows, int width, float eps,
+                      cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_SOFTMAX, args_of(in, nullptr, nullptr, nullptr, out,
+                                                       nullptr, rows, width, eps,
+                                                       TILE_DTYPE_F16)),
+                    stream);
+}
+
+int tile_layernorm_affine_f16(const void *in, const void *residual, const float *gamma,
+                               const float *beta, void *out, int rows, int width, float eps,
+                               cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_LAYERNORM_AFFINE,
+                              args_of(in, residual, gamma, beta, out, nullptr, rows, width, eps,
+                                      TILE_DTYPE_F16)),
+                    stream);
+}
+
+int tile_rmsnorm_weighted_f16(const void *in, const float *gamma, void *out, int rows,
+                               int width, float eps, cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_RMSNORM_WEIGHTED,
+                              args_of(in, nullptr, gamma, nullptr, out, nullptr, rows, width, eps,
+                                      TILE_DTYPE_F16)),
+                    stream);
+}
+
+int tile_row_sum_f16(const void *in, float *sums, int rows, int width, cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_ROW_SUM, args_of(in, nullptr, nullptr, nullptr, sums,
+                                                       nullptr, rows, width, 0.0f,
+                                                       TILE_DTYPE_F16)),
+                    stream);
+}
+
+int tile_row_minmax_f16(const void *in, float *mins, float *maxs, int rows, int width,
+                         cudaStream_t stream) {
+    return run_call(make_call(TILE_OP_ROW_MINMAX, args_of(in, nullptr, nullptr, nullptr, mins,
+                                                          maxs, rows, width, 0.0f,
+                                                          TILE_DTYPE_F16)),
+                    stream);
+}
+
 int tile_run_plan_args_f32(int op, int plan_id, const tile_row_args_t *args, cudaStream_t stream) {
     if (args == nullptr) return TILE_ERR_NULL;
     return run_call_plan(make_call(op, *args), plan_id, stream);
@@ -671,7 +728,7 @@ int tile_run_plan_f32(int op, int plan_id, const float *in, const float *residua
 
 int tile_describe_plan_ex(int op, int dtype, int rows, int width, tile_plan_t *plan) {
     if (!valid_op(op)) return TILE_ERR_OP;
-    if (dtype != TILE_DTYPE_F32 && dtype != TILE_DTYPE_BF16) return TILE_ERR_DTYPE;
+    if (!valid_dtype(dtype)) return TILE_ERR_DTYPE;
     if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH) return TILE_ERR_SHAPE;
     if (plan == nullptr) return TILE_ERR_NULL;
     const int id = select_plan(op, rows, width, true, dtype, true);
@@ -689,7 +746,7 @@ int tile_plan_count(void) { return kAllPlans; }
 int tile_plan_info_ex(int id, int op, int dtype, int rows, int width, tile_plan_t *plan) {
     if (id < 0 || id >= kAllPlans) return TILE_ERR_PLAN;
     if (!valid_op(op)) return TILE_ERR_OP;
-    if (dtype != TILE_DTYPE_F32 && dtype != TILE_DTYPE_BF16) return TILE_ERR_DTYPE;
+    if (!valid_dtype(dtype)) return TILE_ERR_DTYPE;
     if (!built(kPlans[id], dtype)) return TILE_ERR_PLAN;
     // the staged kernel has no row-reduction (sum, min/max) variant
     if (kPlans[id].staged && (op == TILE_OP_ROW_SUM || op == TILE_OP_ROW_MINMAX))
@@ -734,7 +791,10 @@ int tile_check_device_status(cudaStream_t stream) {
         tile::status_softmax, tile::status_row_sum, tile::status_row_minmax,
         tile::status_residual_layernorm_bf16, tile::status_layernorm_bf16,
         tile::status_rmsnorm_bf16, tile::status_softmax_bf16, tile::status_row_sum_bf16,
-        tile::status_row_minmax_bf16, tile::status_pairs, tile::status_backward,
+        tile::status_row_minmax_bf16, tile::status_residual_layernorm_f16,
+        tile::status_layernorm_f16, tile::status_rmsnorm_f16, tile::status_softmax_f16,
+        tile::status_row_sum_f16, tile::status_row_minmax_f16, tile::status_pairs,
+        tile::status_backward,
         tile::status_param_grad, tile::status_staged};
     for (auto f : fetch) {
         v = 0;

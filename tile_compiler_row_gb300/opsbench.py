@@ -59,6 +59,7 @@ def main(argv=None):
     vec_b = torch.empty(rows, device="cuda")
     stats = torch.empty(2 * rows, device="cuda")
     xb, rb, yb = x.to(torch.bfloat16), r.to(torch.bfloat16), torch.empty_like(x, dtype=torch.bfloat16)
+    xh, rh, yh = x.to(torch.float16), r.to(torch.float16), torch.empty_like(x, dtype=torch.float16)
     ws = torch.empty(tile.tile_norm_param_grad_workspace_bytes(rows, width), dtype=torch.uint8,
                      device="cuda")
     dg, db = torch.empty(width, device="cuda"), torch.empty(width, device="cuda")
@@ -84,6 +85,10 @@ def main(argv=None):
         "layernorm_bf16": (lambda: tile.tile_layernorm_bf16(xb, yb), 4),
         "rmsnorm_bf16": (lambda: tile.tile_rmsnorm_bf16(xb, yb), 4),
         "softmax_bf16": (lambda: tile.tile_softmax_bf16(xb, yb), 4),
+        "residual_layernorm_f16": (lambda: tile.tile_residual_layernorm_f16(xh, rh, yh), 6),
+        "layernorm_f16": (lambda: tile.tile_layernorm_f16(xh, yh), 4),
+        "rmsnorm_f16": (lambda: tile.tile_rmsnorm_f16(xh, yh), 4),
+        "softmax_f16": (lambda: tile.tile_softmax_f16(xh, yh), 4),
         "layernorm_backward": (lambda: tile.tile_layernorm_backward_f32(x, g, r, y, stats), 12),
         "rmsnorm_backward": (lambda: tile.tile_rmsnorm_backward_f32(x, g, r, y, stats), 12),
         "softmax_backward": (lambda: tile.tile_softmax_backward_f32(sm, r, y), 12),

@@ -60,7 +60,7 @@ def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g
     a.beta = None
     a.out2 = y2.data_ptr() if y2 is not None else None
     a.rows, a.width, a.eps = rows, width, 1e-5
-    a.dtype = 1 if x.dtype == torch.bfloat16 else 0
+    a.dtype = {torch.bfloat16: 1, torch.float16: 2}.get(x.dtype, 0)
     ref = ctypes.byref(a)
 
     def call():
@@ -120,7 +120,7 @@ def main(argv=None):
     ap.add_argument("--graph", action="store_true",
                     help="time calls replayed from a CUDA graph (no host launch overhead)")
     ap.add_argument("--small", action="store_true", help="only the small workload shapes")
-    ap.add_argument("--dtype", default="f32", choices=("f32", "bf16"))
+    ap.add_argument("--dtype", default="f32", choices=("f32", "bf16", "f16"))
     args = ap.parse_args(argv)
 
     import torch
@@ -132,7 +132,7 @@ def main(argv=None):
     torch.cuda.set_device(0)
     stream = torch.cuda.current_stream()
     results = []
-    todo = shapes(args.quick, 27 if args.dtype == "bf16" else 26) if args.shapes is None else \
+    todo = shapes(args.quick, 26 if args.dtype == "f32" else 27) if args.shapes is None else \
         [tuple(int(v) for v in sh.split("x")) for sh in args.shapes.split(",")]
     if args.small:
         todo = list(SMALL)
@@ -141,8 +141,9 @@ def main(argv=None):
         gen = torch.Generator(device="cuda").manual_seed(rows * 131 + width)
         x = torch.rand(rows, width, device="cuda", generator=gen) * 2 - 1
         r = torch.rand(rows, width, device="cuda", generator=gen) * 2 - 1
-        if args.dtype == "bf16":
-            x, r = x.to(torch.bfloat16), r.to(torch.bfloat16)
+        if args.dtype != "f32":
+            t = torch.bfloat16 if args.dtype == "bf16" else torch.float16
+            x, r = x.to(t), r.to(t)
         y = torch.empty_like(x)
         g = torch.rand(width, device="cuda", generator=gen) + 0.5
         y2 = torch.empty(rows, device="cuda")
@@ -163,7 +164,7 @@ def main(argv=None):
                 entry["plans"][pid] = round(us, 3)
             best = min(entry["plans"], key=entry["plans"].get)
             entry["best"] = best
-            scale = 0.5 if args.dtype == "bf16" else 1.0      # 2-byte elements
+            scale = 0.5 if args.dtype != "f32" else 1.0      # 2-byte elements
             entry["best_gbs"] = round(scale * BYTES[op] * n / (entry["plans"][best] * 1e-6) / 1e9, 1)
             entry["selected_over_best"] = round(entry["plans"][chosen] / entry["plans"][best], 4)
             results.append(entry)
