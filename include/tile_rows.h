@@ -286,6 +286,44 @@ int tile_norm_param_grad_f32(const float *in, const float *dy, const float *row_
                              float *dgamma, float *dbeta, int rows, int width, void *workspace,
                              size_t workspace_bytes, cudaStream_t stream);
 
+/* The backward passes with BF16 or FP16 in / y, dy and dx (2 bytes per
+ * element, 2-byte aligned): every element is widened exactly to FP32, the
+ * statistics, sums and maps run in FP32 as above, and dx is rounded to
+ * nearest-even of its type.  gamma, row_stats, dgamma, dbeta and the
+ * workspace stay FP32; tile_norm_param_grad_* uses the same workspace size.
+ * 16-byte vectors (8 elements) are used when in, dy and dx share a 16-byte
+ * phase.  Everything else is the contract of the FP32 entry point. */
+int tile_layernorm_backward_bf16(const void *in, const float *gamma, const void *dy, void *dx,
+                                 float *row_stats, int rows, int width, float eps,
+                                 cudaStream_t stream);
+int tile_rmsnorm_backward_bf16(const void *in, const float *gamma, const void *dy, void *dx,
+                               float *row_stats, int rows, int width, float eps,
+                               cudaStream_t stream);
+int tile_softmax_backward_bf16(const void *y, const void *dy, void *dx, int rows, int width,
+                               cudaStream_t stream);
+int tile_norm_param_grad_bf16(const void *in, const void *dy, const float *row_stats,
+                              float *dgamma, float *dbeta, int rows, int width, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+int tile_layernorm_backward_f16(const void *in, const float *gamma, const void *dy, void *dx,
+                                float *row_stats, int rows, int width, float eps,
+                                cudaStream_t stream);
+int tile_rmsnorm_backward_f16(const void *in, const float *gamma, const void *dy, void *dx,
+                              float *row_stats, int rows, int width, float eps,
+                              cudaStream_t stream);
+int tile_softmax_backward_f16(const void *y, const void *dy, void *dx, int rows, int width,
+                              cudaStream_t stream);
+int tile_norm_param_grad_f16(const void *in, const void *dy, const float *row_stats,
+                             float *dgamma, float *dbeta, int rows, int width, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+/* tile_run_backward_plan_f32 for an element type (TILE_DTYPE_*; in, dy, dx
+ * of that type).  For BF16 / FP16, plans whose stripes would pass 32 floats
+ * (K above 4 with 16-byte vectors) return TILE_ERR_PLAN; an unknown type
+ * TILE_ERR_DTYPE. */
+int tile_run_backward_plan_ex(int op, int plan_id, int dtype, const void *in, const float *gamma,
+                              const void *dy, void *dx, float *row_stats, int rows, int width,
+                              float eps, cudaStream_t stream);
+
 /* ---- pointwise value/derivative pairs ---------------------------------- */
 
 /* value[k] = sigmoid(in[k]) and derivative[k] = sigmoid'(in[k]) for k < n,

@@ -35,7 +35,10 @@ __all__ = [
     "tile_describe_plan_ex", "tile_plan_info_ex",
     "tile_layernorm_backward_f32", "tile_rmsnorm_backward_f32", "tile_softmax_backward_f32",
     "tile_run_backward_plan_f32", "tile_norm_param_grad_workspace_bytes",
-    "tile_norm_param_grad_f32",
+    "tile_norm_param_grad_f32", "tile_run_backward_plan_ex",
+    "tile_layernorm_backward_bf16", "tile_rmsnorm_backward_bf16", "tile_softmax_backward_bf16",
+    "tile_norm_param_grad_bf16", "tile_layernorm_backward_f16", "tile_rmsnorm_backward_f16",
+    "tile_softmax_backward_f16", "tile_norm_param_grad_f16",
     "residual_layernorm", "layernorm", "rmsnorm", "softmax", "run",
 ]
 
@@ -148,6 +151,15 @@ def load():
         "tile_softmax_backward_f32": [P, P, P, I, I, P],
         "tile_run_backward_plan_f32": [I, I, P, P, P, P, P, I, I, F, P],
         "tile_norm_param_grad_f32": [P, P, P, P, P, I, I, P, ctypes.c_size_t, P],
+        "tile_run_backward_plan_ex": [I, I, I, P, P, P, P, P, I, I, F, P],
+        "tile_layernorm_backward_bf16": [P, P, P, P, P, I, I, F, P],
+        "tile_rmsnorm_backward_bf16": [P, P, P, P, P, I, I, F, P],
+        "tile_softmax_backward_bf16": [P, P, P, I, I, P],
+        "tile_norm_param_grad_bf16": [P, P, P, P, P, I, I, P, ctypes.c_size_t, P],
+        "tile_layernorm_backward_f16": [P, P, P, P, P, I, I, F, P],
+        "tile_rmsnorm_backward_f16": [P, P, P, P, P, I, I, F, P],
+        "tile_softmax_backward_f16": [P, P, P, I, I, P],
+        "tile_norm_param_grad_f16": [P, P, P, P, P, I, I, P, ctypes.c_size_t, P],
         "tile_plan_info_ex": [I, I, I, I, I, ctypes.POINTER(TilePlan)],
     }
     for name, argtypes in sigs.items():
@@ -348,11 +360,11 @@ tile_gelu_tanh_pair_f32 = _pair_fn("tile_gelu_tanh_pair_f32")
 
 # ---- backward passes ----------------------------------------------------------
 
-def _bwd(name):
+def _bwd(name, dtype="f32"):
     def fn(x, gamma, dy, dx, row_stats=None, eps=1e-5, stream=None):
-        px, rows, width = _matrix(x, "x")
-        pd, _, _ = _matrix(dy, "dy")
-        po, _, _ = _matrix(dx, "dx")
+        px, rows, width = _matrix(x, "x", dtype)
+        pd, _, _ = _matrix(dy, "dy", dtype)
+        po, _, _ = _matrix(dx, "dx", dtype)
         _same_shape(x, dy, "x/dy")
         _same_shape(x, dx, "x/dx")
         ps = _vector(row_stats, 2 * rows, "row_stats") if row_stats is not None else None
@@ -387,6 +399,61 @@ def tile_run_backward_plan_f32(op, plan_id, x, gamma, dy, dx, row_stats=None, ep
     _check(load().tile_run_backward_plan_f32(op, plan_id, px, _vector(gamma, width, "gamma"), pd,
                                              po, ps, rows, width, eps, _stream(stream)),
            "tile_run_backward_plan_f32")
+
+
+def _softmax_bwd(name, dtype):
+    def fn(y, dy, dx, stream=None):
+        py, rows, width = _matrix(y, "y", dtype)
+        pd, _, _ = _matrix(dy, "dy", dtype)
+        po, _, _ = _matrix(dx, "dx", dtype)
+        _same_shape(y, dy, "y/dy")
+        _same_shape(y, dx, "y/dx")
+        _check(getattr(load(), name)(py, pd, po, rows, width, _stream(stream)), name)
+    fn.__name__ = name
+    fn.__doc__ = f"Calls ``{name}`` (see include/tile_rows.h)."
+    return fn
+
+
+def _param_grad(name, dtype):
+    def fn(x, dy, row_stats, dgamma, dbeta, workspace, stream=None):
+        px, rows, width = _matrix(x, "x", dtype)
+        pd, _, _ = _matrix(dy, "dy", dtype)
+        if not workspace.is_cuda:
+            raise ValueError("workspace must be a CUDA tensor")
+        _check(getattr(load(), name)(
+            px, pd, _vector(row_stats, 2 * rows, "row_stats"), _vector(dgamma, width, "dgamma"),
+            _vector(dbeta, width, "dbeta"), rows, width, workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream(stream)), name)
+    fn.__name__ = name
+    fn.__doc__ = f"Calls ``{name}`` (see include/tile_rows.h)."
+    return fn
+
+
+tile_layernorm_backward_bf16 = _bwd("tile_layernorm_backward_bf16", "bf16")
+tile_rmsnorm_backward_bf16 = _bwd("tile_rmsnorm_backward_bf16", "bf16")
+tile_softmax_backward_bf16 = _softmax_bwd("tile_softmax_backward_bf16", "bf16")
+tile_norm_param_grad_bf16 = _param_grad("tile_norm_param_grad_bf16", "bf16")
+tile_layernorm_backward_f16 = _bwd("tile_layernorm_backward_f16", "f16")
+tile_rmsnorm_backward_f16 = _bwd("tile_rmsnorm_backward_f16", "f16")
+tile_softmax_backward_f16 = _softmax_bwd("tile_softmax_backward_f16", "f16")
+tile_norm_param_grad_f16 = _param_grad("tile_norm_param_grad_f16", "f16")
+
+
+def tile_run_backward_plan_ex(op, plan_id, x, gamma, dy, dx, row_stats=None, eps=1e-5,
+                              stream=None):
+    """tile_run_backward_plan_f32 for the element type of ``x`` (float32,
+    bfloat16 or float16)."""
+    import torch
+    op = OPS[op] if isinstance(op, str) else op
+    dt = {torch.bfloat16: "bf16", torch.float16: "f16"}.get(x.dtype, "f32")
+    px, rows, width = _matrix(x, "x", dt)
+    pd, _, _ = _matrix(dy, "dy", dt)
+    po, _, _ = _matrix(dx, "dx", dt)
+    ps = _vector(row_stats, 2 * rows, "row_stats") if row_stats is not None else None
+    _check(load().tile_run_backward_plan_ex(op, plan_id, DTYPES[dt], px,
+                                            _vector(gamma, width, "gamma"), pd, po, ps, rows,
+                                            width, eps, _stream(stream)),
+           "tile_run_backward_plan_ex")
 
 
 def tile_norm_param_grad_workspace_bytes(rows, width):

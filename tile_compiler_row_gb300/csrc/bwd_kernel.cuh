@@ -23,12 +23,13 @@ namespace tile {
 
 enum { BWD_LN = BWD_LN_OP, BWD_RMS = BWD_RMS_OP, BWD_SOFTMAX = BWD_SOFTMAX_OP };
 
-template <int OP, int V, int S, int P, int K, int C>
+template <int OP, class T, int V, int S, int P, int K, int C>
 __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
-    static_assert(V == 1 || V == 4, "V is 1 (scalar) or 4 (float4)");
+    static_assert(V == 1 || V == 4, "V is 1 (scalar) or 4 (16-byte vectors)");
     static_assert(C == 1 || P == 1, "a cluster row has one program per CTA");
     constexpr int W = 32 * S;
-    constexpr int EV = V;                         // FP32: 4 per 16-byte vector
+    // elements per access: one 16-byte vector (4 FP32 or 8 BF16 / FP16), or one
+    constexpr int EV = (V == 4) ? Elem<T>::kVec : 1;
 
     // Reduction partials, one buffer per round: [N][P*S] floats (N = 2, 4).
     __shared__ float part1[S > 1 ? 2 * P * S : 1];
@@ -56,17 +57,18 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
     if (!active) row = a.rows - 1;                // replay the last row
 
     const long long base = row * static_cast<long long>(width);
-    const float *xr = a.x + base;
-    const float *dr = a.dy + base;
-    float *outr = a.dx + base;
+    const T *xr = static_cast<const T *>(a.x) + base;
+    const T *dr = static_cast<const T *>(a.dy) + base;
+    T *outr = static_cast<T *>(a.dx) + base;
 
     int h = 0, tl = 0, nb;
     if constexpr (V == 4) {
-        const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(xr) >> 2) & 3);
-        h = (4 - mis) & 3;
+        const int mis =
+            static_cast<int>((reinterpret_cast<uintptr_t>(xr) / sizeof(T)) & (EV - 1));
+        h = (EV - mis) & (EV - 1);
         if (h > width) h = width;
-        nb = (width - h) >> 2;
-        tl = width - h - (nb << 2);
+        nb = (width - h) / EV;
+        tl = width - h - nb * EV;
     } else {
         nb = width;
     }
@@ -79,11 +81,11 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
         const int i = k * (C * W) + gw;
         if (i < nb) {
             if constexpr (V == 4) {
-                Elem<float>::load_vec(xr + h + 4 * i, v[k]);
-                Elem<float>::load_vec(dr + h + 4 * i, u[k]);
+                Elem<T>::load_vec(xr + h + EV * i, v[k]);
+                Elem<T>::load_vec(dr + h + EV * i, u[k]);
             } else {
-                v[k][0] = Elem<float>::load(xr + i);
-                u[k][0] = Elem<float>::load(dr + i);
+                v[k][0] = Elem<T>::load(xr + i);
+                u[k][0] = Elem<T>::load(dr + i);
             }
         } else {
 #pragma unroll
@@ -99,20 +101,20 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
     if constexpr (V == 4) {
         has_h = (rank == 0) && (worker < h);
         has_t = (rank == 0) && (worker < tl);
-        te = h + 4 * nb + worker;
+        te = h + EV * nb + worker;
         if (has_h) {
-            hv = Elem<float>::load(xr + worker);
-            hu = Elem<float>::load(dr + worker);
+            hv = Elem<T>::load(xr + worker);
+            hu = Elem<T>::load(dr + worker);
         }
         if (has_t) {
-            tv = Elem<float>::load(xr + te);
-            tu = Elem<float>::load(dr + te);
+            tv = Elem<T>::load(xr + te);
+            tu = Elem<T>::load(dr + te);
         }
     }
 
     const float n = static_cast<float>(width);
     const float *gam = a.gamma;
-    auto col_of = [&](int i) { return (V == 4) ? h + 4 * i : i; };
+    auto col_of = [&](int i) { return (V == 4) ? h + EV * i : i; };
 
     if constexpr (OP == BWD_SOFTMAX) {
         // ---- sum(dy * y), then dx = y (dy - sum) -------------------------
@@ -130,25 +132,43 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
         hv = hv * (hu - dot);
         tv = tv * (tu - dot);
     } else {
-        // ---- g = dy * gamma in place ---------------------------------------
+        // ---- g = dy * gamma in place (2-byte rows, bound by instruction
+        // issue: gamma as float4 when its phase allows; FP32 rows, bound by
+        // DRAM, measured faster with scalar loads)
         if (gam != nullptr) {
+            bool gvec = false;
+            if constexpr (V == 4 && sizeof(T) == 2)
+                gvec = (reinterpret_cast<uintptr_t>(gam + h) & 15) == 0;
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const int i = k * (C * W) + gw;
                 if (i < nb) {
+                    if (gvec) {
 #pragma unroll
-                    for (int j = 0; j < EV; ++j) u[k][j] *= __ldg(gam + col_of(i) + j);
+                        for (int q = 0; q < EV / 4; ++q) {
+                            const float4 g4 =
+                                __ldg(reinterpret_cast<const float4 *>(gam + col_of(i)) + q);
+                            u[k][4 * q] *= g4.x;
+                            u[k][4 * q + 1] *= g4.y;
+                            u[k][4 * q + 2] *= g4.z;
+                            u[k][4 * q + 3] *= g4.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < EV; ++j) u[k][j] *= __ldg(gam + col_of(i) + j);
+                    }
                 }
             }
             if (has_h) hu *= __ldg(gam + worker);
             if (has_t) tu *= __ldg(gam + te);
         }
-        // ---- row statistics and the two gradient sums, xhat in place ------
+        // ---- row statistics and the two gradient sums -----------------------
         // The gradient sums need no extra reduction round: with d = x - m0
         // (LayerNorm) sum(g xhat) = rstd (sum(g d) - mu1 sum(g)), and for
         // RMSNorm sum(g xhat) = rstd sum(g x), so they are reduced together
         // with the statistics they depend on.
         float rstd, mean = 0.0f, mean_g = 0.0f, mean_gx;
+        float ca = 0.0f, cb = 0.0f;   // 2-byte rows: dx = rstd g + ca v + cb, v = d (or x)
         if constexpr (OP == BWD_LN) {
             float s[1] = {hv + tv};
 #pragma unroll
@@ -184,14 +204,20 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
             mean = mean0 + mu1;
             mean_g = q[2] / n;
             mean_gx = rstd * fmaf(-mu1, q[2], q[3]) / n;
+            if constexpr (sizeof(T) == 2) {
+                // rstd (g - mean_g - (d - mu1) rstd mean_gx)
+                ca = -rstd * rstd * mean_gx;
+                cb = rstd * fmaf(rstd * mean_gx, mu1, -mean_g);
+            } else {
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
-                const bool ok = k * (C * W) + gw < nb;
+                for (int k = 0; k < K; ++k) {
+                    const bool ok = k * (C * W) + gw < nb;
 #pragma unroll
-                for (int j = 0; j < EV; ++j) v[k][j] = ok ? (v[k][j] - mu1) * rstd : 0.0f;
+                    for (int j = 0; j < EV; ++j) v[k][j] = ok ? (v[k][j] - mu1) * rstd : 0.0f;
+                }
+                hv = has_h ? (hv - mu1) * rstd : 0.0f;
+                tv = has_t ? (tv - mu1) * rstd : 0.0f;
             }
-            hv = has_h ? (hv - mu1) * rstd : 0.0f;
-            tv = has_t ? (tv - mu1) * rstd : 0.0f;
         } else {
             float q[2] = {fmaf(hv, hv, tv * tv), fmaf(hu, hv, tu * tv)};
 #pragma unroll
@@ -204,12 +230,16 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
             row_allreduce<Sum, 2, S, P, C>(q, part1, cpart, program, warp, lane);
             rstd = 1.0f / sqrtf(q[0] / n + a.eps);
             mean_gx = rstd * q[1] / n;
+            if constexpr (sizeof(T) == 2) {
+                ca = -rstd * rstd * mean_gx;         // rstd (g - x rstd mean_gx)
+            } else {
 #pragma unroll
-            for (int k = 0; k < K; ++k)
+                for (int k = 0; k < K; ++k)
 #pragma unroll
-                for (int j = 0; j < EV; ++j) v[k][j] *= rstd;
-            hv *= rstd;
-            tv *= rstd;
+                    for (int j = 0; j < EV; ++j) v[k][j] *= rstd;
+                hv *= rstd;
+                tv *= rstd;
+            }
         }
 
         if (a.stats != nullptr && active && worker == 0 && rank == 0) {
@@ -217,14 +247,27 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
             a.stats[2 * row + 1] = rstd;
         }
 
-        // ---- dx = rstd (g - mean(g) - xhat mean(g xhat)) --------------------
+        // ---- dx = rstd (g - mean(g) - xhat mean(g xhat)) ----------------------
+        if constexpr (sizeof(T) == 2) {
+            // 2-byte rows: written in d (or x) directly, rstd g + ca v + cb,
+            // two FMAs (xhat is never formed)
 #pragma unroll
-        for (int k = 0; k < K; ++k)
+            for (int k = 0; k < K; ++k)
 #pragma unroll
-            for (int j = 0; j < EV; ++j)
-                v[k][j] = rstd * (u[k][j] - mean_g - v[k][j] * mean_gx);
-        hv = rstd * (hu - mean_g - hv * mean_gx);
-        tv = rstd * (tu - mean_g - tv * mean_gx);
+                for (int j = 0; j < EV; ++j)
+                    v[k][j] = fmaf(rstd, u[k][j], fmaf(ca, v[k][j], cb));
+            hv = fmaf(rstd, hu, fmaf(ca, hv, cb));
+            tv = fmaf(rstd, tu, fmaf(ca, tv, cb));
+        } else {
+            // FP32 rows: v holds xhat
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int j = 0; j < EV; ++j)
+                    v[k][j] = rstd * (u[k][j] - mean_g - v[k][j] * mean_gx);
+            hv = rstd * (hu - mean_g - hv * mean_gx);
+            tv = rstd * (tu - mean_g - tv * mean_gx);
+        }
     }
 
     if constexpr (C > 1) cluster_arrive();
@@ -234,14 +277,14 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
             const int i = k * (C * W) + gw;
             if (i < nb) {
                 if constexpr (V == 4)
-                    Elem<float>::store_vec(outr + h + 4 * i, v[k]);
+                    Elem<T>::store_vec(outr + h + EV * i, v[k]);
                 else
-                    Elem<float>::store(outr + i, v[k][0]);
+                    Elem<T>::store(outr + i, v[k][0]);
             }
         }
         if constexpr (V == 4) {
-            if (has_h) Elem<float>::store(outr + worker, hv);
-            if (has_t) Elem<float>::store(outr + te, tv);
+            if (has_h) Elem<T>::store(outr + worker, hv);
+            if (has_t) Elem<T>::store(outr + te, tv);
         }
     }
     if constexpr (C > 1) cluster_wait();

@@ -29,13 +29,14 @@ struct RowArgs {
 
 // Arguments of one backward-kernel launch (bwd_kernel.cuh).  x: forward
 // input (LayerNorm / RMSNorm) or forward output y (softmax); dy: upstream
-// gradient; gamma: optional FP32 [width]; dx: input gradient; stats:
-// optional [rows][2] (mean, rstd) output.  All FP32 [rows][width].
+// gradient; dx: input gradient; all [rows][width] of the launch's element
+// type (FP32, BF16 or FP16).  gamma: optional FP32 [width]; stats: optional
+// FP32 [rows][2] (mean, rstd) output.
 struct BwdArgs {
-    const float *x;
-    const float *dy;
+    const void *x;
+    const void *dy;
     const float *gamma;
-    float *dx;
+    void *dx;
     float *stats;
     long long rows;
     int width;
@@ -56,17 +57,23 @@ cudaError_t status_staged(unsigned int *value, cudaStream_t stream);
 enum { BWD_LN_OP = 0, BWD_RMS_OP = 1, BWD_SOFTMAX_OP = 2 };
 cudaError_t launch_backward(int op, int plan_id, BwdArgs args, cudaStream_t stream);
 cudaError_t status_backward(unsigned int *value, cudaStream_t stream);
+cudaError_t launch_backward_bf16(int op, int plan_id, BwdArgs args, cudaStream_t stream);
+cudaError_t status_backward_bf16(unsigned int *value, cudaStream_t stream);
+cudaError_t launch_backward_f16(int op, int plan_id, BwdArgs args, cudaStream_t stream);
+cudaError_t status_backward_f16(unsigned int *value, cudaStream_t stream);
 
 // Parameter gradients (param_grad.cu): column sums of dy * xhat and dy over
 // param_blocks(rows) fixed row blocks into ws [nblk][2][width], then summed.
 int param_blocks(long long rows);
-cudaError_t launch_param_grad(const float *x, const float *dy, const float *stats, float *dgamma,
-                              float *dbeta, long long rows, int width, float *ws,
+// x, dy: [rows][width] of element type elem (ELEM_F32, ELEM_BF16, ELEM_F16).
+cudaError_t launch_param_grad(int elem, const void *x, const void *dy, const float *stats,
+                              float *dgamma, float *dbeta, long long rows, int width, float *ws,
                               cudaStream_t stream);
 cudaError_t status_param_grad(unsigned int *value, cudaStream_t stream);
 
 // Largest register stripe per input (floats per thread) of a backward plan:
-// two stripes are held, so plans above it are not built for backward.
+// two stripes are held, so plans above it (K * elements per vector) are not
+// built for backward.
 constexpr int kMaxStripeBwd = 32;
 
 #define TILE_DECLARE_OP(name)                                                            \

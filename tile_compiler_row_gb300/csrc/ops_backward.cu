@@ -1,94 +1,4 @@
-// Backward row kernels (bwd_kernel.cuh): every built plan whose two stripes
-// fit the register budget, for LayerNorm, RMSNorm and softmax, plus the
-// launcher and device error word.
-#include <atomic>
-
-#include "bwd_kernel.cuh"
-#include "launch.h"
-#include "plans.h"
-
-namespace tile {
-namespace {
-__device__ unsigned int g_status;   // device error word of the backward kernels
-
-unsigned int *status_address(cudaError_t *err) {
-    static std::atomic<unsigned int *> cache[kMaxDevices];
-    int dev = 0;
-    *err = cudaGetDevice(&dev);
-    if (*err != cudaSuccess) return nullptr;
-    if (dev < 0 || dev >= kMaxDevices) {
-        *err = cudaErrorInvalidDevice;
-        return nullptr;
-    }
-    unsigned int *p = cache[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
-        *err = cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_status);
-        if (*err != cudaSuccess) return nullptr;
-        cache[dev].store(p, std::memory_order_release);
-    }
-    return p;
-}
-
-template <int OP, int V, int S, int P, int K, int C>
-cudaError_t launch_plan(BwdArgs args, cudaStream_t stream) {
-    if constexpr (K * V > kMaxStripeBwd) {
-        (void)args;
-        (void)stream;
-        return cudaErrorInvalidValue;     // not built: two stripes too large
-    } else {
-        cudaError_t err = cudaSuccess;
-        args.status = status_address(&err);
-        if (args.status == nullptr) return err;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned int>(((args.rows + P - 1) / P) * C), 1, 1);
-        cfg.blockDim = dim3(32 * S * P, 1, 1);
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        if (C > 1) {
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = C;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-        }
-        return cudaLaunchKernelEx(&cfg, row_bwd_kernel<OP, V, S, P, K, C>, args);
-    }
-}
-
-template <int OP>
-cudaError_t launch_op(int plan_id, BwdArgs args, cudaStream_t stream) {
-    switch (plan_id) {
-#define TILE_CASE(id, V, S, P, K, C) \
-    case id: return launch_plan<OP, V, S, P, K, C>(args, stream);
-        TILE_PLAN_LIST(TILE_CASE)
-#undef TILE_CASE
-        default: return cudaErrorInvalidValue;
-    }
-}
-}  // namespace
-
-cudaError_t launch_backward(int op, int plan_id, BwdArgs args, cudaStream_t stream) {
-    switch (op) {
-        case BWD_LN: return launch_op<BWD_LN>(plan_id, args, stream);
-        case BWD_RMS: return launch_op<BWD_RMS>(plan_id, args, stream);
-        case BWD_SOFTMAX: return launch_op<BWD_SOFTMAX>(plan_id, args, stream);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-cudaError_t status_backward(unsigned int *value, cudaStream_t stream) {
-    cudaError_t err = cudaMemcpyFromSymbolAsync(value, g_status, sizeof(unsigned int), 0,
-                                                cudaMemcpyDeviceToHost, stream);
-    if (err != cudaSuccess) return err;
-    err = cudaStreamSynchronize(stream);
-    if (err != cudaSuccess) return err;
-    if (*value == 0) return cudaSuccess;
-    const unsigned int zero = 0;
-    err = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(unsigned int), 0,
-                                  cudaMemcpyHostToDevice, stream);
-    if (err != cudaSuccess) return err;
-    return cudaStreamSynchronize(stream);
-}
-
-}  // namespace tile
+// Backward row kernels on FP32 rows (FP32 arithmetic): every built plan (see bwd_inst.cuh).
+#define TILE_BWD_T float
+#define TILE_BWD_NAME 
+#include "bwd_inst.cuh"

@@ -4,8 +4,10 @@
 // with (mean_i, rstd_i) the row statistics the backward kernel wrote
 // (mean 0 for RMSNorm).
 //
-// Stage 1 splits the rows into nblk fixed blocks; a thread owns 4 adjacent
-// columns (one float4 when rows are 16-byte aligned, else 4 scalars) and
+// x and dy are FP32, BF16 or FP16 (widened exactly; all sums are FP32).
+// Stage 1 splits the rows into nblk fixed blocks; a thread owns the columns
+// of one 16-byte vector (4 FP32 or 8 BF16 / FP16: one aligned load when the
+// rows allow it, else scalars) and
 // accumulates compensated (TwoSum) sums over its block's rows, four rows in
 // flight.  Block partials go to the caller's workspace [nblk][2][width].
 // Stage 2 sums the nblk partials of each column in a fixed order (eight
@@ -17,6 +19,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "launch.h"
 #include "row_kernel.cuh"
@@ -28,8 +31,24 @@ __device__ unsigned int g_status;   // device error word of the parameter kernel
 constexpr int kThreads = 256;
 constexpr int kRowsInFlight = 4;
 
+// Columns a stage-1 thread owns: one 16-byte vector of the element type.
+template <class T>
+__host__ __device__ constexpr int cols_per_thread() { return 16 / static_cast<int>(sizeof(T)); }
+
+// The 16-byte vector of a row at p (4 FP32 or 8 BF16 / FP16), widened.
+template <class T>
+__device__ __forceinline__ void load_cols(const T *p, float (&v)[cols_per_thread<T>()]) {
+    if constexpr (sizeof(T) == 4) {
+        const float4 t = __ldcs(reinterpret_cast<const float4 *>(p));
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+        Elem<T>::load_vec(p, v);
+    }
+}
+
+template <class T>
 __global__ void __launch_bounds__(kThreads)
-    param_partial_kernel(const float *__restrict__ x, const float *__restrict__ dy,
+    param_partial_kernel(const T *__restrict__ x, const T *__restrict__ dy,
                          const float *__restrict__ stats, float *__restrict__ ws, long long rows,
                          int width, int rows_per_block, int vec, int with_beta,
                          unsigned int *status) {
@@ -37,38 +56,40 @@ __global__ void __launch_bounds__(kThreads)
         if (threadIdx.x == 0) atomicOr(status, 1u);
         return;
     }
-    const int c0 = (blockIdx.x * kThreads + threadIdx.x) * 4;   // first owned column
+    constexpr int CPT = cols_per_thread<T>();
+    const int c0 = (blockIdx.x * kThreads + threadIdx.x) * CPT;   // first owned column
     if (c0 >= width) return;
     const long long r0 = static_cast<long long>(blockIdx.y) * rows_per_block;
     long long r1 = r0 + rows_per_block;
     if (r1 > rows) r1 = rows;
-    const int ncol = width - c0 < 4 ? width - c0 : 4;
+    const int ncol = width - c0 < CPT ? width - c0 : CPT;
 
-    float sg[4] = {0, 0, 0, 0}, cg[4] = {0, 0, 0, 0};
-    float sb[4] = {0, 0, 0, 0}, cb[4] = {0, 0, 0, 0};
+    float sg[CPT], cg[CPT], sb[CPT], cb[CPT];
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) sg[j] = cg[j] = sb[j] = cb[j] = 0.0f;
     for (long long r = r0; r < r1; r += kRowsInFlight) {
-        float xv[kRowsInFlight][4], dv[kRowsInFlight][4], mu[kRowsInFlight], rs[kRowsInFlight];
+        float xv[kRowsInFlight][CPT], dv[kRowsInFlight][CPT], mu[kRowsInFlight], rs[kRowsInFlight];
 #pragma unroll
         for (int q = 0; q < kRowsInFlight; ++q) {
             const long long rr = r + q;
             if (rr < r1) {
-                const float *xr = x + rr * width + c0;
-                const float *dr = dy + rr * width + c0;
+                const T *xr = x + rr * width + c0;
+                const T *dr = dy + rr * width + c0;
                 if (vec) {
-                    Elem<float>::load_vec(xr, xv[q]);
-                    Elem<float>::load_vec(dr, dv[q]);
+                    load_cols<T>(xr, xv[q]);
+                    load_cols<T>(dr, dv[q]);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        xv[q][j] = j < ncol ? Elem<float>::load(xr + j) : 0.0f;
-                        dv[q][j] = j < ncol ? Elem<float>::load(dr + j) : 0.0f;
+                    for (int j = 0; j < CPT; ++j) {
+                        xv[q][j] = j < ncol ? Elem<T>::load(xr + j) : 0.0f;
+                        dv[q][j] = j < ncol ? Elem<T>::load(dr + j) : 0.0f;
                     }
                 }
                 mu[q] = __ldg(stats + 2 * rr);
                 rs[q] = __ldg(stats + 2 * rr + 1);
             } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < CPT; ++j) {
                     xv[q][j] = 0.0f;
                     dv[q][j] = 0.0f;
                 }
@@ -76,13 +97,28 @@ __global__ void __launch_bounds__(kThreads)
                 rs[q] = 0.0f;
             }
         }
+        if constexpr (sizeof(T) == 2 && kRowsInFlight == 4) {
+            // 2-byte rows (bound by instruction issue): the four rows are
+            // summed as a pairwise tree, then added once, compensated.  The
+            // tree adds at most 2u sum|terms| of error, the compensated
+            // running sum and the final rounding u each: within 3u sum|terms|.
 #pragma unroll
-        for (int q = 0; q < kRowsInFlight; ++q)
+            for (int j = 0; j < CPT; ++j) {
+                float t[kRowsInFlight];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                comp_add(sg[j], cg[j], dv[q][j] * ((xv[q][j] - mu[q]) * rs[q]));
-                comp_add(sb[j], cb[j], dv[q][j]);
+                for (int q = 0; q < kRowsInFlight; ++q) t[q] = dv[q][j] * ((xv[q][j] - mu[q]) * rs[q]);
+                comp_add(sg[j], cg[j], (t[0] + t[1]) + (t[2] + t[3]));
+                comp_add(sb[j], cb[j], (dv[0][j] + dv[1][j]) + (dv[2][j] + dv[3][j]));
             }
+        } else {
+#pragma unroll
+            for (int q = 0; q < kRowsInFlight; ++q)
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) {
+                    comp_add(sg[j], cg[j], dv[q][j] * ((xv[q][j] - mu[q]) * rs[q]));
+                    comp_add(sb[j], cb[j], dv[q][j]);
+                }
+        }
     }
     float *wg = ws + static_cast<long long>(blockIdx.y) * 2 * width + c0;
     float *wb = wg + width;
@@ -163,22 +199,24 @@ int param_blocks(long long rows) {
 
 namespace {
 
-// CTA slots of stage 1 on this device (SMs x resident CTAs), cached.
-int partial_slots() {
-    static std::atomic<int> cache[kMaxDevices];
+// CTA slots of stage 1 on this device (SMs x resident CTAs) for the kernel
+// of element type elem, cached.
+template <class T>
+int partial_slots_of(int elem) {
+    static std::atomic<int> cache[kMaxDevices][3];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-    int v = cache[dev].load(std::memory_order_relaxed);
+    int v = cache[dev][elem].load(std::memory_order_relaxed);
     if (v == 0) {
         int sms = 0, per_sm = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, param_partial_kernel,
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, param_partial_kernel<T>,
                                                           kThreads, 0) != cudaSuccess) {
             (void)cudaGetLastError();
             return 0;
         }
         v = sms * per_sm;
-        cache[dev].store(v, std::memory_order_relaxed);
+        cache[dev][elem].store(v, std::memory_order_relaxed);
     }
     return v;
 }
@@ -187,9 +225,8 @@ int partial_slots() {
 // holds), lowered so the grid (column tiles x row blocks) fills whole waves
 // of the device's CTA slots when it spans more than one wave: a last wave
 // half full leaves half the SMs idle for its duration.
-int balanced_blocks(long long rows, int col_tiles) {
+int balanced_blocks(long long rows, int col_tiles, long long slots) {
     const int nmax = param_blocks(rows);
-    const long long slots = partial_slots();
     const long long total = static_cast<long long>(col_tiles) * nmax;
     if (slots <= 0 || total <= slots) return nmax;
     const long long waves = total / slots;
@@ -197,28 +234,51 @@ int balanced_blocks(long long rows, int col_tiles) {
     return n >= 1 && n <= nmax ? static_cast<int>(n) : nmax;
 }
 
-}  // namespace
-
-cudaError_t launch_param_grad(const float *x, const float *dy, const float *stats, float *dgamma,
-                              float *dbeta, long long rows, int width, float *ws,
-                              cudaStream_t stream) {
-    cudaError_t err = cudaSuccess;
-    unsigned int *status = status_address(&err);
-    if (status == nullptr) return err;
-    const int col_tiles = (width + 4 * kThreads - 1) / (4 * kThreads);
-    const int nblk = balanced_blocks(rows, col_tiles);
+template <class T>
+cudaError_t launch_typed(int elem, const T *x, const T *dy, const float *stats, float *dgamma,
+                         float *dbeta, long long rows, int width, float *ws, unsigned int *status,
+                         cudaStream_t stream) {
+    const int cpt = cols_per_thread<T>();
+    const int col_tiles = (width + cpt * kThreads - 1) / (cpt * kThreads);
+    const int nblk = balanced_blocks(rows, col_tiles, partial_slots_of<T>(elem));
     const int rows_per_block = static_cast<int>((rows + nblk - 1) / nblk);
     const uintptr_t a = reinterpret_cast<uintptr_t>(x), b = reinterpret_cast<uintptr_t>(dy);
-    const int vec = (width % 4 == 0) && (a % 16 == 0) && (b % 16 == 0);
+    // 16-byte loads need 16-byte aligned rows of whole vectors
+    const int vec = (width % cpt == 0) && (a % 16 == 0) && (b % 16 == 0);
     const dim3 grid1(col_tiles, nblk, 1);
-    param_partial_kernel<<<grid1, kThreads, 0, stream>>>(x, dy, stats, ws, rows, width,
-                                                         rows_per_block, vec, dbeta != nullptr,
-                                                         status);
-    err = cudaGetLastError();
+    param_partial_kernel<T><<<grid1, kThreads, 0, stream>>>(x, dy, stats, ws, rows, width,
+                                                            rows_per_block, vec,
+                                                            dbeta != nullptr, status);
+    cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     const dim3 grid2((width + 31) / 32, 1, 1);
     param_final_kernel<<<grid2, kThreads, 0, stream>>>(ws, nblk, width, dgamma, dbeta, status);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_param_grad(int elem, const void *x, const void *dy, const float *stats,
+                              float *dgamma, float *dbeta, long long rows, int width, float *ws,
+                              cudaStream_t stream) {
+    cudaError_t err = cudaSuccess;
+    unsigned int *status = status_address(&err);
+    if (status == nullptr) return err;
+    switch (elem) {
+        case ELEM_F32:
+            return launch_typed<float>(elem, static_cast<const float *>(x),
+                                       static_cast<const float *>(dy), stats, dgamma, dbeta,
+                                       rows, width, ws, status, stream);
+        case ELEM_BF16:
+            return launch_typed<__nv_bfloat16>(elem, static_cast<const __nv_bfloat16 *>(x),
+                                               static_cast<const __nv_bfloat16 *>(dy), stats,
+                                               dgamma, dbeta, rows, width, ws, status, stream);
+        case ELEM_F16:
+            return launch_typed<__half>(elem, static_cast<const __half *>(x),
+                                        static_cast<const __half *>(dy), stats, dgamma, dbeta,
+                                        rows, width, ws, status, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t status_param_grad(unsigned int *value, cudaStream_t stream) {

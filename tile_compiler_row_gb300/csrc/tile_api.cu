@@ -442,28 +442,41 @@ tile_row_args_t args_of(const void *in, const void *res, const float *gamma, con
 }
 
 // Backward plans hold two stripes (input and upstream gradient): the
-// table uses plans with K * V <= 32 floats per stripe.
+// tables use plans with K * (elements per vector) <= 32 floats per stripe.
+// FP32 from the measured backward sweep; the 2-byte table takes, per width,
+// plans with K <= 4 (a stripe of 4 vectors of 8) and at most 512 threads per
+// CTA (two 32-float stripes spill under the 64-register cap of 1024).
 constexpr Bucket kVec4Backward[] = {
     {131, 0}, {259, 1}, {515, 2}, {1027, 4}, {2051, 6}, {4099, 7},
     {8195, 11}, {16387, 13}, {32771, 16}, {65539, 18}, {TILE_MAX_WIDTH, 20},
 };
+constexpr Bucket kTwoByteBackward[] = {
+    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {4103, 6}, {8199, 8},
+    {16391, 11}, {32775, 15}, {65543, 16}, {TILE_MAX_WIDTH, 18},
+};
 
-bool built_backward(const PlanDesc &p) { return p.K * p.V <= tile::kMaxStripeBwd; }
+bool built_backward(const PlanDesc &p, int dtype = TILE_DTYPE_F32) {
+    return p.K * elems_per_vec(p, dtype) <= tile::kMaxStripeBwd;
+}
 
 int bwd_kernel_op(int op) {
     return op == TILE_OP_LAYERNORM ? tile::BWD_LN_OP : op == TILE_OP_RMSNORM ? tile::BWD_RMS_OP
                                                                              : tile::BWD_SOFTMAX_OP;
 }
 
-// Checks and launch of a backward call; plan_id < 0 selects a plan.
-int run_backward(int op, int plan_id, const float *x, const float *gamma, const float *dy,
-                 float *dx, float *stats, int rows, int width, float eps, cudaStream_t stream) {
+// Checks and launch of a backward call; plan_id < 0 selects a plan.  x, dy,
+// dx are [rows][width] of element type dtype; gamma and stats are FP32.
+int run_backward(int op, int plan_id, int dtype, const void *x, const float *gamma,
+                 const void *dy, void *dx, float *stats, int rows, int width, float eps,
+                 cudaStream_t stream) {
     if (op != TILE_OP_LAYERNORM && op != TILE_OP_RMSNORM && op != TILE_OP_SOFTMAX)
         return TILE_ERR_OP;
+    if (!valid_dtype(dtype)) return TILE_ERR_DTYPE;
     if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH) return TILE_ERR_SHAPE;
     if (op != TILE_OP_SOFTMAX && !(std::isfinite(eps) && eps >= 0.0f)) return TILE_ERR_EPS;
     if (plan_id >= TILE_PLAN_COUNT) return TILE_ERR_PLAN;   // register plans only
-    if (plan_id >= 0 && (!built_backward(kPlans[plan_id]) || !covers(kPlans[plan_id], width)))
+    if (plan_id >= 0 &&
+        (!built_backward(kPlans[plan_id], dtype) || !covers(kPlans[plan_id], width, dtype)))
         return TILE_ERR_PLAN;
     if (rows == 0) return TILE_OK;
     if (op == TILE_OP_SOFTMAX) {
@@ -471,11 +484,11 @@ int run_backward(int op, int plan_id, const float *x, const float *gamma, const 
         stats = nullptr;
     }
     if (x == nullptr || dy == nullptr || dx == nullptr) return TILE_ERR_NULL;
-    for (const void *p : {static_cast<const void *>(x), static_cast<const void *>(dy),
-                          static_cast<const void *>(dx), static_cast<const void *>(gamma),
-                          static_cast<const void *>(stats)})
-        if (misaligned(p)) return TILE_ERR_ALIGN;
-    const size_t mat = static_cast<size_t>(rows) * static_cast<size_t>(width) * sizeof(float);
+    const size_t es = elem_size(dtype);
+    if (misaligned_to(x, es) || misaligned_to(dy, es) || misaligned_to(dx, es) ||
+        misaligned(gamma) || misaligned(stats))
+        return TILE_ERR_ALIGN;
+    const size_t mat = static_cast<size_t>(rows) * static_cast<size_t>(width) * es;
     const size_t vec = static_cast<size_t>(width) * sizeof(float);
     const size_t st = static_cast<size_t>(rows) * 2 * sizeof(float);
     if (overlaps(dx, mat, x, mat) || overlaps(dx, mat, dy, mat) || overlaps(dx, mat, gamma, vec) ||
@@ -485,12 +498,65 @@ int run_backward(int op, int plan_id, const float *x, const float *gamma, const 
     const uintptr_t a = reinterpret_cast<uintptr_t>(x);
     const bool vec4 = ((a ^ reinterpret_cast<uintptr_t>(dy)) & 15u) == 0 &&
                       ((a ^ reinterpret_cast<uintptr_t>(dx)) & 15u) == 0;
-    if (plan_id < 0) plan_id = vec4 ? pick(kVec4Backward, width) : pick(kVec1, width);
+    if (plan_id < 0)
+        plan_id = !vec4 ? pick(kVec1, width)
+                        : two_byte(dtype) ? pick(kTwoByteBackward, width)
+                                          : pick(kVec4Backward, width);
     if (plan_id < 0) return TILE_ERR_SHAPE;
     if (kPlans[plan_id].V == 4 && !vec4) return TILE_ERR_PLAN;
     if (grid_of(kPlans[plan_id], rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
     tile::BwdArgs args{x, dy, gamma, dx, stats, rows, width, eps, nullptr};
-    const cudaError_t err = tile::launch_backward(bwd_kernel_op(op), plan_id, args, stream);
+    const int kop = bwd_kernel_op(op);
+    const cudaError_t err =
+        dtype == TILE_DTYPE_BF16  ? tile::launch_backward_bf16(kop, plan_id, args, stream)
+        : dtype == TILE_DTYPE_F16 ? tile::launch_backward_f16(kop, plan_id, args, stream)
+                                  : tile::launch_backward(kop, plan_id, args, stream);
+    if (err != cudaSuccess) {
+        tile::set_last_cuda_error(static_cast<int>(err));
+        return TILE_ERR_CUDA;
+    }
+    return TILE_OK;
+}
+
+// Checks and launch of the parameter gradients; in and dy of element type
+// dtype.
+int run_param_grad(int dtype, const void *in, const void *dy, const float *row_stats,
+                   float *dgamma, float *dbeta, int rows, int width, void *workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
+    if (!valid_dtype(dtype)) return TILE_ERR_DTYPE;
+    if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH) return TILE_ERR_SHAPE;
+    if (in == nullptr || dy == nullptr || dgamma == nullptr) return TILE_ERR_NULL;
+    if (rows > 0 && (row_stats == nullptr || workspace == nullptr)) return TILE_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if (misaligned_to(in, es) || misaligned_to(dy, es))
+        return TILE_ERR_ALIGN;
+    for (const void *p : {static_cast<const void *>(row_stats), static_cast<const void *>(dgamma),
+                          static_cast<const void *>(dbeta), static_cast<const void *>(workspace)})
+        if (misaligned(p)) return TILE_ERR_ALIGN;
+    const size_t vec = static_cast<size_t>(width) * sizeof(float);
+    if (rows == 0) {
+        // no rows: the sums are zero
+        cudaError_t err = cudaMemsetAsync(dgamma, 0, vec, stream);
+        if (err == cudaSuccess && dbeta != nullptr) err = cudaMemsetAsync(dbeta, 0, vec, stream);
+        if (err != cudaSuccess) {
+            tile::set_last_cuda_error(static_cast<int>(err));
+            return TILE_ERR_CUDA;
+        }
+        return TILE_OK;
+    }
+    const size_t need = tile_norm_param_grad_workspace_bytes(rows, width);
+    if (workspace_bytes < need) return TILE_ERR_WORKSPACE;
+    const size_t mat = static_cast<size_t>(rows) * static_cast<size_t>(width) * es;
+    const size_t st = static_cast<size_t>(rows) * 2 * sizeof(float);
+    for (const void *o : {static_cast<const void *>(dgamma), static_cast<const void *>(dbeta)})
+        if (overlaps(o, vec, in, mat) || overlaps(o, vec, dy, mat) || overlaps(o, vec, row_stats, st) ||
+            overlaps(o, vec, workspace, need))
+            return TILE_ERR_ALIAS;
+    if (overlaps(dgamma, vec, dbeta, vec) || overlaps(workspace, need, in, mat) ||
+        overlaps(workspace, need, dy, mat) || overlaps(workspace, need, row_stats, st))
+        return TILE_ERR_ALIAS;
+    const cudaError_t err = tile::launch_param_grad(dtype, in, dy, row_stats, dgamma, dbeta, rows,
+                                                    width, static_cast<float *>(workspace), stream);
     if (err != cudaSuccess) {
         tile::set_last_cuda_error(static_cast<int>(err));
         return TILE_ERR_CUDA;
@@ -794,7 +860,7 @@ int tile_check_device_status(cudaStream_t stream) {
         tile::status_row_minmax_bf16, tile::status_residual_layernorm_f16,
         tile::status_layernorm_f16, tile::status_rmsnorm_f16, tile::status_softmax_f16,
         tile::status_row_sum_f16, tile::status_row_minmax_f16, tile::status_pairs,
-        tile::status_backward,
+        tile::status_backward, tile::status_backward_bf16, tile::status_backward_f16,
         tile::status_param_grad, tile::status_staged};
     for (auto f : fetch) {
         v = 0;
@@ -811,29 +877,67 @@ int tile_check_device_status(cudaStream_t stream) {
 int tile_layernorm_backward_f32(const float *in, const float *gamma, const float *dy, float *dx,
                                 float *row_stats, int rows, int width, float eps,
                                 cudaStream_t stream) {
-    return run_backward(TILE_OP_LAYERNORM, -1, in, gamma, dy, dx, row_stats, rows, width, eps,
-                        stream);
+    return run_backward(TILE_OP_LAYERNORM, -1, TILE_DTYPE_F32, in, gamma, dy, dx, row_stats, rows,
+                        width, eps, stream);
 }
 
 int tile_rmsnorm_backward_f32(const float *in, const float *gamma, const float *dy, float *dx,
                               float *row_stats, int rows, int width, float eps,
                               cudaStream_t stream) {
-    return run_backward(TILE_OP_RMSNORM, -1, in, gamma, dy, dx, row_stats, rows, width, eps,
-                        stream);
+    return run_backward(TILE_OP_RMSNORM, -1, TILE_DTYPE_F32, in, gamma, dy, dx, row_stats, rows,
+                        width, eps, stream);
 }
 
 int tile_softmax_backward_f32(const float *y, const float *dy, float *dx, int rows, int width,
                               cudaStream_t stream) {
-    return run_backward(TILE_OP_SOFTMAX, -1, y, nullptr, dy, dx, nullptr, rows, width, 0.0f,
-                        stream);
+    return run_backward(TILE_OP_SOFTMAX, -1, TILE_DTYPE_F32, y, nullptr, dy, dx, nullptr, rows,
+                        width, 0.0f, stream);
 }
 
 int tile_run_backward_plan_f32(int op, int plan_id, const float *in, const float *gamma,
                                const float *dy, float *dx, float *row_stats, int rows, int width,
                                float eps, cudaStream_t stream) {
     if (plan_id < 0) return TILE_ERR_PLAN;
-    return run_backward(op, plan_id, in, gamma, dy, dx, row_stats, rows, width, eps, stream);
+    return run_backward(op, plan_id, TILE_DTYPE_F32, in, gamma, dy, dx, row_stats, rows, width,
+                        eps, stream);
 }
+
+int tile_run_backward_plan_ex(int op, int plan_id, int dtype, const void *in, const float *gamma,
+                              const void *dy, void *dx, float *row_stats, int rows, int width,
+                              float eps, cudaStream_t stream) {
+    if (plan_id < 0) return TILE_ERR_PLAN;
+    return run_backward(op, plan_id, dtype, in, gamma, dy, dx, row_stats, rows, width, eps,
+                        stream);
+}
+
+#define TILE_BWD_2BYTE(suffix, dtype)                                                           \
+    int tile_layernorm_backward_##suffix(const void *in, const float *gamma, const void *dy,     \
+                                         void *dx, float *row_stats, int rows, int width,       \
+                                         float eps, cudaStream_t stream) {                      \
+        return run_backward(TILE_OP_LAYERNORM, -1, dtype, in, gamma, dy, dx, row_stats, rows,    \
+                            width, eps, stream);                                                \
+    }                                                                                           \
+    int tile_rmsnorm_backward_##suffix(const void *in, const float *gamma, const void *dy,       \
+                                       void *dx, float *row_stats, int rows, int width,         \
+                                       float eps, cudaStream_t stream) {                        \
+        return run_backward(TILE_OP_RMSNORM, -1, dtype, in, gamma, dy, dx, row_stats, rows,      \
+                            width, eps, stream);                                                \
+    }                                                                                           \
+    int tile_softmax_backward_##suffix(const void *y, const void *dy, void *dx, int rows,        \
+                                       int width, cudaStream_t stream) {                        \
+        return run_backward(TILE_OP_SOFTMAX, -1, dtype, y, nullptr, dy, dx, nullptr, rows,       \
+                            width, 0.0f, stream);                                               \
+    }                                                                                           \
+    int tile_norm_param_grad_##suffix(const void *in, const void *dy, const float *row_stats,    \
+                                      float *dgamma, float *dbeta, int rows, int width,         \
+                                      void *workspace, size_t workspace_bytes,                  \
+                                      cudaStream_t stream) {                                    \
+        return run_param_grad(dtype, in, dy, row_stats, dgamma, dbeta, rows, width, workspace,   \
+                              workspace_bytes, stream);                                         \
+    }
+TILE_BWD_2BYTE(bf16, TILE_DTYPE_BF16)
+TILE_BWD_2BYTE(f16, TILE_DTYPE_F16)
+#undef TILE_BWD_2BYTE
 
 size_t tile_norm_param_grad_workspace_bytes(int rows, int width) {
     if (rows < 1 || width < 1) return 0;
@@ -844,42 +948,8 @@ size_t tile_norm_param_grad_workspace_bytes(int rows, int width) {
 int tile_norm_param_grad_f32(const float *in, const float *dy, const float *row_stats,
                              float *dgamma, float *dbeta, int rows, int width, void *workspace,
                              size_t workspace_bytes, cudaStream_t stream) {
-    if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH) return TILE_ERR_SHAPE;
-    if (in == nullptr || dy == nullptr || dgamma == nullptr) return TILE_ERR_NULL;
-    if (rows > 0 && (row_stats == nullptr || workspace == nullptr)) return TILE_ERR_NULL;
-    for (const void *p : {static_cast<const void *>(in), static_cast<const void *>(dy),
-                          static_cast<const void *>(row_stats), static_cast<const void *>(dgamma),
-                          static_cast<const void *>(dbeta), static_cast<const void *>(workspace)})
-        if (misaligned(p)) return TILE_ERR_ALIGN;
-    const size_t vec = static_cast<size_t>(width) * sizeof(float);
-    if (rows == 0) {
-        // no rows: the sums are zero
-        cudaError_t err = cudaMemsetAsync(dgamma, 0, vec, stream);
-        if (err == cudaSuccess && dbeta != nullptr) err = cudaMemsetAsync(dbeta, 0, vec, stream);
-        if (err != cudaSuccess) {
-            tile::set_last_cuda_error(static_cast<int>(err));
-            return TILE_ERR_CUDA;
-        }
-        return TILE_OK;
-    }
-    const size_t need = tile_norm_param_grad_workspace_bytes(rows, width);
-    if (workspace_bytes < need) return TILE_ERR_WORKSPACE;
-    const size_t mat = static_cast<size_t>(rows) * static_cast<size_t>(width) * sizeof(float);
-    const size_t st = static_cast<size_t>(rows) * 2 * sizeof(float);
-    for (const void *o : {static_cast<const void *>(dgamma), static_cast<const void *>(dbeta)})
-        if (overlaps(o, vec, in, mat) || overlaps(o, vec, dy, mat) || overlaps(o, vec, row_stats, st) ||
-            overlaps(o, vec, workspace, need))
-            return TILE_ERR_ALIAS;
-    if (overlaps(dgamma, vec, dbeta, vec) || overlaps(workspace, need, in, mat) ||
-        overlaps(workspace, need, dy, mat) || overlaps(workspace, need, row_stats, st))
-        return TILE_ERR_ALIAS;
-    const cudaError_t err = tile::launch_param_grad(in, dy, row_stats, dgamma, dbeta, rows, width,
-                                                    static_cast<float *>(workspace), stream);
-    if (err != cudaSuccess) {
-        tile::set_last_cuda_error(static_cast<int>(err));
-        return TILE_ERR_CUDA;
-    }
-    return TILE_OK;
+    return run_param_grad(TILE_DTYPE_F32, in, dy, row_stats, dgamma, dbeta, rows, width,
+                          workspace, workspace_bytes, stream);
 }
 
 int tile_sigmoid_pair_f32(const float *in, float *value, float *derivative, long long n,

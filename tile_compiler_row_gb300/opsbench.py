@@ -66,6 +66,7 @@ def main(argv=None):
     # softmax backward wants a softmax output
     tile.tile_softmax_f32(x, y2)
     sm = y2.clone()
+    smb = sm.to(torch.bfloat16)
     tile.tile_layernorm_backward_f32(x, None, r, y, stats)
 
     ops = {
@@ -93,6 +94,12 @@ def main(argv=None):
         "rmsnorm_backward": (lambda: tile.tile_rmsnorm_backward_f32(x, g, r, y, stats), 12),
         "softmax_backward": (lambda: tile.tile_softmax_backward_f32(sm, r, y), 12),
         "norm_param_grad": (lambda: tile.tile_norm_param_grad_f32(x, r, stats, dg, db, ws), 8),
+        "layernorm_backward_bf16": (lambda: tile.tile_layernorm_backward_bf16(xb, g, rb, yb, stats),
+                                    6),
+        "rmsnorm_backward_bf16": (lambda: tile.tile_rmsnorm_backward_bf16(xb, g, rb, yb, stats), 6),
+        "softmax_backward_bf16": (lambda: tile.tile_softmax_backward_bf16(smb, rb, yb), 6),
+        "norm_param_grad_bf16": (lambda: tile.tile_norm_param_grad_bf16(xb, rb, stats, dg, db, ws),
+                                 4),
     }
     only = set(args.only.split(",")) if args.only else None
     peak, src = measured_hbm_gbs()
