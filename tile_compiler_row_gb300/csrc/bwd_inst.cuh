@@ -37,7 +37,10 @@ unsigned int *status_address(cudaError_t *err) {
 template <int OP, int V, int S, int P, int K, int C>
 cudaError_t launch_plan(BwdArgs args, cudaStream_t stream) {
     constexpr int EV = (V == 4) ? Elem<TILE_BWD_T>::kVec : 1;
-    if constexpr (K * EV > kMaxStripeBwd) {
+    // 2-byte rows of 16-byte vectors use the raw-word kernel
+    constexpr bool kRaw = sizeof(TILE_BWD_T) == 2 && V == 4;
+    constexpr int kBudget = kRaw ? kMaxStripeBwdRaw : kMaxStripeBwd;
+    if constexpr (K * EV > kBudget) {
         (void)args;
         (void)stream;
         return cudaErrorInvalidValue;     // not built: two stripes too large
@@ -58,7 +61,10 @@ cudaError_t launch_plan(BwdArgs args, cudaStream_t stream) {
             cfg.attrs = attr;
             cfg.numAttrs = 1;
         }
-        return cudaLaunchKernelEx(&cfg, row_bwd_kernel<OP, TILE_BWD_T, V, S, P, K, C>, args);
+        if constexpr (kRaw)
+            return cudaLaunchKernelEx(&cfg, row_bwd_raw_kernel<OP, TILE_BWD_T, S, P, K, C>, args);
+        else
+            return cudaLaunchKernelEx(&cfg, row_bwd_kernel<OP, TILE_BWD_T, V, S, P, K, C>, args);
     }
 }
 

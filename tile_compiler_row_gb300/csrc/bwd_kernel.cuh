@@ -291,3 +291,258 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
 }
 
 }  // namespace tile
+
+namespace tile {
+
+// The two values of a 32-bit word of 2-byte elements (lower address in the
+// low half), widened exactly.  Volatile asm, so the compiler widens again in
+// every phase instead of keeping the widened values live (which would take
+// back the registers the raw words save).
+template <class T>
+__device__ __forceinline__ void widen_word(unsigned int w, float &lo, float &hi) {
+    if constexpr (std::is_same<T, __half>::value) {
+        asm volatile("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+                     "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+                     : "=f"(lo), "=f"(hi) : "r"(w));
+    } else {
+        unsigned int a, b;
+        asm volatile("shl.b32 %0, %2, 16;\n\tand.b32 %1, %2, 0xffff0000;"
+                     : "=r"(a), "=r"(b) : "r"(w));
+        lo = __uint_as_float(a);
+        hi = __uint_as_float(b);
+    }
+}
+
+template <class T>
+__device__ __forceinline__ void widen_raw8(const unsigned int (&w)[4], float (&f)[8]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) widen_word<T>(w[i], f[2 * i], f[2 * i + 1]);
+}
+
+// Backward kernel for 2-byte rows of 16-byte vectors (BF16, FP16): the
+// arithmetic and mapping of row_bwd_kernel, but the two stripes hold the raw
+// 2-byte words (4 per vector of 8) and every phase widens them again, so a
+// register carries 4 bytes of DRAM data instead of 2 and a thread keeps as
+// many bytes in flight as the FP32 kernel.  gamma is applied where g is used,
+// the output map is d rstd-form dx = rstd g + ca d + cb computed per vector
+// just before its store.
+template <int OP, class T, int S, int P, int K, int C>
+__global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a) {
+    static_assert(sizeof(T) == 2, "2-byte element types");
+    static_assert(C == 1 || P == 1, "a cluster row has one program per CTA");
+    constexpr int W = 32 * S;
+    constexpr int EV = 8;
+
+    __shared__ float part1[S > 1 ? 2 * P * S : 1];
+    __shared__ float part2[S > 1 ? 4 * P * S : 1];
+    __shared__ float cpart[C > 1 ? 5 : 1];
+
+    if (blockDim.x != 32 * S * P) {
+        if (threadIdx.x == 0) atomicOr(a.status, STATUS_BAD_LAUNCH);
+        return;
+    }
+    const int width = a.width;
+    const int tid = threadIdx.x;
+    const int program = tid / W;
+    const int worker = tid - program * W;
+    const int warp = worker >> 5;
+    const int lane = tid & 31;
+    int rank = 0;
+    long long group = blockIdx.x;
+    if constexpr (C > 1) {
+        rank = static_cast<int>(cluster_rank());
+        group = cluster_index();
+    }
+    long long row = group * P + program;
+    const bool active = row < a.rows;
+    if (!active) row = a.rows - 1;                // replay the last row
+
+    const long long base = row * static_cast<long long>(width);
+    const T *xr = static_cast<const T *>(a.x) + base;
+    const T *dr = static_cast<const T *>(a.dy) + base;
+    T *outr = static_cast<T *>(a.dx) + base;
+
+    const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(xr) / sizeof(T)) & (EV - 1));
+    int h = (EV - mis) & (EV - 1);
+    if (h > width) h = width;
+    const int nb = (width - h) / EV;
+    const int tl = width - h - nb * EV;
+    const int gw = rank * W + worker;
+
+    // ---- load both stripes once, as raw words --------------------------
+    unsigned int xw[K][4], dw[K][4];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int i = k * (C * W) + gw;
+        if (i < nb) {
+            const uint4 tx = __ldcs(reinterpret_cast<const uint4 *>(xr + h + EV * i));
+            const uint4 td = __ldcs(reinterpret_cast<const uint4 *>(dr + h + EV * i));
+            xw[k][0] = tx.x; xw[k][1] = tx.y; xw[k][2] = tx.z; xw[k][3] = tx.w;
+            dw[k][0] = td.x; dw[k][1] = td.y; dw[k][2] = td.z; dw[k][3] = td.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) xw[k][q] = dw[k][q] = 0u;   // +0.0 in both types
+        }
+    }
+    const bool has_h = (rank == 0) && (worker < h);
+    const bool has_t = (rank == 0) && (worker < tl);
+    const int te = h + EV * nb + worker;
+    float hv = 0.0f, tv = 0.0f, hu = 0.0f, tu = 0.0f;
+    if (has_h) {
+        hv = Elem<T>::load(xr + worker);
+        hu = Elem<T>::load(dr + worker);
+    }
+    if (has_t) {
+        tv = Elem<T>::load(xr + te);
+        tu = Elem<T>::load(dr + te);
+    }
+
+    const float n = static_cast<float>(width);
+    const float *gam = (OP == BWD_SOFTMAX) ? nullptr : a.gamma;
+    const bool gvec = gam != nullptr && (reinterpret_cast<uintptr_t>(gam + h) & 15) == 0;
+    if (gam != nullptr) {
+        if (has_h) hu *= __ldg(gam + worker);
+        if (has_t) tu *= __ldg(gam + te);
+    }
+    // x (or y) and g = dy * gamma of stripe vector k (column block i)
+    auto vec_xg = [&](int k, int i, float (&xf)[EV], float (&gf)[EV]) {
+        widen_raw8<T>(xw[k], xf);
+        widen_raw8<T>(dw[k], gf);
+        if (gam != nullptr) {
+            const float *gp = gam + h + EV * i;
+            if (gvec) {
+#pragma unroll
+                for (int q = 0; q < EV / 4; ++q) {
+                    const float4 g4 = __ldg(reinterpret_cast<const float4 *>(gp) + q);
+                    gf[4 * q] *= g4.x;
+                    gf[4 * q + 1] *= g4.y;
+                    gf[4 * q + 2] *= g4.z;
+                    gf[4 * q + 3] *= g4.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < EV; ++j) gf[j] *= __ldg(gp + j);
+            }
+        }
+    };
+
+    float mean0 = 0.0f, rstd = 1.0f, mean = 0.0f, ca = 0.0f, cb = 0.0f, dot = 0.0f;
+    if constexpr (OP == BWD_SOFTMAX) {
+        // ---- sum(dy * y) ---------------------------------------------------
+        float s[1] = {fmaf(hu, hv, tu * tv)};
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            float yf[EV], uf[EV];
+            widen_raw8<T>(xw[k], yf);
+            widen_raw8<T>(dw[k], uf);
+#pragma unroll
+            for (int j = 0; j < EV; ++j) s[0] = fmaf(uf[j], yf[j], s[0]);
+        }
+        row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
+        dot = s[0];
+        hv = hv * (hu - dot);
+        tv = tv * (tu - dot);
+    } else {
+        float mean_g = 0.0f, mean_gx;
+        if constexpr (OP == BWD_LN) {
+            float s[1] = {hv + tv};
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                float xf[EV];
+                widen_raw8<T>(xw[k], xf);                 // empty slots widen to 0
+#pragma unroll
+                for (int j = 0; j < EV; ++j) s[0] += xf[j];
+            }
+            row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
+            mean0 = s[0] / n;
+            float q[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int i = k * (C * W) + gw;
+                if (i < nb) {
+                    float xf[EV], gf[EV];
+                    vec_xg(k, i, xf, gf);
+#pragma unroll
+                    for (int j = 0; j < EV; ++j) {
+                        const float d = xf[j] - mean0;
+                        q[0] += d;
+                        q[1] = fmaf(d, d, q[1]);
+                        q[2] += gf[j];
+                        q[3] = fmaf(gf[j], d, q[3]);
+                    }
+                }
+            }
+            hv = has_h ? hv - mean0 : 0.0f;
+            tv = has_t ? tv - mean0 : 0.0f;
+            q[0] += hv + tv;
+            q[1] = fmaf(hv, hv, fmaf(tv, tv, q[1]));
+            q[2] += hu + tu;
+            q[3] = fmaf(hu, hv, fmaf(tu, tv, q[3]));
+            row_allreduce<Sum, 4, S, P, C>(q, part2, cpart + 1, program, warp, lane);
+            const float mu1 = q[0] / n;
+            const float var = fmaxf(q[1] / n - mu1 * mu1, 0.0f);
+            rstd = 1.0f / sqrtf(var + a.eps);
+            mean = mean0 + mu1;
+            mean_g = q[2] / n;
+            mean_gx = rstd * fmaf(-mu1, q[2], q[3]) / n;
+            ca = -rstd * rstd * mean_gx;
+            cb = rstd * fmaf(rstd * mean_gx, mu1, -mean_g);
+        } else {
+            float q[2] = {fmaf(hv, hv, tv * tv), fmaf(hu, hv, tu * tv)};
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int i = k * (C * W) + gw;
+                if (i < nb) {
+                    float xf[EV], gf[EV];
+                    vec_xg(k, i, xf, gf);
+#pragma unroll
+                    for (int j = 0; j < EV; ++j) {
+                        q[0] = fmaf(xf[j], xf[j], q[0]);
+                        q[1] = fmaf(gf[j], xf[j], q[1]);
+                    }
+                }
+            }
+            row_allreduce<Sum, 2, S, P, C>(q, part1, cpart, program, warp, lane);
+            rstd = 1.0f / sqrtf(q[0] / n + a.eps);
+            mean_gx = rstd * q[1] / n;
+            ca = -rstd * rstd * mean_gx;
+        }
+        if (a.stats != nullptr && active && worker == 0 && rank == 0) {
+            a.stats[2 * row] = mean;
+            a.stats[2 * row + 1] = rstd;
+        }
+        hv = fmaf(rstd, hu, fmaf(ca, hv, cb));
+        tv = fmaf(rstd, tu, fmaf(ca, tv, cb));
+    }
+
+    if constexpr (C > 1) cluster_arrive();
+    // ---- dx per vector, stored at once -----------------------------------
+    if (active) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int i = k * (C * W) + gw;
+            if (i < nb) {
+                float xf[EV], gf[EV], o[EV];
+                if constexpr (OP == BWD_SOFTMAX) {
+                    widen_raw8<T>(xw[k], xf);
+                    widen_raw8<T>(dw[k], gf);
+#pragma unroll
+                    for (int j = 0; j < EV; ++j) o[j] = xf[j] * (gf[j] - dot);
+                } else {
+                    vec_xg(k, i, xf, gf);
+#pragma unroll
+                    for (int j = 0; j < EV; ++j) {
+                        const float v = (OP == BWD_LN) ? xf[j] - mean0 : xf[j];
+                        o[j] = fmaf(rstd, gf[j], fmaf(ca, v, cb));
+                    }
+                }
+                Elem<T>::store_vec(outr + h + EV * i, o);
+            }
+        }
+        if (has_h) Elem<T>::store(outr + worker, hv);
+        if (has_t) Elem<T>::store(outr + te, tv);
+    }
+    if constexpr (C > 1) cluster_wait();
+}
+
+}  // namespace tile

@@ -75,6 +75,10 @@ cudaError_t status_param_grad(unsigned int *value, cudaStream_t stream);
 // two stripes are held, so plans above it (K * elements per vector) are not
 // built for backward.
 constexpr int kMaxStripeBwd = 32;
+// The same budget for the raw-word kernel of 2-byte rows of 16-byte vectors,
+// in elements per stripe (two 2-byte elements per register: 64 elements are
+// 32 registers per stripe).
+constexpr int kMaxStripeBwdRaw = 64;
 
 #define TILE_DECLARE_OP(name)                                                            \
     cudaError_t launch_##name(int plan_id, RowArgs args, cudaStream_t stream);          \

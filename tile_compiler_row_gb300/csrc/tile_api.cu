@@ -443,20 +443,21 @@ tile_row_args_t args_of(const void *in, const void *res, const float *gamma, con
 
 // Backward plans hold two stripes (input and upstream gradient): the
 // tables use plans with K * (elements per vector) <= 32 floats per stripe.
-// FP32 from the measured backward sweep; the 2-byte table takes, per width,
-// plans with K <= 4 (a stripe of 4 vectors of 8) and at most 512 threads per
-// CTA (two 32-float stripes spill under the 64-register cap of 1024).
+// Both from measured backward sweeps.  2-byte rows of 16-byte vectors use
+// the raw-word kernel (stripes of up to 8 vectors of 8); its table avoids
+// 1024-thread CTAs, whose 64-register cap the two stripes would spill.
 constexpr Bucket kVec4Backward[] = {
     {131, 0}, {259, 1}, {515, 2}, {1027, 4}, {2051, 6}, {4099, 7},
     {8195, 11}, {16387, 13}, {32771, 16}, {65539, 18}, {TILE_MAX_WIDTH, 20},
 };
 constexpr Bucket kTwoByteBackward[] = {
-    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {4103, 6}, {8199, 8},
-    {16391, 11}, {32775, 15}, {65543, 16}, {TILE_MAX_WIDTH, 18},
+    {263, 0}, {519, 1}, {1031, 2}, {2055, 39}, {4103, 6}, {8199, 8},
+    {16391, 10}, {32775, 14}, {65543, 17}, {TILE_MAX_WIDTH, 19},
 };
 
 bool built_backward(const PlanDesc &p, int dtype = TILE_DTYPE_F32) {
-    return p.K * elems_per_vec(p, dtype) <= tile::kMaxStripeBwd;
+    const bool raw = two_byte(dtype) && p.V == 4;     // raw-word stripes (bwd_kernel.cuh)
+    return p.K * elems_per_vec(p, dtype) <= (raw ? tile::kMaxStripeBwdRaw : tile::kMaxStripeBwd);
 }
 
 int bwd_kernel_op(int op) {
