@@ -5,11 +5,11 @@
 // (mean 0 for RMSNorm).
 //
 // x and dy are FP32, BF16 or FP16 (widened exactly; all sums are FP32).
-// Stage 1 splits the rows into nblk fixed blocks; a thread owns the columns
-// of one 16-byte vector (4 FP32 or 8 BF16 / FP16: one aligned load when the
-// rows allow it, else scalars) and
-// accumulates compensated (TwoSum) sums over its block's rows, four rows in
-// flight.  Block partials go to the caller's workspace [nblk][2][width].
+// Stage 1 splits the rows into nblk fixed blocks; a thread owns 4 adjacent
+// columns (one aligned load per row when the rows allow it, else scalars)
+// and accumulates compensated (TwoSum) sums over its block's rows: FP32 rows
+// four in flight, each added compensated; 2-byte rows eight in flight as raw
+// words, added as pairwise trees of four.  Block partials go to the caller's workspace [nblk][2][width].
 // Stage 2 sums the nblk partials of each column in a fixed order (eight
 // interleaved warp slices, then the slices in warp order).  The partition
 // depends only on (rows, width) and the device (its SM count and the
@@ -31,44 +31,40 @@ __device__ unsigned int g_status;   // device error word of the parameter kernel
 constexpr int kThreads = 256;
 constexpr int kRowsInFlight = 4;
 
-// Columns a stage-1 thread owns: one 16-byte vector of the element type.
+// Element `hi` (0: lower address) of a 32-bit word of two 2-byte values.
 template <class T>
-__host__ __device__ constexpr int cols_per_thread() { return 16 / static_cast<int>(sizeof(T)); }
-
-// The 16-byte vector of a row at p (4 FP32 or 8 BF16 / FP16), widened.
-template <class T>
-__device__ __forceinline__ void load_cols(const T *p, float (&v)[cols_per_thread<T>()]) {
-    if constexpr (sizeof(T) == 4) {
-        const float4 t = __ldcs(reinterpret_cast<const float4 *>(p));
-        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+__device__ __forceinline__ float widen_half(unsigned int w, int hi) {
+    if constexpr (std::is_same<T, __half>::value) {
+        const __half2 h = *reinterpret_cast<const __half2 *>(&w);
+        return hi ? __high2float(h) : __low2float(h);
     } else {
-        Elem<T>::load_vec(p, v);
+        return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16));
     }
 }
 
-template <class T>
-__global__ void __launch_bounds__(kThreads)
-    param_partial_kernel(const T *__restrict__ x, const T *__restrict__ dy,
-                         const float *__restrict__ stats, float *__restrict__ ws, long long rows,
-                         int width, int rows_per_block, int vec, int with_beta,
-                         unsigned int *status) {
-    if (blockDim.x != kThreads) {
-        if (threadIdx.x == 0) atomicOr(status, 1u);
-        return;
-    }
-    constexpr int CPT = cols_per_thread<T>();
-    const int c0 = (blockIdx.x * kThreads + threadIdx.x) * CPT;   // first owned column
-    if (c0 >= width) return;
-    const long long r0 = static_cast<long long>(blockIdx.y) * rows_per_block;
-    long long r1 = r0 + rows_per_block;
-    if (r1 > rows) r1 = rows;
-    const int ncol = width - c0 < CPT ? width - c0 : CPT;
+// Columns a stage-1 thread owns: four (one 16-byte FP32 or 8-byte BF16 /
+// FP16 load per row).
+constexpr int kCols = 4;
 
-    float sg[CPT], cg[CPT], sb[CPT], cb[CPT];
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) sg[j] = cg[j] = sb[j] = cb[j] = 0.0f;
+// Two pairwise trees of four rows each go into one compensated add; the
+// tree adds at most 2u sum|terms| of error, the compensated running sum and
+// the final rounding u each: within 3u sum|terms| (4u is what the tests
+// allow).  FP32 rows (bound by DRAM) add every row compensated.
+__device__ __forceinline__ float tree4(float a, float b, float c, float d) {
+    return (a + b) + (c + d);
+}
+
+// FP32 rows, and 2-byte rows that are not whole aligned groups of four:
+// four rows in flight, widened at load.
+template <class T>
+__device__ __forceinline__ void rows_widened(const T *__restrict__ x, const T *__restrict__ dy,
+                                             const float *__restrict__ stats, long long r0,
+                                             long long r1, int width, int c0, int ncol, int vec,
+                                             float (&sg)[kCols], float (&cg)[kCols],
+                                             float (&sb)[kCols], float (&cb)[kCols]) {
     for (long long r = r0; r < r1; r += kRowsInFlight) {
-        float xv[kRowsInFlight][CPT], dv[kRowsInFlight][CPT], mu[kRowsInFlight], rs[kRowsInFlight];
+        float xv[kRowsInFlight][kCols], dv[kRowsInFlight][kCols], mu[kRowsInFlight],
+            rs[kRowsInFlight];
 #pragma unroll
         for (int q = 0; q < kRowsInFlight; ++q) {
             const long long rr = r + q;
@@ -76,11 +72,22 @@ __global__ void __launch_bounds__(kThreads)
                 const T *xr = x + rr * width + c0;
                 const T *dr = dy + rr * width + c0;
                 if (vec) {
-                    load_cols<T>(xr, xv[q]);
-                    load_cols<T>(dr, dv[q]);
+                    if constexpr (sizeof(T) == 4) {
+                        const float4 tx = __ldcs(reinterpret_cast<const float4 *>(xr));
+                        const float4 td = __ldcs(reinterpret_cast<const float4 *>(dr));
+                        xv[q][0] = tx.x; xv[q][1] = tx.y; xv[q][2] = tx.z; xv[q][3] = tx.w;
+                        dv[q][0] = td.x; dv[q][1] = td.y; dv[q][2] = td.z; dv[q][3] = td.w;
+                    } else {
+                        const uint2 tx = __ldcs(reinterpret_cast<const uint2 *>(xr));
+                        const uint2 td = __ldcs(reinterpret_cast<const uint2 *>(dr));
+                        xv[q][0] = widen_half<T>(tx.x, 0); xv[q][1] = widen_half<T>(tx.x, 1);
+                        xv[q][2] = widen_half<T>(tx.y, 0); xv[q][3] = widen_half<T>(tx.y, 1);
+                        dv[q][0] = widen_half<T>(td.x, 0); dv[q][1] = widen_half<T>(td.x, 1);
+                        dv[q][2] = widen_half<T>(td.y, 0); dv[q][3] = widen_half<T>(td.y, 1);
+                    }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < CPT; ++j) {
+                    for (int j = 0; j < kCols; ++j) {
                         xv[q][j] = j < ncol ? Elem<T>::load(xr + j) : 0.0f;
                         dv[q][j] = j < ncol ? Elem<T>::load(dr + j) : 0.0f;
                     }
@@ -89,36 +96,108 @@ __global__ void __launch_bounds__(kThreads)
                 rs[q] = __ldg(stats + 2 * rr + 1);
             } else {
 #pragma unroll
-                for (int j = 0; j < CPT; ++j) {
-                    xv[q][j] = 0.0f;
-                    dv[q][j] = 0.0f;
-                }
-                mu[q] = 0.0f;
-                rs[q] = 0.0f;
+                for (int j = 0; j < kCols; ++j) xv[q][j] = dv[q][j] = 0.0f;
+                mu[q] = rs[q] = 0.0f;
             }
         }
-        if constexpr (sizeof(T) == 2 && kRowsInFlight == 4) {
-            // 2-byte rows (bound by instruction issue): the four rows are
-            // summed as a pairwise tree, then added once, compensated.  The
-            // tree adds at most 2u sum|terms| of error, the compensated
-            // running sum and the final rounding u each: within 3u sum|terms|.
+        if constexpr (sizeof(T) == 2) {
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) {
+            for (int j = 0; j < kCols; ++j) {
                 float t[kRowsInFlight];
 #pragma unroll
-                for (int q = 0; q < kRowsInFlight; ++q) t[q] = dv[q][j] * ((xv[q][j] - mu[q]) * rs[q]);
-                comp_add(sg[j], cg[j], (t[0] + t[1]) + (t[2] + t[3]));
-                comp_add(sb[j], cb[j], (dv[0][j] + dv[1][j]) + (dv[2][j] + dv[3][j]));
+                for (int q = 0; q < kRowsInFlight; ++q)
+                    t[q] = dv[q][j] * ((xv[q][j] - mu[q]) * rs[q]);
+                comp_add(sg[j], cg[j], tree4(t[0], t[1], t[2], t[3]));
+                comp_add(sb[j], cb[j], tree4(dv[0][j], dv[1][j], dv[2][j], dv[3][j]));
             }
         } else {
 #pragma unroll
             for (int q = 0; q < kRowsInFlight; ++q)
 #pragma unroll
-                for (int j = 0; j < CPT; ++j) {
+                for (int j = 0; j < kCols; ++j) {
                     comp_add(sg[j], cg[j], dv[q][j] * ((xv[q][j] - mu[q]) * rs[q]));
                     comp_add(sb[j], cb[j], dv[q][j]);
                 }
         }
+    }
+}
+
+// 2-byte rows of whole aligned groups of four: eight rows in flight kept as
+// raw words (a register carries 4 bytes of DRAM data instead of 2), summed
+// as two trees of four.
+template <class T>
+__device__ __forceinline__ void rows_raw(const T *__restrict__ x, const T *__restrict__ dy,
+                                         const float *__restrict__ stats, long long r0,
+                                         long long r1, int width, int c0,
+                                         float (&sg)[kCols], float (&cg)[kCols],
+                                         float (&sb)[kCols], float (&cb)[kCols]) {
+    constexpr int R = 2 * kRowsInFlight;   // a multiple of 4
+    for (long long r = r0; r < r1; r += R) {
+        unsigned int xw[R][2], dw[R][2];
+        float mu[R], rs[R];
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const long long rr = r + q;
+            if (rr < r1) {
+                const uint2 tx = __ldcs(reinterpret_cast<const uint2 *>(x + rr * width + c0));
+                const uint2 td = __ldcs(reinterpret_cast<const uint2 *>(dy + rr * width + c0));
+                xw[q][0] = tx.x; xw[q][1] = tx.y;
+                dw[q][0] = td.x; dw[q][1] = td.y;
+                mu[q] = __ldg(stats + 2 * rr);
+                rs[q] = __ldg(stats + 2 * rr + 1);
+            } else {
+                xw[q][0] = xw[q][1] = dw[q][0] = dw[q][1] = 0u;   // +0.0
+                mu[q] = rs[q] = 0.0f;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kCols; ++j)
+#pragma unroll
+            for (int g = 0; g < R / 4; ++g) {
+                float t[4], d[4];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int q = 4 * g + q4;
+                    const float xq = widen_half<T>(xw[q][j >> 1], j & 1);
+                    d[q4] = widen_half<T>(dw[q][j >> 1], j & 1);
+                    t[q4] = d[q4] * ((xq - mu[q]) * rs[q]);
+                }
+                comp_add(sg[j], cg[j], tree4(t[0], t[1], t[2], t[3]));
+                comp_add(sb[j], cb[j], tree4(d[0], d[1], d[2], d[3]));
+            }
+    }
+}
+
+// Two resident CTAs per SM (at most 128 registers a thread): the 2-byte
+// kernel keeps its eight raw rows and two trees without spilling; three
+// (85 registers) ran 2 % slower at 65536 x 4096 BF16.
+template <class T>
+__global__ void __launch_bounds__(kThreads, 2)
+    param_partial_kernel(const T *__restrict__ x, const T *__restrict__ dy,
+                         const float *__restrict__ stats, float *__restrict__ ws, long long rows,
+                         int width, int rows_per_block, int vec, int with_beta,
+                         unsigned int *status) {
+    if (blockDim.x != kThreads) {
+        if (threadIdx.x == 0) atomicOr(status, 1u);
+        return;
+    }
+    const int c0 = (blockIdx.x * kThreads + threadIdx.x) * kCols;   // first owned column
+    if (c0 >= width) return;
+    const long long r0 = static_cast<long long>(blockIdx.y) * rows_per_block;
+    long long r1 = r0 + rows_per_block;
+    if (r1 > rows) r1 = rows;
+    const int ncol = width - c0 < kCols ? width - c0 : kCols;
+
+    float sg[kCols], cg[kCols], sb[kCols], cb[kCols];
+#pragma unroll
+    for (int j = 0; j < kCols; ++j) sg[j] = cg[j] = sb[j] = cb[j] = 0.0f;
+    if constexpr (sizeof(T) == 2) {
+        if (vec)
+            rows_raw<T>(x, dy, stats, r0, r1, width, c0, sg, cg, sb, cb);
+        else
+            rows_widened<T>(x, dy, stats, r0, r1, width, c0, ncol, vec, sg, cg, sb, cb);
+    } else {
+        rows_widened<T>(x, dy, stats, r0, r1, width, c0, ncol, vec, sg, cg, sb, cb);
     }
     float *wg = ws + static_cast<long long>(blockIdx.y) * 2 * width + c0;
     float *wb = wg + width;
@@ -222,29 +301,31 @@ int partial_slots_of(int elem) {
 }
 
 // Row blocks for stage 1: at most param_blocks(rows) (what the workspace
-// holds), lowered so the grid (column tiles x row blocks) fills whole waves
-// of the device's CTA slots when it spans more than one wave: a last wave
-// half full leaves half the SMs idle for its duration.
+// holds), and no more than one wave of the device's CTA slots fits (column
+// tiles x row blocks <= slots).  Long CTAs pay their load ramp once, and
+// fewer block partials shorten stage 2: at 65536 x 4096 BF16 one wave ran in
+// 173 us, four full waves of short CTAs in 187 us (FP32 rows, bound by DRAM,
+// ran at 328 us either way).
 int balanced_blocks(long long rows, int col_tiles, long long slots) {
     const int nmax = param_blocks(rows);
-    const long long total = static_cast<long long>(col_tiles) * nmax;
-    if (slots <= 0 || total <= slots) return nmax;
-    const long long waves = total / slots;
-    const long long n = waves * slots / col_tiles;
-    return n >= 1 && n <= nmax ? static_cast<int>(n) : nmax;
+    if (slots <= 0) return nmax;
+    const long long fit = slots / col_tiles;
+    if (fit < 1) return 1;
+    return fit < nmax ? static_cast<int>(fit) : nmax;
 }
 
 template <class T>
 cudaError_t launch_typed(int elem, const T *x, const T *dy, const float *stats, float *dgamma,
                          float *dbeta, long long rows, int width, float *ws, unsigned int *status,
                          cudaStream_t stream) {
-    const int cpt = cols_per_thread<T>();
-    const int col_tiles = (width + cpt * kThreads - 1) / (cpt * kThreads);
+    const int col_tiles = (width + kCols * kThreads - 1) / (kCols * kThreads);
     const int nblk = balanced_blocks(rows, col_tiles, partial_slots_of<T>(elem));
     const int rows_per_block = static_cast<int>((rows + nblk - 1) / nblk);
     const uintptr_t a = reinterpret_cast<uintptr_t>(x), b = reinterpret_cast<uintptr_t>(dy);
-    // 16-byte loads need 16-byte aligned rows of whole vectors
-    const int vec = (width % cpt == 0) && (a % 16 == 0) && (b % 16 == 0);
+    // aligned loads of 4 columns: rows of whole groups of 4, aligned to
+    // 16 bytes (FP32) or 8 bytes (BF16 / FP16)
+    const uintptr_t group = kCols * sizeof(T);
+    const int vec = (width % kCols == 0) && (a % group == 0) && (b % group == 0);
     const dim3 grid1(col_tiles, nblk, 1);
     param_partial_kernel<T><<<grid1, kThreads, 0, stream>>>(x, dy, stats, ws, rows, width,
                                                             rows_per_block, vec,
