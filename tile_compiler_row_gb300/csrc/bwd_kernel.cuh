@@ -445,14 +445,18 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
     } else {
         float mean_g = 0.0f, mean_gx;
         if constexpr (OP == BWD_LN) {
-            float s[1] = {hv + tv};
+            // four independent partial sums (the first estimate of the mean
+            // only shifts the data; measured faster than one chain or packed
+            // pairs)
+            float s4[4] = {hv + tv, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 float xf[EV];
                 widen_raw8<T>(xw[k], xf);                 // empty slots widen to 0
 #pragma unroll
-                for (int j = 0; j < EV; ++j) s[0] += xf[j];
+                for (int j = 0; j < EV; ++j) s4[j & 3] += xf[j];
             }
+            float s[1] = {(s4[0] + s4[1]) + (s4[2] + s4[3])};
             row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
             mean0 = s[0] / n;
             float q[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -516,7 +520,8 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
     }
 
     if constexpr (C > 1) cluster_arrive();
-    // ---- dx per vector, stored at once -----------------------------------
+    // ---- dx per vector, stored at once; the output map on packed pairs
+    // (the same two FMAs per element, rounded the same way) --------------
     if (active) {
 #pragma unroll
         for (int k = 0; k < K; ++k) {
@@ -527,13 +532,21 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
                     widen_raw8<T>(xw[k], xf);
                     widen_raw8<T>(dw[k], gf);
 #pragma unroll
-                    for (int j = 0; j < EV; ++j) o[j] = xf[j] * (gf[j] - dot);
+                    for (int j = 0; j < EV; j += 2) {
+                        add_x2(gf[j], gf[j + 1], -dot, -dot);
+                        o[j] = xf[j];
+                        o[j + 1] = xf[j + 1];
+                        mul_x2(o[j], o[j + 1], gf[j], gf[j + 1]);
+                    }
                 } else {
                     vec_xg(k, i, xf, gf);
 #pragma unroll
-                    for (int j = 0; j < EV; ++j) {
-                        const float v = (OP == BWD_LN) ? xf[j] - mean0 : xf[j];
-                        o[j] = fmaf(rstd, gf[j], fmaf(ca, v, cb));
+                    for (int j = 0; j < EV; j += 2) {
+                        if constexpr (OP == BWD_LN) add_x2(xf[j], xf[j + 1], -mean0, -mean0);
+                        o[j] = cb;
+                        o[j + 1] = cb;
+                        fma_x2(o[j], o[j + 1], ca, ca, xf[j], xf[j + 1]);
+                        fma_x2(o[j], o[j + 1], rstd, rstd, gf[j], gf[j + 1]);
                     }
                 }
                 Elem<T>::store_vec(outr + h + EV * i, o);

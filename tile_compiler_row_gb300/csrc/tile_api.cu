@@ -451,7 +451,7 @@ constexpr Bucket kVec4Backward[] = {
     {8195, 11}, {16387, 13}, {32771, 16}, {65539, 18}, {TILE_MAX_WIDTH, 20},
 };
 constexpr Bucket kTwoByteBackward[] = {
-    {263, 0}, {519, 1}, {1031, 2}, {2055, 39}, {4103, 6}, {8199, 8},
+    {263, 0}, {519, 1}, {1031, 2}, {2055, 39}, {4103, 6}, {8199, 7},
     {16391, 10}, {32775, 14}, {65543, 17}, {TILE_MAX_WIDTH, 19},
 };
 
