@@ -319,6 +319,61 @@ __device__ __forceinline__ void widen_raw8(const unsigned int (&w)[4], float (&f
     for (int i = 0; i < 4; ++i) widen_word<T>(w[i], f[2 * i], f[2 * i + 1]);
 }
 
+// v[j] = element j of a raw vector of 8 + c, one mixed-precision add
+// (add.rn.f32.bf16 / .f16) per element: the 2-byte value enters exactly, so
+// each lane is round(x + c) as after an explicit widening.  Volatile, like
+// the widening, so that no phase keeps another phase's values live.
+template <class T>
+__device__ __forceinline__ void add_raw8(const unsigned int (&w)[4], float c, float (&v)[8]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (std::is_same<T, __half>::value)
+            asm volatile("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+                         "add.rn.f32.f16 %0, lo, %3;\n\tadd.rn.f32.f16 %1, hi, %3;\n\t}"
+                         : "=f"(v[2 * i]), "=f"(v[2 * i + 1]) : "r"(w[i]), "f"(c));
+        else
+            asm volatile("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+                         "add.rn.f32.bf16 %0, lo, %3;\n\tadd.rn.f32.bf16 %1, hi, %3;\n\t}"
+                         : "=f"(v[2 * i]), "=f"(v[2 * i + 1]) : "r"(w[i]), "f"(c));
+    }
+}
+
+// s[j % 4] += element j of a raw vector of 8, one mixed-precision add each.
+template <class T>
+__device__ __forceinline__ void acc_raw8(const unsigned int (&w)[4], float (&s)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (std::is_same<T, __half>::value)
+            asm volatile("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+                         "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+                         : "+f"(s[(2 * i) & 3]), "+f"(s[(2 * i + 1) & 3]) : "r"(w[i]));
+        else
+            asm volatile("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+                         "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+                         : "+f"(s[(2 * i) & 3]), "+f"(s[(2 * i + 1) & 3]) : "r"(w[i]));
+    }
+}
+
+// Mixed-precision fused multiply-add on two 2-byte operands and an FP32
+// addend (fma.rn.f32.bf16 / .f16): the product of two BF16 or FP16 values is
+// exact in FP32, so each step rounds once.
+#define TILE_MIXED_FMA(TY)                                                               \
+    "{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t" \
+    "fma.rn.f32." TY " %0, al, bl, %0;\n\tfma.rn.f32." TY " %1, ah, bh, %1;\n\t}"
+
+// (s0, s1) += the products of elements 2i and 2i + 1 of two raw vectors.
+template <class T>
+__device__ __forceinline__ void dot_raw8(const unsigned int (&a)[4], const unsigned int (&b)[4],
+                                         float &s0, float &s1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (std::is_same<T, __half>::value)
+            asm volatile(TILE_MIXED_FMA("f16") : "+f"(s0), "+f"(s1) : "r"(a[i]), "r"(b[i]));
+        else
+            asm volatile(TILE_MIXED_FMA("bf16") : "+f"(s0), "+f"(s1) : "r"(a[i]), "r"(b[i]));
+    }
+}
+
 // Backward kernel for 2-byte rows of 16-byte vectors (BF16, FP16): the
 // arithmetic and mapping of row_bwd_kernel, but the two stripes hold the raw
 // 2-byte words (4 per vector of 8) and every phase widens them again, so a
@@ -404,9 +459,8 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
         if (has_h) hu *= __ldg(gam + worker);
         if (has_t) tu *= __ldg(gam + te);
     }
-    // x (or y) and g = dy * gamma of stripe vector k (column block i)
-    auto vec_xg = [&](int k, int i, float (&xf)[EV], float (&gf)[EV]) {
-        widen_raw8<T>(xw[k], xf);
+    // g = dy * gamma of stripe vector k (column block i)
+    auto vec_g = [&](int k, int i, float (&gf)[EV]) {
         widen_raw8<T>(dw[k], gf);
         if (gam != nullptr) {
             const float *gp = gam + h + EV * i;
@@ -425,19 +479,19 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
             }
         }
     };
+    // x (or y) and g of stripe vector k
+    auto vec_xg = [&](int k, int i, float (&xf)[EV], float (&gf)[EV]) {
+        widen_raw8<T>(xw[k], xf);
+        vec_g(k, i, gf);
+    };
 
     float mean0 = 0.0f, rstd = 1.0f, mean = 0.0f, ca = 0.0f, cb = 0.0f, dot = 0.0f;
     if constexpr (OP == BWD_SOFTMAX) {
         // ---- sum(dy * y) ---------------------------------------------------
-        float s[1] = {fmaf(hu, hv, tu * tv)};
+        float s0 = fmaf(hu, hv, tu * tv), s1 = 0.0f;
 #pragma unroll
-        for (int k = 0; k < K; ++k) {
-            float yf[EV], uf[EV];
-            widen_raw8<T>(xw[k], yf);
-            widen_raw8<T>(dw[k], uf);
-#pragma unroll
-            for (int j = 0; j < EV; ++j) s[0] = fmaf(uf[j], yf[j], s[0]);
-        }
+        for (int k = 0; k < K; ++k) dot_raw8<T>(dw[k], xw[k], s0, s1);   // empty slots add 0
+        float s[1] = {s0 + s1};
         row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
         dot = s[0];
         hv = hv * (hu - dot);
@@ -450,12 +504,7 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
             // pairs)
             float s4[4] = {hv + tv, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
-                float xf[EV];
-                widen_raw8<T>(xw[k], xf);                 // empty slots widen to 0
-#pragma unroll
-                for (int j = 0; j < EV; ++j) s4[j & 3] += xf[j];
-            }
+            for (int k = 0; k < K; ++k) acc_raw8<T>(xw[k], s4);   // empty slots add 0
             float s[1] = {(s4[0] + s4[1]) + (s4[2] + s4[3])};
             row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
             mean0 = s[0] / n;
@@ -464,15 +513,15 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
             for (int k = 0; k < K; ++k) {
                 const int i = k * (C * W) + gw;
                 if (i < nb) {
-                    float xf[EV], gf[EV];
-                    vec_xg(k, i, xf, gf);
+                    float d[EV], gf[EV];
+                    add_raw8<T>(xw[k], -mean0, d);       // d = x - mean0
+                    vec_g(k, i, gf);
 #pragma unroll
                     for (int j = 0; j < EV; ++j) {
-                        const float d = xf[j] - mean0;
-                        q[0] += d;
-                        q[1] = fmaf(d, d, q[1]);
+                        q[0] += d[j];
+                        q[1] = fmaf(d[j], d[j], q[1]);
                         q[2] += gf[j];
-                        q[3] = fmaf(gf[j], d, q[3]);
+                        q[3] = fmaf(gf[j], d[j], q[3]);
                     }
                 }
             }
@@ -492,20 +541,32 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
             ca = -rstd * rstd * mean_gx;
             cb = rstd * fmaf(rstd * mean_gx, mu1, -mean_g);
         } else {
-            float q[2] = {fmaf(hv, hv, tv * tv), fmaf(hu, hv, tu * tv)};
+            float q0 = fmaf(hv, hv, tv * tv), q1 = 0.0f;
+            float g0 = fmaf(hu, hv, tu * tv), g1 = 0.0f;
+            if (gam == nullptr) {
+                // sum x^2 and sum dy x straight from the raw words (mixed
+                // fma: the products are exact), two accumulators each
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
-                const int i = k * (C * W) + gw;
-                if (i < nb) {
-                    float xf[EV], gf[EV];
-                    vec_xg(k, i, xf, gf);
+                for (int k = 0; k < K; ++k) {
+                    dot_raw8<T>(xw[k], xw[k], q0, q1);        // empty slots add 0
+                    dot_raw8<T>(dw[k], xw[k], g0, g1);
+                }
+            } else {
 #pragma unroll
-                    for (int j = 0; j < EV; ++j) {
-                        q[0] = fmaf(xf[j], xf[j], q[0]);
-                        q[1] = fmaf(gf[j], xf[j], q[1]);
+                for (int k = 0; k < K; ++k) {
+                    const int i = k * (C * W) + gw;
+                    if (i < nb) {
+                        float xf[EV], gf[EV];
+                        vec_xg(k, i, xf, gf);
+#pragma unroll
+                        for (int j = 0; j < EV; ++j) {
+                            q0 = fmaf(xf[j], xf[j], q0);
+                            g0 = fmaf(gf[j], xf[j], g0);
+                        }
                     }
                 }
             }
+            float q[2] = {q0 + q1, g0 + g1};
             row_allreduce<Sum, 2, S, P, C>(q, part1, cpart, program, warp, lane);
             rstd = 1.0f / sqrtf(q[0] / n + a.eps);
             mean_gx = rstd * q[1] / n;
@@ -539,10 +600,14 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
                         mul_x2(o[j], o[j + 1], gf[j], gf[j + 1]);
                     }
                 } else {
-                    vec_xg(k, i, xf, gf);
+                    if constexpr (OP == BWD_LN) {
+                        add_raw8<T>(xw[k], -mean0, xf);  // x - mean0
+                        vec_g(k, i, gf);
+                    } else {
+                        vec_xg(k, i, xf, gf);
+                    }
 #pragma unroll
                     for (int j = 0; j < EV; j += 2) {
-                        if constexpr (OP == BWD_LN) add_x2(xf[j], xf[j + 1], -mean0, -mean0);
                         o[j] = cb;
                         o[j + 1] = cb;
                         fma_x2(o[j], o[j + 1], ca, ca, xf[j], xf[j + 1]);

@@ -454,6 +454,13 @@ constexpr Bucket kTwoByteBackward[] = {
     {263, 0}, {519, 1}, {1031, 2}, {2055, 39}, {4103, 6}, {8199, 7},
     {16391, 10}, {32775, 14}, {65543, 17}, {TILE_MAX_WIDTH, 19},
 };
+// Softmax backward (one reduction, no gamma) differs at 32768 columns, where
+// plan 15 (a cluster of two 16-warp CTAs, K = 4) ran 11 % faster than plan 14
+// (one 16-warp CTA, K = 8).
+constexpr Bucket kTwoByteSoftmaxBackward[] = {
+    {263, 0}, {519, 1}, {1031, 2}, {2055, 39}, {4103, 6}, {8199, 7},
+    {16391, 10}, {32775, 15}, {65543, 17}, {TILE_MAX_WIDTH, 19},
+};
 
 bool built_backward(const PlanDesc &p, int dtype = TILE_DTYPE_F32) {
     const bool raw = two_byte(dtype) && p.V == 4;     // raw-word stripes (bwd_kernel.cuh)
@@ -501,8 +508,9 @@ int run_backward(int op, int plan_id, int dtype, const void *x, const float *gam
                       ((a ^ reinterpret_cast<uintptr_t>(dx)) & 15u) == 0;
     if (plan_id < 0)
         plan_id = !vec4 ? pick(kVec1, width)
-                        : two_byte(dtype) ? pick(kTwoByteBackward, width)
-                                          : pick(kVec4Backward, width);
+                        : !two_byte(dtype)      ? pick(kVec4Backward, width)
+                        : op == TILE_OP_SOFTMAX ? pick(kTwoByteSoftmaxBackward, width)
+                                                : pick(kTwoByteBackward, width);
     if (plan_id < 0) return TILE_ERR_SHAPE;
     if (kPlans[plan_id].V == 4 && !vec4) return TILE_ERR_PLAN;
     if (grid_of(kPlans[plan_id], rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
