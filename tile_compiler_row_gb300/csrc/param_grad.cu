@@ -42,6 +42,29 @@ __device__ __forceinline__ float widen_half(unsigned int w, int hi) {
     }
 }
 
+// Element `hi` of a 32-bit word of two 2-byte values plus c, one
+// mixed-precision add (add.rn.f32.bf16 / .f16): the 2-byte value enters
+// exactly, so this is round(x + c) as after an explicit widening.
+#define TILE_ADD_HALF(TY, HALF)                                                          \
+    "{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32." TY " %0, " HALF ", %2;\n\t}"
+template <class T>
+__device__ __forceinline__ float add_half(unsigned int w, int hi, float c) {
+    float r;
+    if constexpr (std::is_same<T, __half>::value) {
+        if (hi)
+            asm(TILE_ADD_HALF("f16", "h") : "=f"(r) : "r"(w), "f"(c));
+        else
+            asm(TILE_ADD_HALF("f16", "l") : "=f"(r) : "r"(w), "f"(c));
+    } else {
+        if (hi)
+            asm(TILE_ADD_HALF("bf16", "h") : "=f"(r) : "r"(w), "f"(c));
+        else
+            asm(TILE_ADD_HALF("bf16", "l") : "=f"(r) : "r"(w), "f"(c));
+    }
+    return r;
+}
+#undef TILE_ADD_HALF
+
 // Columns a stage-1 thread owns: four (one 16-byte FP32 or 8-byte BF16 /
 // FP16 load per row).
 constexpr int kCols = 4;
@@ -158,9 +181,9 @@ __device__ __forceinline__ void rows_raw(const T *__restrict__ x, const T *__res
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     const int q = 4 * g + q4;
-                    const float xq = widen_half<T>(xw[q][j >> 1], j & 1);
+                    const float xc = add_half<T>(xw[q][j >> 1], j & 1, -mu[q]);   // x - mu
                     d[q4] = widen_half<T>(dw[q][j >> 1], j & 1);
-                    t[q4] = d[q4] * ((xq - mu[q]) * rs[q]);
+                    t[q4] = d[q4] * (xc * rs[q]);
                 }
                 comp_add(sg[j], cg[j], tree4(t[0], t[1], t[2], t[3]));
                 comp_add(sb[j], cb[j], tree4(d[0], d[1], d[2], d[3]));
