@@ -337,6 +337,8 @@ def run_ours(args, dist):
                      "algorithmic_bytes_per_launch": nbytes,
                      "kernel_ms_mean": round(kernel_ms, 6),
                      "kernel_ms_median": round(statistics.median(per), 6),
+                     "kernel_ms_min": round(min(per), 6),
+                     "kernel_ms_p90": round(sorted(per)[(9 * len(per)) // 10], 6),
                      "frac_of_8TBps_nominal": round(achieved / 8000.0, 4)},
         "clocks": clocks,
         "gpu_launches": args.steps,
