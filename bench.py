@@ -403,12 +403,12 @@ def run_ours(args, dist):
             e2e_step()
         torch.cuda.synchronize()
         n_e2e = max(3, min(args.steps, 10))
-        # Five rounds of n_e2e steps (about 0.1 s each); the median round is
+        # Nine rounds of n_e2e steps (about 0.1 s each); the median round is
         # reported (the host side of the link is shared with other jobs on the
-        # machine, and an interruption of a few tens of ms would otherwise
-        # decide the number; one earlier run saw a first round 2.5x slow).
+        # machine: runs have seen two and three of five rounds at about twice
+        # the time of the others, so five rounds were not enough).
         rounds = []
-        for _ in range(5):
+        for _ in range(9):
             dist.barrier()
             _, ms = time_calls(e2e_step, n_e2e, stream)
             rounds.append(dist.max(ms))
