@@ -225,3 +225,28 @@ def test_bf16_constant_rows_normalise_to_zero(op, rows, width):
     torch.cuda.synchronize()
     got = y.float().cpu().numpy()
     assert np.all(np.abs(got) <= ATOL), f"{op} {rows}x{width}: max |y| {np.abs(got).max():.3e}"
+
+
+def test_bf16_residual_layernorm_65536x4096_sampled_rows():
+    """The BF16 residual LayerNorm launch that bench.py times (65536 x 4096,
+    512 MiB per tensor, the shared-memory-staged plan): 64 sampled rows,
+    including the first, the last and the ends of the persistent grid's
+    first pass, against the oracle; every output finite."""
+    rows, width = 65536, 4096
+    x, _ = _bf16_rows(5, rows, width)
+    r, _ = _bf16_rows(5, rows, width, "r")
+    info = tile.tile_describe_plan_ex("residual_layernorm", "bf16", rows, width)
+    assert info["path"] == 2, info
+    tx, tr = x.cuda(), r.cuda()
+    y = torch.empty_like(tx)
+    tile.tile_residual_layernorm_bf16(tx, tr, y, EPS)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    pick = set(rng.choice(rows, size=56, replace=False).tolist())
+    pick |= {0, 1, 607, 608, 32767, 32768, rows - 2, rows - 1}
+    pick = sorted(pick)
+    xs, rs = x[pick].float().numpy(), r[pick].float().numpy()
+    ref = oracle.get().residual_layernorm(xs, rs, ref_eps())
+    check_bf16(y[pick].cpu(), ref, what="bf16 residual_layernorm 65536x4096 sampled rows")
+    assert bool(torch.isfinite(y.float()).all())
+    del tx, tr, y
