@@ -354,6 +354,18 @@ __device__ __forceinline__ void acc_raw8(const unsigned int (&w)[4], float (&s)[
     }
 }
 
+// Eight consecutive FP32 values from a 32-byte aligned address in one
+// 256-bit load (sm_100 and later): a warp's loads then cover one contiguous
+// kilobyte, where two 16-byte loads per thread (32 bytes apart between
+// threads) each span a kilobyte for half of it and double the L1 traffic.
+// Volatile, so that no phase keeps another phase's values live.
+__device__ __forceinline__ void ldg_v8(const float *p, float (&v)[8]) {
+    asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                   "=f"(v[6]), "=f"(v[7])
+                 : "l"(p));
+}
+
 // Mixed-precision fused multiply-add on two 2-byte operands and an FP32
 // addend (fma.rn.f32.bf16 / .f16): the product of two BF16 or FP16 values is
 // exact in FP32, so each step rounds once.
@@ -381,7 +393,7 @@ __device__ __forceinline__ void dot_raw8(const unsigned int (&a)[4], const unsig
 // many bytes in flight as the FP32 kernel.  gamma is applied where g is used,
 // the output map is d rstd-form dx = rstd g + ca d + cb computed per vector
 // just before its store.
-template <int OP, class T, int S, int P, int K, int C>
+template <int OP, class T, int S, int P, int K, int C, bool G>
 __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a) {
     static_assert(sizeof(T) == 2, "2-byte element types");
     static_assert(C == 1 || P == 1, "a cluster row has one program per CTA");
@@ -453,8 +465,10 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
     }
 
     const float n = static_cast<float>(width);
-    const float *gam = (OP == BWD_SOFTMAX) ? nullptr : a.gamma;
+    // G = false: no gamma (compiled out); G = true: gamma if a.gamma is set
+    const float *gam = (OP != BWD_SOFTMAX && G) ? a.gamma : nullptr;
     const bool gvec = gam != nullptr && (reinterpret_cast<uintptr_t>(gam + h) & 15) == 0;
+    const bool g32 = gam != nullptr && (reinterpret_cast<uintptr_t>(gam + h) & 31) == 0;
     if (gam != nullptr) {
         if (has_h) hu *= __ldg(gam + worker);
         if (has_t) tu *= __ldg(gam + te);
@@ -464,7 +478,12 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
         widen_raw8<T>(dw[k], gf);
         if (gam != nullptr) {
             const float *gp = gam + h + EV * i;
-            if (gvec) {
+            if (g32) {
+                float gv[EV];
+                ldg_v8(gp, gv);
+#pragma unroll
+                for (int j = 0; j < EV; ++j) gf[j] *= gv[j];
+            } else if (gvec) {
 #pragma unroll
                 for (int q = 0; q < EV / 4; ++q) {
                     const float4 g4 = __ldg(reinterpret_cast<const float4 *>(gp) + q);
