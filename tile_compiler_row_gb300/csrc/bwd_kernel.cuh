@@ -354,18 +354,6 @@ __device__ __forceinline__ void acc_raw8(const unsigned int (&w)[4], float (&s)[
     }
 }
 
-// Eight consecutive FP32 values from a 32-byte aligned address in one
-// 256-bit load (sm_100 and later): a warp's loads then cover one contiguous
-// kilobyte, where two 16-byte loads per thread (32 bytes apart between
-// threads) each span a kilobyte for half of it and double the L1 traffic.
-// Volatile, so that no phase keeps another phase's values live.
-__device__ __forceinline__ void ldg_v8(const float *p, float (&v)[8]) {
-    asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
-                   "=f"(v[6]), "=f"(v[7])
-                 : "l"(p));
-}
-
 // Mixed-precision fused multiply-add on two 2-byte operands and an FP32
 // addend (fma.rn.f32.bf16 / .f16): the product of two BF16 or FP16 values is
 // exact in FP32, so each step rounds once.

@@ -201,6 +201,18 @@ __device__ __forceinline__ void add_raw_vec(float (&v)[16 / sizeof(T)], uint4 t)
     }
 }
 
+// Eight consecutive FP32 values from a 32-byte aligned address in one
+// 256-bit load (sm_100 and later): a warp's loads then cover one contiguous
+// kilobyte, where two 16-byte loads per thread (32 bytes apart between
+// threads) each span a kilobyte for half of it and double the L1 traffic.
+// Volatile, so that no phase keeps another phase's values live.
+__device__ __forceinline__ void ldg_v8(const float *p, float (&v)[8]) {
+    asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                   "=f"(v[6]), "=f"(v[7])
+                 : "l"(p));
+}
+
 // ---------------------------------------------------------------------------
 // Lane-wise arithmetic on a vector of EV FP32 lanes.  With PK (BF16 rows,
 // whose kernels are bound by instruction issue) two lanes go through one
@@ -477,8 +489,19 @@ __device__ __forceinline__ void row_allreduce_comp(float &s, float &c, float *pa
 // the kernel
 // ---------------------------------------------------------------------------
 
+// Resident CTAs the register budget must allow: 2-byte rows of 16-byte
+// vectors with a stripe of at most 32 floats are held to 64 registers a
+// thread (the count these plans reach without gamma's 256-bit loads; at 70
+// registers BF16 LayerNorm lost a CTA per SM and ran 4 % slower at 4096
+// columns); other plans leave the count to the compiler.
+template <class T, int V, int S, int P, int K>
+constexpr int row_min_blocks() {
+    return (sizeof(T) == 2 && V == 4 && K * 8 <= 32) ? 32 / (S * P) : 0;
+}
+
 template <int OP, class T, int V, int S, int P, int K, int C>
-__global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
+__global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
+    row_kernel(const RowArgs a) {
     static_assert(V == 1 || V == 4, "V is 1 (scalar) or 4 (16-byte vectors)");
     // elements per access: one 16-byte vector (4 FP32 or 8 BF16), or one
     constexpr int EV = (V == 4) ? Elem<T>::kVec : 1;
@@ -734,15 +757,20 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
     // Optional per-column scale and shift (affine LayerNorm, weighted
     // RMSNorm): y = y * gamma[col] + beta[col], loaded through the read-only
     // cache (every row reuses them).  float4 loads when gamma/beta share the
-    // row's 16-byte phase, scalar loads otherwise.
+    // row's 16-byte phase (one 256-bit load per 8-column vector of a 2-byte
+    // row when they are 32-byte aligned), scalar loads otherwise.
     if constexpr (OP == OP_RESLN || OP == OP_LN || OP == OP_RMS) {
         if (a.gamma != nullptr) {
             const float *g = a.gamma;
             const float *b = a.beta;
-            bool gvec = false;
-            if constexpr (V == 4)
+            bool gvec = false, g32 = false;
+            if constexpr (V == 4) {
                 gvec = ((reinterpret_cast<uintptr_t>(g + h) & 15) == 0) &&
                        (b == nullptr || (reinterpret_cast<uintptr_t>(b + h) & 15) == 0);
+                if constexpr (EV == 8)       // 2-byte rows: one 256-bit load each
+                    g32 = ((reinterpret_cast<uintptr_t>(g + h) & 31) == 0) &&
+                          (b == nullptr || (reinterpret_cast<uintptr_t>(b + h) & 31) == 0);
+            }
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const int i = k * (C * W) + gw;
@@ -750,8 +778,20 @@ __global__ void __launch_bounds__(32 * S * P) row_kernel(const RowArgs a) {
                     const int col = (V == 4) ? h + EV * i : i;
                     float gg[EV], bb[EV];
                     bool loaded = false;
+                    if constexpr (V == 4 && EV == 8) {
+                        if (g32) {
+                            ldg_v8(g + col, gg);
+                            if (b != nullptr) {
+                                ldg_v8(b + col, bb);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < EV; ++j) bb[j] = 0.0f;
+                            }
+                            loaded = true;
+                        }
+                    }
                     if constexpr (V == 4) {
-                        if (gvec) {
+                        if (!loaded && gvec) {
 #pragma unroll
                             for (int q = 0; q < EV / 4; ++q) {
                                 const float4 g4 =

@@ -86,6 +86,8 @@ def main(argv=None):
         "layernorm_bf16": (lambda: tile.tile_layernorm_bf16(xb, yb), 4),
         "rmsnorm_bf16": (lambda: tile.tile_rmsnorm_bf16(xb, yb), 4),
         "softmax_bf16": (lambda: tile.tile_softmax_bf16(xb, yb), 4),
+        "layernorm_affine_bf16": (lambda: tile.tile_layernorm_affine_bf16(xb, None, g, b, yb), 4),
+        "rmsnorm_weighted_bf16": (lambda: tile.tile_rmsnorm_weighted_bf16(xb, g, yb), 4),
         "residual_layernorm_f16": (lambda: tile.tile_residual_layernorm_f16(xh, rh, yh), 6),
         "layernorm_f16": (lambda: tile.tile_layernorm_f16(xh, yh), 4),
         "rmsnorm_f16": (lambda: tile.tile_rmsnorm_f16(xh, yh), 4),
