@@ -437,7 +437,9 @@ int tile_describe_plan(int op, int rows, int width, tile_plan_t *plan);
  * an unknown one.  For BF16 and FP16 the answer may be a shared-memory-staged plan
  * (path TILE_PATH_STAGED), which a call takes only when every pointer is
  * 16-byte aligned and width is a multiple of 8 (whole 16-byte rows); other
- * calls of that shape take the register plan of the same width. */
+ * calls of that shape take the register plan of the same width.  For
+ * TILE_OP_LAYERNORM_AFFINE the answer is that of a call without a residual
+ * (2-byte calls with a residual take a staged plan at 8200-16384 columns). */
 int tile_describe_plan_ex(int op, int dtype, int rows, int width, tile_plan_t *plan);
 
 /* Number of plans built into the library, and plan `id` of that table

@@ -250,3 +250,24 @@ def test_bf16_residual_layernorm_65536x4096_sampled_rows():
     check_bf16(y[pick].cpu(), ref, what="bf16 residual_layernorm 65536x4096 sampled rows")
     assert bool(torch.isfinite(y.float()).all())
     del tx, tr, y
+
+
+@pytest.mark.parametrize("rows,width", [(400, 12288), (512, 16384)])
+def test_bf16_residual_affine_and_weighted_on_staged_plans(rows, width):
+    """2-byte affine LayerNorm with a residual takes the shared-memory-staged
+    plan at these widths (weighted RMSNorm at 12288), gamma and beta applied
+    in the staged kernel: both against the oracle."""
+    x, xf = _bf16_rows(3, rows, width)
+    r, rf = _bf16_rows(3, rows, width, "r")
+    g = synth.uniform_pm1(3001, width) * np.float32(2.0)
+    b = synth.uniform_pm1(3002, width)
+    tg, tb = torch.from_numpy(g).cuda(), torch.from_numpy(b).cuda()
+    out = torch.empty(rows, width, dtype=torch.bfloat16, device="cuda")
+    tile.tile_layernorm_affine_bf16(x.cuda(), r.cuda(), tg, tb, out, EPS)
+    ref = oracle.get().layernorm_affine(xf, g, b, r=rf, eps=ref_eps())
+    check_bf16(out, ref, atol=1e-5, what=f"bf16 residual affine {rows}x{width}")
+    tile.tile_rmsnorm_weighted_bf16(x.cuda(), tg, out, EPS)
+    ref = oracle.get().rmsnorm_weighted(xf, g, eps=ref_eps())
+    check_bf16(out, ref, what=f"bf16 weighted {rows}x{width}")
+    staged = tile.tile_describe_plan_ex("rmsnorm_weighted", "bf16", rows, width)["path"] == 2
+    assert staged == (width == 12288)
