@@ -771,15 +771,41 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
                     g32 = ((reinterpret_cast<uintptr_t>(g + h) & 31) == 0) &&
                           (b == nullptr || (reinterpret_cast<uintptr_t>(b + h) & 31) == 0);
             }
+            if constexpr (EV == 8) {
+                // one loop per load form, chosen once per launch
+                auto apply = [&](auto load) {
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
-                const int i = k * (C * W) + gw;
-                if (i < nb) {
-                    const int col = (V == 4) ? h + EV * i : i;
-                    float gg[EV], bb[EV];
-                    bool loaded = false;
-                    if constexpr (V == 4 && EV == 8) {
-                        if (g32) {
+                    for (int k = 0; k < K; ++k) {
+                        const int i = k * (C * W) + gw;
+                        if (i < nb) {
+                            float gg[EV], bb[EV];
+                            load((V == 4) ? h + EV * i : i, gg, bb);
+                            vfma<PK, EV>(v[k], gg, bb);
+                        }
+                    }
+                };
+                auto scalar = [&](int col, float (&gg)[EV], float (&bb)[EV]) {
+#pragma unroll
+                    for (int j = 0; j < EV; ++j) {
+                        gg[j] = __ldg(g + col + j);
+                        bb[j] = b != nullptr ? __ldg(b + col + j) : 0.0f;
+                    }
+                };
+                if constexpr (V == 4) {
+                    auto quad = [&](int col, float (&gg)[EV], float (&bb)[EV]) {
+#pragma unroll
+                        for (int q = 0; q < EV / 4; ++q) {
+                            const float4 g4 = __ldg(reinterpret_cast<const float4 *>(g + col) + q);
+                            gg[4 * q] = g4.x; gg[4 * q + 1] = g4.y;
+                            gg[4 * q + 2] = g4.z; gg[4 * q + 3] = g4.w;
+                            float4 b4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                            if (b != nullptr) b4 = __ldg(reinterpret_cast<const float4 *>(b + col) + q);
+                            bb[4 * q] = b4.x; bb[4 * q + 1] = b4.y;
+                            bb[4 * q + 2] = b4.z; bb[4 * q + 3] = b4.w;
+                        }
+                    };
+                    if constexpr (EV == 8) {
+                        auto wide = [&](int col, float (&gg)[EV], float (&bb)[EV]) {
                             ldg_v8(g + col, gg);
                             if (b != nullptr) {
                                 ldg_v8(b + col, bb);
@@ -787,34 +813,63 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
 #pragma unroll
                                 for (int j = 0; j < EV; ++j) bb[j] = 0.0f;
                             }
-                            loaded = true;
-                        }
+                        };
+                        if (g32) apply(wide);
+                        else if (gvec) apply(quad);
+                        else apply(scalar);
+                    } else {
+                        if (gvec) apply(quad);
+                        else apply(scalar);
                     }
-                    if constexpr (V == 4) {
-                        if (!loaded && gvec) {
+                } else {
+                    apply(scalar);
+                }
+            } else {
 #pragma unroll
-                            for (int q = 0; q < EV / 4; ++q) {
-                                const float4 g4 =
-                                    __ldg(reinterpret_cast<const float4 *>(g + col) + q);
-                                gg[4 * q] = g4.x; gg[4 * q + 1] = g4.y;
-                                gg[4 * q + 2] = g4.z; gg[4 * q + 3] = g4.w;
-                                float4 b4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                                if (b != nullptr)
-                                    b4 = __ldg(reinterpret_cast<const float4 *>(b + col) + q);
-                                bb[4 * q] = b4.x; bb[4 * q + 1] = b4.y;
-                                bb[4 * q + 2] = b4.z; bb[4 * q + 3] = b4.w;
+                for (int k = 0; k < K; ++k) {
+                    const int i = k * (C * W) + gw;
+                    if (i < nb) {
+                        const int col = (V == 4) ? h + EV * i : i;
+                        float gg[EV], bb[EV];
+                        bool loaded = false;
+                        if constexpr (V == 4 && EV == 8) {
+                            if (g32) {
+                                ldg_v8(g + col, gg);
+                                if (b != nullptr) {
+                                    ldg_v8(b + col, bb);
+                                } else {
+#pragma unroll
+                                    for (int j = 0; j < EV; ++j) bb[j] = 0.0f;
+                                }
+                                loaded = true;
                             }
-                            loaded = true;
                         }
-                    }
-                    if (!loaded) {
+                        if constexpr (V == 4) {
+                            if (!loaded && gvec) {
 #pragma unroll
-                        for (int j = 0; j < EV; ++j) {
-                            gg[j] = __ldg(g + col + j);
-                            bb[j] = b != nullptr ? __ldg(b + col + j) : 0.0f;
+                                for (int q = 0; q < EV / 4; ++q) {
+                                    const float4 g4 =
+                                        __ldg(reinterpret_cast<const float4 *>(g + col) + q);
+                                    gg[4 * q] = g4.x; gg[4 * q + 1] = g4.y;
+                                    gg[4 * q + 2] = g4.z; gg[4 * q + 3] = g4.w;
+                                    float4 b4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                                    if (b != nullptr)
+                                        b4 = __ldg(reinterpret_cast<const float4 *>(b + col) + q);
+                                    bb[4 * q] = b4.x; bb[4 * q + 1] = b4.y;
+                                    bb[4 * q + 2] = b4.z; bb[4 * q + 3] = b4.w;
+                                }
+                                loaded = true;
+                            }
                         }
+                        if (!loaded) {
+#pragma unroll
+                            for (int j = 0; j < EV; ++j) {
+                                gg[j] = __ldg(g + col + j);
+                                bb[j] = b != nullptr ? __ldg(b + col + j) : 0.0f;
+                            }
+                        }
+                        vfma<PK, EV>(v[k], gg, bb);
                     }
-                    vfma<PK, EV>(v[k], gg, bb);
                 }
             }
             if constexpr (V == 4) {
