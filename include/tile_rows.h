@@ -379,8 +379,10 @@ int tile_run_host_f32(int op, const float *h_in, const float *h_residual, float 
  * chunk (0 for invalid arguments).  Host only. */
 size_t tile_host_workspace_bytes(int op, int width, int chunk_rows);
 
-/* The schedule tile_run_host_f32 uses for these arguments: rows per chunk
- * (the last chunk may be shorter) and the number of workspace buffers in the
+/* The schedule tile_run_host_f32 uses for these arguments: rows per full
+ * chunk (the first and the last chunk are a quarter of that when a quarter
+ * still holds 1 MiB of an input and there are more than two chunks; the
+ * last may otherwise be shorter) and the number of workspace buffers in the
  * ring.  `direct_output` != 0 describes a call whose h_out is pinned and
  * device-addressable (results stored straight into it), 0 one whose results
  * are copied out.  Host only: no CUDA call.  Returns TILE_OK, TILE_ERR_OP,

@@ -11,7 +11,9 @@
 // are enqueued in order), so chunk c+slots reuses slot b only once chunk c's
 // kernel has consumed the inputs and chunk c's output has left the device.
 // More than two slots let the copies in run ahead of a kernel that is slow
-// to finish (one that writes its results over the host link).
+// to finish (one that writes its results over the host link).  Every chunk
+// runs the plan a device call on the whole matrix would select, so the
+// results are bitwise those of that call whatever the chunking.
 //
 // When the output buffer is pinned host memory the device can address (over
 // NVLink-C2C on Grace systems), the kernels store each chunk's results
@@ -160,7 +162,37 @@ int run_host(int op, const float *h_in, const float *h_res, float *h_out, int ro
     schedule(op, rows, width, work_bytes, out_dev != nullptr, &chunk, &slots);
     const int per_slot = inputs_of(op) + (out_dev != nullptr ? 0 : 1);
     const size_t buf = round_up(static_cast<size_t>(chunk) * width * sizeof(float));
-    const long long nchunks = (rows + chunk - 1) / chunk;
+    // The first and the last chunk are a quarter of a full one when that
+    // still holds kMinChunkBytes of an input and there are more than two
+    // chunks: the pipeline fills with one chunk's copy in and drains with
+    // one chunk's kernel, so short ends shorten both.
+    const long long ramp_min = static_cast<long long>(
+        (kMinChunkBytes + static_cast<size_t>(width) * sizeof(float) - 1) /
+        (static_cast<size_t>(width) * sizeof(float)));
+    const long long ramp = (chunk / 4 >= ramp_min && rows > 2 * chunk) ? chunk / 4 : 0;
+    const long long body = rows - 2 * ramp;
+    const long long nchunks = ramp > 0 ? (body + chunk - 1) / chunk + 2 : (rows + chunk - 1) / chunk;
+    // rows [*r0, *r0 + *n) of chunk c
+    auto range = [&](long long c, long long *r0, int *n) {
+        long long a, e;
+        if (ramp == 0) {
+            a = c * chunk;
+            e = a + chunk;
+        } else if (c == 0) {
+            a = 0;
+            e = ramp;
+        } else if (c == nchunks - 1) {
+            a = rows - ramp;
+            e = rows;
+        } else {
+            a = ramp + (c - 1) * chunk;
+            e = a + chunk;
+            if (e > rows - ramp) e = rows - ramp;
+        }
+        if (e > rows) e = rows;
+        *r0 = a;
+        *n = static_cast<int>(e - a);
+    };
     char *base = static_cast<char *>(d_work);
     float *dx[kMaxSlots], *dr[kMaxSlots], *dy[kMaxSlots];
     for (int b = 0; b < slots; ++b) {
@@ -187,8 +219,9 @@ int run_host(int op, const float *h_in, const float *h_res, float *h_out, int ro
 
     for (long long c = 0; c < nchunks; ++c) {
         const int b = static_cast<int>(c % slots);
-        const long long r0 = c * chunk;
-        const int n = static_cast<int>(rows - r0 < chunk ? rows - r0 : chunk);
+        long long r0 = 0;
+        int n = 0;
+        range(c, &r0, &n);
         const size_t off = static_cast<size_t>(r0) * width;
         const size_t bytes = static_cast<size_t>(n) * width * sizeof(float);
         if (c >= slots) TILE_TRY(cudaStreamWaitEvent(q.h2d, q.compute_ev[b], 0));
@@ -199,13 +232,14 @@ int run_host(int op, const float *h_in, const float *h_res, float *h_out, int ro
 
         TILE_TRY(cudaStreamWaitEvent(stream, q.h2d_ev[b], 0));
         if (out_dev != nullptr) {
-            const int st = run_selected(op, dx[b], dr[b], out_dev + off, n, width, eps, stream);
+            const int st =
+                run_selected(op, dx[b], dr[b], out_dev + off, n, width, eps, stream, rows);
             if (st != TILE_OK) return st;
             TILE_TRY(cudaEventRecord(q.compute_ev[b], stream));
             continue;
         }
         if (c >= slots) TILE_TRY(cudaStreamWaitEvent(stream, q.d2h_ev[b], 0));
-        const int st = run_selected(op, dx[b], dr[b], dy[b], n, width, eps, stream);
+        const int st = run_selected(op, dx[b], dr[b], dy[b], n, width, eps, stream, rows);
         if (st != TILE_OK) return st;
         TILE_TRY(cudaEventRecord(q.compute_ev[b], stream));
 

@@ -119,9 +119,12 @@ int run_pairs(int kind, const float *in, float *value, float *derivative, long l
               cudaStream_t stream);
 
 // Check arguments, pick a plan and launch `op` on device buffers (the body of
-// the four compute entry points).  Returns a TILE_* status.
+// the four compute entry points).  select_rows > 0 picks the plan as for a
+// call of that many rows (a chunk of a larger matrix takes the whole
+// matrix's plan, so its results are bitwise those of a single call).
+// Returns a TILE_* status.
 int run_selected(int op, const float *in, const float *res, float *out, int rows, int width,
-                 float eps, cudaStream_t stream);
+                 float eps, cudaStream_t stream, long long select_rows = 0);
 
 // The pipeline of tile_run_host_f32 over a given device workspace.
 int run_host(int op, const float *h_in, const float *h_res, float *h_out, int rows, int width,

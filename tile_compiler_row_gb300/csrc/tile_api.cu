@@ -417,12 +417,15 @@ int launch(const Call &c, int plan_id, cudaStream_t stream) {
     return TILE_OK;
 }
 
-int run_call(const Call &c, cudaStream_t stream) {
+// select_rows > 0: choose the plan as for a call of that many rows (a chunk
+// of a larger matrix takes the whole matrix's plan, so its results are
+// bitwise those of one call on the whole matrix).
+int run_call(const Call &c, cudaStream_t stream, long long select_rows = 0) {
     bool noop = false;
     const int st = validate(c, &noop);
     if (st != TILE_OK || noop) return st;
-    const int plan = select_plan(c.op, c.rows, c.width, coaligned16(c), c.dtype, staged_ok(c),
-                                 c.res != nullptr);
+    const int plan = select_plan(c.op, select_rows > 0 ? select_rows : c.rows, c.width,
+                                 coaligned16(c), c.dtype, staged_ok(c), c.res != nullptr);
     if (plan < 0) return TILE_ERR_SHAPE;
     return launch(c, plan, stream);
 }
@@ -600,9 +603,9 @@ void set_last_cuda_error(int err) { t_last_cuda_error = err; }
 int last_cuda_error() { return t_last_cuda_error; }
 
 int run_selected(int op, const float *in, const float *res, float *out, int rows, int width,
-                 float eps, cudaStream_t stream) {
+                 float eps, cudaStream_t stream, long long select_rows) {
     return run_call(make_call(op, args_of(in, res, nullptr, nullptr, out, nullptr, rows, width, eps)),
-                    stream);
+                    stream, select_rows);
 }
 
 int run_pairs(int kind, const float *in, float *value, float *derivative, long long n,
