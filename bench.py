@@ -418,13 +418,15 @@ def run_ours(args, dist):
                        "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": elems * 4,
                        "steps": n_e2e, "ms_per_step": round(e2e_ms / n_e2e, 4),
                        "rounds_ms_per_step": [round(r / n_e2e, 4) for r in rounds],
-                       "path": f"tile_run_host_f32: pinned host buffers, {chunk}-row chunks "
-                               f"in a ring of {slots} device slots, copies in overlapped with "
-                               "kernels that store straight into the pinned output"}
+                       "path": "tile_run_host_f32 on pinned, device-addressable host "
+                               "buffers: one kernel reads x and r and writes y over the host "
+                               "link (no staging copies; pageable buffers would take the "
+                               f"copy pipeline of {chunk}-row chunks in {slots} slots)"}
         ref = torch.empty_like(x)
         call_op(op, ref, args.plan)
         torch.cuda.synchronize()
-        # rows from every pipeline chunk (both ends of each), bit for bit
+        # rows spread over the matrix (both ends of every pipeline-sized
+        # chunk), bit for bit
         pick = sorted({i for c in range(0, rows, chunk) for i in (c, min(rows, c + chunk) - 1)}
                       | {rows // 2 + 1})
         idx = torch.tensor(pick)

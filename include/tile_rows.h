@@ -359,14 +359,17 @@ int tile_gelu_tanh_pair_f32(const float *in, float *value, float *derivative, lo
  * (cudaHostAlloc / cudaHostRegister) for the copies to overlap; pageable
  * memory gives the same results more slowly.  When h_out is pinned the
  * kernels store the results straight into it through its device address
- * (NVLink-C2C on Grace systems) and no device->host copies are made.  Ownership: the caller owns all
+ * (NVLink-C2C on Grace systems) and no device->host copies are made.  When
+ * h_in, h_residual and h_out are all pinned and device-addressable, there is
+ * no pipeline: one launch of the selected kernel reads and writes the host
+ * buffers directly (d_work is then not touched).  Ownership: the caller owns all
  * buffers and must keep them alive and untouched until `stream` has passed
  * this call (the call returns once everything is enqueued; `stream` is
- * ordered after the last copy).  Results meet the same tolerance as the
- * device entry points, and are bitwise equal to them when width is a
- * multiple of 4 and the chunk and the full matrix get the same plan (chunks
- * start 256-byte aligned in the workspace, so row start phases can differ
- * from the full matrix otherwise).  `h_residual` is read only by
+ * ordered after the last copy or the kernel).  Results meet the same tolerance
+ * as the device entry points, and are bitwise equal to those of a device
+ * call on the whole matrix when width is a multiple of 4: every chunk runs
+ * the whole matrix's plan (chunks start 256-byte aligned in the workspace,
+ * so row start phases can differ from the full matrix otherwise).  `h_residual` is read only by
  * TILE_OP_RESIDUAL_LAYERNORM.  Errors: as the compute entry points, plus
  * TILE_ERR_NULL for a NULL d_work, TILE_ERR_ALIGN for a misaligned d_work and
  * TILE_ERR_WORKSPACE when not even one row fits twice.  Calls from several
@@ -406,7 +409,8 @@ int tile_host_schedule(int op, int rows, int width, size_t work_bytes, int direc
  * device allocation (which can synchronise the device) is not allowed.  This
  * call allocates nothing: rows are staged through a static device array of
  * TILE_STATIC_STAGING_BYTES inside the library instead of a caller
- * workspace.  Arguments, results, errors and ownership are those of
+ * workspace (pinned, device-addressable buffers are processed in place, as
+ * by tile_run_host_f32).  Arguments, results, errors and ownership are those of
  * tile_run_host_f32 without d_work/work_bytes.
  *
  * Limits: any number of rows (they stream through the area in chunks);

@@ -29,14 +29,18 @@ def _host(a, pinned):
     return t.pin_memory() if pinned else t.clone()
 
 
-def _run_host(op, x, r, chunk_rows, pinned=True, stream=None):
+def _run_host(op, x, r, chunk_rows, pinned=True, stream=None, pinned_out=None):
+    """pinned: inputs (and, unless pinned_out says otherwise, the output) in
+    pinned memory.  All pinned: one kernel on the host buffers; pageable
+    inputs with a pinned output: the copy pipeline with direct output
+    stores; all pageable: the pipeline with copies out."""
     rows, width = x.shape
     ws_bytes = tile.tile_host_workspace_bytes(op, width, chunk_rows)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     hx = _host(x, pinned)
     hr = _host(r, pinned) if r is not None else None
     out = torch.full(x.shape, float("nan"))
-    out = out.pin_memory() if pinned else out
+    out = out.pin_memory() if (pinned if pinned_out is None else pinned_out) else out
     tile.tile_run_host_f32(op, hx, hr, out, ws, EPS, stream)
     (stream or torch.cuda.current_stream()).synchronize()
     return out.numpy().copy()
@@ -54,10 +58,14 @@ def _run_device(op, x, r):
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("rows,width,chunk", [(37, 1537, 1), (37, 1537, 7), (1000, 4096, 125),
                                               (1000, 4096, 300), (5, 131072, 2), (3, 127, 64)])
-def test_host_path_matches_oracle_and_device_path(op, rows, width, chunk):
+@pytest.mark.parametrize("mode", ["in_place", "pipeline"])
+def test_host_path_matches_oracle_and_device_path(op, rows, width, chunk, mode):
+    """in_place: every buffer pinned, one kernel on the host buffers;
+    pipeline: pageable inputs, pinned output (chunked copies in, direct
+    stores out)."""
     x = synth.rows_of(3, rows, width, which="x")
     r = synth.rows_of(3, rows, width, which="r") if op == "residual_layernorm" else None
-    got = _run_host(op, x, r, chunk)
+    got = _run_host(op, x, r, chunk, pinned=mode == "in_place", pinned_out=True)
     compare(got, oracle_of(op, x, r), f"host {op} {rows}x{width} chunk {chunk}")
     # Every chunk runs the whole matrix's plan, so the results are bitwise
     # those of the device call wherever every row start has the same 16-byte
@@ -71,6 +79,7 @@ def test_host_path_matches_oracle_and_device_path(op, rows, width, chunk):
 @pytest.mark.parametrize("rows,width", [(20000, 257), (9001, 1024), (8192, 4096)])
 @pytest.mark.parametrize("pinned", [True, False])
 def test_host_path_ring_of_four_slots(op, rows, width, pinned):
+    # pageable inputs, so the copy pipeline runs; pinned: direct output stores
     """Workspace for the whole matrix: about 16 chunks cycle through a ring
     of four slots (each slot reused four times), with results stored
     directly (pinned) or copied out (pageable); bitwise those of the device
@@ -80,7 +89,7 @@ def test_host_path_ring_of_four_slots(op, rows, width, pinned):
     assert slots == 4 and -(-rows // chunk) >= 12
     x = synth.rows_of(3, rows, width, which="x")
     r = synth.rows_of(3, rows, width, which="r") if op == "residual_layernorm" else None
-    got = _run_host(op, x, r, rows, pinned=pinned)
+    got = _run_host(op, x, r, rows, pinned=False, pinned_out=pinned)
     compare(got, oracle_of(op, x, r), f"ring {op} {rows}x{width} pinned={pinned}")
     # (8192 x 4096: quarter-size first and last chunks of 128 rows)
     if width % 4 == 0:
