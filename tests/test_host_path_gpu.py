@@ -105,9 +105,11 @@ def test_host_path_pageable_memory_and_side_stream(op):
     compare(got, oracle_of(op, x, r), f"pageable {op}")
 
 
-def test_host_path_back_to_back_calls_share_the_workspace():
-    """Two calls in a row on one stream through one workspace: the second
-    must not overwrite the first call's chunks before they are copied out."""
+@pytest.mark.parametrize("pinned_out", [True, False])
+def test_host_path_back_to_back_calls_share_the_workspace(pinned_out):
+    """Two calls in a row on one stream through one workspace (pageable
+    inputs, so the copy pipeline runs): the second must not overwrite the
+    first call's chunks before they are consumed or copied out."""
     op = "residual_layernorm"
     rows, width = 300, 2048
     x = synth.rows_of(3, rows, width, which="x")
@@ -117,8 +119,9 @@ def test_host_path_back_to_back_calls_share_the_workspace():
                      device="cuda")
     outs = []
     for xi in (x, x2):
-        o = torch.empty(rows, width).pin_memory()
-        tile.tile_run_host_f32(op, _host(xi, True), _host(r, True), o, ws, EPS)
+        o = torch.empty(rows, width)
+        o = o.pin_memory() if pinned_out else o
+        tile.tile_run_host_f32(op, _host(xi, False), _host(r, False), o, ws, EPS)
         outs.append(o)
     torch.cuda.synchronize()
     compare(outs[0].numpy(), oracle_of(op, x, r), "first call")
