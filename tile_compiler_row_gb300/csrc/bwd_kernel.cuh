@@ -375,12 +375,17 @@ __device__ __forceinline__ void dot_raw8(const unsigned int (&a)[4], const unsig
 }
 
 // Backward kernel for 2-byte rows of 16-byte vectors (BF16, FP16): the
-// arithmetic and mapping of row_bwd_kernel, but the two stripes hold the raw
-// 2-byte words (4 per vector of 8) and every phase widens them again, so a
-// register carries 4 bytes of DRAM data instead of 2 and a thread keeps as
-// many bytes in flight as the FP32 kernel.  gamma is applied where g is used,
-// the output map is d rstd-form dx = rstd g + ca d + cb computed per vector
-// just before its store.
+// mapping and reduction order of row_bwd_kernel, but the two stripes hold the
+// raw 2-byte words (4 per vector of 8) and every phase reads them again, so
+// a register carries 4 bytes of DRAM data instead of 2 and a thread keeps as
+// many bytes in flight as the FP32 kernel.  Where a phase needs x - m, a sum
+// of x, or a product of two 2-byte values, mixed-precision adds and FMAs take
+// the raw halves directly (each exact or rounded once, as after a
+// widening); elsewhere the words are widened.  gamma comes in one 256-bit
+// load per vector where g is used, and the output map
+// dx = rstd g + ca d + cb runs on packed f32x2 pairs per vector just before
+// its store.  G: gamma may be present (the host launches G = false for
+// RMSNorm without gamma, whose kernel then has no gamma code).
 template <int OP, class T, int S, int P, int K, int C, bool G>
 __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a) {
     static_assert(sizeof(T) == 2, "2-byte element types");

@@ -9,7 +9,8 @@
 // columns (one aligned load per row when the rows allow it, else scalars)
 // and accumulates compensated (TwoSum) sums over its block's rows: FP32 rows
 // four in flight, each added compensated; 2-byte rows eight in flight as raw
-// words, added as pairwise trees of four.  Block partials go to the caller's workspace [nblk][2][width].
+// words, added as pairwise trees of four.  Block partials go to the caller's
+// workspace [nblk][2][width].
 // Stage 2 sums the nblk partials of each column in a fixed order (eight
 // interleaved warp slices, then the slices in warp order).  The partition
 // depends only on (rows, width) and the device (its SM count and the
