@@ -353,3 +353,45 @@ def test_f16_plans_are_the_bf16_plans(lib):
         a = tile.tile_plan_info_ex(pid, "layernorm", "f16", 4, 1024)
         b = tile.tile_plan_info_ex(pid, "layernorm", "bf16", 4, 1024)
         assert (a is None) == (b is None)
+
+
+@fake_pointers
+def test_backward_entry_points_reject_bad_arguments(lib):
+    """Backward and parameter-gradient calls check their arguments on the
+    host like the forward ones (rows == 0 is a no-op for the input
+    gradients; the parameter gradients then write zeros, so that case is
+    left to the GPU tests)."""
+    X, DY, DX = A, A + 4096, B
+    ln = lib.tile_layernorm_backward_f32        # (in, gamma, dy, dx, stats, rows, width, eps, s)
+    assert ln(None, None, DY, DX, None, 2, 8, 1e-5, None) == NULL
+    assert ln(X, None, None, DX, None, 2, 8, 1e-5, None) == NULL
+    assert ln(X, None, DY, None, None, 2, 8, 1e-5, None) == NULL
+    assert ln(X, None, DY, DX, None, -1, 8, 1e-5, None) == SHAPE
+    assert ln(X, None, DY, DX, None, 2, 0, 1e-5, None) == SHAPE
+    assert ln(X, None, DY, DX, None, 2, 8, -1.0, None) == EPS
+    assert ln(X, None, DY, X + 32, None, 2, 8, 1e-5, None) == ALIAS      # dx overlaps in
+    assert ln(X, None, DY, DX, X + 4, 2, 8, 1e-5, None) == ALIAS         # stats inside in
+    assert ln(X, None, DY, DX + 2, None, 2, 8, 1e-5, None) == ALIGN
+    assert ln(None, None, None, None, None, 0, 8, 1e-5, None) == OK
+    rms = lib.tile_rmsnorm_backward_f32
+    assert rms(X, None, DY, DX, None, 2, 8, float("nan"), None) == EPS
+    assert rms(X, DX, DY, DX, None, 2, 8, 1e-5, None) == ALIAS           # dx overlaps gamma
+    sm = lib.tile_softmax_backward_f32          # (y, dy, dx, rows, width, s)
+    assert sm(X, None, DX, 2, 8, None) == NULL
+    assert sm(X, DY, X, 2, 8, None) == ALIAS
+    assert sm(X, DY, DX, 2, 0, None) == SHAPE
+    bf = lib.tile_layernorm_backward_bf16
+    assert bf(X, None, None, DX, None, 2, 8, 1e-5, None) == NULL
+    assert bf(X, None, DY, DX + 1, None, 2, 8, 1e-5, None) == ALIGN     # 2-byte alignment
+    pg = lib.tile_norm_param_grad_f32           # (in, dy, stats, dg, db, rows, width, ws, bytes, s)
+    need = lib.tile_norm_param_grad_workspace_bytes(2, 8)
+    assert need > 0
+    WS, DG, ST = B + 65536, B + 8192, B + 16384
+    assert pg(X, DY, ST, DG, None, 2, 8, WS, need - 1, None) == WORKSPACE
+    assert pg(X, DY, None, DG, None, 2, 8, WS, need, None) == NULL
+    assert pg(X, DY, ST, None, None, 2, 8, WS, need, None) == NULL
+    assert pg(X, DY, ST, DG, None, -1, 8, WS, need, None) == SHAPE
+    ex = lib.tile_run_backward_plan_ex          # (op, plan, dtype, in, gamma, dy, dx, stats, ...)
+    assert ex(1, 0, 7, X, None, DY, DX, None, 2, 8, 1e-5, None) == -11  # TILE_ERR_DTYPE
+    assert ex(1, 10 ** 6, 0, X, None, DY, DX, None, 2, 8, 1e-5, None) == PLAN
+    assert ex(9, 0, 0, X, None, DY, DX, None, 2, 8, 1e-5, None) == OP
