@@ -107,7 +107,8 @@ def test_softmax_backward(rows, width):
     _check(dx.cpu().numpy(), ref, bound, f"softmax backward {rows}x{width}")
 
 
-@pytest.mark.parametrize("rows,width", [(17, 257), (1024, 4096), (3000, 1537), (64, 65536)])
+@pytest.mark.parametrize("rows,width", [(17, 257), (1024, 4096), (3000, 1537), (64, 65536),
+                                        (1, 1), (3, 131072), (100000, 5)])
 @pytest.mark.parametrize("op", ["layernorm", "rmsnorm"])
 def test_param_grad(op, rows, width):
     x = synth.rows_of(3, rows, width, which="x")

@@ -134,3 +134,29 @@ def test_host_path_workspace_too_small_raises():
     with pytest.raises(tile.TileError) as e:
         tile.tile_run_host_f32("layernorm", x, None, torch.zeros(4, 4096), ws)
     assert e.value.status == -10
+
+
+def _pinned_off(a):
+    """A pinned host view of `a` starting one float into its allocation:
+    device-addressable but not 16-byte aligned."""
+    buf = torch.empty(a.size + 1).pin_memory()
+    v = buf[1:1 + a.size].view(a.shape)
+    v.copy_(torch.from_numpy(np.ascontiguousarray(a)))
+    return v
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("rows,width", [(33, 1029), (1, 4096), (5, 4100)])
+def test_host_path_in_place_on_unaligned_pinned_buffers(op, rows, width):
+    """Pinned buffers that start off the 16-byte phase run in place on the
+    scalar plans; a single row too."""
+    x = synth.rows_of(3, rows, width, which="x")
+    r = synth.rows_of(3, rows, width, which="r") if op == "residual_layernorm" else None
+    hx = _pinned_off(x)
+    hr = _pinned_off(r) if r is not None else None
+    out = _pinned_off(np.full((rows, width), np.nan, np.float32))
+    ws = torch.empty(tile.tile_host_workspace_bytes(op, width, max(1, rows // 2)),
+                     dtype=torch.uint8, device="cuda")
+    tile.tile_run_host_f32(op, hx, hr, out, ws, EPS)
+    torch.cuda.current_stream().synchronize()
+    compare(out.numpy(), oracle_of(op, x, r), f"in place unaligned {op} {rows}x{width}")
