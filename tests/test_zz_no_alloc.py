@@ -11,7 +11,8 @@ Each case calls it twice in a row through the C ABI (the second call is
 enqueued before the first has finished, with different inputs, so stale
 contents of the shared array or an overlap between the calls would show)
 and checks both results against tile_run_host_f32 with a caller workspace,
-within the tolerance of the other parity tests.  This file is collected last
+within the tolerance of the other parity tests: with pageable inputs (the
+rows stage through the array) and with every buffer pinned (in place).  This file is collected last
 and depends on nothing that earlier tests set up.
 """
 
@@ -41,10 +42,11 @@ def _pinned(a):
     return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
 
 
-def _inputs(op, rows, width, scale):
+def _inputs(op, rows, width, scale, pinned=True):
     x = synth.rows_of(3, rows, width, which="x") * np.float32(scale)
     r = synth.rows_of(3, rows, width, which="r") if op == "residual_layernorm" else None
-    return _pinned(x), (_pinned(r) if r is not None else None)
+    host = _pinned if pinned else (lambda a: torch.from_numpy(np.ascontiguousarray(a)).clone())
+    return host(x), (host(r) if r is not None else None)
 
 
 def _with_workspace(op, x, r):
@@ -57,14 +59,24 @@ def _with_workspace(op, x, r):
     return out.numpy().copy()
 
 
+# staged: pageable inputs go through the static array (with the output
+# pinned, stored directly; or pageable, copied out); in_place: every buffer
+# pinned, one kernel on the host buffers and no staging
+MODES = {"staged_direct_out": (False, True), "staged_copy_out": (False, False),
+         "in_place": (True, True)}
+
+
+@pytest.mark.parametrize("mode", list(MODES))
 @pytest.mark.parametrize("op,rows,width", CASES)
-def test_static_staging_matches_workspace_entry_point_on_two_calls(op, rows, width):
+def test_static_staging_matches_workspace_entry_point_on_two_calls(op, rows, width, mode):
     lib = tile.load()
     stream = torch.cuda.current_stream().cuda_stream
-    calls = [_inputs(op, rows, width, 1.0), _inputs(op, rows, width, -2.5)]
+    pin_in, pin_out = MODES[mode]
+    calls = [_inputs(op, rows, width, 1.0, pin_in), _inputs(op, rows, width, -2.5, pin_in)]
     outs = []
     for x, r in calls:                       # two calls in a row, no sync between
-        out = torch.full((rows, width), float("nan")).pin_memory()
+        out = torch.full((rows, width), float("nan"))
+        out = out.pin_memory() if pin_out else out
         st = lib.tile_run_host_static_f32(tile.OPS[op], x.data_ptr(),
                                           r.data_ptr() if r is not None else None,
                                           out.data_ptr(), rows, width, EPS, stream)
