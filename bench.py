@@ -8,8 +8,8 @@ in HBM before the timed region; the 3 GiB working set is far larger than the
 129 MB L2, so no flush is needed between steps.
 
 Printed: one JSON line with the device-timed throughput (algorithmic GB/s),
-the end-to-end throughput through the C ABI with host buffers (copies in the
-timed region), the roofline of the kernel against the measured HBM copy
+the end-to-end throughput through the C ABI with host buffers (the inputs
+cross the host link and the result comes back inside the timed region), the roofline of the kernel against the measured HBM copy
 bandwidth, the SM clocks seen during the run, and the FP64 CPU oracle timed
 on this host as a baseline.
 
@@ -434,9 +434,9 @@ def run_ours(args, dist):
             raise SystemExit("e2e output differs from the device path")
         # The link alone on this machine, for context (these overwrite ref and
         # yp): a plain host->device copy of one pinned input tensor (the
-        # pipeline's floor is its host->device bytes at this rate), the
+        # call's floor is its host->device bytes at this rate), the
         # device->host copy, and kernel stores into the pinned output (the
-        # pipeline's way out).
+        # call's way out).
         for _ in range(2):
             ref.copy_(xp, non_blocking=True)
         _, link_ms = time_calls(lambda: ref.copy_(xp, non_blocking=True), 5, stream)
