@@ -605,7 +605,9 @@ def _host_matrix(t, name):
 
 
 def tile_run_host_f32(op, x, residual, out, workspace, eps=1e-5, stream=None):
-    """``op`` on host tensors through the device ``workspace`` (a CUDA tensor)."""
+    """``op`` on host tensors: in place when every tensor is pinned (one kernel
+    reads and writes them over the host link), otherwise through the device
+    ``workspace`` (a CUDA tensor) in chunks."""
     op = OPS[op] if isinstance(op, str) else op
     px, rows, width = _host_matrix(x, "x")
     po, _, _ = _host_matrix(out, "out")
