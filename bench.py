@@ -43,6 +43,7 @@ FALLBACK_HBM_GBS = 6800.0
 BYTES_PER_ELEM = {"residual_layernorm": 12, "layernorm": 8, "rmsnorm": 8, "softmax": 8}
 EPS = 1e-5
 SEED_CFG = 5
+L2_BYTES = 129 * 10**6      # GB300 L2
 
 
 def parse_args():
@@ -225,6 +226,42 @@ def profile_traffic(op, rows, width, plan_id):
         return None
 
 
+def workload_config(op, rows, width, world):
+    """The ``config`` object of the JSON line: the workload alone, the same
+    in both arms (plan and host-thread details go in their own keys)."""
+    elems = rows * width
+    nin = 2 if op == "residual_layernorm" else 1
+    return {"workload": f"{op.replace('_', ' ')} FP32 {rows}x{width}", "rows": rows,
+            "width": width, "eps": EPS,
+            "l2": (f"inputs larger than L2: {(nin + 1) * elems * 4 / 2**30:.2f} GiB working set, "
+                   "no flush") if (nin + 1) * elems * 4 > L2_BYTES else
+                  f"L2-resident: {(nin + 1) * elems * 4 / 2**20:.1f} MiB working set, no flush",
+            "parallelism": f"replicas x{world}"}
+
+
+def provenance():
+    """What the line was measured on: the git commit when the tree has one,
+    the SHA-256 of the kernel sources and of the loaded library, the GPU."""
+    from tile_compiler_row_gb300 import _build
+    try:
+        head = subprocess.run(["git", "rev-parse", "HEAD"], cwd=ROOT, capture_output=True,
+                              text=True, timeout=10)
+        git = head.stdout.strip() if head.returncode == 0 and head.stdout.strip() else None
+    except (OSError, subprocess.SubprocessError):
+        git = None
+    h = hashlib.sha256()
+    with open(_build.LIBRARY, "rb") as fh:
+        for block in iter(lambda: fh.read(1 << 20), b""):
+            h.update(block)
+    out = {"git": git, "source_sha256": _build.source_hash(), "so_sha256": h.hexdigest()}
+    try:
+        import torch
+        out["gpu_name"] = torch.cuda.get_device_name(torch.cuda.current_device())
+    except Exception:
+        out["gpu_name"] = None
+    return out
+
+
 def job_throughput(world, bytes_per_step, steps, max_ms):
     """Whole-job GB/s: every rank moves ``bytes_per_step`` per step (weak
     scaling), divided by the slowest rank's time."""
@@ -305,6 +342,7 @@ def run_ours(args, dist):
     clocks = sampler.summary(t0, t1)
     if tile.tile_check_device_status() != 0:
         raise SystemExit("device status word set after the timed region")
+    timed_out = y.cpu().numpy() if not args.no_cpu and dist.rank == 0 else None
 
     ms_per_step = total_ms / args.steps
     value = job_throughput(dist.world, nbytes, args.steps, total_ms)
@@ -322,15 +360,10 @@ def run_ours(args, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": f"synthetic: SplitMix64 uniform[-1,1), seeds {synth.x_seed(SEED_CFG)}/"
                 f"{synth.r_seed(SEED_CFG)}",
-        "config": {
-            "workload": f"{op.replace('_', ' ')} FP32 {rows}x{width}",
-            "rows": rows, "width": width, "eps": EPS,
-            "plan": {k: plan[k] for k in ("id", "path", "vec", "warps_per_program",
-                                          "programs_per_cta", "chunks", "cluster", "threads",
-                                          "grid")},
-            "l2": f"inputs larger than L2: {3 * elems * 4 / 2**30:.2f} GiB working set, no flush",
-            "parallelism": f"replicas x{dist.world}",
-        },
+        "config": workload_config(op, rows, width, dist.world),
+        "plan": {k: plan[k] for k in ("id", "path", "vec", "warps_per_program",
+                                      "programs_per_cta", "chunks", "cluster", "threads",
+                                      "grid")},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} HBM copy bandwidth",
@@ -342,7 +375,10 @@ def run_ours(args, dist):
                      "frac_of_8TBps_nominal": round(achieved / 8000.0, 4)},
         "clocks": clocks,
         "gpu_launches": args.steps,
+        "per_call_ms": [round(v, 5) for v in per],
+        "provenance": provenance(),
     }
+
 
     # --- the other two large-shape ops (same inputs; one launch per call) ---
     if not args.no_extra and (rows, width) == (65536, 4096) and args.plan is None:
@@ -381,7 +417,9 @@ def run_ours(args, dist):
             "plan_id": tile.tile_describe_plan_ex("residual_layernorm", "bf16", rows, width)["id"]}
         del xb, rb, yb
         line["other_ops"] = extra
-        line["small_shapes"] = small_shapes(tile)
+        with_cpu = not args.no_cpu and dist.world == 1 and dist.rank == 0
+        line["small_shapes"] = small_shapes(tile, cpu=with_cpu)
+        line["single_call"] = single_call(tile, lib, x, r, y, stream)
 
     # --- end to end through the C ABI with pinned host buffers -------------
     if not args.no_e2e:
@@ -455,9 +493,11 @@ def run_ours(args, dist):
         _, st_ms = time_calls(store_to_host, 5, stream)
         line["e2e"]["kernel_store_to_host_gbs"] = round(elems * 4 * 5 / (st_ms * 1e-3) / 1e9, 1)
 
-    # --- the FP64 CPU oracle on this host (rank 0, N = 1 only) -------------
+    # --- the FP64 CPU oracle on this host (rank 0, N = 1 only); its output
+    # also checks every element of the timed call's output (untimed) --------
     if not args.no_cpu and dist.world == 1 and dist.rank == 0:
-        line["cpu_baseline"] = cpu_baseline(op, x_h, r_h)
+        line["cpu_baseline"], line["parity"] = cpu_baseline(
+            op, x_h, r_h if op == "residual_layernorm" else None, got=timed_out)
 
     dist.close()
     if dist.rank == 0:
@@ -502,20 +542,22 @@ SMALL_SHAPES = (
 )
 
 
-def small_shapes(tile, calls=200):
+def small_shapes(tile, calls=200, cpu=False):
     """Device time per call of the small workloads: `calls` back-to-back calls
     captured in one CUDA graph and replayed (so host launch overhead is not
     counted).  Their working sets sit in the L2, so the GB/s are labelled
-    effective (L2), not HBM."""
+    effective (L2), not HBM.  With ``cpu``, each entry also carries the FP64
+    oracle timed on the same inputs, on one core and on every host core."""
     import torch
 
     import synth
     out = []
     cap = torch.cuda.Stream()
     for cfg, op, rows, width in SMALL_SHAPES:
-        x = torch.from_numpy(synth.rows_of(cfg, rows, width, which="x")).cuda()
-        r = torch.from_numpy(synth.rows_of(cfg, rows, width, which="r")).cuda() \
-            if op == "residual_layernorm" else None
+        x_h = synth.rows_of(cfg, rows, width, which="x")
+        r_h = synth.rows_of(cfg, rows, width, which="r") if op == "residual_layernorm" else None
+        x = torch.from_numpy(x_h).cuda()
+        r = torch.from_numpy(r_h).cuda() if r_h is not None else None
         y = torch.empty_like(x)
         tile.run(op, x, r, y, EPS)                   # first call: lazy set-up
         torch.cuda.synchronize()
@@ -533,17 +575,110 @@ def small_shapes(tile, calls=200):
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / (5 * calls)
         b = BYTES_PER_ELEM[op] * rows * width
-        out.append({"workload": cfg, "op": op, "shape": f"{rows}x{width}",
-                    "us_per_call": round(us, 3), "rows_per_s": round(rows / (us * 1e-6)),
-                    "gbs_effective_l2": round(b / (us * 1e-6) / 1e9, 1)})
+        entry = {"workload": cfg, "op": op, "shape": f"{rows}x{width}",
+                 "us_per_call": round(us, 3), "rows_per_s": round(rows / (us * 1e-6)),
+                 "gbs_effective_l2": round(b / (us * 1e-6) / 1e9, 1)}
+        if cpu:
+            entry["cpu_baseline"] = oracle_per_call(op, x_h, r_h)
+        out.append(entry)
         del g, x, r, y
     return out
 
 
-def cpu_baseline(op, x_h, r_h):
+def oracle_per_call(op, x_h, r_h, min_seconds=0.05):
+    """The FP64 oracle on one workload, as it stands: repeated until at least
+    ``min_seconds`` have passed, on one core and on every host core (row
+    blocks, at most one per row).  µs per call, rows/s and GB/s of FP32
+    input and output moved."""
+    import oracle
+    orc = oracle.get()
+    eps = oracle.kernel_eps(EPS)
+    rows, width = x_h.shape
+    b = BYTES_PER_ELEM[op] * rows * width
+    res = {}
+    for name, threads in (("single_core", 1), ("all_cores", min(host_cores(), rows))):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            oracle_rows(orc, op, x_h, r_h, eps, threads)
+            n += 1
+            dt = time.perf_counter() - t0
+            if dt >= min_seconds:
+                break
+        sec = dt / n
+        res[name] = {"us_per_call": round(sec * 1e6, 2), "rows_per_s": round(rows / sec),
+                     "gbs": round(b / sec / 1e9, 4), "cores": threads, "calls": n}
+    return res
+
+
+def single_call(tile, lib, x_big, r_big, y_big, stream, samples=60):
+    """Latency of one call on its own, as a caller sees it, in two separate
+    phases per workload: (1) GPU time, CUDA events around one call with the
+    device idle before it; (2) host wall, from the C-ABI call (through
+    ctypes) to the return of cudaStreamSynchronize on the call's stream.
+    ``samples`` of each, after 5 warm-up calls; p50, minimum and p90 in µs.
+    Workloads: the 1024x4096 softmax, RMSNorm and LayerNorm and the
+    65536x4096 residual LayerNorm."""
+    import torch
+
+    import synth
+    x2 = torch.from_numpy(synth.rows_of(2, 1024, 4096, which="x")).cuda()
+    y2 = torch.empty_like(x2)
+    s = stream.cuda_stream
+    cases = [("softmax", x2, None, y2), ("rmsnorm", x2, None, y2), ("layernorm", x2, None, y2),
+             ("residual_layernorm", x_big, r_big, y_big)]
+
+    def stats(v):
+        v = sorted(v)
+        return {"p50": round(statistics.median(v), 3), "min": round(v[0], 3),
+                "p90": round(v[(9 * len(v)) // 10], 3)}
+
+    out = []
+    for op, x, r, y in cases:
+        rows, width = x.shape
+        fn = getattr(lib, f"tile_{op}_f32")
+        args = ((x.data_ptr(), r.data_ptr(), y.data_ptr()) if r is not None
+                else (x.data_ptr(), y.data_ptr())) + (rows, width, EPS, s)
+
+        def call():
+            st = fn(*args)
+            if st != 0:
+                raise tile.TileError(st, op)
+
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        gpu = []
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(samples):
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            stream.synchronize()
+            gpu.append(e0.elapsed_time(e1) * 1e3)
+        wall = []
+        for _ in range(samples):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter_ns()
+            call()
+            stream.synchronize()
+            wall.append((time.perf_counter_ns() - t0) / 1e3)
+        out.append({"op": op, "shape": f"{rows}x{width}", "samples": samples,
+                    "gpu_us": stats(gpu), "host_wall_us": stats(wall)})
+    del x2, y2
+    return out
+
+
+ATOL, RTOL = 2e-6, 2e-5      # the acceptance bound |y - ref| <= ATOL + RTOL*|ref|
+
+
+def cpu_baseline(op, x_h, r_h, got=None):
     """The FP64 oracle over the whole workload on this host: once on every
     host core (row blocks in parallel, the reported value) and once on one
-    core."""
+    core.  With ``got`` (the timed call's output, on the host), the
+    all-core pass's result also checks every element of it, after the
+    timing: returns (baseline, parity)."""
+    import numpy as np
+
     import oracle
     orc = oracle.get()
     rows, width = x_h.shape
@@ -551,25 +686,45 @@ def cpu_baseline(op, x_h, r_h):
     b = BYTES_PER_ELEM[op] * rows * width
     cores = host_cores()
     t = time.perf_counter()
-    oracle_rows(orc, op, x_h, r_h, eps, cores)
+    blocks = oracle_rows(orc, op, x_h, r_h, eps, cores)
     dt_all = time.perf_counter() - t
+    parity = None
+    if got is not None:
+        worst_abs, worst_rel, worst_ratio, bad, row0 = 0.0, 0.0, 0.0, 0, 0
+        for ref in blocks:
+            g = got[row0:row0 + ref.shape[0]].astype(np.float64)
+            row0 += ref.shape[0]
+            err = np.abs(g - ref)
+            mag = np.abs(ref)
+            worst_abs = max(worst_abs, float(err.max()))
+            big = mag > 1e-6
+            if big.any():
+                worst_rel = max(worst_rel, float((err[big] / mag[big]).max()))
+            ratio = err / (ATOL + RTOL * mag)
+            worst_ratio = max(worst_ratio, float(ratio.max()))
+            bad += int(np.count_nonzero(~(ratio <= 1.0)))
+        parity = {"against": "FP64 oracle, every element", "elements": int(got.size),
+                  "max_abs_err": worst_abs, "max_rel_err": worst_rel,
+                  "max_err_over_bound": round(worst_ratio, 4),
+                  "bound": f"{ATOL} + {RTOL}*|ref|", "beyond_bound": bad}
+        if bad:
+            print(f"warning: {bad} outputs beyond the bound", file=sys.stderr)
+    del blocks
     t = time.perf_counter()
     orc.run(op, x_h, r_h, eps)
     dt_one = time.perf_counter() - t
-    return {"value": round(b / dt_all / 1e9, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+    base = {"value": round(b / dt_all / 1e9, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"all {rows} rows x {width}, one pass, FP64 C, row blocks on {cores} "
                       "threads",
             "seconds": round(dt_all, 3),
             "single_core": {"value": round(b / dt_one / 1e9, 4), "unit": UNIT, "cores": 1,
                             "seconds": round(dt_one, 3)}}
+    return base, parity
 
 
 # ---------------------------------------------------------------------------
 # reference arm: the FP64 CPU oracle as it stands, on host cores
 # ---------------------------------------------------------------------------
-
-SAMPLE_ROWS_PER_CORE = 1024
-
 
 def run_reference(args, dist):
     if dist.rank != 0:
@@ -579,9 +734,9 @@ def run_reference(args, dist):
 
     rows, width, op = args.rows, args.width, args.op
     cores = host_cores()
-    n = min(SAMPLE_ROWS_PER_CORE * cores, rows)
-    x_h = synth.rows_of(SEED_CFG, rows, width, row_ids=range(n), which="x")
-    r_h = synth.rows_of(SEED_CFG, rows, width, row_ids=range(n), which="r")
+    n = rows                                 # every step: the whole workload
+    x_h = synth.rows_of(SEED_CFG, rows, width, which="x")
+    r_h = synth.rows_of(SEED_CFG, rows, width, which="r") if op == "residual_layernorm" else None
     orc = oracle.get()
     eps = oracle.kernel_eps(EPS)
     for _ in range(args.warmup):
@@ -592,15 +747,19 @@ def run_reference(args, dist):
     total = time.perf_counter() - t0
     b = BYTES_PER_ELEM[op] * n * width
     value = b * args.steps / total / 1e9
-    sample = f"{n} of {rows} rows x {width} per step, FP64 C, row blocks on {cores} threads"
+    sample = f"all {n} rows x {width} per step, FP64 C, row blocks on {cores} threads"
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "impl": "reference",
+        "metric": METRIC if (op, rows, width) == ("residual_layernorm", 65536, 4096) else
+        f"HBM GB/s and µs/call, {op} FP32 {rows}×{width}",
+        "value": round(value, 4), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic: SplitMix64 uniform[-1,1), seeds 1005/2005",
-        "config": {"workload": f"{op.replace('_', ' ')} FP32 {rows}x{width}", "rows": rows,
-                   "width": width, "eps": EPS, "parallelism": f"host, {cores} threads"},
+        "data": f"synthetic: SplitMix64 uniform[-1,1), seeds {synth.x_seed(SEED_CFG)}/"
+                f"{synth.r_seed(SEED_CFG)}",
+        "config": workload_config(op, rows, width, dist.world),
+        "host_threads": cores,
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,

@@ -460,6 +460,22 @@ int tile_plan_info(int id, int op, int rows, int width, tile_plan_t *plan);
  * which only the register plans implement. */
 int tile_plan_info_ex(int id, int op, int dtype, int rows, int width, tile_plan_t *plan);
 
+/* Test hook for the bounded waits of the shared-memory-staged kernel (the
+ * notes have no counterpart: their kernels have no copy engine to wait on).
+ * Runs the staged plan `plan_id` (path TILE_PATH_STAGED) of `op` on `args`
+ * as tile_run_plan_args_f32 would, except that no CTA issues the bulk copy
+ * of its first row and every barrier wait gives up after `spin_limit` polls
+ * (0 counts as 1).  The first wait of every CTA therefore runs out: the
+ * kernel sets its wait-timeout bit in the device status word, stops
+ * waiting and copying, waits (bounded) for the copies it did issue, and
+ * returns with its outputs invalid.  tile_check_device_status then returns
+ * TILE_ERR_DEVICE and clears the word.  Nothing is left in flight (the
+ * withheld copy is never issued).  No other entry point withholds a copy;
+ * library calls wait up to 2^20 polls.  Errors as tile_run_plan_args_f32;
+ * TILE_ERR_PLAN also for a plan that is not staged. */
+int tile_test_staged_wait_timeout(int op, int plan_id, const tile_row_args_t *args,
+                                  unsigned int spin_limit, cudaStream_t stream);
+
 /* Run `op` (one of the first four op codes) with the built plan `plan_id`
  * instead of the selector's choice (used by the measured plan sweep and by
  * tests that check every plan; tile_run_plan_args_f32 covers every op).

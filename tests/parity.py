@@ -40,3 +40,48 @@ def compare(got, ref, what=""):
 
 def oracle_of(op, x, r=None, eps=EPS):
     return oracle.get().run(op, x, r, ref_eps(eps))
+
+
+def host_threads():
+    """Host cores this process may run on."""
+    import os
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_blocks(op, x, r=None, eps=EPS, block_rows=1024, threads=None):
+    """The oracle over a large matrix in contiguous row blocks, computed on
+    every host core (the C oracle runs with the GIL released) a wave of
+    blocks at a time, so at most ``threads`` FP64 blocks are held at once.
+    Yields ``(row0, row1, ref)`` in row order; each block is exactly what one
+    call over all rows gives for those rows (rows are independent)."""
+    from concurrent.futures import ThreadPoolExecutor
+    rows = x.shape[0]
+    threads = threads or host_threads()
+    orc = oracle.get()
+    e = ref_eps(eps)
+    spans = [(a, min(rows, a + block_rows)) for a in range(0, rows, block_rows)]
+
+    def one(ab):
+        a, b = ab
+        return orc.run(op, x[a:b], None if r is None else r[a:b], e)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        for w in range(0, len(spans), threads):
+            wave = spans[w:w + threads]
+            for (a, b), ref in zip(wave, ex.map(one, wave)):
+                yield a, b, ref
+
+
+def compare_full(got, op, x, r=None, eps=EPS, what="", block_rows=1024):
+    """``compare`` over every element of a whole [rows, width] output, block
+    by block against ``oracle_blocks``.  Returns (max abs err, max rel err)
+    over the whole output."""
+    assert got.shape == x.shape, f"{what}: shape {got.shape} != {x.shape}"
+    worst_abs, worst_rel = 0.0, 0.0
+    for a, b, ref in oracle_blocks(op, x, r, eps, block_rows):
+        ea, er = compare(got[a:b], ref, f"{what} rows {a}..{b - 1}")
+        worst_abs, worst_rel = max(worst_abs, ea), max(worst_rel, er)
+    return worst_abs, worst_rel

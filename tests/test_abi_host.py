@@ -200,6 +200,36 @@ def test_host_entry_rejects_bad_arguments(lib):
     assert f(1, A, None, B, 2, 4096, 1e-5, W, 65535, None) == -10
 
 
+@fake_pointers
+def test_static_host_entry_rejects_bad_arguments_before_any_cuda_call(lib):
+    """The entry point without a workspace finds argument errors on the host,
+    before it looks up its device array (this container has no GPU, so any
+    CUDA call would fail with TILE_ERR_CUDA instead)."""
+    f = lib.tile_run_host_static_f32
+    assert f(0, A, A, B, 0, 8, 1e-5, None) == OK            # rows == 0
+    assert f(5, A, A, B, 2, 8, 1e-5, None) == OP
+    assert f(0, A, A, B, 2, 0, 1e-5, None) == SHAPE
+    assert f(1, A, None, B, 2, 8, -1.0, None) == EPS
+    assert f(0, A, None, B, 2, 8, 1e-5, None) == NULL          # residual LN without r
+    assert f(1, None, None, B, 2, 8, 1e-5, None) == NULL
+    assert f(1, A, None, None, 2, 8, 1e-5, None) == NULL
+    assert f(1, A, None, A + 8, 2, 8, 1e-5, None) == ALIAS
+    assert f(0, A, B, B + 16, 2, 8, 1e-5, None) == ALIAS        # out overlaps r
+
+
+@fake_pointers
+def test_staged_wait_hook_rejects_bad_arguments(lib):
+    a = tile.TileRowArgs()
+    a.in_, a.out, a.rows, a.width, a.eps, a.dtype = A, B, 4, 256, 1e-5, 1
+    f = lib.tile_test_staged_wait_timeout
+    assert f(1, 45, None, 16, None) == NULL
+    assert f(1, 7, ctypes.byref(a), 16, None) == PLAN           # a register plan
+    assert f(1, 99, ctypes.byref(a), 16, None) == PLAN
+    assert f(4, 45, ctypes.byref(a), 16, None) == PLAN          # row sum: no staged kernel
+    a.rows = 0
+    assert f(1, 45, ctypes.byref(a), 16, None) == OK            # nothing to launch
+
+
 def test_host_workspace_bytes(lib):
     assert tile.tile_host_workspace_bytes("layernorm", 4096, 1) == 2 * 2 * 16384
     assert tile.tile_host_workspace_bytes("residual_layernorm", 100, 3) == 2 * 3 * 1280

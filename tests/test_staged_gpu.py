@@ -116,3 +116,48 @@ def test_staged_results_are_deterministic():
     tile.tile_run_plan_args_f32("layernorm", pid, x, a, eps=EPS)
     tile.tile_run_plan_args_f32("layernorm", pid, x, b, eps=EPS)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("op,dtype,pid", [("layernorm", "bf16", 45),
+                                          ("residual_layernorm", "f32", 41)])
+def test_staged_wait_runs_out_and_the_next_call_is_correct(op, dtype, pid):
+    """The bounded wait made to run out, with no fault: through the test
+    entry point no CTA issues the copy of its first row, and waits give up
+    after 4096 polls.  Every CTA (4096 rows: several rows, and so several
+    copies in flight, per CTA) times out on its first row, stops copying,
+    drains the copies it did issue and returns.  The device status word then
+    reports the error once (read and cleared by tile_check_device_status),
+    and a normal call of the same plan on the same buffers is correct."""
+    import time
+    rows, width = 4096, 4096
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]
+    x = torch.from_numpy(synth.rows_of(3, rows, width, which="x")).to(tdt)
+    r = torch.from_numpy(synth.rows_of(3, rows, width, which="r")).to(tdt)
+    xf, rf = x.float().numpy(), r.float().numpy()
+    with_res = op == "residual_layernorm"
+    xd, rd = x.cuda(), (r.cuda() if with_res else None)
+    out = torch.full((rows, width), float("nan"), dtype=tdt, device="cuda")
+    assert tile.tile_check_device_status() == 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    tile.tile_test_staged_wait_timeout(op, pid, xd, out, 4096, residual=rd, eps=EPS)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 30.0
+    assert tile.tile_check_device_status() == -9          # TILE_ERR_DEVICE, then cleared
+    assert tile.tile_check_device_status() == 0
+    out.fill_(float("nan"))
+    tile.tile_run_plan_args_f32(op, pid, xd, out, residual=rd, eps=EPS)
+    ref = _reference(op, xf, rf if with_res else None, None, None)
+    got = out.float().cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref)
+    bad = ~(err <= ATOL + (RTOL + HALF_ULP_REL[dtype]) * np.abs(ref))
+    assert not bad.any(), f"{int(bad.sum())} beyond the bound after the timed-out launch"
+    assert tile.tile_check_device_status() == 0
+
+
+def test_staged_wait_hook_rejects_register_plans():
+    x = torch.zeros(4, 256, device="cuda")
+    out = torch.zeros(4, 256, device="cuda")
+    with pytest.raises(tile.TileError) as e:
+        tile.tile_test_staged_wait_timeout("rmsnorm", 7, x, out, 16)
+    assert e.value.status == -8

@@ -7,13 +7,19 @@ allocator, or latency-critical code that must not call cudaMalloc.  It
 stages rows through a static device array inside the library instead of a
 workspace the caller allocates.
 
-Each case calls it twice in a row through the C ABI (the second call is
-enqueued before the first has finished, with different inputs, so stale
+Each case calls it twice in a row through the C ABI with different inputs
+(the second call is enqueued before the first has finished, so stale
 contents of the shared array or an overlap between the calls would show)
-and checks both results against tile_run_host_f32 with a caller workspace,
-within the tolerance of the other parity tests: with pageable inputs (the
-rows stage through the array) and with every buffer pinned (in place).  This file is collected last
-and depends on nothing that earlier tests set up.
+and checks both results against the FP64 oracle under the acceptance bound
+of the other parity tests, and against tile_run_host_f32 with a caller
+workspace: bit for bit where rows are whole 16-byte vectors (both entry
+points then run the same plan on rows of the same alignment), within the
+bound otherwise.  Modes: pageable inputs (the rows stage through the array)
+with the output pinned or pageable, and every buffer pinned (in place).
+One more case issues the two calls on two different streams with no
+synchronisation between them: only the library's ordering of calls on the
+shared array keeps them apart there.  This file is collected last and
+depends on nothing that earlier tests set up.
 """
 
 import numpy as np
@@ -22,7 +28,7 @@ import torch
 
 import synth
 import tile_compiler_row_gb300 as tile
-from parity import ATOL, EPS, RTOL
+from parity import ATOL, EPS, RTOL, compare, oracle_of
 
 pytestmark = pytest.mark.gpu
 
@@ -38,15 +44,17 @@ def device():
     torch.cuda.set_device(0)
 
 
-def _pinned(a):
-    return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+def _host(a, pinned):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.pin_memory() if pinned else t.clone()
 
 
 def _inputs(op, rows, width, scale, pinned=True):
+    """(x, r) host tensors and the FP32 arrays they hold: workload-3 rows,
+    x scaled by `scale` in FP32 (the oracle gets the same rounded values)."""
     x = synth.rows_of(3, rows, width, which="x") * np.float32(scale)
     r = synth.rows_of(3, rows, width, which="r") if op == "residual_layernorm" else None
-    host = _pinned if pinned else (lambda a: torch.from_numpy(np.ascontiguousarray(a)).clone())
-    return host(x), (host(r) if r is not None else None)
+    return (_host(x, pinned), _host(r, pinned) if r is not None else None), (x, r)
 
 
 def _with_workspace(op, x, r):
@@ -59,6 +67,25 @@ def _with_workspace(op, x, r):
     return out.numpy().copy()
 
 
+def _call_static(op, x, r, out, stream):
+    lib = tile.load()
+    rows, width = x.shape
+    st = lib.tile_run_host_static_f32(tile.OPS[op], x.data_ptr(),
+                                      r.data_ptr() if r is not None else None,
+                                      out.data_ptr(), rows, width, EPS, stream)
+    assert st == 0, tile.tile_status_string(st)
+
+
+def _check(op, got, host_in, values, what):
+    x, r = values
+    compare(got, oracle_of(op, x, r), f"{what}: against the oracle")
+    want = _with_workspace(op, *host_in)
+    if x.shape[1] % 4 == 0:
+        assert np.array_equal(got, want), f"{what}: differs from tile_run_host_f32"
+    else:
+        assert np.all(np.abs(got - want) <= ATOL + RTOL * np.abs(want)), what
+
+
 # staged: pageable inputs go through the static array (with the output
 # pinned, stored directly; or pageable, copied out); in_place: every buffer
 # pinned, one kernel on the host buffers and no staging
@@ -68,26 +95,39 @@ MODES = {"staged_direct_out": (False, True), "staged_copy_out": (False, False),
 
 @pytest.mark.parametrize("mode", list(MODES))
 @pytest.mark.parametrize("op,rows,width", CASES)
-def test_static_staging_matches_workspace_entry_point_on_two_calls(op, rows, width, mode):
-    lib = tile.load()
+def test_static_staging_matches_oracle_on_two_calls(op, rows, width, mode):
     stream = torch.cuda.current_stream().cuda_stream
     pin_in, pin_out = MODES[mode]
     calls = [_inputs(op, rows, width, 1.0, pin_in), _inputs(op, rows, width, -2.5, pin_in)]
     outs = []
-    for x, r in calls:                       # two calls in a row, no sync between
+    for (x, r), _ in calls:                  # two calls in a row, no sync between
         out = torch.full((rows, width), float("nan"))
         out = out.pin_memory() if pin_out else out
-        st = lib.tile_run_host_static_f32(tile.OPS[op], x.data_ptr(),
-                                          r.data_ptr() if r is not None else None,
-                                          out.data_ptr(), rows, width, EPS, stream)
-        assert st == 0, tile.tile_status_string(st)
+        _call_static(op, x, r, out, stream)
         outs.append(out)
     torch.cuda.synchronize()
-    for (x, r), out in zip(calls, outs):
-        got = out.numpy()
-        want = _with_workspace(op, x, r)
-        assert np.all(np.isfinite(got))
-        assert np.all(np.abs(got - want) <= ATOL + RTOL * np.abs(want))
+    for k, ((host_in, values), out) in enumerate(zip(calls, outs)):
+        _check(op, out.numpy(), host_in, values, f"{op} {rows}x{width} {mode} call {k}")
+
+
+@pytest.mark.parametrize("op,rows,width", CASES)
+def test_static_staging_calls_on_two_streams(op, rows, width):
+    """Two calls on two different streams, enqueued back to back with no
+    synchronisation: pageable inputs stage through the shared array and the
+    results go straight into pinned outputs, so nothing on the host orders
+    the two calls and only the library's ordering on the GPU keeps the
+    second call's copies from overwriting rows the first call's kernels
+    have not read yet."""
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    calls = [_inputs(op, rows, width, 1.0, False), _inputs(op, rows, width, -2.5, False)]
+    outs = []
+    for ((x, r), _), s in zip(calls, streams):
+        out = torch.full((rows, width), float("nan")).pin_memory()
+        _call_static(op, x, r, out, s.cuda_stream)
+        outs.append(out)
+    torch.cuda.synchronize()
+    for k, ((host_in, values), out) in enumerate(zip(calls, outs)):
+        _check(op, out.numpy(), host_in, values, f"{op} {rows}x{width} stream {k}")
 
 
 def test_static_staging_rejects_a_width_beyond_the_maximum():

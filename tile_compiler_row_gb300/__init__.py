@@ -38,7 +38,7 @@ __all__ = [
     "tile_norm_param_grad_f32", "tile_run_backward_plan_ex",
     "tile_layernorm_backward_bf16", "tile_rmsnorm_backward_bf16", "tile_softmax_backward_bf16",
     "tile_norm_param_grad_bf16", "tile_layernorm_backward_f16", "tile_rmsnorm_backward_f16",
-    "tile_softmax_backward_f16", "tile_norm_param_grad_f16",
+    "tile_softmax_backward_f16", "tile_norm_param_grad_f16", "tile_test_staged_wait_timeout",
     "residual_layernorm", "layernorm", "rmsnorm", "softmax", "run",
 ]
 
@@ -161,6 +161,7 @@ def load():
         "tile_softmax_backward_f16": [P, P, P, I, I, P],
         "tile_norm_param_grad_f16": [P, P, P, P, P, I, I, P, ctypes.c_size_t, P],
         "tile_plan_info_ex": [I, I, I, I, I, ctypes.POINTER(TilePlan)],
+        "tile_test_staged_wait_timeout": [I, I, ctypes.POINTER(TileRowArgs), ctypes.c_uint, P],
     }
     for name, argtypes in sigs.items():
         fn = getattr(lib, name)
@@ -310,12 +311,8 @@ def tile_row_minmax_f32(x, mins, maxs, stream=None):
            "tile_row_minmax_f32")
 
 
-def tile_run_plan_args_f32(op, plan_id, x, out, residual=None, gamma=None, beta=None, out2=None,
-                           eps=1e-5, stream=None):
-    """Any row op with a forced plan (``out``: matrix, or [rows] for row_sum/row_minmax).
-    ``x`` may be float32, bfloat16 or float16; the element type follows it."""
+def _row_args(x, out, residual, gamma, beta, out2, eps):
     import torch
-    op = OPS[op] if isinstance(op, str) else op
     dt = {torch.bfloat16: "bf16", torch.float16: "f16"}.get(
         x.dtype if isinstance(x, torch.Tensor) else None, "f32")
     px, rows, width = _matrix(x, "x", dt)
@@ -328,8 +325,29 @@ def tile_run_plan_args_f32(op, plan_id, x, out, residual=None, gamma=None, beta=
     a.out = out.data_ptr()
     a.out2 = out2.data_ptr() if out2 is not None else None
     a.rows, a.width, a.eps = rows, width, eps
+    return a
+
+
+def tile_run_plan_args_f32(op, plan_id, x, out, residual=None, gamma=None, beta=None, out2=None,
+                           eps=1e-5, stream=None):
+    """Any row op with a forced plan (``out``: matrix, or [rows] for row_sum/row_minmax).
+    ``x`` may be float32, bfloat16 or float16; the element type follows it."""
+    op = OPS[op] if isinstance(op, str) else op
+    a = _row_args(x, out, residual, gamma, beta, out2, eps)
     _check(load().tile_run_plan_args_f32(op, plan_id, ctypes.byref(a), _stream(stream)),
            "tile_run_plan_args_f32")
+
+
+def tile_test_staged_wait_timeout(op, plan_id, x, out, spin_limit, residual=None, gamma=None,
+                                  beta=None, eps=1e-5, stream=None):
+    """Test hook: the staged plan with every CTA's first copy withheld and
+    waits limited to ``spin_limit`` polls (the outputs are invalid; the
+    device status word reports the timeout)."""
+    op = OPS[op] if isinstance(op, str) else op
+    a = _row_args(x, out, residual, gamma, beta, None, eps)
+    _check(load().tile_test_staged_wait_timeout(op, plan_id, ctypes.byref(a), int(spin_limit),
+                                                _stream(stream)),
+           "tile_test_staged_wait_timeout")
 
 
 def _flat(t, name):

@@ -124,21 +124,37 @@ void *device_address(const void *p) {
     return nullptr;
 }
 
-// The pipeline over caller-provided workspace (also used by the entry point
-// that stages through the library's static device area).
-int run_host(int op, const float *h_in, const float *h_res, float *h_out, int rows, int width,
-             float eps, void *d_work, size_t work_bytes, cudaStream_t stream) {
+// Argument checks of the host entry points that need no CUDA call and no
+// workspace: op, shape, eps, NULL buffers and an output overlapping an
+// input.  TILE_OK for rows == 0 too (the caller then returns at once).
+int check_host_args(int op, const float *h_in, const float *h_res, const float *h_out,
+                    int rows, int width, float eps) {
     if (op < TILE_OP_RESIDUAL_LAYERNORM || op > TILE_OP_SOFTMAX) return TILE_ERR_OP;
     if (rows < 0 || width < 1 || width > tile_max_width()) return TILE_ERR_SHAPE;
     if (op != TILE_OP_SOFTMAX && !(std::isfinite(eps) && eps >= 0.0f)) return TILE_ERR_EPS;
     if (rows == 0) return TILE_OK;
     const bool residual = op == TILE_OP_RESIDUAL_LAYERNORM;
-    if (h_in == nullptr || h_out == nullptr || (residual && h_res == nullptr) || d_work == nullptr)
+    if (h_in == nullptr || h_out == nullptr || (residual && h_res == nullptr))
         return TILE_ERR_NULL;
-    if ((reinterpret_cast<uintptr_t>(d_work) & (kAlign - 1)) != 0) return TILE_ERR_ALIGN;
     const size_t total = static_cast<size_t>(rows) * static_cast<size_t>(width) * sizeof(float);
     if (overlaps(h_out, h_in, total) || (residual && overlaps(h_out, h_res, total)))
         return TILE_ERR_ALIAS;
+    return TILE_OK;
+}
+
+// The pipeline over caller-provided workspace (also used by the entry point
+// that stages through the library's static device area).  If a CUDA call
+// fails after work was enqueued, `stream` is still ordered after everything
+// this call enqueued on the internal copy streams (as far as the runtime
+// accepts the joins), so work the caller orders after `stream` never
+// overlaps it.
+int run_host(int op, const float *h_in, const float *h_res, float *h_out, int rows, int width,
+             float eps, void *d_work, size_t work_bytes, cudaStream_t stream) {
+    const int arg = check_host_args(op, h_in, h_res, h_out, rows, width, eps);
+    if (arg != TILE_OK || rows == 0) return arg;
+    const bool residual = op == TILE_OP_RESIDUAL_LAYERNORM;
+    if (d_work == nullptr) return TILE_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(d_work) & (kAlign - 1)) != 0) return TILE_ERR_ALIGN;
     // Checked on the host before any CUDA call: one row of every tensor must
     // fit twice (whether or not the output later turns out to be stored
     // directly).
@@ -220,12 +236,21 @@ int run_host(int op, const float *h_in, const float *h_res, float *h_out, int ro
                                    : reinterpret_cast<float *>(p + (residual ? 2 : 1) * buf);
     }
 
-    // Everything enqueued here runs after the work already on `stream`.
+    // Everything enqueued here runs after the work already on `stream`.  On
+    // a failure `stream` first waits for both copy streams (best effort; the
+    // error reported is the first one).
+    auto join = [&]() {
+        if (cudaEventRecord(q.done, q.d2h) == cudaSuccess)
+            (void)cudaStreamWaitEvent(stream, q.done, 0);
+        if (cudaEventRecord(q.done, q.h2d) == cudaSuccess)
+            (void)cudaStreamWaitEvent(stream, q.done, 0);
+    };
 #define TILE_TRY(call)                                          \
     do {                                                        \
         err = (call);                                           \
         if (err != cudaSuccess) {                               \
             set_last_cuda_error(static_cast<int>(err));         \
+            join();                                             \
             return TILE_ERR_CUDA;                               \
         }                                                       \
     } while (0)
@@ -251,13 +276,19 @@ int run_host(int op, const float *h_in, const float *h_res, float *h_out, int ro
         if (out_dev != nullptr) {
             const int st =
                 run_selected(op, dx[b], dr[b], out_dev + off, n, width, eps, stream, rows);
-            if (st != TILE_OK) return st;
+            if (st != TILE_OK) {
+                join();
+                return st;
+            }
             TILE_TRY(cudaEventRecord(q.compute_ev[b], stream));
             continue;
         }
         if (c >= slots) TILE_TRY(cudaStreamWaitEvent(stream, q.d2h_ev[b], 0));
         const int st = run_selected(op, dx[b], dr[b], dy[b], n, width, eps, stream, rows);
-        if (st != TILE_OK) return st;
+        if (st != TILE_OK) {
+            join();
+            return st;
+        }
         TILE_TRY(cudaEventRecord(q.compute_ev[b], stream));
 
         TILE_TRY(cudaStreamWaitEvent(q.d2h, q.compute_ev[b], 0));

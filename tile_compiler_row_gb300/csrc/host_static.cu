@@ -40,11 +40,11 @@ StaticStaging g_staging[tile::kMaxDevices];
 extern "C" int tile_run_host_static_f32(int op, const float *h_in, const float *h_residual,
                                         float *h_out, int rows, int width, float eps,
                                         cudaStream_t stream) {
-    // Argument errors are reported before any CUDA call.
-    if (op < TILE_OP_RESIDUAL_LAYERNORM || op > TILE_OP_SOFTMAX) return TILE_ERR_OP;
-    if (rows < 0 || width < 1 || width > tile_max_width()) return TILE_ERR_SHAPE;
-    if (op != TILE_OP_SOFTMAX && !(std::isfinite(eps) && eps >= 0.0f)) return TILE_ERR_EPS;
-    if (rows == 0) return TILE_OK;
+    // Argument errors (op, shape, eps, NULL buffers, an output overlapping
+    // an input, a row too large for the area) are reported before any CUDA
+    // call.
+    const int arg = tile::check_host_args(op, h_in, h_residual, h_out, rows, width, eps);
+    if (arg != TILE_OK || rows == 0) return arg;
     // One row of every tensor must fit the area twice (double buffering).
     if (tile_host_workspace_bytes(op, width, 1) > TILE_STATIC_STAGING_BYTES)
         return TILE_ERR_WORKSPACE;
@@ -77,9 +77,11 @@ extern "C" int tile_run_host_static_f32(int op, const float *h_in, const float *
     }
     const int st = tile::run_host(op, h_in, h_residual, h_out, rows, width, eps, s.device_ptr,
                                   TILE_STATIC_STAGING_BYTES, stream);
-    if (st != TILE_OK) return st;
-    // run_host leaves `stream` ordered after its last copy out.
+    // run_host leaves `stream` ordered after everything it enqueued, on
+    // success and on failure alike, so the next call waits for this one
+    // either way.
     err = cudaEventRecord(s.done, stream);
+    if (st != TILE_OK) return st;
     if (err != cudaSuccess) {
         tile::set_last_cuda_error(static_cast<int>(err));
         return TILE_ERR_CUDA;

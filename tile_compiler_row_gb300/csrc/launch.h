@@ -52,6 +52,10 @@ enum { ELEM_F32 = 0, ELEM_BF16 = 1, ELEM_F16 = 2 };
 cudaError_t launch_staged(int kernel_op, int elem, int plan_id, RowArgs args,
                           cudaStream_t stream);
 cudaError_t status_staged(unsigned int *value, cudaStream_t stream);
+// The staged kernel with each CTA's first copy withheld and the barrier
+// waits limited to `spin_limit` polls (tile_test_staged_wait_timeout).
+cudaError_t launch_staged_withheld(int kernel_op, int elem, int plan_id, RowArgs args,
+                                   unsigned int spin_limit, cudaStream_t stream);
 
 // Backward kernel ops (bwd_kernel.cuh).
 enum { BWD_LN_OP = 0, BWD_RMS_OP = 1, BWD_SOFTMAX_OP = 2 };
@@ -125,6 +129,11 @@ int run_pairs(int kind, const float *in, float *value, float *derivative, long l
 // Returns a TILE_* status.
 int run_selected(int op, const float *in, const float *res, float *out, int rows, int width,
                  float eps, cudaStream_t stream, long long select_rows = 0);
+
+// The argument checks of the host entry points that need no CUDA call (op,
+// shape, eps, NULL buffers, output overlapping an input); a TILE_* status.
+int check_host_args(int op, const float *h_in, const float *h_res, const float *h_out,
+                    int rows, int width, float eps);
 
 // The pipeline of tile_run_host_f32 over a given device workspace.
 int run_host(int op, const float *h_in, const float *h_res, float *h_out, int rows, int width,

@@ -45,10 +45,11 @@ int sm_count(cudaError_t *err) {
 }
 
 template <int OP, class T, int S, int K, int KB>
-cudaError_t launch_one(RowArgs a, cudaStream_t stream) {
+cudaError_t launch_one(RowArgs a, StagedHooks hooks, cudaStream_t stream) {
     constexpr int EV = 16 / sizeof(T);
     if constexpr (K * EV > 64) {
         (void)a;
+        (void)hooks;
         (void)stream;
         return cudaErrorInvalidValue;     // not built: stripe above 64 floats
     } else {
@@ -74,16 +75,16 @@ cudaError_t launch_one(RowArgs a, cudaStream_t stream) {
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
         long long grid = static_cast<long long>(sms) * per_sm;
         if (grid > a.rows) grid = a.rows;
-        kernel<<<static_cast<unsigned int>(grid), 32 * S, dyn, stream>>>(a, nst);
+        kernel<<<static_cast<unsigned int>(grid), 32 * S, dyn, stream>>>(a, nst, hooks);
         return cudaGetLastError();
     }
 }
 
 template <int OP, class T>
-cudaError_t launch_op(int staged_id, RowArgs a, cudaStream_t stream) {
+cudaError_t launch_op(int staged_id, RowArgs a, StagedHooks h, cudaStream_t stream) {
     switch (staged_id) {
 #define TILE_CASE(id, S, K, KB) \
-    case id: return launch_one<OP, T, S, K, KB>(a, stream);
+    case id: return launch_one<OP, T, S, K, KB>(a, h, stream);
         TILE_STAGED_LIST(TILE_CASE)
 #undef TILE_CASE
         default: return cudaErrorInvalidValue;
@@ -91,12 +92,22 @@ cudaError_t launch_op(int staged_id, RowArgs a, cudaStream_t stream) {
 }
 
 template <class T>
-cudaError_t launch_type(int op, int staged_id, RowArgs a, cudaStream_t stream) {
+cudaError_t launch_type(int op, int staged_id, RowArgs a, StagedHooks h, cudaStream_t stream) {
     switch (op) {
-        case OP_RESLN: return launch_op<OP_RESLN, T>(staged_id, a, stream);
-        case OP_LN: return launch_op<OP_LN, T>(staged_id, a, stream);
-        case OP_RMS: return launch_op<OP_RMS, T>(staged_id, a, stream);
-        case OP_SOFTMAX: return launch_op<OP_SOFTMAX, T>(staged_id, a, stream);
+        case OP_RESLN: return launch_op<OP_RESLN, T>(staged_id, a, h, stream);
+        case OP_LN: return launch_op<OP_LN, T>(staged_id, a, h, stream);
+        case OP_RMS: return launch_op<OP_RMS, T>(staged_id, a, h, stream);
+        case OP_SOFTMAX: return launch_op<OP_SOFTMAX, T>(staged_id, a, h, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_hooked(int kernel_op, int elem, int plan_id, RowArgs a, StagedHooks h,
+                          cudaStream_t stream) {
+    switch (elem) {
+        case ELEM_F32: return launch_type<float>(kernel_op, plan_id, a, h, stream);
+        case ELEM_BF16: return launch_type<__nv_bfloat16>(kernel_op, plan_id, a, h, stream);
+        case ELEM_F16: return launch_type<__half>(kernel_op, plan_id, a, h, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -104,12 +115,13 @@ cudaError_t launch_type(int op, int staged_id, RowArgs a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_staged(int kernel_op, int elem, int plan_id, RowArgs a, cudaStream_t stream) {
-    switch (elem) {
-        case ELEM_F32: return launch_type<float>(kernel_op, plan_id, a, stream);
-        case ELEM_BF16: return launch_type<__nv_bfloat16>(kernel_op, plan_id, a, stream);
-        case ELEM_F16: return launch_type<__half>(kernel_op, plan_id, a, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    return launch_hooked(kernel_op, elem, plan_id, a, StagedHooks{kWaitSpins, 0}, stream);
+}
+
+cudaError_t launch_staged_withheld(int kernel_op, int elem, int plan_id, RowArgs a,
+                                   unsigned int spin_limit, cudaStream_t stream) {
+    if (spin_limit < 1) return cudaErrorInvalidValue;
+    return launch_hooked(kernel_op, elem, plan_id, a, StagedHooks{spin_limit, 1}, stream);
 }
 
 cudaError_t status_staged(unsigned int *value, cudaStream_t stream) {

@@ -20,20 +20,33 @@
 // multiple of 16 bytes long (width * sizeof(T) % 16 == 0, bases 16-byte
 // aligned), K * W * EV >= width, S >= 2.
 //
-// Waits are bounded: a wait that does not complete within kWaitSpins polls
-// sets STATUS_WAIT_TIMEOUT in the op's device status word and a CTA-wide
-// abort flag; from then on no thread of the CTA waits and no copy is issued
-// (the CTA's outputs are then invalid, which the status word reports), so no
-// wait can hang the GPU.
+// Waits are bounded: a wait that does not complete within `spin_limit`
+// polls (kWaitSpins in every library call) sets STATUS_WAIT_TIMEOUT in the
+// op's device status word and a CTA-wide abort flag; from then on no thread
+// of the CTA waits and no copy is issued (the CTA's outputs are then
+// invalid, which the status word reports), so no wait can hang the GPU.
+// Before an aborted CTA exits, thread 0 waits (again bounded) for every copy
+// it issued that no wait has seen complete, so no bulk copy is still landing
+// in shared memory the CTA no longer owns; a copy that does not complete in
+// that time sets STATUS_DRAIN_TIMEOUT as well.
 #pragma once
 
 #include "row_kernel.cuh"
 
 namespace tile {
 
-enum { STATUS_WAIT_TIMEOUT = 2u };
+enum { STATUS_WAIT_TIMEOUT = 2u, STATUS_DRAIN_TIMEOUT = 4u };
 constexpr int kMaxStages = 8;
 constexpr unsigned int kWaitSpins = 1u << 20;
+
+// Launch-time settings of the staged kernel.  Library calls use
+// {kWaitSpins, 0}; the test entry point that makes the wait run out passes a
+// short limit and withhold_first = 1, so that no CTA ever issues the copy
+// of its first row (nothing is left in flight for the wait to outlive).
+struct StagedHooks {
+    unsigned int spin_limit;   // polls of a stage barrier before a wait gives up
+    int withhold_first;        // 1: skip the copy of each CTA's first row
+};
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -109,7 +122,8 @@ __device__ __forceinline__ void widen_vec(uint4 t, float (&v)[16 / sizeof(T)]) {
 }
 
 template <int OP, class T, int S, int K>
-__global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int nst) {
+__global__ void __launch_bounds__(32 * S)
+    row_staged_kernel(const RowArgs a, int nst, const StagedHooks hooks) {
     static_assert(S >= 2, "the stage refill relies on the first CTA barrier");
     static_assert(OP == OP_RESLN || OP == OP_LN || OP == OP_RMS || OP == OP_SOFTMAX,
                   "normalisers and softmax");
@@ -159,10 +173,16 @@ __global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int
     __syncthreads();
     volatile int *abort_seen = &abort_flag;
     bool aborted = false;
+    // Thread 0 only: stages with a copy issued that no wait of thread 0 has
+    // seen complete (bit s), and the barrier phase parity of that copy.
+    unsigned int pending = 0, pending_parity = 0;
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
             const long long row = blockIdx.x + s * G;
-            if (row < rows) issue(s, row);
+            if (row < rows && !(hooks.withhold_first && s == 0)) {
+                issue(s, row);
+                pending |= 1u << s;        // phase 0: parity bit stays 0
+            }
         }
     }
 
@@ -177,13 +197,14 @@ __global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int
         if (!aborted) {
             unsigned int spins = 0;
             while (!mbar_try_wait(&full[s], parity)) {
-                if (++spins == kWaitSpins || *abort_seen) {
+                if (++spins == hooks.spin_limit || *abort_seen) {
                     atomicOr(a.status, STATUS_WAIT_TIMEOUT);
                     *abort_seen = 1;
                     aborted = true;
                     break;
                 }
             }
+            if (!aborted) pending &= ~(1u << s);
         }
 
         // ---- stage -> FP32 register stripe ---------------------------------
@@ -238,6 +259,8 @@ __global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int
             if (next < rows) {
                 fence_proxy_async();
                 issue(s, next);
+                pending |= 1u << s;
+                pending_parity = (pending_parity & ~(1u << s)) | ((parity ^ 1u) << s);
             }
         }
 
@@ -322,6 +345,22 @@ __global__ void __launch_bounds__(32 * S) row_staged_kernel(const RowArgs a, int
         for (int k = 0; k < K; ++k) {
             const int i = k * W + tid;
             if (i < nb) Elem<T>::store_vec(yr + EV * i, v[k]);
+        }
+    }
+
+    // ---- drain: only after an abort can a copy still be in flight ---------
+    // (on the normal path every copy issued was waited for by thread 0)
+    if (tid == 0 && pending != 0) {
+        for (int s = 0; s < nst; ++s) {
+            if (((pending >> s) & 1u) == 0) continue;
+            const unsigned int par = (pending_parity >> s) & 1u;
+            unsigned int spins = 0;
+            while (!mbar_try_wait(&full[s], par)) {
+                if (++spins == hooks.spin_limit) {
+                    atomicOr(a.status, STATUS_DRAIN_TIMEOUT);
+                    break;
+                }
+            }
         }
     }
 }

@@ -814,6 +814,28 @@ int tile_run_plan_args_f32(int op, int plan_id, const tile_row_args_t *args, cud
     return run_call_plan(make_call(op, *args), plan_id, stream);
 }
 
+int tile_test_staged_wait_timeout(int op, int plan_id, const tile_row_args_t *args,
+                                  unsigned int spin_limit, cudaStream_t stream) {
+    if (args == nullptr) return TILE_ERR_NULL;
+    const Call c = make_call(op, *args);
+    bool noop = false;
+    const int st = validate(c, &noop);
+    if (st != TILE_OK) return st;
+    if (plan_id < 0 || plan_id >= kAllPlans || !kPlans[plan_id].staged ||
+        !covers(kPlans[plan_id], c.width, c.dtype) || !staged_ok(c))
+        return TILE_ERR_PLAN;
+    if (noop) return TILE_OK;
+    if (grid_of(kPlans[plan_id], c.rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
+    tile::RowArgs a{c.in, c.res, c.gamma, c.beta, c.out, c.out2, c.rows, c.width, c.eps, nullptr};
+    const cudaError_t err = tile::launch_staged_withheld(kernel_op_of(c), c.dtype, plan_id, a,
+                                                         spin_limit < 1 ? 1u : spin_limit, stream);
+    if (err != cudaSuccess) {
+        tile::set_last_cuda_error(static_cast<int>(err));
+        return TILE_ERR_CUDA;
+    }
+    return TILE_OK;
+}
+
 int tile_run_plan_f32(int op, int plan_id, const float *in, const float *residual, float *out,
                       int rows, int width, float eps, cudaStream_t stream) {
     if (op > TILE_OP_SOFTMAX) return TILE_ERR_OP;

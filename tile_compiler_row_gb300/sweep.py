@@ -57,7 +57,8 @@ def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g
     import tile_compiler_row_gb300 as tile
     s = stream.cuda_stream
     a = tile.TileRowArgs()
-    a.in_, a.residual, a.out = x.data_ptr(), r.data_ptr(), y.data_ptr()
+    a.in_, a.out = x.data_ptr(), y.data_ptr()
+    a.residual = r.data_ptr() if r is not None else None
     a.gamma = g.data_ptr() if g is not None else None
     a.beta = None
     a.out2 = y2.data_ptr() if y2 is not None else None
@@ -111,6 +112,67 @@ def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g
     return statistics.median(per)
 
 
+#: ops whose calls take the residual in a sweep: residual LayerNorm always;
+#: affine LayerNorm is timed without one (tile_describe_plan_ex describes
+#: that call).
+USES_RESIDUAL = ("residual_layernorm",)
+
+
+def make_tensors(rows, width, dtype):
+    """Uniform random device inputs of one sweep shape, seeded by the shape."""
+    import torch
+    gen = torch.Generator(device="cuda").manual_seed(rows * 131 + width)
+    x = torch.rand(rows, width, device="cuda", generator=gen) * 2 - 1
+    r = torch.rand(rows, width, device="cuda", generator=gen) * 2 - 1
+    if dtype != "f32":
+        t = torch.bfloat16 if dtype == "bf16" else torch.float16
+        x, r = x.to(t), r.to(t)
+    return {"x": x, "r": r, "y": torch.empty_like(x),
+            "g": torch.rand(width, device="cuda", generator=gen) + 0.5,
+            "y2": torch.empty(rows, device="cuda")}
+
+
+def sweep_entry(lib, op, dtype, rows, width, t, warmup, iters, stream, graph=False):
+    """Every covering 16-byte-vector plan of ``op`` at one shape, timed (µs,
+    median); then the two fastest again in alternating order A B B A: the two
+    runs of A give the A/A noise floor that B's margin is read against."""
+    import tile_compiler_row_gb300 as tile
+    code = tile.OPS[op]
+    r = t["r"] if op in USES_RESIDUAL else None
+    chosen = tile.tile_describe_plan_ex(op, dtype, rows, width)["id"]
+    entry = {"op": op, "rows": rows, "width": width, "selected": chosen, "plans": {},
+             "dtype": dtype,
+             "timing": "cuda graph replay" if graph else "back-to-back launches"}
+    for pid in range(tile.tile_plan_count()):
+        info = tile.tile_plan_info_ex(pid, op, dtype, rows, width)
+        if info is None or info["vec"] == 1 or info["grid"] > 0x7FFFFFFF:
+            continue
+        best_so_far = min(entry["plans"].values(), default=None)
+        us = time_plan(lib, code, pid, t["x"], r, t["y"], rows, width, warmup, iters, stream,
+                       g=t["g"], y2=t["y2"], graph=graph,
+                       cutoff=None if best_so_far is None else 3.0 * best_so_far)
+        entry["plans"][pid] = round(us, 3)
+    best = min(entry["plans"], key=entry["plans"].get)
+    ranked = sorted(entry["plans"], key=entry["plans"].get)
+    if len(ranked) >= 2:
+        a, b = ranked[0], ranked[1]
+        rerun = {a: [], b: []}
+        for pid in (a, b, b, a):
+            rerun[pid].append(round(time_plan(lib, code, pid, t["x"], r, t["y"], rows, width,
+                                              warmup, iters, stream, g=t["g"], y2=t["y2"],
+                                              graph=graph), 3))
+        entry["confirm"] = {
+            "order": [a, b, b, a], "us": {str(a): rerun[a], str(b): rerun[b]},
+            "aa_noise": round(abs(rerun[a][0] - rerun[a][1]) / min(rerun[a]), 4),
+            "margin": round(min(rerun[b]) / min(rerun[a]) - 1.0, 4)}
+    entry["best"] = best
+    scale = 0.5 if dtype != "f32" else 1.0      # 2-byte elements
+    entry["best_gbs"] = round(scale * BYTES[op] * rows * width / (entry["plans"][best] * 1e-6)
+                              / 1e9, 1)
+    entry["selected_over_best"] = round(entry["plans"][chosen] / entry["plans"][best], 4)
+    return entry
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default=None)
@@ -139,54 +201,13 @@ def main(argv=None):
     if args.small:
         todo = list(SMALL)
     for rows, width in todo:
-        n = rows * width
-        gen = torch.Generator(device="cuda").manual_seed(rows * 131 + width)
-        x = torch.rand(rows, width, device="cuda", generator=gen) * 2 - 1
-        r = torch.rand(rows, width, device="cuda", generator=gen) * 2 - 1
-        if args.dtype != "f32":
-            t = torch.bfloat16 if args.dtype == "bf16" else torch.float16
-            x, r = x.to(t), r.to(t)
-        y = torch.empty_like(x)
-        g = torch.rand(width, device="cuda", generator=gen) + 0.5
-        y2 = torch.empty(rows, device="cuda")
+        t = make_tensors(rows, width, args.dtype)
         for op in args.ops.split(","):
-            code = tile.OPS[op]
-            chosen = tile.tile_describe_plan_ex(op, args.dtype, rows, width)["id"]
-            entry = {"op": op, "rows": rows, "width": width, "selected": chosen, "plans": {},
-                     "dtype": args.dtype,
-                     "timing": "cuda graph replay" if args.graph else "back-to-back launches"}
-            for pid in range(tile.tile_plan_count()):
-                info = tile.tile_plan_info_ex(pid, op, args.dtype, rows, width)
-                if info is None or info["vec"] == 1 or info["grid"] > 0x7FFFFFFF:
-                    continue
-                best_so_far = min(entry["plans"].values(), default=None)
-                us = time_plan(lib, code, pid, x, r, y, rows, width, args.warmup, args.iters, stream,
-                               g=g, y2=y2, graph=args.graph,
-                               cutoff=None if best_so_far is None else 3.0 * best_so_far)
-                entry["plans"][pid] = round(us, 3)
-            best = min(entry["plans"], key=entry["plans"].get)
-            ranked = sorted(entry["plans"], key=entry["plans"].get)
-            if len(ranked) >= 2:
-                # the two fastest again, in alternating order A B B A: the two
-                # runs of A give the A/A noise floor that B's margin is read
-                # against
-                a, b = ranked[0], ranked[1]
-                rerun = {a: [], b: []}
-                for pid in (a, b, b, a):
-                    rerun[pid].append(round(time_plan(lib, code, pid, x, r, y, rows, width,
-                                                      args.warmup, args.iters, stream, g=g,
-                                                      y2=y2, graph=args.graph), 3))
-                entry["confirm"] = {
-                    "order": [a, b, b, a], "us": {str(a): rerun[a], str(b): rerun[b]},
-                    "aa_noise": round(abs(rerun[a][0] - rerun[a][1]) / min(rerun[a]), 4),
-                    "margin": round(min(rerun[b]) / min(rerun[a]) - 1.0, 4)}
-            entry["best"] = best
-            scale = 0.5 if args.dtype != "f32" else 1.0      # 2-byte elements
-            entry["best_gbs"] = round(scale * BYTES[op] * n / (entry["plans"][best] * 1e-6) / 1e9, 1)
-            entry["selected_over_best"] = round(entry["plans"][chosen] / entry["plans"][best], 4)
+            entry = sweep_entry(lib, op, args.dtype, rows, width, t, args.warmup, args.iters,
+                                stream, graph=args.graph)
             results.append(entry)
             print(json.dumps(entry), flush=True)
-        del x, r, y, g, y2
+        del t
     assert tile.tile_check_device_status() == 0
     if args.out:
         with open(args.out, "w") as fh:
