@@ -226,6 +226,14 @@ def profile_traffic(op, rows, width, plan_id):
         return None
 
 
+def metric_of(op, rows, width):
+    """The metric name of a run: the headline's for its workload, else the
+    same measure named for the workload that ran."""
+    if (op, rows, width) == ("residual_layernorm", 65536, 4096):
+        return METRIC
+    return f"HBM GB/s and µs/call, {op} FP32 {rows}×{width}"
+
+
 def workload_config(op, rows, width, world):
     """The ``config`` object of the JSON line: the workload alone, the same
     in both arms (plan and host-thread details go in their own keys)."""
@@ -351,8 +359,7 @@ def run_ours(args, dist):
     achieved = nbytes / (kernel_ms / 1e3) / 1e9
     traffic = profile_traffic(op, rows, width, plan["id"])
     line = {
-        "metric": METRIC if (op, rows, width) == ("residual_layernorm", 65536, 4096) else
-        f"HBM GB/s and µs/call, {op} FP32 {rows}×{width}",
+        "metric": metric_of(op, rows, width),
         "value": round(value, 2), "unit": UNIT, "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "us_per_call": round(ms_per_step * 1e3, 3),
@@ -750,8 +757,7 @@ def run_reference(args, dist):
     sample = f"all {n} rows x {width} per step, FP64 C, row blocks on {cores} threads"
     line = {
         "impl": "reference",
-        "metric": METRIC if (op, rows, width) == ("residual_layernorm", 65536, 4096) else
-        f"HBM GB/s and µs/call, {op} FP32 {rows}×{width}",
+        "metric": metric_of(op, rows, width),
         "value": round(value, 4), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total / args.steps * 1e3, 4),

@@ -85,3 +85,22 @@ def compare_full(got, op, x, r=None, eps=EPS, what="", block_rows=1024):
         ea, er = compare(got[a:b], ref, f"{what} rows {a}..{b - 1}")
         worst_abs, worst_rel = max(worst_abs, ea), max(worst_rel, er)
     return worst_abs, worst_rel
+
+
+def staged_table(op):
+    """The 2-byte selector's measured staged-plan table for `op` (a table op
+    name of the selector generator, e.g. "layernorm_affine+residual"), read
+    from the generated header: [(widest width, plan or -1)]."""
+    import re
+    from tile_compiler_row_gb300 import selector_tables
+    text = open(selector_tables.HEADER).read()
+    m = re.search(r"kB16Staged%s\[\] = \{(.*?)\};" % selector_tables.STEM[op], text)
+    return [(int(a), int(b)) for a, b in re.findall(r"\{(\d+), (-?\d+)\}", m.group(1))]
+
+
+def expects_staged(op, rows, width):
+    """Whether the selector should take a staged plan for 2-byte rows of
+    whole 16-byte vectors on aligned pointers (large problems only)."""
+    if rows * width <= (1 << 22) or width % 8:
+        return False
+    return next(p for w, p in staged_table(op) if width <= w) >= 0

@@ -97,14 +97,18 @@ def _bench(args, env_extra=None):
 
 def test_reference_arm_prints_one_contract_line():
     """`bench.py --impl reference`: the FP64 oracle on the host cores, one
-    JSON line with the headline's metric and unit, no GPU work."""
+    JSON line with the metric and unit our arm prints for the same workload
+    (and the same config object), no GPU work."""
     sys.path.insert(0, ROOT)
     import bench
     out = _bench(["--impl", "reference", "--steps", "3", "--warmup", "3", "--rows", "2048",
                   "--width", "512"])
     assert len(out) == 1
     d = out[0]
-    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["impl"] == "reference" and d["unit"] == "GB/s"
+    assert d["metric"] == bench.metric_of("residual_layernorm", 2048, 512)
+    assert bench.metric_of("residual_layernorm", 65536, 4096) == bench.METRIC
+    assert d["config"] == bench.workload_config("residual_layernorm", 2048, 512, 1)
     assert d["value"] > 0 and d["steps"] == 3 and d["warmup"] == 3
     assert d["higher_is_better"] is True and d["gpu_launches"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1

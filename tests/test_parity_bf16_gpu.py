@@ -21,7 +21,7 @@ import torch
 import oracle
 import synth
 import tile_compiler_row_gb300 as tile
-from parity import ATOL, EPS, RTOL, oracle_blocks, ref_eps
+from parity import ATOL, EPS, RTOL, oracle_blocks, ref_eps, expects_staged
 
 pytestmark = pytest.mark.gpu
 
@@ -202,9 +202,8 @@ def test_bf16_selected_staged_plans(op, rows, width):
         else:
             getattr(tile, f"tile_{op}_bf16")(_placed(x, off), out, EPS)
         check_bf16(out, ref, what=f"bf16 {op} {rows}x{width} offset {off}")
-    # The sweep found the staged kernel faster only for these BF16 shapes.
-    staged = (op == "residual_layernorm" or (op == "layernorm" and width >= 8192)
-              or (op == "rmsnorm" and width == 12288))
+    # the staged kernel exactly where the measured table takes it
+    staged = expects_staged(op, rows, width)
     assert (tile.tile_describe_plan_ex(op, "bf16", rows, width)["path"] == 2) == staged
 
 
@@ -279,4 +278,4 @@ def test_bf16_residual_affine_and_weighted_on_staged_plans(rows, width):
     ref = oracle.get().rmsnorm_weighted(xf, g, eps=ref_eps())
     check_bf16(out, ref, what=f"bf16 weighted {rows}x{width}")
     staged = tile.tile_describe_plan_ex("rmsnorm_weighted", "bf16", rows, width)["path"] == 2
-    assert staged == (width == 12288)
+    assert staged == expects_staged("rmsnorm_weighted", rows, width)

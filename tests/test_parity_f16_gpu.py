@@ -23,7 +23,7 @@ import torch
 import oracle
 import synth
 import tile_compiler_row_gb300 as tile
-from parity import ATOL, EPS, RTOL, ref_eps
+from parity import ATOL, EPS, RTOL, ref_eps, expects_staged
 
 pytestmark = pytest.mark.gpu
 
@@ -205,9 +205,8 @@ def test_f16_selected_staged_plans(op, rows, width):
         else:
             getattr(tile, f"tile_{op}_f16")(_placed(x, off), out, EPS)
         check_f16(out, ref, what=f"f16 {op} {rows}x{width} offset {off}")
-    # The sweep found the staged kernel faster only for these FP16 shapes.
-    staged = (op == "residual_layernorm" or (op == "layernorm" and width >= 8192)
-              or (op == "rmsnorm" and width == 12288))
+    # the staged kernel exactly where the measured table takes it
+    staged = expects_staged(op, rows, width)
     assert (tile.tile_describe_plan_ex(op, "f16", rows, width)["path"] == 2) == staged
 
 

@@ -7,10 +7,10 @@ These tests parse that summary and check, without a GPU, that the library
 still selects the recorded plan at every recorded shape (so the tables in
 the source and the evidence cannot drift apart), that the evidence covers
 every bucket the library reports today, and that every selected plan was
-within 3 % of the fastest plan measured there (the tables take the fastest
-plan, or one within about 1 % of it that also wins the neighbouring
-widths; 3 % allows for run-to-run noise between the sweep the tables were
-frozen from and this one)."""
+within 5 % of the fastest plan measured there (the generated tables take
+the fastest plan of the sweeps they were made from, or the previous plan
+within 0.5 % of it; 5 % allows for run-to-run and GPU-to-GPU differences
+between those sweeps and this independent one)."""
 
 import os
 import re
@@ -22,7 +22,7 @@ from tile_compiler_row_gb300 import _build, selector_evidence
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUMMARY = os.path.join(ROOT, "profiles", "selector_sweep.md")
-WITHIN = 1.03
+WITHIN = 1.05
 
 
 def _rows(section):
@@ -74,6 +74,6 @@ def test_every_bucket_of_the_selector_has_a_line_of_evidence():
                 assert (op, dtype, lo, hi) in have, f"no evidence for {op} {dtype} {lo}-{hi} (plan {pid})"
 
 
-def test_every_selected_plan_was_within_3_percent_of_the_fastest():
+def test_every_selected_plan_was_within_5_percent_of_the_fastest():
     slow = [e for e in large() + small() if e["ratio"] > WITHIN]
     assert not slow, f"selected plans slower than {WITHIN} x the fastest: {slow}"

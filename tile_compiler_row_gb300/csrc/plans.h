@@ -80,9 +80,16 @@
     X(44, 4, 4, 48)         \
     X(45, 4, 8, 48)         \
     X(46, 2, 8, 32)         \
-    X(47, 4, 4, 32)
+    X(47, 4, 4, 32)         \
+    /* more workers, shorter stripes: fewer gamma/beta registers per    */ \
+    /* thread where the 2-byte affine rows keep them across rows        */ \
+    X(48, 8, 2, 48)         \
+    X(49, 8, 2, 96)         \
+    X(50, 16, 1, 64)        \
+    X(51, 16, 2, 100)       \
+    X(52, 4, 2, 32)
 
-#define TILE_STAGED_COUNT 8
+#define TILE_STAGED_COUNT 13
 
 // Widest row covered by both a V = 4 and a V = 1 plan.
 #define TILE_MAX_WIDTH 131072

@@ -44,21 +44,24 @@ int sm_count(cudaError_t *err) {
     return v;
 }
 
-template <int OP, class T, int S, int K, int KB>
-cudaError_t launch_one(RowArgs a, StagedHooks hooks, cudaStream_t stream) {
-    constexpr int EV = 16 / sizeof(T);
-    if constexpr (K * EV > 64) {
-        (void)a;
-        (void)hooks;
-        (void)stream;
-        return cudaErrorInvalidValue;     // not built: stripe above 64 floats
-    } else {
+// Whether a plan keeps gamma/beta in registers across rows: 2-byte rows
+// (where reloading them per row costs the most against the row's bytes),
+// the normalisers, and a stripe of at most 32 floats (gamma and beta then
+// take 64 registers more).
+template <int OP, class T, int K>
+constexpr bool resident_params() {
+    return sizeof(T) == 2 && OP != OP_SOFTMAX && K * (16 / sizeof(T)) <= 32;
+}
+
+template <int OP, class T, int S, int K, int KB, bool AFF>
+cudaError_t launch_kernel(RowArgs a, StagedHooks hooks, cudaStream_t stream) {
+    {
         cudaError_t err = cudaSuccess;
         a.status = status_address(&err);
         if (a.status == nullptr) return err;
         const int sms = sm_count(&err);
         if (sms == 0) return err;
-        auto kernel = row_staged_kernel<OP, T, S, K>;
+        auto kernel = row_staged_kernel<OP, T, S, K, AFF>;
         const int nin = (OP == OP_RESLN) ? 2 : 1;
         const size_t stage = static_cast<size_t>(a.width) * sizeof(T) * nin;
         // as many stages as fit the plan's budget of KB kilobytes, 1 to 8
@@ -77,6 +80,22 @@ cudaError_t launch_one(RowArgs a, StagedHooks hooks, cudaStream_t stream) {
         if (grid > a.rows) grid = a.rows;
         kernel<<<static_cast<unsigned int>(grid), 32 * S, dyn, stream>>>(a, nst, hooks);
         return cudaGetLastError();
+    }
+}
+
+template <int OP, class T, int S, int K, int KB>
+cudaError_t launch_one(RowArgs a, StagedHooks hooks, cudaStream_t stream) {
+    constexpr int EV = 16 / sizeof(T);
+    if constexpr (K * EV > 64) {
+        (void)a;
+        (void)hooks;
+        (void)stream;
+        return cudaErrorInvalidValue;     // not built: stripe above 64 floats
+    } else if constexpr (resident_params<OP, T, K>()) {
+        if (a.gamma != nullptr) return launch_kernel<OP, T, S, K, KB, true>(a, hooks, stream);
+        return launch_kernel<OP, T, S, K, KB, false>(a, hooks, stream);
+    } else {
+        return launch_kernel<OP, T, S, K, KB, false>(a, hooks, stream);
     }
 }
 

@@ -121,7 +121,12 @@ __device__ __forceinline__ void widen_vec(uint4 t, float (&v)[16 / sizeof(T)]) {
     }
 }
 
-template <int OP, class T, int S, int K>
+// AFF: affine LayerNorm / weighted RMSNorm with each thread's gamma (and
+// beta) columns loaded into registers once, before the CTA's first row, and
+// kept for every row it normalises (the other instantiations load gamma and
+// beta again for every row).  The per-element arithmetic is the same FMA
+// either way, so the results are bitwise those of the other paths.
+template <int OP, class T, int S, int K, bool AFF = false>
 __global__ void __launch_bounds__(32 * S)
     row_staged_kernel(const RowArgs a, int nst, const StagedHooks hooks) {
     static_assert(S >= 2, "the stage refill relies on the first CTA barrier");
@@ -182,6 +187,30 @@ __global__ void __launch_bounds__(32 * S)
             if (row < rows && !(hooks.withhold_first && s == 0)) {
                 issue(s, row);
                 pending |= 1u << s;        // phase 0: parity bit stays 0
+            }
+        }
+    }
+
+    // gamma / beta of this thread's columns, for every row (AFF only)
+    static_assert(!AFF || OP != OP_SOFTMAX, "softmax has no affine form");
+    float gam[AFF ? K : 1][AFF ? EV : 1], bet[AFF ? K : 1][AFF ? EV : 1];
+    if constexpr (AFF) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int i = k * W + tid;
+#pragma unroll
+            for (int q = 0; q < EV / 4; ++q) {
+                float4 g4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                float4 b4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (i < nb) {
+                    g4 = __ldg(reinterpret_cast<const float4 *>(a.gamma + EV * i) + q);
+                    if (a.beta != nullptr)
+                        b4 = __ldg(reinterpret_cast<const float4 *>(a.beta + EV * i) + q);
+                }
+                gam[k][4 * q] = g4.x; gam[k][4 * q + 1] = g4.y;
+                gam[k][4 * q + 2] = g4.z; gam[k][4 * q + 3] = g4.w;
+                bet[k][4 * q] = b4.x; bet[k][4 * q + 1] = b4.y;
+                bet[k][4 * q + 2] = b4.z; bet[k][4 * q + 3] = b4.w;
             }
         }
     }
@@ -316,7 +345,12 @@ __global__ void __launch_bounds__(32 * S)
         }
 
         // optional per-column scale and shift (gamma/beta FP32, 16-byte aligned)
-        if constexpr (OP == OP_RESLN || OP == OP_LN || OP == OP_RMS) {
+        if constexpr (AFF) {
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int j = 0; j < EV; ++j) v[k][j] = fmaf(v[k][j], gam[k][j], bet[k][j]);
+        } else if constexpr (OP == OP_RESLN || OP == OP_LN || OP == OP_RMS) {
             if (a.gamma != nullptr) {
 #pragma unroll
                 for (int k = 0; k < K; ++k) {

@@ -66,101 +66,45 @@ int max_width_of(const PlanDesc &p, int dtype = TILE_DTYPE_F32) {
 }
 
 // Selector: for each op, the first entry whose width bound covers the row.
-// The float4 tables (16-byte co-aligned pointers) are frozen from the
-// measured plan sweep on GB300 (sweep.py: every covering plan timed with
-// CUDA events at about 2^26 elements per tensor for each width of a ladder,
-// plus the small workload shapes and 65536 x 4096); each bucket takes the
-// fastest plan, or one within 1 % of it that also wins the neighbouring
-// widths.  Pointers with different 16-byte phases use the scalar plans.
+// The tables (16-byte co-aligned pointers) are generated from a measured
+// plan sweep on GB300 (selector_tables.py: every built plan timed at each
+// width of a ladder, about 2^26 FP32 / 2^27 2-byte elements per tensor,
+// plus the small workload shapes), so measurement, not a score, picks each
+// mapping; profiles/selector_sweep.md holds an independent sweep of every
+// bucket.  Pointers with different 16-byte phases use the scalar plans.
 struct Bucket {
     int max_width;
     int plan;
 };
 
-// Residual LayerNorm at 3588-4099 columns takes plan 10 (8 warps, K = 8:
-// half its stripe is empty at 4096), which an alternating A/B against plan 7
-// measured 0.9-2.3 % faster from 16384 rows up and 0.4 % slower at 3584
-// columns; L2-resident problems keep plan 7 (kSmallResidualLN).
-constexpr Bucket kVec4ResidualLN[] = {
-    {131, 0}, {259, 1}, {515, 39}, {1027, 4}, {1540, 37}, {2051, 6}, {3075, 35}, {3587, 7},
-    {4099, 10}, {8195, 10}, {12291, 31}, {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 20},
+#include "selector_tables.h"
+
+struct Table {
+    const Bucket *b;
+    int n;
 };
-constexpr Bucket kVec4LN[] = {
-    {131, 0}, {259, 1}, {515, 2}, {1027, 4}, {2051, 6}, {4099, 7},
-    {8195, 10}, {16387, 31}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
-};
-// RMSNorm at 3076-4099 columns: plan 32 (K = 16) measured 1-2 % faster than
-// plan 10 in an alternating A/B at 3968 and 4096 columns.
-constexpr Bucket kVec4RMS[] = {
-    {131, 0}, {259, 2}, {515, 39}, {1027, 6}, {1540, 35}, {2051, 5}, {3075, 8}, {4099, 32},
-    {8195, 10},
-    {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
-};
-constexpr Bucket kVec4Softmax[] = {
-    {131, 0}, {259, 1}, {515, 2}, {1027, 3}, {2051, 6}, {4099, 7},
-    {8195, 10}, {16387, 31}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
-};
-// Affine LayerNorm (with or without residual), weighted RMSNorm, and the
-// row reductions (sum, min/max), from the same sweep.
-constexpr Bucket kVec4Affine[] = {
-    {131, 0}, {259, 1}, {515, 39}, {1540, 37}, {2051, 6}, {4099, 7},
-    {8195, 10}, {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 20},
-};
-constexpr Bucket kVec4Weighted[] = {
-    {131, 0}, {515, 2}, {1027, 4}, {1540, 6}, {2051, 5}, {4099, 8},
-    {8195, 10}, {16387, 14}, {32771, 17}, {65539, 19}, {TILE_MAX_WIDTH, 30},
-};
-constexpr Bucket kVec4RowReduce[] = {
-    {131, 0}, {259, 1}, {515, 2}, {1027, 39}, {1540, 37}, {2051, 6}, {3075, 35}, {4099, 7},
-    {6147, 32}, {8195, 10}, {16387, 31}, {32771, 34}, {65539, 33}, {TILE_MAX_WIDTH, 30},
-};
-// Small problems (rows * width <= kSmallElems, L2 resident): the few
-// buckets where the CUDA-graph sweep of the small workload shapes picked a
-// different plan than the large-row sweep; other widths use the tables above.
+#define TILE_TABLE(name) Table{name, static_cast<int>(sizeof(name) / sizeof(Bucket))}
+#define TILE_TABLES(fam, kind)                                                              \
+    {TILE_TABLE(k##fam##kind##ResidualLN), TILE_TABLE(k##fam##kind##LN),                     \
+     TILE_TABLE(k##fam##kind##RMS),        TILE_TABLE(k##fam##kind##Softmax),                \
+     TILE_TABLE(k##fam##kind##RowSum),     TILE_TABLE(k##fam##kind##RowMinmax),              \
+     TILE_TABLE(k##fam##kind##Affine),     TILE_TABLE(k##fam##kind##Weighted),               \
+     TILE_TABLE(k##fam##kind##ResidualAffine)}
+// Indexed by table op: the TILE_OP_* code, and 8 for affine LayerNorm with
+// a residual (three row streams instead of two).
+constexpr Table kRegF32[9] = TILE_TABLES(F32, Reg);
+constexpr Table kStagedF32[9] = TILE_TABLES(F32, Staged);
+constexpr Table kRegB16[9] = TILE_TABLES(B16, Reg);        // BF16 and FP16 rows
+constexpr Table kStagedB16[9] = TILE_TABLES(B16, Staged);
+constexpr Table kTinyF32[9] = TILE_TABLES(F32, Tiny);
+constexpr Table kSmallF32[9] = TILE_TABLES(F32, Small);
+#undef TILE_TABLES
+#undef TILE_TABLE
+
+// Small problems: rows * width <= kSmallElems (L2 resident), in two tiers
+// (up to kTinyElems, and above).
 constexpr long long kSmallElems = 1LL << 22;
-constexpr Bucket kSmallResidualLN[] = {{3075, -1}, {4099, 7}, {32771, -1}, {65539, 33}};
-constexpr Bucket kSmallLN[] = {{131, -1}, {259, 2}, {4099, -1}, {8195, 32}, {32771, -1}, {65539, 33}};
-constexpr Bucket kSmallRMS[] = {{1027, -1}, {2051, 6}, {3075, -1}, {4099, 7}, {32771, -1}, {65539, 33}};
-constexpr Bucket kSmallSoftmax[] = {{32771, -1}, {65539, 33}};
-
-// BF16 rows (16-byte vectors of 8 values), from the BF16 sweep.  Weighted
-// RMSNorm uses the RMSNorm table, affine LayerNorm the LayerNorm table.
-constexpr Bucket kBf16ResidualLN[] = {
-    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {4103, 6}, {8199, 8},
-    {16391, 10}, {32775, 13}, {65543, 17}, {TILE_MAX_WIDTH, 33},
-};
-constexpr Bucket kBf16LN[] = {
-    {263, 0}, {519, 1}, {1031, 2}, {1543, 39}, {2055, 4}, {4103, 6}, {8199, 8},
-    {16391, 10}, {32775, 14}, {65543, 17}, {TILE_MAX_WIDTH, 19},
-};
-constexpr Bucket kBf16RMS[] = {
-    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {3079, 37}, {4103, 6}, {6151, 7}, {8199, 8},
-    {16391, 11}, {32775, 13}, {65543, 17}, {TILE_MAX_WIDTH, 19},
-};
-constexpr Bucket kBf16Softmax[] = {
-    {263, 0}, {519, 1}, {1031, 2}, {2055, 4}, {3079, 37}, {4103, 6}, {8199, 7},
-    {16391, 10}, {32775, 15}, {65543, 16}, {TILE_MAX_WIDTH, 18},
-};
-constexpr Bucket kBf16RowReduce[] = {
-    {263, 0}, {519, 1}, {1031, 2}, {1543, 39}, {2055, 4}, {4103, 37}, {8199, 7},
-    {16391, 10}, {32775, 15}, {65543, 17}, {TILE_MAX_WIDTH, 19},
-};
-
-// BF16 rows of whole 16-byte vectors on 16-byte aligned pointers, more than
-// kSmallElems elements: the widths where a shared-memory-staged plan beat
-// every register plan in the BF16 sweep (residual LayerNorm 65536x4096:
-// 269 us vs 322 us; 4096x16384: 66 us vs 125 us).  -1: use the table above.
-// (BF16 softmax, with its base-2 exponential, is fastest on register plans.)
-constexpr Bucket kStagedBf16ResidualLN[] = {{1024, -1}, {2048, 46}, {3072, 44}, {4096, 45},
-                                            {6144, 42}, {8192, 45}, {16384, 43}};
-constexpr Bucket kStagedBf16LN[] = {{4096, -1}, {6144, 45}, {8192, 42}, {16384, 43}};
-constexpr Bucket kStagedBf16RMS[] = {{8192, -1}, {12288, 43}};
-// Affine LayerNorm with a residual (three 2-byte streams, plus gamma and
-// beta): the staged plan measured 28 % faster than register plan 10 at 12288
-// and 16384 columns; without a residual the register plans win or tie.
-// Weighted RMSNorm follows kStagedBf16RMS (staged 10 % faster at 12288,
-// 10 % slower at 16384).
-constexpr Bucket kStagedBf16ResidualAffine[] = {{8192, -1}, {16384, 43}};
+constexpr long long kTinyElems = 1LL << 19;
 
 constexpr Bucket kVec1[] = {
     {128, 25}, {1024, 26}, {4096, 27}, {16384, 28}, {TILE_MAX_WIDTH, 29},
@@ -173,57 +117,35 @@ int pick(const Bucket (&table)[N], int width) {
     return -1;
 }
 
+int pick(const Table &t, int width) {
+    for (int i = 0; i < t.n; ++i)
+        if (width <= t.b[i].max_width) return t.b[i].plan;
+    return -1;
+}
+
+int table_op(int op, bool residual) {
+    return (op == TILE_OP_LAYERNORM_AFFINE && residual) ? 8 : op;
+}
+
+// staged_eligible: every pointer 16-byte aligned (rows of whole vectors are
+// checked by covers()); residual: affine LayerNorm called with a residual.
 int select_plan(int op, long long rows, int width, bool vec4, int dtype,
                 bool staged_eligible = false, bool residual = false) {
     if (!vec4) return pick(kVec1, width);
-    if (two_byte(dtype)) {     // FP16 rows share the BF16 tables (same geometry)
-        if (staged_eligible && rows * static_cast<long long>(width) > kSmallElems) {
-            int sid = -1;
-            switch (op) {
-                case TILE_OP_RESIDUAL_LAYERNORM: sid = pick(kStagedBf16ResidualLN, width); break;
-                case TILE_OP_LAYERNORM: sid = pick(kStagedBf16LN, width); break;
-                case TILE_OP_RMSNORM:
-                case TILE_OP_RMSNORM_WEIGHTED: sid = pick(kStagedBf16RMS, width); break;
-                case TILE_OP_LAYERNORM_AFFINE:
-                    if (residual) sid = pick(kStagedBf16ResidualAffine, width);
-                    break;
-                default: break;
-            }
-            if (sid >= 0 && covers(kPlans[sid], width, dtype)) return sid;
-        }
-        int id;
-        switch (op) {
-            case TILE_OP_RESIDUAL_LAYERNORM: id = pick(kBf16ResidualLN, width); break;
-            case TILE_OP_LAYERNORM:
-            case TILE_OP_LAYERNORM_AFFINE: id = pick(kBf16LN, width); break;
-            case TILE_OP_SOFTMAX: id = pick(kBf16Softmax, width); break;
-            case TILE_OP_ROW_SUM:
-            case TILE_OP_ROW_MINMAX: id = pick(kBf16RowReduce, width); break;
-            default: id = pick(kBf16RMS, width); break;
-        }
-        return (id >= 0 && covers(kPlans[id], width, dtype)) ? id : -1;
+    const int t = table_op(op, residual);
+    const bool b16 = two_byte(dtype);      // FP16 rows share the BF16 tables
+    const long long elems = rows * static_cast<long long>(width);
+    const bool small = elems <= kSmallElems;
+    if (staged_eligible && !small) {
+        const int sid = pick(b16 ? kStagedB16[t] : kStagedF32[t], width);
+        if (sid >= 0 && covers(kPlans[sid], width, dtype)) return sid;
     }
-    if (rows * static_cast<long long>(width) <= kSmallElems) {
-        int id = -1;
-        switch (op) {
-            case TILE_OP_RESIDUAL_LAYERNORM: id = pick(kSmallResidualLN, width); break;
-            case TILE_OP_LAYERNORM: id = pick(kSmallLN, width); break;
-            case TILE_OP_RMSNORM: id = pick(kSmallRMS, width); break;
-            case TILE_OP_SOFTMAX: id = pick(kSmallSoftmax, width); break;
-            default: break;
-        }
+    if (small && !b16) {
+        const int id = pick(elems <= kTinyElems ? kTinyF32[t] : kSmallF32[t], width);
         if (id >= 0) return id;
     }
-    switch (op) {
-        case TILE_OP_RESIDUAL_LAYERNORM: return pick(kVec4ResidualLN, width);
-        case TILE_OP_LAYERNORM: return pick(kVec4LN, width);
-        case TILE_OP_LAYERNORM_AFFINE: return pick(kVec4Affine, width);
-        case TILE_OP_RMSNORM: return pick(kVec4RMS, width);
-        case TILE_OP_RMSNORM_WEIGHTED: return pick(kVec4Weighted, width);
-        case TILE_OP_ROW_SUM:
-        case TILE_OP_ROW_MINMAX: return pick(kVec4RowReduce, width);
-        default: return pick(kVec4Softmax, width);
-    }
+    const int id = pick(b16 ? kRegB16[t] : kRegF32[t], width);
+    return (id >= 0 && covers(kPlans[id], width, dtype)) ? id : -1;
 }
 
 long long grid_of(const PlanDesc &p, long long rows) {

@@ -146,23 +146,34 @@ def summary(paths):
         "time over the best plan's (1 = the selector picked the fastest).",
         "Affine LayerNorm is timed without a residual (the call",
         "`tile_describe_plan_ex` describes); BF16/FP16 rows of whole vectors on",
-        "16-byte aligned pointers may take the shared-memory-staged plans (40-47).",
+        "16-byte aligned pointers may take the shared-memory-staged plans (40-52).",
         "The second table is the small, L2-resident workload shapes (FP32), timed",
         "from CUDA graph replays of 200 calls.",
+        "",
+        "Over all rows: {n} buckets and shapes, selected/best mean {mean:.4f},",
+        "maximum {worst:.4f}; {over3} rows above 1.03.",
         "",
         "Command (one GB300):",
         "",
         "    python -m tile_compiler_row_gb300.selector_evidence sweep --out ev.json",
         "    python -m tile_compiler_row_gb300.selector_evidence summary ev.json",
         "",
-        "tests/test_selector_evidence.py parses the tables: the library must still",
-        "select the recorded plan at every row's shape.",
+        "The selector's tables were generated from other sweeps",
+        "(`tile_compiler_row_gb300/selector_tables.py`); this one is an independent",
+        "run on another GB300 lease. tests/test_selector_evidence.py parses the",
+        "tables: the library must still select the recorded plan at every row's",
+        "shape, and every selected plan must be within 5 % of the fastest.",
         "",
         "## Large problems",
         "",
         "| op | dtype | widths | width | rows | selected | µs | best | µs | 2nd | µs | A/A | margin | sel/best |",
         "|---|---|---|---:|---:|---:|---:|---:|---:|---:|---:|---:|---:|---:|",
     ]
+
+    ratios = [e["selected_over_best"] for e in records]
+    lines = [ln.format(n=len(ratios), mean=sum(ratios) / len(ratios), worst=max(ratios),
+                       over3=sum(r > 1.03 for r in ratios)) if "{" in ln else ln
+             for ln in lines]
 
     def fmt(v, nd=3):
         return "—" if v is None else (f"{v:.{nd}f}" if isinstance(v, float) else str(v))

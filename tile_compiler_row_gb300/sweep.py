@@ -23,7 +23,8 @@ OPS = ("residual_layernorm", "layernorm", "rmsnorm", "softmax")
 MORE_OPS = ("row_sum", "row_minmax", "layernorm_affine", "rmsnorm_weighted")
 #: algorithmic bytes per element (row outputs and gamma/beta are negligible)
 BYTES = {"residual_layernorm": 12, "layernorm": 8, "rmsnorm": 8, "softmax": 8, "row_sum": 4,
-         "row_minmax": 4, "layernorm_affine": 8, "rmsnorm_weighted": 8}
+         "row_minmax": 4, "layernorm_affine": 8, "rmsnorm_weighted": 8,
+         "layernorm_affine+residual": 12}
 
 #: widths of the sweep ladder; ``rows`` fills about 2**26 elements per tensor
 #: (256 MiB, well above L2) so the large-row regime is HBM bound.
@@ -132,20 +133,25 @@ def make_tensors(rows, width, dtype):
             "y2": torch.empty(rows, device="cuda")}
 
 
-def sweep_entry(lib, op, dtype, rows, width, t, warmup, iters, stream, graph=False):
+def sweep_entry(lib, op, dtype, rows, width, t, warmup, iters, stream, graph=False,
+                only=None):
     """Every covering 16-byte-vector plan of ``op`` at one shape, timed (µs,
     median); then the two fastest again in alternating order A B B A: the two
     runs of A give the A/A noise floor that B's margin is read against."""
     import tile_compiler_row_gb300 as tile
-    code = tile.OPS[op]
-    r = t["r"] if op in USES_RESIDUAL else None
-    chosen = tile.tile_describe_plan_ex(op, dtype, rows, width)["id"]
+    base = op.split("+")[0]          # "layernorm_affine+residual": with a residual
+    code = tile.OPS[base]
+    r = t["r"] if (op in USES_RESIDUAL or op.endswith("+residual")) else None
+    # the selector's choice, where tile_describe_plan_ex can describe the call
+    chosen = tile.tile_describe_plan_ex(base, dtype, rows, width)["id"] if base == op else None
     entry = {"op": op, "rows": rows, "width": width, "selected": chosen, "plans": {},
              "dtype": dtype,
              "timing": "cuda graph replay" if graph else "back-to-back launches"}
     for pid in range(tile.tile_plan_count()):
-        info = tile.tile_plan_info_ex(pid, op, dtype, rows, width)
+        info = tile.tile_plan_info_ex(pid, base, dtype, rows, width)
         if info is None or info["vec"] == 1 or info["grid"] > 0x7FFFFFFF:
+            continue
+        if only is not None and pid not in only:
             continue
         best_so_far = min(entry["plans"].values(), default=None)
         us = time_plan(lib, code, pid, t["x"], r, t["y"], rows, width, warmup, iters, stream,
@@ -169,7 +175,8 @@ def sweep_entry(lib, op, dtype, rows, width, t, warmup, iters, stream, graph=Fal
     scale = 0.5 if dtype != "f32" else 1.0      # 2-byte elements
     entry["best_gbs"] = round(scale * BYTES[op] * rows * width / (entry["plans"][best] * 1e-6)
                               / 1e9, 1)
-    entry["selected_over_best"] = round(entry["plans"][chosen] / entry["plans"][best], 4)
+    entry["selected_over_best"] = (round(entry["plans"][chosen] / entry["plans"][best], 4)
+                                   if chosen is not None and chosen in entry["plans"] else None)
     return entry
 
 
@@ -185,7 +192,10 @@ def main(argv=None):
                     help="time calls replayed from a CUDA graph (no host launch overhead)")
     ap.add_argument("--small", action="store_true", help="only the small workload shapes")
     ap.add_argument("--dtype", default="f32", choices=("f32", "bf16", "f16"))
+    ap.add_argument("--plans", default=None,
+                    help="comma list of plan ids to time (default: every covering plan)")
     args = ap.parse_args(argv)
+    only = None if args.plans is None else {int(p) for p in args.plans.split(",")}
 
     import torch
 
@@ -204,7 +214,7 @@ def main(argv=None):
         t = make_tensors(rows, width, args.dtype)
         for op in args.ops.split(","):
             entry = sweep_entry(lib, op, args.dtype, rows, width, t, args.warmup, args.iters,
-                                stream, graph=args.graph)
+                                stream, graph=args.graph, only=only)
             results.append(entry)
             print(json.dumps(entry), flush=True)
         del t
