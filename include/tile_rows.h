@@ -460,6 +460,21 @@ int tile_plan_info(int id, int op, int rows, int width, tile_plan_t *plan);
  * which only the register plans implement. */
 int tile_plan_info_ex(int id, int op, int dtype, int rows, int width, tile_plan_t *plan);
 
+/* Test hook for failure detection without a GPU fault (the notes have no
+ * counterpart: their runner has no error path to test).  After `skip` more
+ * launch attempts that proceed normally, the next `count` kernel launch
+ * attempts of the library's entry points fail on the host with the CUDA
+ * error `cuda_error` (a nonzero cudaError_t value) instead of launching:
+ * the entry point returns TILE_ERR_CUDA and tile_last_cuda_error() on that
+ * thread gives `cuda_error`.  Argument errors are still reported first.
+ * Nothing reaches the GPU for an injected failure; work the same call
+ * enqueued before it (copies and kernels of earlier chunks of
+ * tile_run_host_f32 / tile_run_host_static_f32) stays enqueued, and the
+ * caller's stream stays ordered after it.  count = 0 disarms.  Process-wide,
+ * thread-safe, host only.  Returns TILE_OK, or TILE_ERR_SHAPE for a negative
+ * skip or count, or a zero error with count > 0. */
+int tile_inject_launch_failure(int cuda_error, int skip, int count);
+
 /* Test hook for the bounded waits of the shared-memory-staged kernel (the
  * notes have no counterpart: their kernels have no copy engine to wait on).
  * Runs the staged plan `plan_id` (path TILE_PATH_STAGED) of `op` on `args`

@@ -218,6 +218,44 @@ def test_static_host_entry_rejects_bad_arguments_before_any_cuda_call(lib):
 
 
 @fake_pointers
+def test_injected_launch_failures_are_reported_without_a_cuda_call(lib):
+    """tile_inject_launch_failure: the armed launch attempts of every kind of
+    entry point return TILE_ERR_CUDA with the injected error, before any
+    CUDA call (this container has no GPU, so a CUDA call would report
+    something else); argument errors still come first; skip and count are
+    honoured and the hook disarms itself."""
+    code = 719                                   # cudaErrorLaunchFailure
+    assert lib.tile_inject_launch_failure(code, -1, 1) == SHAPE
+    assert lib.tile_inject_launch_failure(code, 0, -1) == SHAPE
+    assert lib.tile_inject_launch_failure(0, 0, 1) == SHAPE
+    try:
+        assert lib.tile_inject_launch_failure(code, 0, 6) == OK
+        assert lib.tile_rmsnorm_f32(None, B, 2, 8, 1e-5, None) == NULL      # arguments first
+        assert lib.tile_rmsnorm_f32(A, B, 2, 8, 1e-5, None) == CUDA
+        assert lib.tile_last_cuda_error() == code
+        assert lib.tile_residual_layernorm_bf16(A, A + 64, B, 2, 8, 1e-5, None) == CUDA
+        assert lib.tile_softmax_backward_f32(A, A + 64, B, 2, 8, None) == CUDA
+        assert lib.tile_sigmoid_pair_f32(A, B, B + 64, 16, None) == CUDA
+        a = tile.TileRowArgs()
+        a.in_, a.out, a.rows, a.width, a.eps, a.dtype = A, B, 4, 256, 1e-5, 1
+        assert lib.tile_test_staged_wait_timeout(1, 45, ctypes.byref(a), 16, None) == CUDA
+        ws, dg, db, st = 0x40000000, 0x50000000, 0x50001000, 0x60000000
+        need = lib.tile_norm_param_grad_workspace_bytes(2, 8)
+        assert lib.tile_norm_param_grad_f32(A, A + 64, st, dg, db, 2, 8, ws, need, None) == CUDA
+        # the six armed attempts are used up: disarmed
+        assert lib.tile_inject_launch_failure(code, 0, 0) == OK
+        # skip: two attempts proceed (here they reach CUDA and fail otherwise),
+        # the third reports the injected error
+        assert lib.tile_inject_launch_failure(700, 2, 1) == OK
+        assert lib.tile_rmsnorm_f32(A, B, 2, 8, 1e-5, None) != OK
+        assert lib.tile_rmsnorm_f32(A, B, 2, 8, 1e-5, None) != OK
+        assert lib.tile_rmsnorm_f32(A, B, 2, 8, 1e-5, None) == CUDA
+        assert lib.tile_last_cuda_error() == 700
+    finally:
+        assert lib.tile_inject_launch_failure(0, 0, 0) == OK
+
+
+@fake_pointers
 def test_staged_wait_hook_rejects_bad_arguments(lib):
     a = tile.TileRowArgs()
     a.in_, a.out, a.rows, a.width, a.eps, a.dtype = A, B, 4, 256, 1e-5, 1

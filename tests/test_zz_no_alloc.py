@@ -18,7 +18,8 @@ bound otherwise.  Modes: pageable inputs (the rows stage through the array)
 with the output pinned or pageable, and every buffer pinned (in place).
 One more case issues the two calls on two different streams with no
 synchronisation between them: only the library's ordering of calls on the
-shared array keeps them apart there.  This file is collected last and
+shared array keeps them apart there; another makes the first call fail
+part-way (a launch failure injected on the host) before the second.  This file is collected last and
 depends on nothing that earlier tests set up.
 """
 
@@ -128,6 +129,34 @@ def test_static_staging_calls_on_two_streams(op, rows, width):
     torch.cuda.synchronize()
     for k, ((host_in, values), out) in enumerate(zip(calls, outs)):
         _check(op, out.numpy(), host_in, values, f"{op} {rows}x{width} stream {k}")
+
+
+def test_static_staging_stays_ordered_after_a_failed_call():
+    """A call that fails part-way (a kernel launch failure injected on the
+    host after two chunks were launched, with their copies and the next
+    chunk's copies already enqueued) returns TILE_ERR_CUDA; the next call,
+    on another stream with no synchronisation, must still wait for
+    everything the failed call enqueued on the shared array: its results
+    match the oracle."""
+    op, rows, width = "residual_layernorm", 3000, 4096
+    lib = tile.load()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    (x0, r0), _ = _inputs(op, rows, width, 1.0, False)
+    (x1, r1), values = _inputs(op, rows, width, -2.5, False)
+    out0 = torch.full((rows, width), float("nan")).pin_memory()
+    out1 = torch.full((rows, width), float("nan")).pin_memory()
+    try:
+        assert lib.tile_inject_launch_failure(719, 2, 1) == 0
+        st = lib.tile_run_host_static_f32(tile.OPS[op], x0.data_ptr(), r0.data_ptr(),
+                                          out0.data_ptr(), rows, width, EPS,
+                                          streams[0].cuda_stream)
+        assert st == -5 and lib.tile_last_cuda_error() == 719
+    finally:
+        assert lib.tile_inject_launch_failure(0, 0, 0) == 0
+    _call_static(op, x1, r1, out1, streams[1].cuda_stream)
+    torch.cuda.synchronize()
+    _check(op, out1.numpy(), (x1, r1), values, f"{op} {rows}x{width} after a failed call")
+    assert tile.tile_check_device_status() == 0
 
 
 def test_static_staging_rejects_a_width_beyond_the_maximum():

@@ -39,6 +39,7 @@ __all__ = [
     "tile_layernorm_backward_bf16", "tile_rmsnorm_backward_bf16", "tile_softmax_backward_bf16",
     "tile_norm_param_grad_bf16", "tile_layernorm_backward_f16", "tile_rmsnorm_backward_f16",
     "tile_softmax_backward_f16", "tile_norm_param_grad_f16", "tile_test_staged_wait_timeout",
+    "tile_inject_launch_failure",
     "residual_layernorm", "layernorm", "rmsnorm", "softmax", "run",
 ]
 
@@ -162,6 +163,7 @@ def load():
         "tile_norm_param_grad_f16": [P, P, P, P, P, I, I, P, ctypes.c_size_t, P],
         "tile_plan_info_ex": [I, I, I, I, I, ctypes.POINTER(TilePlan)],
         "tile_test_staged_wait_timeout": [I, I, ctypes.POINTER(TileRowArgs), ctypes.c_uint, P],
+        "tile_inject_launch_failure": [I, I, I],
     }
     for name, argtypes in sigs.items():
         fn = getattr(lib, name)
@@ -336,6 +338,13 @@ def tile_run_plan_args_f32(op, plan_id, x, out, residual=None, gamma=None, beta=
     a = _row_args(x, out, residual, gamma, beta, out2, eps)
     _check(load().tile_run_plan_args_f32(op, plan_id, ctypes.byref(a), _stream(stream)),
            "tile_run_plan_args_f32")
+
+
+def tile_inject_launch_failure(cuda_error, skip=0, count=1):
+    """Test hook: after ``skip`` launch attempts, the next ``count`` fail on
+    the host with ``cuda_error`` (``count=0`` disarms)."""
+    _check(load().tile_inject_launch_failure(int(cuda_error), int(skip), int(count)),
+           "tile_inject_launch_failure")
 
 
 def tile_test_staged_wait_timeout(op, plan_id, x, out, spin_limit, residual=None, gamma=None,

@@ -139,6 +139,11 @@ int check_host_args(int op, const float *h_in, const float *h_res, const float *
 int run_host(int op, const float *h_in, const float *h_res, float *h_out, int rows, int width,
              float eps, void *d_work, size_t work_bytes, cudaStream_t stream);
 
+// A launch failure injected on the host for tests (tile_inject_launch_failure):
+// cudaSuccess, or the error the next launch attempt must report instead of
+// launching.
+cudaError_t injected_launch_failure();
+
 // The cudaError_t behind the last TILE_ERR_CUDA on this host thread.
 void set_last_cuda_error(int err);
 int last_cuda_error();

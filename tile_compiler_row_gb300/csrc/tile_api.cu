@@ -3,8 +3,10 @@
 // the contract of every entry point.
 #include "../../include/tile_rows.h"
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "launch.h"
 #include "plans.h"
@@ -296,9 +298,21 @@ bool staged_ok(const Call &c) {
            (c.gamma == nullptr || aligned16(c.gamma)) && (c.beta == nullptr || aligned16(c.beta));
 }
 
+// A launch failure injected on the host for tests: TILE_ERR_CUDA with the
+// injected error, nothing launched.
+#define TILE_INJECTED_FAILURE()                                              \
+    do {                                                                     \
+        const cudaError_t inj = tile::injected_launch_failure();             \
+        if (inj != cudaSuccess) {                                            \
+            tile::set_last_cuda_error(static_cast<int>(inj));                \
+            return TILE_ERR_CUDA;                                            \
+        }                                                                    \
+    } while (0)
+
 int launch(const Call &c, int plan_id, cudaStream_t stream) {
     const PlanDesc &p = kPlans[plan_id];
     if (grid_of(p, c.rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
+    TILE_INJECTED_FAILURE();
     tile::RowArgs a{c.in, c.res, c.gamma, c.beta, c.out, c.out2, c.rows, c.width, c.eps, nullptr};
     cudaError_t err;
     if (p.staged) {
@@ -457,6 +471,7 @@ int run_backward(int op, int plan_id, int dtype, const void *x, const float *gam
     if (plan_id < 0) return TILE_ERR_SHAPE;
     if (kPlans[plan_id].V == 4 && !vec4) return TILE_ERR_PLAN;
     if (grid_of(kPlans[plan_id], rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
+    TILE_INJECTED_FAILURE();
     tile::BwdArgs args{x, dy, gamma, dx, stats, rows, width, eps, nullptr};
     const int kop = bwd_kernel_op(op);
     const cudaError_t err =
@@ -507,6 +522,7 @@ int run_param_grad(int dtype, const void *in, const void *dy, const float *row_s
     if (overlaps(dgamma, vec, dbeta, vec) || overlaps(workspace, need, in, mat) ||
         overlaps(workspace, need, dy, mat) || overlaps(workspace, need, row_stats, st))
         return TILE_ERR_ALIAS;
+    TILE_INJECTED_FAILURE();
     const cudaError_t err = tile::launch_param_grad(dtype, in, dy, row_stats, dgamma, dbeta, rows,
                                                     width, static_cast<float *>(workspace), stream);
     if (err != cudaSuccess) {
@@ -522,10 +538,27 @@ namespace tile {
 
 namespace {
 thread_local int t_last_cuda_error = 0;
-}
+
+// Launch failures injected on the host (tile_inject_launch_failure).
+std::mutex g_inject_mu;
+std::atomic<int> g_inject_armed{0};
+int g_inject_skip = 0, g_inject_count = 0, g_inject_code = 0;
+}  // namespace
 
 void set_last_cuda_error(int err) { t_last_cuda_error = err; }
 int last_cuda_error() { return t_last_cuda_error; }
+
+cudaError_t injected_launch_failure() {
+    if (g_inject_armed.load(std::memory_order_acquire) == 0) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(g_inject_mu);
+    if (g_inject_count <= 0) return cudaSuccess;
+    if (g_inject_skip > 0) {
+        --g_inject_skip;
+        return cudaSuccess;
+    }
+    if (--g_inject_count == 0) g_inject_armed.store(0, std::memory_order_release);
+    return static_cast<cudaError_t>(g_inject_code);
+}
 
 int run_selected(int op, const float *in, const float *res, float *out, int rows, int width,
                  float eps, cudaStream_t stream, long long select_rows) {
@@ -543,6 +576,7 @@ int run_pairs(int kind, const float *in, float *value, float *derivative, long l
     if (overlaps(value, bytes, in, bytes) || overlaps(derivative, bytes, in, bytes) ||
         overlaps(value, bytes, derivative, bytes))
         return TILE_ERR_ALIAS;
+    TILE_INJECTED_FAILURE();
     const cudaError_t err = launch_pairs(kind, in, value, derivative, n, stream);
     if (err != cudaSuccess) {
         set_last_cuda_error(static_cast<int>(err));
@@ -748,6 +782,7 @@ int tile_test_staged_wait_timeout(int op, int plan_id, const tile_row_args_t *ar
         return TILE_ERR_PLAN;
     if (noop) return TILE_OK;
     if (grid_of(kPlans[plan_id], c.rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
+    TILE_INJECTED_FAILURE();
     tile::RowArgs a{c.in, c.res, c.gamma, c.beta, c.out, c.out2, c.rows, c.width, c.eps, nullptr};
     const cudaError_t err = tile::launch_staged_withheld(kernel_op_of(c), c.dtype, plan_id, a,
                                                          spin_limit < 1 ? 1u : spin_limit, stream);
@@ -805,6 +840,16 @@ int tile_plan_info(int id, int op, int rows, int width, tile_plan_t *plan) {
 int tile_max_width(void) { return TILE_MAX_WIDTH; }
 
 int tile_last_cuda_error(void) { return tile::last_cuda_error(); }
+
+int tile_inject_launch_failure(int cuda_error, int skip, int count) {
+    if (skip < 0 || count < 0 || (count > 0 && cuda_error == 0)) return TILE_ERR_SHAPE;
+    std::lock_guard<std::mutex> lock(tile::g_inject_mu);
+    tile::g_inject_code = cuda_error;
+    tile::g_inject_skip = skip;
+    tile::g_inject_count = count;
+    tile::g_inject_armed.store(count > 0 ? 1 : 0, std::memory_order_release);
+    return TILE_OK;
+}
 
 const char *tile_status_string(int status) {
     switch (status) {
