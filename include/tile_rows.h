@@ -88,6 +88,12 @@ extern "C" {
                               /* copy engine (mbarrier completion), several  */
                               /* rows in flight per CTA; 16-byte aligned     */
                               /* rows of whole vectors; normalisers, softmax */
+#define TILE_PATH_ROWS     3  /* one CTA normalises R rows, each thread      */
+                              /* owning the same columns of all R (one       */
+                              /* reduction round and one gamma/beta load     */
+                              /* serve R rows); 16-byte aligned rows of      */
+                              /* whole vectors; normalisers, softmax;        */
+                              /* programs_per_cta reports R                  */
 
 /*
  * A launch plan: how rows map onto the GPU.  Worker w of program p in a CTA

@@ -154,9 +154,12 @@ def test_plan_info_table(lib):
     seen_vec1 = False
     for pid in range(n):
         info = tile.tile_plan_info(pid, 0, 3, 1)
-        if info is None:                               # staged: whole vectors only
+        if info is None:                 # staged and R-row plans: whole vectors only
             info = tile.tile_plan_info(pid, 0, 3, 4)
-            assert info is not None and info["path"] == 2 and info["id"] == pid
+            assert info is not None and info["path"] in (2, 3) and info["id"] == pid
+            if info["path"] == 3:        # R rows per CTA on the same threads
+                r = info["programs_per_cta"]
+                assert r > 1 and info["grid"] == -(-3 // r)
             assert tile.tile_plan_info(pid, 0, 3, 6) is None
             continue
         assert info["id"] == pid
@@ -386,7 +389,7 @@ def test_bf16_plans(lib):
 
 def test_staged_plans_have_no_row_reductions(lib):
     staged = [pid for pid in range(tile.tile_plan_count())
-              if (tile.tile_plan_info(pid, "layernorm", 8, 4096) or {}).get("path") == 2]
+              if (tile.tile_plan_info(pid, "layernorm", 8, 4096) or {}).get("path") in (2, 3)]
     assert staged
     for pid in staged:
         for op in ("row_sum", "row_minmax"):

@@ -1,11 +1,15 @@
-"""GPU parity of the shared-memory-staged plans (bulk row copies into a ring
-of shared-memory stages, persistent CTAs) against the FP64 oracle.
+"""GPU parity of the plans that need 16-byte aligned rows of whole vectors
+against the FP64 oracle: the shared-memory-staged plans (bulk row copies
+into a ring of shared-memory stages, persistent CTAs) and the
+R-rows-per-CTA plans (each thread owning the same columns of R rows).
 
-Row counts are chosen so every CTA walks several times round its ring of
-stages (stage reuse, barrier phase flips).  Bounds as for the register
-plans: 2e-6 + 2e-5 |ref| (affine LayerNorm atol 1e-5), BF16 and FP16
-outputs plus half an ulp of their type.  The staged plans need 16-byte aligned rows of whole
-vectors; anything else is rejected with TILE_ERR_PLAN."""
+Row counts are chosen so every staged CTA walks several times round its
+ring of stages (stage reuse, barrier phase flips) and so the last R-row CTA
+replays a row.  Bounds as for the register plans: 2e-6 + 2e-5 |ref| (affine
+LayerNorm atol 1e-5), BF16 and FP16 outputs plus half an ulp of their type.
+Anything but aligned rows of whole vectors is rejected with TILE_ERR_PLAN.
+An R-row plan gives bitwise the results of the register plan with the same
+warps and vectors per row."""
 
 from __future__ import annotations
 
@@ -38,7 +42,7 @@ def _staged_plans():
     out = []
     for pid in range(tile.tile_plan_count()):
         info = tile.tile_plan_info(pid, 0, 1, 8)
-        if info is not None and info["path"] == 2:
+        if info is not None and info["path"] in (2, 3):
             out.append(pid)
     return out
 
@@ -64,12 +68,15 @@ def _reference(op, x, r, g, b):
 @pytest.mark.parametrize("pid", STAGED)
 def test_staged_plan(pid, op, dtype):
     info = tile.tile_plan_info_ex(pid, 0, dtype, 1, 8)
-    assert info is not None and info["path"] == 2
+    if info is None:                      # R-row plan not built for this type
+        assert tile.tile_plan_info(pid, 0, 1, 8)["path"] == 3
+        return
+    assert info["path"] in (2, 3)
     ev = info["vec"]
     cap = info["max_width"]
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
     for width in sorted({ev, 256, cap // 2, cap}):
-        rows = 20000 if width <= 512 else 3000
+        rows = 20001 if width <= 512 else 3001      # odd: an R-row CTA replays a row
         x = torch.from_numpy(synth.rows_of(3, rows, width, which="x")).to(tdt)
         r = torch.from_numpy(synth.rows_of(3, rows, width, which="r")).to(tdt)
         xf, rf = x.float().numpy(), r.float().numpy()
@@ -161,3 +168,50 @@ def test_staged_wait_hook_rejects_register_plans():
     with pytest.raises(tile.TileError) as e:
         tile.tile_test_staged_wait_timeout("rmsnorm", 7, x, out, 16)
     assert e.value.status == -8
+
+
+def _register_twin(pid):
+    """The register plan with the same warps and vectors per row as R-row
+    plan `pid` (one CTA or program per row), or None."""
+    info = tile.tile_plan_info(pid, 0, 1, 8)
+    for q in range(tile.tile_plan_count()):
+        other = tile.tile_plan_info(q, 0, 1, 8)
+        if (other is not None and other["path"] == 0 and other["vec"] == 4
+                and other["warps_per_program"] == info["warps_per_program"]
+                and other["chunks"] == info["chunks"]):
+            return q
+    return None
+
+
+# R-row plans that have a register plan with the same warps and vectors
+# per row (all but S = 16, K = 1)
+ROWS_PLANS = [pid for pid in STAGED if tile.tile_plan_info(pid, 0, 1, 8)["path"] == 3
+              and _register_twin(pid) is not None]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("pid", ROWS_PLANS)
+def test_rows_plan_is_bitwise_its_register_twin(pid, dtype):
+    twin = _register_twin(pid)
+    assert tile.tile_plan_info_ex(pid, 0, dtype, 1, 8) is not None
+    assert tile.tile_plan_info_ex(twin, 0, dtype, 1, 8) is not None
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]
+    cap = min(tile.tile_plan_info_ex(pid, 0, dtype, 1, 8)["max_width"],
+              tile.tile_plan_info_ex(twin, 0, dtype, 1, 8)["max_width"] // 8 * 8)
+    rows, width = 999, cap
+    x = torch.from_numpy(synth.rows_of(3, rows, width, which="x")).to(tdt).cuda()
+    r = torch.from_numpy(synth.rows_of(3, rows, width, which="r")).to(tdt).cuda()
+    g = torch.from_numpy(synth.uniform_pm1(3001, width) * np.float32(2.0)).cuda()
+    b = torch.from_numpy(synth.uniform_pm1(3002, width)).cuda()
+    for op in OPS:
+        outs = []
+        for plan in (pid, twin):
+            out = torch.full((rows, width), float("nan"), dtype=tdt, device="cuda")
+            tile.tile_run_plan_args_f32(
+                op, plan, x, out,
+                residual=r if op in ("residual_layernorm", "layernorm_affine") else None,
+                gamma=g if op in ("layernorm_affine", "rmsnorm_weighted") else None,
+                beta=b if op == "layernorm_affine" else None, eps=EPS)
+            outs.append(out)
+        assert torch.equal(outs[0], outs[1]), f"plan {pid} vs {twin}: {op} {dtype}"
+    assert tile.tile_check_device_status() == 0

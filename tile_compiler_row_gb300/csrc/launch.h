@@ -52,6 +52,11 @@ enum { ELEM_F32 = 0, ELEM_BF16 = 1, ELEM_F16 = 2 };
 cudaError_t launch_staged(int kernel_op, int elem, int plan_id, RowArgs args,
                           cudaStream_t stream);
 cudaError_t status_staged(unsigned int *value, cudaStream_t stream);
+// R-rows-per-CTA kernel (multi.cu): kernel_op as launch_staged; plan_id one
+// of TILE_MULTI_LIST.
+cudaError_t launch_multi(int kernel_op, int elem, int plan_id, RowArgs args,
+                         cudaStream_t stream);
+cudaError_t status_multi(unsigned int *value, cudaStream_t stream);
 // The staged kernel with each CTA's first copy withheld and the barrier
 // waits limited to `spin_limit` polls (tile_test_staged_wait_timeout).
 cudaError_t launch_staged_withheld(int kernel_op, int elem, int plan_id, RowArgs args,

@@ -91,5 +91,22 @@
 
 #define TILE_STAGED_COUNT 13
 
+// R-rows-per-CTA plans (multi_kernel.cuh): X(id, S, K, R), a CTA of 32*S
+// threads normalising R rows, every thread owning the same columns of each
+// (K 16-byte vectors per row), so reductions and gamma/beta loads serve R
+// rows.  16-byte vectors on aligned rows of whole vectors, as the staged
+// plans; their ids follow the staged plans.
+#define TILE_MULTI_LIST(X) \
+    X(53, 4, 4, 2)         \
+    X(54, 8, 2, 2)         \
+    X(55, 8, 4, 2)         \
+    X(56, 16, 1, 2)        \
+    X(57, 8, 2, 4)         \
+    X(58, 16, 2, 2)        \
+    X(59, 4, 2, 4)         \
+    X(60, 16, 4, 2)
+
+#define TILE_MULTI_COUNT 8
+
 // Widest row covered by both a V = 4 and a V = 1 plan.
 #define TILE_MAX_WIDTH 131072

@@ -17,18 +17,26 @@ struct PlanDesc {
     int id, V, S, P, K, C;
     bool staged;   // shared-memory-staged persistent kernel (staged_kernel.cuh)
     int stage_kb;  // staged plans: shared memory budget of the ring of stages
+    int R;         // rows per CTA sharing each thread's columns (multi_kernel.cuh); 1 else
 };
 
-constexpr int kAllPlans = TILE_PLAN_COUNT + TILE_STAGED_COUNT;
+constexpr int kAllPlans = TILE_PLAN_COUNT + TILE_STAGED_COUNT + TILE_MULTI_COUNT;
 
 constexpr PlanDesc kPlans[kAllPlans] = {
-#define TILE_ROW(id, V, S, P, K, C) {id, V, S, P, K, C, false, 0},
+#define TILE_ROW(id, V, S, P, K, C) {id, V, S, P, K, C, false, 0, 1},
     TILE_PLAN_LIST(TILE_ROW)
 #undef TILE_ROW
-#define TILE_STAGED_ROW(id, S, K, KB) {id, 4, S, 1, K, 1, true, KB},
+#define TILE_STAGED_ROW(id, S, K, KB) {id, 4, S, 1, K, 1, true, KB, 1},
     TILE_STAGED_LIST(TILE_STAGED_ROW)
 #undef TILE_STAGED_ROW
+#define TILE_MULTI_ROW(id, S, K, R) {id, 4, S, 1, K, 1, false, 0, R},
+    TILE_MULTI_LIST(TILE_MULTI_ROW)
+#undef TILE_MULTI_ROW
 };
+
+// Plans that run on 16-byte aligned rows of whole vectors only: the staged
+// plans and the R-rows-per-CTA plans.
+constexpr bool whole_vectors(const PlanDesc &p) { return p.staged || p.R > 1; }
 
 // Vector slots a plan's workers own for one row.
 constexpr long long capacity(const PlanDesc &p) {
@@ -44,15 +52,17 @@ int elems_per_vec(const PlanDesc &p, int dtype) {
     return p.V == 4 ? (two_byte(dtype) ? 8 : 4) : 1;
 }
 
-// 2-byte plans whose stripe would exceed the register budget are not built.
+// 2-byte plans whose stripe would exceed the register budget are not built,
+// nor R-row plans whose R stripes would (for any element type).
 bool built(const PlanDesc &p, int dtype) {
+    if (p.R > 1) return p.R * p.K * elems_per_vec(p, dtype) <= 64;
     return !two_byte(dtype) || p.K * elems_per_vec(p, dtype) <= tile::kMaxStripeBf16;
 }
 
 bool covers(const PlanDesc &p, int width, int dtype = TILE_DTYPE_F32) {
     if (width < 1 || !built(p, dtype)) return false;
     const int ev = elems_per_vec(p, dtype);
-    if (p.staged)   // whole 16-byte vectors only: no head or tail
+    if (whole_vectors(p))   // whole 16-byte vectors only: no head or tail
         return width % ev == 0 && width / ev <= capacity(p);
     return (width / ev) <= capacity(p);
 }
@@ -63,7 +73,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int max_width_of(const PlanDesc &p, int dtype = TILE_DTYPE_F32) {
     const int ev = elems_per_vec(p, dtype);
-    const long long w = capacity(p) * ev + (p.staged ? 0 : ev - 1);
+    const long long w = capacity(p) * ev + (whole_vectors(p) ? 0 : ev - 1);
     return w > TILE_MAX_WIDTH ? TILE_MAX_WIDTH : static_cast<int>(w);
 }
 
@@ -151,7 +161,8 @@ int select_plan(int op, long long rows, int width, bool vec4, int dtype,
 }
 
 long long grid_of(const PlanDesc &p, long long rows) {
-    return ((rows + p.P - 1) / p.P) * p.C;
+    const long long per_cta = static_cast<long long>(p.P) * p.R;
+    return ((rows + per_cta - 1) / per_cta) * p.C;
 }
 
 void fill_plan(const PlanDesc &p, int op, int dtype, int rows, int width, tile_plan_t *out) {
@@ -159,18 +170,21 @@ void fill_plan(const PlanDesc &p, int op, int dtype, int rows, int width, tile_p
     out->rows = rows;
     out->width = width;
     out->id = p.id;
-    out->path = p.staged ? TILE_PATH_STAGED : p.C > 1 ? TILE_PATH_CLUSTER : TILE_PATH_CTA;
+    out->path = p.staged  ? TILE_PATH_STAGED
+                : p.R > 1 ? TILE_PATH_ROWS
+                : p.C > 1 ? TILE_PATH_CLUSTER
+                          : TILE_PATH_CTA;
     out->vec = elems_per_vec(p, dtype);
     out->warps_per_program = p.S;
-    out->programs_per_cta = p.P;
+    out->programs_per_cta = p.P * p.R;
     out->chunks = p.K;
     out->cluster = p.C;
-    out->threads = 32 * p.S * p.P;
+    out->threads = 32 * p.S * p.P;       // R-row plans: R rows on the same threads
     out->workers = 32 * p.S;
     out->stripe_floats = p.K * elems_per_vec(p, dtype);
     out->max_width = max_width_of(p, dtype);
     out->dtype = dtype;
-    const int part = p.S > 1 ? 3 * p.P * p.S : 0;
+    const int part = p.S > 1 ? 3 * p.P * p.S * p.R : 0;
     out->smem_bytes = 4 * (part + (p.C > 1 ? 4 : 0));
     if (p.staged) {
         // the launcher's stage count: the plan's budget, 1..8 stages
@@ -315,8 +329,9 @@ int launch(const Call &c, int plan_id, cudaStream_t stream) {
     TILE_INJECTED_FAILURE();
     tile::RowArgs a{c.in, c.res, c.gamma, c.beta, c.out, c.out2, c.rows, c.width, c.eps, nullptr};
     cudaError_t err;
-    if (p.staged) {
-        err = tile::launch_staged(kernel_op_of(c), c.dtype, plan_id, a, stream);
+    if (whole_vectors(p)) {
+        err = p.staged ? tile::launch_staged(kernel_op_of(c), c.dtype, plan_id, a, stream)
+                       : tile::launch_multi(kernel_op_of(c), c.dtype, plan_id, a, stream);
         if (err != cudaSuccess) {
             tile::set_last_cuda_error(static_cast<int>(err));
             return TILE_ERR_CUDA;
@@ -377,7 +392,7 @@ int run_call_plan(const Call &c, int plan_id, cudaStream_t stream) {
         return TILE_ERR_PLAN;
     if (noop) return TILE_OK;
     if (kPlans[plan_id].V == 4 && !coaligned16(c)) return TILE_ERR_PLAN;
-    if (kPlans[plan_id].staged && !staged_ok(c)) return TILE_ERR_PLAN;
+    if (whole_vectors(kPlans[plan_id]) && !staged_ok(c)) return TILE_ERR_PLAN;
     return launch(c, plan_id, stream);
 }
 
@@ -823,8 +838,8 @@ int tile_plan_info_ex(int id, int op, int dtype, int rows, int width, tile_plan_
     if (!valid_op(op)) return TILE_ERR_OP;
     if (!valid_dtype(dtype)) return TILE_ERR_DTYPE;
     if (!built(kPlans[id], dtype)) return TILE_ERR_PLAN;
-    // the staged kernel has no row-reduction (sum, min/max) variant
-    if (kPlans[id].staged && (op == TILE_OP_ROW_SUM || op == TILE_OP_ROW_MINMAX))
+    // the staged and R-row kernels have no row-reduction (sum, min/max) variant
+    if (whole_vectors(kPlans[id]) && (op == TILE_OP_ROW_SUM || op == TILE_OP_ROW_MINMAX))
         return TILE_ERR_PLAN;
     if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH || !covers(kPlans[id], width, dtype))
         return TILE_ERR_SHAPE;
@@ -880,7 +895,7 @@ int tile_check_device_status(cudaStream_t stream) {
         tile::status_layernorm_f16, tile::status_rmsnorm_f16, tile::status_softmax_f16,
         tile::status_row_sum_f16, tile::status_row_minmax_f16, tile::status_pairs,
         tile::status_backward, tile::status_backward_bf16, tile::status_backward_f16,
-        tile::status_param_grad, tile::status_staged};
+        tile::status_param_grad, tile::status_staged, tile::status_multi};
     for (auto f : fetch) {
         v = 0;
         const cudaError_t err = f(&v, stream);

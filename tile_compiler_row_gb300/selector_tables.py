@@ -12,10 +12,11 @@ sweep into ``csrc/selector_tables.h``:
   16-byte vector less one element (3 FP32, 7 BF16), and takes the fastest
   register plan measured at w, or the plan built before if that one is
   within 0.5 % of the fastest (measurement noise does not flip a choice);
-* one staged-plan table per (family, op): the fastest shared-memory-staged
-  plan at w where it beat the fastest register plan by more than 1 %
-  (-1 elsewhere); calls take it only on 16-byte aligned rows of whole
-  vectors;
+* one whole-vector-plan table per (family, op): the fastest plan among
+  those that need 16-byte aligned rows of whole vectors (the shared-memory-
+  staged plans and the R-rows-per-CTA plans) at w where it beat the fastest
+  register plan by more than 1 % (-1 elsewhere); calls take it only on such
+  rows;
 * two small-problem tables per op (FP32, L2-resident): "tiny" for
   rows * width <= 2**19, "small" up to 2**22.  At the ladder bucket of each
   small workload width of the tier, the plan fastest over that width's
@@ -23,8 +24,9 @@ sweep into ``csrc/selector_tables.h``:
   (-1 elsewhere: the large-problem table).
 
 Several sweeps may be given: each plan's time at a shape is then the mean
-of the runs that timed it, and FP16 runs count for the 2-byte tables with
-the BF16 ones (the two types share the tables).
+of the runs that timed it (plans built after an older sweep count from the
+newer ones only), and FP16 runs count for the 2-byte tables with the BF16
+ones (the two types share the tables).
 
     python -m tile_compiler_row_gb300.selector_tables sweep --out tables.json   (GPU)
     python -m tile_compiler_row_gb300.selector_tables emit tables.json          (writes the header)
@@ -61,7 +63,7 @@ SMALL = ((1, 127), (17, 257), (7, 1537), (64, 4096), (1024, 4096), (128, 8192), 
 KEEP = 0.005       # keep the previous plan within 0.5 % of the fastest
 STAGED_WIN = 0.01  # a staged plan must win by more than 1 %
 SMALL_WIN = 0.01
-FIRST_STAGED = 40  # ids of the shared-memory-staged plans start here
+FIRST_STAGED = 40  # ids of the whole-vector plans (staged, then R rows per CTA) start here
 
 
 def sweep_rows(dtype, width):
@@ -126,11 +128,15 @@ def tier(rows, width):
 
 
 def merged(entries):
-    """One entry whose plan times are the means over ``entries`` (plans
-    every entry timed); "selected" is the first entry's."""
-    common = set.intersection(*(set(e["plans"]) for e in entries))
+    """One entry whose plan times are the means over the ``entries`` that
+    timed each plan (a plan built after an older sweep counts from the
+    newer ones only); "selected" is the first entry's."""
+    plans = set().union(*(set(e["plans"]) for e in entries))
     e = dict(entries[0])
-    e["plans"] = {p: sum(x["plans"][p] for x in entries) / len(entries) for p in common}
+    e["plans"] = {}
+    for p in plans:
+        times = [x["plans"][p] for x in entries if p in x["plans"]]
+        e["plans"][p] = sum(times) / len(times)
     return e
 
 
