@@ -433,7 +433,11 @@ int tile_host_schedule(int op, int rows, int width, size_t work_bytes, int direc
  * chunk is copied in before the kernel reads it).  Calls that overlapped on
  * the GPU would race on the array, so the library orders each call's work
  * on the GPU after the previous call's end (an event), whatever stream it
- * was given; calls on different streams therefore run one after another. */
+ * was given; calls on different streams therefore run one after another.
+ * A call that fails part-way (TILE_ERR_CUDA after some chunks were
+ * enqueued) still marks its end after everything it enqueued, so the next
+ * call waits for that work too.  Argument errors are returned before any
+ * CUDA call. */
 int tile_run_host_static_f32(int op, const float *h_in, const float *h_residual, float *h_out,
                              int rows, int width, float eps, cudaStream_t stream);
 
