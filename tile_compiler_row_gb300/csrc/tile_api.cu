@@ -154,7 +154,7 @@ int select_plan(int op, long long rows, int width, bool vec4, int dtype,
     }
     if (small && !b16) {
         const int id = pick(elems <= kTinyElems ? kTinyF32[t] : kSmallF32[t], width);
-        if (id >= 0) return id;
+        if (id >= 0 && covers(kPlans[id], width, dtype)) return id;
     }
     const int id = pick(b16 ? kRegB16[t] : kRegF32[t], width);
     return (id >= 0 && covers(kPlans[id], width, dtype)) ? id : -1;
