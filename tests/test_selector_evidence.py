@@ -77,3 +77,11 @@ def test_every_bucket_of_the_selector_has_a_line_of_evidence():
 def test_every_selected_plan_was_within_5_percent_of_the_fastest():
     slow = [e for e in large() + small() if e["ratio"] > WITHIN]
     assert not slow, f"selected plans slower than {WITHIN} x the fastest: {slow}"
+
+
+def test_the_committed_tables_are_what_the_committed_sweeps_generate():
+    """csrc/selector_tables.h is generated, not edited: regenerating it from
+    the committed sweep records gives the same text."""
+    from tile_compiler_row_gb300 import selector_tables
+    text = selector_tables.render(selector_tables.committed_records())
+    assert text == open(selector_tables.HEADER).read()

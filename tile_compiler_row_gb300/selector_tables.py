@@ -30,6 +30,9 @@ ones (the two types share the tables).
 
     python -m tile_compiler_row_gb300.selector_tables sweep --out tables.json   (GPU)
     python -m tile_compiler_row_gb300.selector_tables emit tables.json          (writes the header)
+
+``sweeps/selector_sweeps.json.gz`` holds the sweeps the committed header was
+generated from; ``emit`` with no file regenerates it from them.
 """
 
 from __future__ import annotations
@@ -41,6 +44,8 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 HEADER = os.path.join(HERE, "csrc", "selector_tables.h")
+#: the committed sweeps the header was generated from
+SWEEPS = os.path.join(HERE, "sweeps", "selector_sweeps.json.gz")
 
 #: ops with their own tables.  "layernorm_affine+residual" is affine
 #: LayerNorm called with a residual (a different stream count).
@@ -194,7 +199,16 @@ def tables(records):
     return out, small
 
 
-def emit(records, path=HEADER):
+def committed_records(path=SWEEPS):
+    """The sweep records the committed header was generated from."""
+    import gzip
+    with gzip.open(path, "rt") as fh:
+        data = json.load(fh)
+    return [e for run in data["runs"] for e in run]
+
+
+def render(records):
+    """The text of csrc/selector_tables.h for these sweep records."""
     big, small = tables(records)
 
     def arr(name, rows, comment=None):
@@ -214,8 +228,12 @@ def emit(records, path=HEADER):
     for tr, name in (("tiny", "Tiny"), ("small", "Small")):
         for op in TABLE_OPS:
             parts.append(arr(f"kF32{name}{STEM[op]}", small.get((tr, op), [(MAX_WIDTH, -1)])))
+    return "\n".join(parts)
+
+
+def emit(records, path=HEADER):
     with open(path, "w") as fh:
-        fh.write("\n".join(parts))
+        fh.write(render(records))
     return path
 
 
@@ -225,8 +243,9 @@ def main(argv=None):
     sub = ap.add_subparsers(dest="cmd", required=True)
     sw = sub.add_parser("sweep")
     sw.add_argument("--out", required=True)
-    em = sub.add_parser("emit")
-    em.add_argument("paths", nargs="+")
+    em = sub.add_parser("emit", help="sweep JSON files -> the header (default: the "
+                                       "committed sweeps)")
+    em.add_argument("paths", nargs="*")
     em.add_argument("--header", default=HEADER)
     args = ap.parse_args(argv)
     if args.cmd == "sweep":
@@ -236,7 +255,7 @@ def main(argv=None):
         for p in args.paths:
             with open(p) as fh:
                 records.extend(json.load(fh))
-        print(emit(records, args.header))
+        print(emit(records or committed_records(), args.header))
     return 0
 
 
