@@ -215,3 +215,21 @@ def test_rows_plan_is_bitwise_its_register_twin(pid, dtype):
             outs.append(out)
         assert torch.equal(outs[0], outs[1]), f"plan {pid} vs {twin}: {op} {dtype}"
     assert tile.tile_check_device_status() == 0
+
+
+@pytest.mark.parametrize("rows", [1, 2, 3, 5])
+@pytest.mark.parametrize("pid", [p for p in STAGED if tile.tile_plan_info(p, 0, 1, 8)["path"] == 3])
+def test_rows_plan_with_fewer_rows_than_a_cta_holds(pid, rows):
+    """R-row plans on row counts below and just above R: the replayed rows
+    write nothing (sentinels past the output stay), the real rows match the
+    oracle."""
+    width = 256
+    x = synth.rows_of(3, rows, width, which="x")
+    buf = torch.full(((rows + 4) * width,), 7.0, device="cuda")
+    out = buf[:rows * width].view(rows, width)
+    tile.tile_run_plan_args_f32("layernorm", pid, torch.from_numpy(x).cuda(), out, eps=EPS)
+    ref = oracle.get().layernorm(x, ref_eps())
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= ATOL + RTOL * np.abs(ref))
+    assert bool((buf[rows * width:] == 7.0).all())
+    assert tile.tile_check_device_status() == 0
