@@ -450,12 +450,14 @@ int tile_run_host_static_f32(int op, const float *h_in, const float *h_residual,
 int tile_describe_plan(int op, int rows, int width, tile_plan_t *plan);
 
 /* tile_describe_plan for an element type (TILE_DTYPE_*); TILE_ERR_DTYPE for
- * an unknown one.  For BF16 and FP16 the answer may be a shared-memory-staged plan
- * (path TILE_PATH_STAGED), which a call takes only when every pointer is
- * 16-byte aligned and width is a multiple of 8 (whole 16-byte rows); other
- * calls of that shape take the register plan of the same width.  For
- * TILE_OP_LAYERNORM_AFFINE the answer is that of a call without a residual
- * (2-byte calls with a residual take a staged plan at 8200-16384 columns). */
+ * an unknown one.  For large problems (rows * width above 2^22) the answer
+ * may be a plan that needs rows of whole 16-byte vectors -- a
+ * shared-memory-staged plan (path TILE_PATH_STAGED) or an R-rows-per-CTA
+ * plan (TILE_PATH_ROWS) -- which a call takes only when every pointer is
+ * 16-byte aligned and width is a multiple of the vector (4 FP32, 8 BF16 /
+ * FP16 elements); other calls of that shape take the register plan of the
+ * same width.  For TILE_OP_LAYERNORM_AFFINE the answer is that of a call
+ * without a residual (a call with a residual has its own measured table). */
 int tile_describe_plan_ex(int op, int dtype, int rows, int width, tile_plan_t *plan);
 
 /* Number of plans built into the library, and plan `id` of that table
