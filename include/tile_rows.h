@@ -330,6 +330,14 @@ int tile_run_backward_plan_ex(int op, int plan_id, int dtype, const void *in, co
                               const void *dy, void *dx, float *row_stats, int rows, int width,
                               float eps, cudaStream_t stream);
 
+/* The plan the backward entry points launch for (op, dtype, rows, width)
+ * with 16-byte co-aligned in, dy and dx (op: TILE_OP_LAYERNORM,
+ * TILE_OP_RMSNORM or TILE_OP_SOFTMAX; the choice depends on the width, not
+ * on the rows).  Host only; touches no GPU.  Returns TILE_OK, TILE_ERR_OP,
+ * TILE_ERR_DTYPE, TILE_ERR_SHAPE or TILE_ERR_NULL; `plan` is written on
+ * success only. */
+int tile_describe_backward_plan(int op, int dtype, int rows, int width, tile_plan_t *plan);
+
 /* ---- pointwise value/derivative pairs ---------------------------------- */
 
 /* value[k] = sigmoid(in[k]) and derivative[k] = sigmoid'(in[k]) for k < n,

@@ -3,7 +3,8 @@ type and row-count regime (tiny and small L2-resident problems, large
 problems) and a dense set of widths, the plan the library describes exists
 for that element type and covers the row (its workers own every element),
 and a plan that needs rows of whole 16-byte vectors is only described for
-such rows."""
+such rows; the backward selector's plans are built for the backward kernels
+and cover every width."""
 
 import random
 
@@ -50,3 +51,19 @@ def test_every_described_plan_is_built_and_covers_the_row(op, dtype):
             assert (w // ev if p["vec"] > 1 else w) <= cap, what
             if p["path"] in (2, 3):           # staged, R rows per CTA: whole vectors only
                 assert w % ev == 0 and rows * w > (1 << 22), what
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("op", ["layernorm", "rmsnorm", "softmax"])
+def test_every_described_backward_plan_is_built_and_covers_the_row(lib, op, dtype):
+    """The backward selector's plans: built for the backward kernels of the
+    element type (a forced run of the plan on zero rows is accepted) and
+    covering every width."""
+    code = tile.OPS[op]
+    dcode = {"f32": 0, "bf16": 1, "f16": 2}[dtype]
+    for w in WIDTHS:
+        p = tile.tile_describe_backward_plan(op, dtype, 1024, w)
+        what = f"{op} backward {dtype} w={w}: plan {p['id']}"
+        assert p["max_width"] >= w and p["path"] in (0, 1), what
+        assert lib.tile_run_backward_plan_ex(code, p["id"], dcode, None, None, None, None, None,
+                                             0, w, 1e-5, None) == 0, what

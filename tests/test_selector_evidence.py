@@ -49,6 +49,12 @@ def large():
                  ratio=float(c[13])) for c in _rows("## Large problems")]
 
 
+def backward():
+    return [dict(op=c[0], dtype=c[1], lo=int(c[2].split("-")[0]), hi=int(c[2].split("-")[1]),
+                 width=int(c[3]), rows=int(c[4]), selected=int(c[5]), best=int(c[7]),
+                 ratio=float(c[13])) for c in _rows("## Backward")]
+
+
 def small():
     return [dict(op=c[0], dtype=c[1], rows=int(c[2].split("x")[0]), width=int(c[2].split("x")[1]),
                  selected=int(c[3]), best=int(c[5]), ratio=float(c[11]))
@@ -57,25 +63,25 @@ def small():
 
 def test_summary_is_committed_and_parses():
     assert os.path.exists(SUMMARY)
-    assert len(large()) > 200 and len(small()) >= 50
+    assert len(large()) > 200 and len(small()) >= 50 and len(backward()) > 50
 
 
 def test_every_recorded_shape_still_selects_the_recorded_plan():
-    for e in large() + small():
-        got = tile.tile_describe_plan_ex(e["op"], e["dtype"], e["rows"], e["width"])["id"]
+    for e in large() + small() + backward():
+        got = selector_evidence.describe(e["op"], e["dtype"], e["rows"], e["width"])["id"]
         assert got == e["selected"], f"{e}: the library now selects plan {got}"
 
 
 def test_every_bucket_of_the_selector_has_a_line_of_evidence():
-    have = {(e["op"], e["dtype"], e["lo"], e["hi"]) for e in large()}
+    have = {(e["op"], e["dtype"], e["lo"], e["hi"]) for e in large() + backward()}
     for dtype in selector_evidence.DTYPES:
-        for op in selector_evidence.OPS:
+        for op in selector_evidence.OPS + selector_evidence.BWD_OPS:
             for lo, hi, pid in selector_evidence.buckets(op, dtype):
                 assert (op, dtype, lo, hi) in have, f"no evidence for {op} {dtype} {lo}-{hi} (plan {pid})"
 
 
 def test_every_selected_plan_was_within_5_percent_of_the_fastest():
-    slow = [e for e in large() + small() if e["ratio"] > WITHIN]
+    slow = [e for e in large() + small() + backward() if e["ratio"] > WITHIN]
     assert not slow, f"selected plans slower than {WITHIN} x the fastest: {slow}"
 
 

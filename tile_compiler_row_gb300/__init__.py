@@ -39,7 +39,7 @@ __all__ = [
     "tile_layernorm_backward_bf16", "tile_rmsnorm_backward_bf16", "tile_softmax_backward_bf16",
     "tile_norm_param_grad_bf16", "tile_layernorm_backward_f16", "tile_rmsnorm_backward_f16",
     "tile_softmax_backward_f16", "tile_norm_param_grad_f16", "tile_test_staged_wait_timeout",
-    "tile_inject_launch_failure",
+    "tile_inject_launch_failure", "tile_describe_backward_plan",
     "residual_layernorm", "layernorm", "rmsnorm", "softmax", "run",
 ]
 
@@ -164,6 +164,7 @@ def load():
         "tile_plan_info_ex": [I, I, I, I, I, ctypes.POINTER(TilePlan)],
         "tile_test_staged_wait_timeout": [I, I, ctypes.POINTER(TileRowArgs), ctypes.c_uint, P],
         "tile_inject_launch_failure": [I, I, I],
+        "tile_describe_backward_plan": [I, I, I, I, ctypes.POINTER(TilePlan)],
     }
     for name, argtypes in sigs.items():
         fn = getattr(lib, name)
@@ -694,6 +695,17 @@ def tile_describe_plan_ex(op, dtype, rows, width):
     plan = TilePlan()
     _check(load().tile_describe_plan_ex(op, dtype, rows, width, ctypes.byref(plan)),
            "tile_describe_plan_ex")
+    return plan.as_dict()
+
+
+def tile_describe_backward_plan(op, dtype, rows, width):
+    """The plan the backward entry points launch for (op, dtype, rows, width)
+    on 16-byte co-aligned tensors."""
+    op = OPS[op] if isinstance(op, str) else op
+    dtype = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    plan = TilePlan()
+    _check(load().tile_describe_backward_plan(op, dtype, rows, width, ctypes.byref(plan)),
+           "tile_describe_backward_plan")
     return plan.as_dict()
 
 

@@ -413,30 +413,30 @@ tile_row_args_t args_of(const void *in, const void *res, const float *gamma, con
     return a;
 }
 
-// Backward plans hold two stripes (input and upstream gradient): the
-// tables use plans with K * (elements per vector) <= 32 floats per stripe.
-// Both from measured backward sweeps.  2-byte rows of 16-byte vectors use
-// the raw-word kernel (stripes of up to 8 vectors of 8); its table avoids
-// 1024-thread CTAs, whose 64-register cap the two stripes would spill.
-constexpr Bucket kVec4Backward[] = {
-    {131, 0}, {259, 1}, {515, 2}, {1027, 4}, {2051, 6}, {4099, 7},
-    {8195, 11}, {16387, 13}, {32771, 16}, {65539, 18}, {TILE_MAX_WIDTH, 20},
-};
-constexpr Bucket kTwoByteBackward[] = {
-    {263, 0}, {519, 1}, {1031, 2}, {2055, 39}, {4103, 6}, {8199, 7},
-    {16391, 10}, {32775, 14}, {65543, 17}, {TILE_MAX_WIDTH, 19},
-};
-// Softmax backward (one reduction, no gamma) differs at 32768 columns, where
-// plan 15 (a cluster of two 16-warp CTAs, K = 4) ran 11 % faster than plan 14
-// (one 16-warp CTA, K = 8).
-constexpr Bucket kTwoByteSoftmaxBackward[] = {
-    {263, 0}, {519, 1}, {1031, 2}, {2055, 39}, {4103, 6}, {8199, 7},
-    {16391, 10}, {32775, 15}, {65543, 17}, {TILE_MAX_WIDTH, 19},
-};
-
+// Backward plans hold two stripes (input and upstream gradient): a plan is
+// built for backward when K * (elements per vector) <= 32 floats per stripe
+// (2-byte rows of 16-byte vectors use the raw-word kernel: stripes of up to
+// 8 vectors of 8).  The per-op tables in selector_tables.h are generated
+// from a measured backward sweep (every built plan at each ladder width).
 bool built_backward(const PlanDesc &p, int dtype = TILE_DTYPE_F32) {
     const bool raw = two_byte(dtype) && p.V == 4;     // raw-word stripes (bwd_kernel.cuh)
     return p.K * elems_per_vec(p, dtype) <= (raw ? tile::kMaxStripeBwdRaw : tile::kMaxStripeBwd);
+}
+
+// The backward plan for a call: 16-byte vectors when x, dy and dx share a
+// 16-byte phase (the generated per-op tables, FP16 sharing BF16's), else the
+// scalar plans.
+int select_backward_plan(int op, int dtype, int width, bool vec4) {
+    if (!vec4) return pick(kVec1, width);
+    const bool b16 = two_byte(dtype);
+    const int id = op == TILE_OP_LAYERNORM ? (b16 ? pick(kB16RegBwdLN, width)
+                                                  : pick(kF32RegBwdLN, width))
+                   : op == TILE_OP_RMSNORM ? (b16 ? pick(kB16RegBwdRMS, width)
+                                                  : pick(kF32RegBwdRMS, width))
+                                           : (b16 ? pick(kB16RegBwdSoftmax, width)
+                                                  : pick(kF32RegBwdSoftmax, width));
+    return (id >= 0 && built_backward(kPlans[id], dtype) && covers(kPlans[id], width, dtype))
+               ? id : -1;
 }
 
 int bwd_kernel_op(int op) {
@@ -478,11 +478,7 @@ int run_backward(int op, int plan_id, int dtype, const void *x, const float *gam
     const uintptr_t a = reinterpret_cast<uintptr_t>(x);
     const bool vec4 = ((a ^ reinterpret_cast<uintptr_t>(dy)) & 15u) == 0 &&
                       ((a ^ reinterpret_cast<uintptr_t>(dx)) & 15u) == 0;
-    if (plan_id < 0)
-        plan_id = !vec4 ? pick(kVec1, width)
-                        : !two_byte(dtype)      ? pick(kVec4Backward, width)
-                        : op == TILE_OP_SOFTMAX ? pick(kTwoByteSoftmaxBackward, width)
-                                                : pick(kTwoByteBackward, width);
+    if (plan_id < 0) plan_id = select_backward_plan(op, dtype, width, vec4);
     if (plan_id < 0) return TILE_ERR_SHAPE;
     if (kPlans[plan_id].V == 4 && !vec4) return TILE_ERR_PLAN;
     if (grid_of(kPlans[plan_id], rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
@@ -934,6 +930,18 @@ int tile_run_backward_plan_f32(int op, int plan_id, const float *in, const float
     if (plan_id < 0) return TILE_ERR_PLAN;
     return run_backward(op, plan_id, TILE_DTYPE_F32, in, gamma, dy, dx, row_stats, rows, width,
                         eps, stream);
+}
+
+int tile_describe_backward_plan(int op, int dtype, int rows, int width, tile_plan_t *plan) {
+    if (op != TILE_OP_LAYERNORM && op != TILE_OP_RMSNORM && op != TILE_OP_SOFTMAX)
+        return TILE_ERR_OP;
+    if (!valid_dtype(dtype)) return TILE_ERR_DTYPE;
+    if (rows < 0 || width < 1 || width > TILE_MAX_WIDTH) return TILE_ERR_SHAPE;
+    if (plan == nullptr) return TILE_ERR_NULL;
+    const int id = select_backward_plan(op, dtype, width, true);
+    if (id < 0) return TILE_ERR_SHAPE;
+    fill_plan(kPlans[id], op, dtype, rows, width, plan);
+    return TILE_OK;
 }
 
 int tile_run_backward_plan_ex(int op, int plan_id, int dtype, const void *in, const float *gamma,

@@ -29,6 +29,8 @@ import sys
 OPS = ("residual_layernorm", "layernorm", "rmsnorm", "softmax", "row_sum", "row_minmax",
        "layernorm_affine", "rmsnorm_weighted")
 DTYPES = ("f32", "bf16", "f16")
+#: backward ops of the selector's backward tables
+BWD_OPS = ("layernorm_backward", "rmsnorm_backward", "softmax_backward")
 #: widths preferred as a bucket's representative (whole 16-byte vectors)
 LADDER = (64, 128, 256, 512, 1024, 1536, 2048, 3072, 4096, 6144, 8192, 12288, 16384, 32768,
           65536, 131072)
@@ -42,14 +44,23 @@ def vec(dtype):
     return 4 if dtype == "f32" else 8
 
 
+def describe(op, dtype, rows, width):
+    """The plan the library takes for a call (backward ops through
+    tile_describe_backward_plan)."""
+    import tile_compiler_row_gb300 as tile
+    if op in BWD_OPS:
+        return tile.tile_describe_backward_plan(op[:-len("_backward")], dtype, rows, width)
+    return tile.tile_describe_plan_ex(op, dtype, rows, width)
+
+
 def buckets(op, dtype):
-    """[(lo, hi, plan)]: the plan tile_describe_plan_ex gives for widths of
-    whole 16-byte vectors, in runs of equal plans.  Host only."""
+    """[(lo, hi, plan)]: the plan the library describes for widths of whole
+    16-byte vectors, in runs of equal plans.  Host only."""
     import tile_compiler_row_gb300 as tile
     out = []
     ev = vec(dtype)
     for w in range(ev, tile.tile_max_width() + 1, ev):
-        pid = tile.tile_describe_plan_ex(op, dtype, SCAN_ROWS, w)["id"]
+        pid = describe(op, dtype, SCAN_ROWS, w)["id"]
         if out and out[-1][2] == pid:
             out[-1][1] = w
         else:
@@ -71,7 +82,7 @@ def plan_cases():
     every bucket, grouped so each shape's tensors are made once."""
     todo = {}
     for dtype in DTYPES:
-        for op in OPS:
+        for op in OPS + BWD_OPS:
             for lo, hi, pid in buckets(op, dtype):
                 todo.setdefault((dtype, representative(lo, hi)), []).append((op, lo, hi, pid))
     return todo
@@ -82,7 +93,7 @@ def run_sweep(out, warmup=5, iters=30):
 
     import tile_compiler_row_gb300 as tile
     from tile_compiler_row_gb300 import _build
-    from tile_compiler_row_gb300.sweep import make_tensors, sweep_entry
+    from tile_compiler_row_gb300.sweep import make_tensors, sweep_backward_entry, sweep_entry
     _build.build()
     lib = tile.load()
     torch.cuda.set_device(0)
@@ -92,7 +103,10 @@ def run_sweep(out, warmup=5, iters=30):
         rows = sweep_rows(dtype, width)
         t = make_tensors(rows, width, dtype)
         for op, lo, hi, pid in cases:
-            e = sweep_entry(lib, op, dtype, rows, width, t, warmup, iters, stream)
+            if op in BWD_OPS:
+                e = sweep_backward_entry(lib, op, dtype, rows, width, t, warmup, iters, stream)
+            else:
+                e = sweep_entry(lib, op, dtype, rows, width, t, warmup, iters, stream)
             e.update({"regime": "large", "bucket": [lo, hi]})
             assert e["selected"] == pid
             records.append(e)
@@ -179,7 +193,23 @@ def summary(paths):
         return "—" if v is None else (f"{v:.{nd}f}" if isinstance(v, float) else str(v))
 
     for e in records:
-        if e.get("regime") != "large":
+        if e.get("regime") != "large" or e["op"] in BWD_OPS:
+            continue
+        c = _cell(e)
+        lo, hi = e["bucket"]
+        lines.append(
+            f"| {e['op']} | {e['dtype']} | {lo}-{hi} | {e['width']} | {e['rows']} | "
+            f"{c['selected']} | {fmt(c['sel_us'], 2)} | {c['best']} | {fmt(c['best_us'], 2)} | "
+            f"{fmt(c['second'])} | {fmt(c['second_us'], 2)} | {fmt(c['aa'], 4)} | "
+            f"{fmt(c['margin'], 4)} | {c['ratio']:.4f} |")
+    lines += ["", "## Backward", "",
+              "LayerNorm and RMSNorm backward with gamma and row statistics, softmax",
+              "backward; every covering register plan the backward kernels build, timed",
+              "as above (`tile_describe_backward_plan` gives the selected plan).", "",
+              "| op | dtype | widths | width | rows | selected | µs | best | µs | 2nd | µs | A/A | margin | sel/best |",
+              "|---|---|---|---:|---:|---:|---:|---:|---:|---:|---:|---:|---:|---:|"]
+    for e in records:
+        if e.get("regime") != "large" or e["op"] not in BWD_OPS:
             continue
         c = _cell(e)
         lo, hi = e["bucket"]

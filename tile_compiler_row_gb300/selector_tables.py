@@ -17,6 +17,9 @@ sweep into ``csrc/selector_tables.h``:
   staged plans and the R-rows-per-CTA plans) at w where it beat the fastest
   register plan by more than 1 % (-1 elsewhere); calls take it only on such
   rows;
+* one register-plan table per (family, backward op) for LayerNorm, RMSNorm
+  and softmax backward (with gamma and row statistics), chosen as the
+  forward register tables are;
 * two small-problem tables per op (FP32, L2-resident): "tiny" for
   rows * width <= 2**19, "small" up to 2**22.  At the ladder bucket of each
   small workload width of the tier, the plan fastest over that width's
@@ -56,6 +59,10 @@ STEM = {"residual_layernorm": "ResidualLN", "layernorm": "LN", "rmsnorm": "RMS",
         "softmax": "Softmax", "row_sum": "RowSum", "row_minmax": "RowMinmax",
         "layernorm_affine": "Affine", "rmsnorm_weighted": "Weighted",
         "layernorm_affine+residual": "ResidualAffine"}
+#: backward ops with their own register-plan tables (no whole-vector plans)
+BWD_OPS = ("layernorm_backward", "rmsnorm_backward", "softmax_backward")
+STEM.update({"layernorm_backward": "BwdLN", "rmsnorm_backward": "BwdRMS",
+             "softmax_backward": "BwdSoftmax"})
 FAMILIES = {"f32": "F32", "bf16": "B16"}
 LADDER = {"f32": (128, 256, 512, 1024, 1536, 2048, 3072, 3584, 4096, 6144, 8192, 12288, 16384,
                   32768, 65536, 131072),
@@ -75,12 +82,12 @@ def sweep_rows(dtype, width):
     return max(16, (1 << (26 if dtype == "f32" else 27)) // width)
 
 
-def run_sweep(out, warmup=5, iters=30):
+def run_sweep(out, warmup=5, iters=30, forward=True, backward=True):
     import torch
 
     import tile_compiler_row_gb300 as tile
     from tile_compiler_row_gb300 import _build
-    from tile_compiler_row_gb300.sweep import make_tensors, sweep_entry
+    from tile_compiler_row_gb300.sweep import make_tensors, sweep_backward_entry, sweep_entry
     _build.build()
     lib = tile.load()
     torch.cuda.set_device(0)
@@ -90,13 +97,16 @@ def run_sweep(out, warmup=5, iters=30):
         for width in LADDER[dtype]:
             rows = sweep_rows(dtype, width)
             t = make_tensors(rows, width, dtype)
-            for op in TABLE_OPS:
-                e = sweep_entry(lib, op, dtype, rows, width, t, warmup, iters, stream)
+            for op in (TABLE_OPS if forward else ()) + (BWD_OPS if backward else ()):
+                if op in BWD_OPS:
+                    e = sweep_backward_entry(lib, op, dtype, rows, width, t, warmup, iters, stream)
+                else:
+                    e = sweep_entry(lib, op, dtype, rows, width, t, warmup, iters, stream)
                 e["regime"] = "large"
                 records.append(e)
                 print(json.dumps(e), flush=True)
             del t
-    for rows, width in SMALL:
+    for rows, width in (SMALL if forward else ()):
         t = make_tensors(rows, width, "f32")
         for op in TABLE_OPS:
             e = sweep_entry(lib, op, "f32", rows, width, t, warmup, 200, stream, graph=True)
@@ -113,7 +123,7 @@ def _fastest(plans, pred):
     cand = {int(k): v for k, v in plans.items() if pred(int(k))}
     if not cand:
         return None, None
-    pid = min(cand, key=cand.get)
+    pid = min(cand, key=lambda q: (cand[q], q))      # equal times: the lower id
     return pid, cand[pid]
 
 
@@ -136,7 +146,7 @@ def merged(entries):
     """One entry whose plan times are the means over the ``entries`` that
     timed each plan (a plan built after an older sweep counts from the
     newer ones only); "selected" is the first entry's."""
-    plans = set().union(*(set(e["plans"]) for e in entries))
+    plans = sorted(set().union(*(set(e["plans"]) for e in entries)), key=int)
     e = dict(entries[0])
     e["plans"] = {}
     for p in plans:
@@ -169,6 +179,19 @@ def tables(records):
                 stg.append((_bound(dtype, w),
                             sid if sid is not None and st < rt * (1 - STAGED_WIN) else -1))
             out[(dtype, op)] = {"reg": reg, "staged": stg}
+        for op in BWD_OPS:
+            if not any((dtype, op, w) in large for w in LADDER[dtype]):
+                continue
+            reg = []
+            for w in LADDER[dtype]:
+                e = large[(dtype, op, w)]
+                rid, rt = _fastest(e["plans"], lambda p: p < FIRST_STAGED)
+                prev = e.get("selected")
+                if prev is not None and str(prev) in e["plans"] \
+                        and e["plans"][str(prev)] <= rt * (1 + KEEP):
+                    rid = prev
+                reg.append((_bound(dtype, w), rid))
+            out[(dtype, op)] = {"reg": reg, "staged": None}
     small = {}
     by_shape = {}
     for e in records:
@@ -189,7 +212,7 @@ def tables(records):
             def worst(p):
                 return max(e["plans"][p] / min(v for k, v in e["plans"].items()
                                                 if int(k) < FIRST_STAGED) for e in group)
-            best = min(plans, key=worst)
+            best = min(sorted(plans, key=int), key=lambda p: (worst(p), int(p)))
             base = worst(str(large_pick)) if str(large_pick) in plans else float("inf")
             if worst(best) * (1 + SMALL_WIN) < base:
                 pick[bound] = int(best)
@@ -225,6 +248,9 @@ def render(records):
             t = big[(dtype, op)]
             parts.append(arr(f"k{fam}Reg{STEM[op]}", t["reg"]))
             parts.append(arr(f"k{fam}Staged{STEM[op]}", t["staged"]))
+        for op in BWD_OPS:
+            if (dtype, op) in big:
+                parts.append(arr(f"k{fam}Reg{STEM[op]}", big[(dtype, op)]["reg"]))
     for tr, name in (("tiny", "Tiny"), ("small", "Small")):
         for op in TABLE_OPS:
             parts.append(arr(f"kF32{name}{STEM[op]}", small.get((tr, op), [(MAX_WIDTH, -1)])))
@@ -243,13 +269,14 @@ def main(argv=None):
     sub = ap.add_subparsers(dest="cmd", required=True)
     sw = sub.add_parser("sweep")
     sw.add_argument("--out", required=True)
+    sw.add_argument("--only", choices=("forward", "backward"), default=None)
     em = sub.add_parser("emit", help="sweep JSON files -> the header (default: the "
                                        "committed sweeps)")
     em.add_argument("paths", nargs="*")
     em.add_argument("--header", default=HEADER)
     args = ap.parse_args(argv)
     if args.cmd == "sweep":
-        run_sweep(args.out)
+        run_sweep(args.out, forward=args.only != "backward", backward=args.only != "forward")
     else:
         records = []
         for p in args.paths:

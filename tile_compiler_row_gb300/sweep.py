@@ -46,54 +46,35 @@ def shapes(quick=False, elems_log2=26):
     return out
 
 
-def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g=None, y2=None,
-              graph=False, cutoff=None):
-    """Median microseconds per call of ``plan``.  With ``cutoff`` (µs), a plan
-    whose first call after one warm-up already takes longer is not timed
-    further: that single call's time is returned."""
-    import ctypes
-
+def time_call(call, warmup, iters, stream, graph=False, cutoff=None):
+    """Median microseconds per call of ``call(s)`` (s: the raw CUDA stream
+    to launch on).  With ``cutoff`` (µs), a call whose first timing after
+    one warm-up already takes longer is not timed further: that single
+    call's time is returned."""
     import torch
 
-    import tile_compiler_row_gb300 as tile
     s = stream.cuda_stream
-    a = tile.TileRowArgs()
-    a.in_, a.out = x.data_ptr(), y.data_ptr()
-    a.residual = r.data_ptr() if r is not None else None
-    a.gamma = g.data_ptr() if g is not None else None
-    a.beta = None
-    a.out2 = y2.data_ptr() if y2 is not None else None
-    a.rows, a.width, a.eps = rows, width, 1e-5
-    a.dtype = {torch.bfloat16: 1, torch.float16: 2}.get(x.dtype, 0)
-    ref = ctypes.byref(a)
-
-    def call():
-        st = lib.tile_run_plan_args_f32(op_code, plan, ref, s)
-        if st != 0:
-            raise RuntimeError(f"plan {plan}: status {st}")
-
     if cutoff is not None and not graph:
-        call()
+        call(s)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        call()
+        call(s)
         e1.record(stream)
         torch.cuda.synchronize()
         first = e0.elapsed_time(e1) * 1e3
         if first > cutoff:
             return first
     for _ in range(warmup):
-        call()
+        call(s)
     if graph:
         # ``iters`` calls captured in one CUDA graph and replayed: the time per
         # call without host launch overhead (what back-to-back device work sees)
         cap = torch.cuda.Stream()
-        s = cap.cuda_stream
         torch.cuda.synchronize()
         cg = torch.cuda.CUDAGraph()
         with torch.cuda.graph(cg, stream=cap):
             for _ in range(iters):
-                call()
+                call(cap.cuda_stream)
         cg.replay()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -106,11 +87,37 @@ def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
     evs[0].record(stream)
     for i in range(iters):
-        call()
+        call(s)
         evs[i + 1].record(stream)
     torch.cuda.synchronize()
     per = [evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(iters)]
     return statistics.median(per)
+
+
+def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g=None, y2=None,
+              graph=False, cutoff=None):
+    """Median microseconds per call of forward plan ``plan`` (time_call)."""
+    import ctypes
+
+    import torch
+
+    import tile_compiler_row_gb300 as tile
+    a = tile.TileRowArgs()
+    a.in_, a.out = x.data_ptr(), y.data_ptr()
+    a.residual = r.data_ptr() if r is not None else None
+    a.gamma = g.data_ptr() if g is not None else None
+    a.beta = None
+    a.out2 = y2.data_ptr() if y2 is not None else None
+    a.rows, a.width, a.eps = rows, width, 1e-5
+    a.dtype = {torch.bfloat16: 1, torch.float16: 2}.get(x.dtype, 0)
+    ref = ctypes.byref(a)
+
+    def call(s):
+        st = lib.tile_run_plan_args_f32(op_code, plan, ref, s)
+        if st != 0:
+            raise RuntimeError(f"plan {plan}: status {st}")
+
+    return time_call(call, warmup, iters, stream, graph, cutoff)
 
 
 #: ops whose calls take the residual in a sweep: residual LayerNorm always;
@@ -177,6 +184,69 @@ def sweep_entry(lib, op, dtype, rows, width, t, warmup, iters, stream, graph=Fal
                               / 1e9, 1)
     entry["selected_over_best"] = (round(entry["plans"][chosen] / entry["plans"][best], 4)
                                    if chosen is not None and chosen in entry["plans"] else None)
+    return entry
+
+
+#: backward ops of the sweeps (the library's op name + "_backward")
+BWD_OPS = ("layernorm_backward", "rmsnorm_backward", "softmax_backward")
+
+
+def sweep_backward_entry(lib, op, dtype, rows, width, t, warmup, iters, stream):
+    """Every covering 16-byte-vector register plan of backward ``op`` at one
+    shape (LayerNorm and RMSNorm with gamma and row statistics; softmax on
+    the tensors as given), timed and rerun as ``sweep_entry`` does."""
+    import torch
+
+    import tile_compiler_row_gb300 as tile
+    base = op[:-len("_backward")]
+    code = tile.OPS[base]
+    dcode = {"f32": 0, "bf16": 1, "f16": 2}[dtype]
+    chosen = tile.tile_describe_backward_plan(base, dtype, rows, width)["id"]
+    norm = base != "softmax"
+    stats = torch.empty(2 * rows, device="cuda") if norm else None
+    x, dy, dx = t["x"], t["r"], t["y"]
+    g = t["g"] if norm else None
+
+    def caller(pid):
+        def call(s):
+            st = lib.tile_run_backward_plan_ex(
+                code, pid, dcode, x.data_ptr(), g.data_ptr() if g is not None else None,
+                dy.data_ptr(), dx.data_ptr(), stats.data_ptr() if stats is not None else None,
+                rows, width, 1e-5, s)
+            if st != 0:
+                raise RuntimeError(f"backward plan {pid}: status {st}")
+        return call
+
+    entry = {"op": op, "rows": rows, "width": width, "selected": chosen, "plans": {},
+             "dtype": dtype, "timing": "back-to-back launches"}
+    for pid in range(tile.tile_plan_count()):
+        info = tile.tile_plan_info_ex(pid, base, dtype, rows, width)
+        if info is None or info["vec"] == 1 or info["path"] in (2, 3) \
+                or info["grid"] > 0x7FFFFFFF:
+            continue
+        # a register plan the backward kernels do not build returns TILE_ERR_PLAN
+        # before launching anything
+        st = lib.tile_run_backward_plan_ex(code, pid, dcode, None, None, None, None, None,
+                                           0, width, 1e-5, None)
+        if st != 0:
+            continue
+        best_so_far = min(entry["plans"].values(), default=None)
+        entry["plans"][pid] = round(time_call(
+            caller(pid), warmup, iters, stream,
+            cutoff=None if best_so_far is None else 3.0 * best_so_far), 3)
+    ranked = sorted(entry["plans"], key=entry["plans"].get)
+    if len(ranked) >= 2:
+        a, b = ranked[0], ranked[1]
+        rerun = {a: [], b: []}
+        for pid in (a, b, b, a):
+            rerun[pid].append(round(time_call(caller(pid), warmup, iters, stream), 3))
+        entry["confirm"] = {
+            "order": [a, b, b, a], "us": {str(a): rerun[a], str(b): rerun[b]},
+            "aa_noise": round(abs(rerun[a][0] - rerun[a][1]) / min(rerun[a]), 4),
+            "margin": round(min(rerun[b]) / min(rerun[a]) - 1.0, 4)}
+    entry["best"] = ranked[0]
+    entry["selected_over_best"] = (round(entry["plans"][chosen] / entry["plans"][ranked[0]], 4)
+                                   if chosen in entry["plans"] else None)
     return entry
 
 
