@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
 #pragma unroll
                 for (int j = 0; j < EV; ++j) s[0] += v[k][j];
             row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
-            const float mean0 = s[0] / n;
+            const float mean0 = over_n<T>(s[0], n, a.inv_n);
             float q[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int k = 0; k < K; ++k) {
@@ -198,12 +198,12 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
             q[2] += hu + tu;
             q[3] = fmaf(hu, hv, fmaf(tu, tv, q[3]));
             row_allreduce<Sum, 4, S, P, C>(q, part2, cpart + 1, program, warp, lane);
-            const float mu1 = q[0] / n;
-            const float var = fmaxf(q[1] / n - mu1 * mu1, 0.0f);
-            rstd = 1.0f / sqrtf(var + a.eps);
+            const float mu1 = over_n<T>(q[0], n, a.inv_n);
+            const float var = fmaxf(over_n<T>(q[1], n, a.inv_n) - mu1 * mu1, 0.0f);
+            rstd = inv_sqrt<T>(var + a.eps);
             mean = mean0 + mu1;
-            mean_g = q[2] / n;
-            mean_gx = rstd * fmaf(-mu1, q[2], q[3]) / n;
+            mean_g = over_n<T>(q[2], n, a.inv_n);
+            mean_gx = over_n<T>(rstd * fmaf(-mu1, q[2], q[3]), n, a.inv_n);
             if constexpr (sizeof(T) == 2) {
                 // rstd (g - mean_g - (d - mu1) rstd mean_gx)
                 ca = -rstd * rstd * mean_gx;
@@ -228,8 +228,8 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_kernel(const BwdArgs a) {
                     q[1] = fmaf(u[k][j], v[k][j], q[1]);
                 }
             row_allreduce<Sum, 2, S, P, C>(q, part1, cpart, program, warp, lane);
-            rstd = 1.0f / sqrtf(q[0] / n + a.eps);
-            mean_gx = rstd * q[1] / n;
+            rstd = inv_sqrt<T>(over_n<T>(q[0], n, a.inv_n) + a.eps);
+            mean_gx = over_n<T>(rstd * q[1], n, a.inv_n);
             if constexpr (sizeof(T) == 2) {
                 ca = -rstd * rstd * mean_gx;         // rstd (g - x rstd mean_gx)
             } else {
@@ -519,7 +519,7 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
             for (int k = 0; k < K; ++k) acc_raw8<T>(xw[k], s4);   // empty slots add 0
             float s[1] = {(s4[0] + s4[1]) + (s4[2] + s4[3])};
             row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
-            mean0 = s[0] / n;
+            mean0 = over_n<T>(s[0], n, a.inv_n);
             float q[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int k = 0; k < K; ++k) {
@@ -544,12 +544,12 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
             q[2] += hu + tu;
             q[3] = fmaf(hu, hv, fmaf(tu, tv, q[3]));
             row_allreduce<Sum, 4, S, P, C>(q, part2, cpart + 1, program, warp, lane);
-            const float mu1 = q[0] / n;
-            const float var = fmaxf(q[1] / n - mu1 * mu1, 0.0f);
-            rstd = 1.0f / sqrtf(var + a.eps);
+            const float mu1 = over_n<T>(q[0], n, a.inv_n);
+            const float var = fmaxf(over_n<T>(q[1], n, a.inv_n) - mu1 * mu1, 0.0f);
+            rstd = inv_sqrt<T>(var + a.eps);
             mean = mean0 + mu1;
-            mean_g = q[2] / n;
-            mean_gx = rstd * fmaf(-mu1, q[2], q[3]) / n;
+            mean_g = over_n<T>(q[2], n, a.inv_n);
+            mean_gx = over_n<T>(rstd * fmaf(-mu1, q[2], q[3]), n, a.inv_n);
             ca = -rstd * rstd * mean_gx;
             cb = rstd * fmaf(rstd * mean_gx, mu1, -mean_g);
         } else {
@@ -580,8 +580,8 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
             }
             float q[2] = {q0 + q1, g0 + g1};
             row_allreduce<Sum, 2, S, P, C>(q, part1, cpart, program, warp, lane);
-            rstd = 1.0f / sqrtf(q[0] / n + a.eps);
-            mean_gx = rstd * q[1] / n;
+            rstd = inv_sqrt<T>(over_n<T>(q[0], n, a.inv_n) + a.eps);
+            mean_gx = over_n<T>(rstd * q[1], n, a.inv_n);
             ca = -rstd * rstd * mean_gx;
         }
         if (a.stats != nullptr && active && worker == 0 && rank == 0) {

@@ -25,6 +25,7 @@ struct RowArgs {
     int width;
     float eps;
     unsigned int *status;
+    float inv_n;           // 1 / width rounded to FP32 (the 2-byte kernels multiply by it)
 };
 
 // Arguments of one backward-kernel launch (bwd_kernel.cuh).  x: forward
@@ -42,6 +43,7 @@ struct BwdArgs {
     int width;
     float eps;
     unsigned int *status;
+    float inv_n;           // 1 / width rounded to FP32 (the 2-byte kernels multiply by it)
 };
 
 // Shared-memory-staged row kernel (staged.cu): kernel_op is OP_RESLN, OP_LN,

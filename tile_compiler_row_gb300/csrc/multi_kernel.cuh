@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(32 * S, (multi_min_blocks<T, S, K, R>()))
         float q[2 * R];
 #pragma unroll
         for (int j = 0; j < R; ++j) {
-            const float mean0 = s[j] / n;
+            const float mean0 = over_n<T>(s[j], n, a.inv_n);
             float a1[EV], a2[EV];
 #pragma unroll
             for (int e = 0; e < EV; ++e) a1[e] = a2[e] = 0.0f;
@@ -146,9 +146,9 @@ __global__ void __launch_bounds__(32 * S, (multi_min_blocks<T, S, K, R>()))
         row_allreduce<Sum, 2 * R, S, 1, 1>(q, part2, nullptr, 0, warp, lane);
 #pragma unroll
         for (int j = 0; j < R; ++j) {
-            const float mu1 = q[2 * j] / n;
-            const float var = fmaxf(q[2 * j + 1] / n - mu1 * mu1, 0.0f);
-            const float rstd = 1.0f / sqrtf(var + a.eps);
+            const float mu1 = over_n<T>(q[2 * j], n, a.inv_n);
+            const float var = fmaxf(over_n<T>(q[2 * j + 1], n, a.inv_n) - mu1 * mu1, 0.0f);
+            const float rstd = inv_sqrt<T>(var + a.eps);
             if constexpr (PK) {
                 const float shift = -mu1 * rstd;
 #pragma unroll
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(32 * S, (multi_min_blocks<T, S, K, R>()))
         row_allreduce<Sum, R, S, 1, 1>(s, part1, nullptr, 0, warp, lane);
 #pragma unroll
         for (int j = 0; j < R; ++j) {
-            const float rstd = 1.0f / sqrtf(s[j] / n + a.eps);
+            const float rstd = inv_sqrt<T>(over_n<T>(s[j], n, a.inv_n) + a.eps);
 #pragma unroll
             for (int k = 0; k < K; ++k) vmul_c<PK, EV>(v[j][k], rstd);
         }

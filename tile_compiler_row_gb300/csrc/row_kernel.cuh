@@ -170,6 +170,30 @@ __device__ __forceinline__ float ln_out(float d, float mu1, float rstd) {
         return (d - mu1) * rstd;
 }
 
+// Row statistics from the reduced sums: s / n and 1 / sqrt(t).  FP32 rows
+// take both as correctly rounded operations.  2-byte rows (BF16, FP16),
+// whose kernels are bound by instruction issue and whose outputs keep 8 or
+// 11 significant bits, multiply by 1 / n rounded once on the host (relative
+// error at most 2^-23 against 2^-24 for the division) and take rsqrtf (at
+// most 2 ulp, the CUDA math library's bound): one instruction each instead
+// of a division or square-root sequence, with errors far inside half an ulp
+// of the output.  (The mean estimate only centres the row, so its rounding
+// does not reach the result.)
+template <class T>
+__device__ __forceinline__ float over_n(float s, float n, float inv_n) {
+    if constexpr (sizeof(T) == 2)
+        return s * inv_n;
+    else
+        return s / n;
+}
+template <class T>
+__device__ __forceinline__ float inv_sqrt(float t) {
+    if constexpr (sizeof(T) == 2)
+        return rsqrtf(t);
+    else
+        return 1.0f / sqrtf(t);
+}
+
 // v[j] += the 16-byte vector `t` of element type T (4 FP32 or 8 BF16 / FP16
 // lanes, the lower address in the lower half of each word).  2-byte lanes
 // use the mixed-precision add (PTX add.rn.f32.bf16 / add.rn.f32.f16, sm_100
@@ -622,7 +646,7 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
         for (int k = 0; k < K; ++k) vadd<PK, EV>(acc, v[k]);
         float s[1] = {lane_total(acc) + (hv + tv)};
         row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
-        const float mean0 = s[0] / n;
+        const float mean0 = over_n<T>(s[0], n, a.inv_n);
         // ---- a3: centre in place; reduce (sum d, sum d^2) -----------------
         float a1[EV], a2[EV];
 #pragma unroll
@@ -655,9 +679,9 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
         float q[2] = {lane_total(a1) + (hv + tv), fmaf(hv, hv, fmaf(tv, tv, lane_total(a2)))};
         row_allreduce<Sum, 2, S, P, C>(q, part2, cpart + 1, program, warp, lane);
         // corrected two-pass: mean = mean0 + mu1, var = E[d^2] - mu1^2
-        const float mu1 = q[0] / n;
-        const float var = fmaxf(q[1] / n - mu1 * mu1, 0.0f);
-        const float rstd = 1.0f / sqrtf(var + a.eps);
+        const float mu1 = over_n<T>(q[0], n, a.inv_n);
+        const float var = fmaxf(over_n<T>(q[1], n, a.inv_n) - mu1 * mu1, 0.0f);
+        const float rstd = inv_sqrt<T>(var + a.eps);
         if constexpr (PK) {
             const float nb_shift = -mu1 * rstd;      // ln_out<T>: one FMA per lane
 #pragma unroll
@@ -679,7 +703,7 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
         for (int k = 0; k < K; ++k) vsq_acc<PK, EV>(acc, v[k]);
         float s[1] = {fmaf(hv, hv, fmaf(tv, tv, lane_total(acc)))};
         row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
-        const float rstd = 1.0f / sqrtf(s[0] / n + a.eps);
+        const float rstd = inv_sqrt<T>(over_n<T>(s[0], n, a.inv_n) + a.eps);
 #pragma unroll
         for (int k = 0; k < K; ++k) vmul_c<PK, EV>(v[k], rstd);
         hv *= rstd;

@@ -278,9 +278,9 @@ __global__ void __launch_bounds__(32 * S)
                 r1[0] = lane_total(acc);
                 row_allreduce<Sum, 1, S, 1, 1>(r1, part1[pb], nullptr, 0, warp, lane);
                 if constexpr (OP == OP_RMS)
-                    rstd = 1.0f / sqrtf(r1[0] / n + a.eps);
+                    rstd = inv_sqrt<T>(over_n<T>(r1[0], n, a.inv_n) + a.eps);
                 else
-                    mean0 = r1[0] / n;
+                    mean0 = over_n<T>(r1[0], n, a.inv_n);
             }
         }
         if (tid == 0 && !aborted && !*abort_seen) {
@@ -311,9 +311,9 @@ __global__ void __launch_bounds__(32 * S)
             }
             float q[2] = {lane_total(a1), lane_total(a2)};
             row_allreduce<Sum, 2, S, 1, 1>(q, part2[pb], nullptr, 0, warp, lane);
-            const float mu1 = q[0] / n;
-            const float var = fmaxf(q[1] / n - mu1 * mu1, 0.0f);
-            rstd = 1.0f / sqrtf(var + a.eps);
+            const float mu1 = over_n<T>(q[0], n, a.inv_n);
+            const float var = fmaxf(over_n<T>(q[1], n, a.inv_n) - mu1 * mu1, 0.0f);
+            rstd = inv_sqrt<T>(var + a.eps);
 #pragma unroll
             for (int k = 0; k < K; ++k)
 #pragma unroll

@@ -327,7 +327,8 @@ int launch(const Call &c, int plan_id, cudaStream_t stream) {
     const PlanDesc &p = kPlans[plan_id];
     if (grid_of(p, c.rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
     TILE_INJECTED_FAILURE();
-    tile::RowArgs a{c.in, c.res, c.gamma, c.beta, c.out, c.out2, c.rows, c.width, c.eps, nullptr};
+    tile::RowArgs a{c.in, c.res, c.gamma, c.beta, c.out, c.out2, c.rows, c.width, c.eps, nullptr,
+                    1.0f / static_cast<float>(c.width)};
     cudaError_t err;
     if (whole_vectors(p)) {
         err = p.staged ? tile::launch_staged(kernel_op_of(c), c.dtype, plan_id, a, stream)
@@ -483,7 +484,8 @@ int run_backward(int op, int plan_id, int dtype, const void *x, const float *gam
     if (kPlans[plan_id].V == 4 && !vec4) return TILE_ERR_PLAN;
     if (grid_of(kPlans[plan_id], rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
     TILE_INJECTED_FAILURE();
-    tile::BwdArgs args{x, dy, gamma, dx, stats, rows, width, eps, nullptr};
+    tile::BwdArgs args{x, dy, gamma, dx, stats, rows, width, eps, nullptr,
+                       1.0f / static_cast<float>(width)};
     const int kop = bwd_kernel_op(op);
     const cudaError_t err =
         dtype == TILE_DTYPE_BF16  ? tile::launch_backward_bf16(kop, plan_id, args, stream)
@@ -794,7 +796,8 @@ int tile_test_staged_wait_timeout(int op, int plan_id, const tile_row_args_t *ar
     if (noop) return TILE_OK;
     if (grid_of(kPlans[plan_id], c.rows) > 0x7fffffffLL) return TILE_ERR_SHAPE;
     TILE_INJECTED_FAILURE();
-    tile::RowArgs a{c.in, c.res, c.gamma, c.beta, c.out, c.out2, c.rows, c.width, c.eps, nullptr};
+    tile::RowArgs a{c.in, c.res, c.gamma, c.beta, c.out, c.out2, c.rows, c.width, c.eps, nullptr,
+                    1.0f / static_cast<float>(c.width)};
     const cudaError_t err = tile::launch_staged_withheld(kernel_op_of(c), c.dtype, plan_id, a,
                                                          spin_limit < 1 ? 1u : spin_limit, stream);
     if (err != cudaSuccess) {
