@@ -61,6 +61,13 @@ cudaError_t launch_plan(RowArgs args, cudaStream_t stream) {
             cfg.attrs = attr;
             cfg.numAttrs = 1;
         }
+        // 2-byte rows that are 16-byte aligned and hold whole vectors take
+        // the kernel without a scalar head and tail (bitwise the same results)
+        if constexpr (V == 4 && sizeof(TILE_INST_T) == 2) {
+            if ((reinterpret_cast<uintptr_t>(args.x) & 15) == 0 && args.width % EV == 0)
+                return cudaLaunchKernelEx(
+                    &cfg, row_kernel<TILE_INST_OP, TILE_INST_T, V, S, P, K, C, true>, args);
+        }
         return cudaLaunchKernelEx(&cfg, row_kernel<TILE_INST_OP, TILE_INST_T, V, S, P, K, C>,
                                   args);
     }

@@ -523,10 +523,19 @@ constexpr int row_min_blocks() {
     return (sizeof(T) == 2 && V == 4 && K * 8 <= 32) ? 32 / (S * P) : 0;
 }
 
-template <int OP, class T, int V, int S, int P, int K, int C>
+// WH (whole vectors; V = 4 only): every row starts on a 16-byte boundary and
+// holds whole vectors, so the row has no scalar head or tail and the kernel
+// carries none of their loads, sums and stores.  The launcher takes it when
+// the rows are aligned and the width is a multiple of the vector; the
+// results are bitwise those of the general kernel (a head and tail of zero
+// elements contribute exact zeros).
+template <int OP, class T, int V, int S, int P, int K, int C, bool WH = false>
 __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
     row_kernel(const RowArgs a) {
     static_assert(V == 1 || V == 4, "V is 1 (scalar) or 4 (16-byte vectors)");
+    static_assert(!WH || V == 4, "whole-vector rows are read as 16-byte vectors");
+    // the row may have a scalar head and tail
+    constexpr bool HT = V == 4 && !WH;
     // elements per access: one 16-byte vector (4 FP32 or 8 BF16), or one
     constexpr int EV = (V == 4) ? Elem<T>::kVec : 1;
     static_assert(C == 1 || P == 1, "a cluster row has one program per CTA");
@@ -579,7 +588,9 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
     // nb vectors of EV elements, then tl scalars.  All row pointers share the
     // 16-byte phase.
     int h = 0, tl = 0, nb;
-    if constexpr (V == 4) {
+    if constexpr (WH) {
+        nb = width / EV;
+    } else if constexpr (V == 4) {
         const int mis =
             static_cast<int>((reinterpret_cast<uintptr_t>(xr) / sizeof(T)) & (EV - 1));
         h = (EV - mis) & (EV - 1);
@@ -621,7 +632,7 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
     bool has_h = false, has_t = false;
     float hv = kFill, tv = kFill;
     int te = 0;
-    if constexpr (V == 4) {
+    if constexpr (HT) {
         has_h = (rank == 0) && (worker < h);
         has_t = (rank == 0) && (worker < tl);
         te = h + EV * nb + worker;
@@ -644,7 +655,7 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
         for (int j = 0; j < EV; ++j) acc[j] = 0.0f;
 #pragma unroll
         for (int k = 0; k < K; ++k) vadd<PK, EV>(acc, v[k]);
-        float s[1] = {lane_total(acc) + (hv + tv)};
+        float s[1] = {HT ? lane_total(acc) + (hv + tv) : lane_total(acc)};
         row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
         const float mean0 = over_n<T>(s[0], n, a.inv_n);
         // ---- a3: centre in place; reduce (sum d, sum d^2) -----------------
@@ -676,7 +687,8 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
         }
         hv = has_h ? hv - mean0 : 0.0f;
         tv = has_t ? tv - mean0 : 0.0f;
-        float q[2] = {lane_total(a1) + (hv + tv), fmaf(hv, hv, fmaf(tv, tv, lane_total(a2)))};
+        float q[2] = {HT ? lane_total(a1) + (hv + tv) : lane_total(a1),
+                      HT ? fmaf(hv, hv, fmaf(tv, tv, lane_total(a2))) : lane_total(a2)};
         row_allreduce<Sum, 2, S, P, C>(q, part2, cpart + 1, program, warp, lane);
         // corrected two-pass: mean = mean0 + mu1, var = E[d^2] - mu1^2
         const float mu1 = over_n<T>(q[0], n, a.inv_n);
@@ -701,7 +713,7 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
         for (int j = 0; j < EV; ++j) acc[j] = 0.0f;
 #pragma unroll
         for (int k = 0; k < K; ++k) vsq_acc<PK, EV>(acc, v[k]);
-        float s[1] = {fmaf(hv, hv, fmaf(tv, tv, lane_total(acc)))};
+        float s[1] = {HT ? fmaf(hv, hv, fmaf(tv, tv, lane_total(acc))) : lane_total(acc)};
         row_allreduce<Sum, 1, S, P, C>(s, part1, cpart, program, warp, lane);
         const float rstd = inv_sqrt<T>(over_n<T>(s[0], n, a.inv_n) + a.eps);
 #pragma unroll
@@ -717,7 +729,7 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
         for (int k = 0; k < K; ++k)
 #pragma unroll
             for (int j = 0; j < EV; ++j) mj[j] = fmaxf(mj[j], v[k][j]);
-        float m[1] = {fmaxf(lane_max(mj), fmaxf(hv, tv))};
+        float m[1] = {HT ? fmaxf(lane_max(mj), fmaxf(hv, tv)) : lane_max(mj)};
         row_allreduce<Max, 1, S, P, C>(m, part1, cpart, program, warp, lane);
         const float mx = m[0];
         // ---- a3: exponentiate in place (exp(-inf) = 0), reduce the sum ---
@@ -742,7 +754,7 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
         }
         hv = softmax_exp<T>(hv - mx);
         tv = softmax_exp<T>(tv - mx);
-        float s[1] = {lane_total(acc) + (hv + tv)};
+        float s[1] = {HT ? lane_total(acc) + (hv + tv) : lane_total(acc)};
         row_allreduce<Sum, 1, S, P, C>(s, part2, cpart + 1, program, warp, lane);
         const float inv = 1.0f / s[0];
 #pragma unroll
@@ -756,8 +768,10 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
         for (int k = 0; k < K; ++k)
 #pragma unroll
             for (int j = 0; j < EV; ++j) comp_add(s, c, v[k][j]);
-        comp_add(s, c, hv);
-        comp_add(s, c, tv);
+        if constexpr (HT) {
+            comp_add(s, c, hv);
+            comp_add(s, c, tv);
+        }
         row_allreduce_comp<S, P, C>(s, c, part1, cpart, program, warp, lane);
         row_out0 = __fadd_rn(s, c);
     } else {
@@ -772,17 +786,27 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
                 hi[j] = fmaxf(hi[j], v[k][j]);
                 lo[j] = fmaxf(lo[j], -v[k][j]);
             }
-        float m[2] = {fmaxf(lane_max(hi), fmaxf(hv, tv)), fmaxf(lane_max(lo), fmaxf(-hv, -tv))};
+        float m[2] = {HT ? fmaxf(lane_max(hi), fmaxf(hv, tv)) : lane_max(hi),
+                      HT ? fmaxf(lane_max(lo), fmaxf(-hv, -tv)) : lane_max(lo)};
         row_allreduce<Max, 2, S, P, C>(m, part1, cpart, program, warp, lane);
         row_out0 = -m[1];
         row_out1 = m[0];
     }
 
+    // Our cluster partials must stay readable until every CTA of the
+    // cluster has read them: arrive now (no cluster read follows), wait
+    // after the stores.
+    if constexpr (C > 1) cluster_arrive();
+
     // Optional per-column scale and shift (affine LayerNorm, weighted
     // RMSNorm): y = y * gamma[col] + beta[col], loaded through the read-only
     // cache (every row reuses them).  float4 loads when gamma/beta share the
     // row's 16-byte phase (one 256-bit load per 8-column vector of a 2-byte
-    // row when they are 32-byte aligned), scalar loads otherwise.
+    // row when they are 32-byte aligned), scalar loads otherwise.  2-byte
+    // rows store each vector as soon as it is scaled, so a vector's gamma
+    // and beta registers and its stripe slot are free before the next one
+    // is loaded.
+    bool vec_stored = false;
     if constexpr (OP == OP_RESLN || OP == OP_LN || OP == OP_RMS) {
         if (a.gamma != nullptr) {
             const float *g = a.gamma;
@@ -796,15 +820,19 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
                           (b == nullptr || (reinterpret_cast<uintptr_t>(b + h) & 31) == 0);
             }
             if constexpr (EV == 8) {
-                // one loop per load form, chosen once per launch
+                // one loop per load form, chosen once per launch; replayed
+                // programs store nothing and skip it
+                vec_stored = true;
                 auto apply = [&](auto load) {
+                    if (!active) return;
 #pragma unroll
                     for (int k = 0; k < K; ++k) {
                         const int i = k * (C * W) + gw;
                         if (i < nb) {
                             float gg[EV], bb[EV];
-                            load((V == 4) ? h + EV * i : i, gg, bb);
+                            load(h + EV * i, gg, bb);
                             vfma<PK, EV>(v[k], gg, bb);
+                            Elem<T>::store_vec(yr + h + EV * i, v[k]);
                         }
                     }
                 };
@@ -896,16 +924,12 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
                     }
                 }
             }
-            if constexpr (V == 4) {
+            if constexpr (HT) {
                 if (has_h) hv = fmaf(hv, __ldg(g + worker), b != nullptr ? __ldg(b + worker) : 0.0f);
                 if (has_t) tv = fmaf(tv, __ldg(g + te), b != nullptr ? __ldg(b + te) : 0.0f);
             }
         }
     }
-
-    // Our cluster partials must stay readable until every CTA of the
-    // cluster has read them: arrive now, wait after the stores.
-    if constexpr (C > 1) cluster_arrive();
 
     // ---- a4: streaming stores, predicated for replayed programs ---------
     if constexpr (kRowOutput) {
@@ -915,17 +939,19 @@ __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
         }
     } else {
         if (active) {
+            if (!vec_stored) {
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
-                const int i = k * (C * W) + gw;
-                if (i < nb) {
-                    if constexpr (V == 4)
-                        Elem<T>::store_vec(yr + h + EV * i, v[k]);
-                    else
-                        Elem<T>::store(yr + i, v[k][0]);
+                for (int k = 0; k < K; ++k) {
+                    const int i = k * (C * W) + gw;
+                    if (i < nb) {
+                        if constexpr (V == 4)
+                            Elem<T>::store_vec(yr + h + EV * i, v[k]);
+                        else
+                            Elem<T>::store(yr + i, v[k][0]);
+                    }
                 }
             }
-            if constexpr (V == 4) {
+            if constexpr (HT) {
                 if (has_h) Elem<T>::store(yr + worker, hv);
                 if (has_t) Elem<T>::store(yr + te, tv);
             }

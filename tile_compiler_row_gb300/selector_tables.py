@@ -32,6 +32,7 @@ newer ones only), and FP16 runs count for the 2-byte tables with the BF16
 ones (the two types share the tables).
 
     python -m tile_compiler_row_gb300.selector_tables sweep --out tables.json   (GPU)
+    python -m tile_compiler_row_gb300.selector_tables sweep --family bf16 --out b16.json
     python -m tile_compiler_row_gb300.selector_tables emit tables.json          (writes the header)
 
 ``sweeps/selector_sweeps.json.gz`` holds the sweeps the committed header was
@@ -82,7 +83,7 @@ def sweep_rows(dtype, width):
     return max(16, (1 << (26 if dtype == "f32" else 27)) // width)
 
 
-def run_sweep(out, warmup=5, iters=30, forward=True, backward=True):
+def run_sweep(out, warmup=5, iters=30, forward=True, backward=True, families=tuple(FAMILIES)):
     import torch
 
     import tile_compiler_row_gb300 as tile
@@ -93,7 +94,7 @@ def run_sweep(out, warmup=5, iters=30, forward=True, backward=True):
     torch.cuda.set_device(0)
     stream = torch.cuda.current_stream()
     records = []
-    for dtype in FAMILIES:
+    for dtype in families:
         for width in LADDER[dtype]:
             rows = sweep_rows(dtype, width)
             t = make_tensors(rows, width, dtype)
@@ -106,7 +107,7 @@ def run_sweep(out, warmup=5, iters=30, forward=True, backward=True):
                 records.append(e)
                 print(json.dumps(e), flush=True)
             del t
-    for rows, width in (SMALL if forward else ()):
+    for rows, width in (SMALL if forward and "f32" in families else ()):
         t = make_tensors(rows, width, "f32")
         for op in TABLE_OPS:
             e = sweep_entry(lib, op, "f32", rows, width, t, warmup, 200, stream, graph=True)
@@ -270,13 +271,16 @@ def main(argv=None):
     sw = sub.add_parser("sweep")
     sw.add_argument("--out", required=True)
     sw.add_argument("--only", choices=("forward", "backward"), default=None)
+    sw.add_argument("--family", choices=tuple(FAMILIES), default=None,
+                    help="sweep one element family (default: both)")
     em = sub.add_parser("emit", help="sweep JSON files -> the header (default: the "
                                        "committed sweeps)")
     em.add_argument("paths", nargs="*")
     em.add_argument("--header", default=HEADER)
     args = ap.parse_args(argv)
     if args.cmd == "sweep":
-        run_sweep(args.out, forward=args.only != "backward", backward=args.only != "forward")
+        run_sweep(args.out, forward=args.only != "backward", backward=args.only != "forward",
+                  families=(args.family,) if args.family else tuple(FAMILIES))
     else:
         records = []
         for p in args.paths:
