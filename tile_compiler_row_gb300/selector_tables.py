@@ -33,6 +33,7 @@ ones (the two types share the tables).
 
     python -m tile_compiler_row_gb300.selector_tables sweep --out tables.json   (GPU)
     python -m tile_compiler_row_gb300.selector_tables sweep --family bf16 --out b16.json
+    python -m tile_compiler_row_gb300.selector_tables sweep --family f16 --out f16.json
     python -m tile_compiler_row_gb300.selector_tables emit tables.json          (writes the header)
 
 ``sweeps/selector_sweeps.json.gz`` holds the sweeps the committed header was
@@ -95,7 +96,7 @@ def run_sweep(out, warmup=5, iters=30, forward=True, backward=True, families=tup
     stream = torch.cuda.current_stream()
     records = []
     for dtype in families:
-        for width in LADDER[dtype]:
+        for width in LADDER[family(dtype)]:
             rows = sweep_rows(dtype, width)
             t = make_tensors(rows, width, dtype)
             for op in (TABLE_OPS if forward else ()) + (BWD_OPS if backward else ()):
@@ -271,8 +272,9 @@ def main(argv=None):
     sw = sub.add_parser("sweep")
     sw.add_argument("--out", required=True)
     sw.add_argument("--only", choices=("forward", "backward"), default=None)
-    sw.add_argument("--family", choices=tuple(FAMILIES), default=None,
-                    help="sweep one element family (default: both)")
+    sw.add_argument("--family", choices=tuple(FAMILIES) + ("f16",), default=None,
+                    help="sweep one element type (default: FP32 and BF16; FP16 records count "
+                         "with the BF16 ones)")
     em = sub.add_parser("emit", help="sweep JSON files -> the header (default: the "
                                        "committed sweeps)")
     em.add_argument("paths", nargs="*")
