@@ -69,6 +69,19 @@ cudaError_t launch_plan(BwdArgs args, cudaStream_t stream) {
             // tests gamma at run time, because its G = false kernel measured
             // up to 28 % slower at 2048-16384 columns; softmax has no gamma.
             if constexpr (OP == BWD_LN_OP) {
+                // Rows 16-byte aligned and of whole vectors (all three
+                // pointers share the phase) take the kernel without a
+                // scalar head and tail where that measured faster: plan 6's
+                // shape (S = 4, P = 1, K = 4), 7 % at 65536 x 4096 BF16 (64
+                // registers instead of 70, 8 CTAs per SM instead of 7).  At
+                // plans 4 and 7 the same kernel measured 3 % and 33 %
+                // slower, at 1024 and 16384 columns within about 1 %.
+                if constexpr (S == 4 && P == 1 && K == 4 && C == 1) {
+                    if ((reinterpret_cast<uintptr_t>(args.x) & 15) == 0 && args.width % EV == 0)
+                        return cudaLaunchKernelEx(
+                            &cfg, row_bwd_raw_kernel<OP, TILE_BWD_T, S, P, K, C, true, true>,
+                            args);
+                }
                 return cudaLaunchKernelEx(&cfg, row_bwd_raw_kernel<OP, TILE_BWD_T, S, P, K, C, true>,
                                           args);
             } else if constexpr (OP == BWD_RMS_OP) {

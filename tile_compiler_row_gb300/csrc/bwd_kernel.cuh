@@ -385,10 +385,14 @@ __device__ __forceinline__ void dot_raw8(const unsigned int (&a)[4], const unsig
 // load per vector where g is used, and the output map
 // dx = rstd g + ca d + cb runs on packed f32x2 pairs per vector just before
 // its store.  G: gamma may be present (the host launches G = false for
-// RMSNorm without gamma, whose kernel then has no gamma code).
-template <int OP, class T, int S, int P, int K, int C, bool G>
+// RMSNorm without gamma, whose kernel then has no gamma code).  WH: every
+// row is 16-byte aligned and holds whole vectors, so the kernel carries no
+// scalar head or tail (the same results: a head and tail of no elements add
+// exact zeros).
+template <int OP, class T, int S, int P, int K, int C, bool G, bool WH = false>
 __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a) {
     static_assert(sizeof(T) == 2, "2-byte element types");
+    constexpr bool HT = !WH;   // the row may have a scalar head and tail
     static_assert(C == 1 || P == 1, "a cluster row has one program per CTA");
     constexpr int W = 32 * S;
     constexpr int EV = 8;
@@ -422,11 +426,14 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
     const T *dr = static_cast<const T *>(a.dy) + base;
     T *outr = static_cast<T *>(a.dx) + base;
 
-    const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(xr) / sizeof(T)) & (EV - 1));
-    int h = (EV - mis) & (EV - 1);
-    if (h > width) h = width;
-    const int nb = (width - h) / EV;
-    const int tl = width - h - nb * EV;
+    int h = 0, nb = width / EV, tl = 0;
+    if constexpr (HT) {
+        const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(xr) / sizeof(T)) & (EV - 1));
+        h = (EV - mis) & (EV - 1);
+        if (h > width) h = width;
+        nb = (width - h) / EV;
+        tl = width - h - nb * EV;
+    }
     const int gw = rank * W + worker;
 
     // ---- load both stripes once, as raw words --------------------------
@@ -444,8 +451,8 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
             for (int q = 0; q < 4; ++q) xw[k][q] = dw[k][q] = 0u;   // +0.0 in both types
         }
     }
-    const bool has_h = (rank == 0) && (worker < h);
-    const bool has_t = (rank == 0) && (worker < tl);
+    const bool has_h = HT && (rank == 0) && (worker < h);
+    const bool has_t = HT && (rank == 0) && (worker < tl);
     const int te = h + EV * nb + worker;
     float hv = 0.0f, tv = 0.0f, hu = 0.0f, tu = 0.0f;
     if (has_h) {
@@ -500,7 +507,7 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
     float mean0 = 0.0f, rstd = 1.0f, mean = 0.0f, ca = 0.0f, cb = 0.0f, dot = 0.0f;
     if constexpr (OP == BWD_SOFTMAX) {
         // ---- sum(dy * y) ---------------------------------------------------
-        float s0 = fmaf(hu, hv, tu * tv), s1 = 0.0f;
+        float s0 = HT ? fmaf(hu, hv, tu * tv) : 0.0f, s1 = 0.0f;
 #pragma unroll
         for (int k = 0; k < K; ++k) dot_raw8<T>(dw[k], xw[k], s0, s1);   // empty slots add 0
         float s[1] = {s0 + s1};
@@ -514,7 +521,7 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
             // four independent partial sums (the first estimate of the mean
             // only shifts the data; measured faster than one chain or packed
             // pairs)
-            float s4[4] = {hv + tv, 0.0f, 0.0f, 0.0f};
+            float s4[4] = {HT ? hv + tv : 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int k = 0; k < K; ++k) acc_raw8<T>(xw[k], s4);   // empty slots add 0
             float s[1] = {(s4[0] + s4[1]) + (s4[2] + s4[3])};
@@ -537,12 +544,14 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
                     }
                 }
             }
-            hv = has_h ? hv - mean0 : 0.0f;
-            tv = has_t ? tv - mean0 : 0.0f;
-            q[0] += hv + tv;
-            q[1] = fmaf(hv, hv, fmaf(tv, tv, q[1]));
-            q[2] += hu + tu;
-            q[3] = fmaf(hu, hv, fmaf(tu, tv, q[3]));
+            if constexpr (HT) {
+                hv = has_h ? hv - mean0 : 0.0f;
+                tv = has_t ? tv - mean0 : 0.0f;
+                q[0] += hv + tv;
+                q[1] = fmaf(hv, hv, fmaf(tv, tv, q[1]));
+                q[2] += hu + tu;
+                q[3] = fmaf(hu, hv, fmaf(tu, tv, q[3]));
+            }
             row_allreduce<Sum, 4, S, P, C>(q, part2, cpart + 1, program, warp, lane);
             const float mu1 = over_n<T>(q[0], n, a.inv_n);
             const float var = fmaxf(over_n<T>(q[1], n, a.inv_n) - mu1 * mu1, 0.0f);
@@ -553,8 +562,8 @@ __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a
             ca = -rstd * rstd * mean_gx;
             cb = rstd * fmaf(rstd * mean_gx, mu1, -mean_g);
         } else {
-            float q0 = fmaf(hv, hv, tv * tv), q1 = 0.0f;
-            float g0 = fmaf(hu, hv, tu * tv), g1 = 0.0f;
+            float q0 = HT ? fmaf(hv, hv, tv * tv) : 0.0f, q1 = 0.0f;
+            float g0 = HT ? fmaf(hu, hv, tu * tv) : 0.0f, g1 = 0.0f;
             if (gam == nullptr) {
                 // sum x^2 and sum dy x straight from the raw words (mixed
                 // fma: the products are exact), two accumulators each
