@@ -146,9 +146,39 @@ __device__ __forceinline__ void rows_widened(const T *__restrict__ x, const T *_
     }
 }
 
+// (a0, a1) -= (b0, b1), one packed instruction (PTX sub.rn.f32x2, sm_100
+// and later); each lane is rounded as the scalar subtraction.
+__device__ __forceinline__ void sub_x2(float &a0, float &a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb;\n\tmov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
+        "sub.rn.f32x2 ra, ra, rb;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
+}
+
+// comp_add on two independent (sum, compensation) pairs at once: the same
+// TwoSum steps lane by lane on packed pairs, so each lane's result is
+// bitwise that of comp_add.
+__device__ __forceinline__ void comp_add_x2(float (&s)[2], float (&c)[2], float v0, float v1) {
+    float n0 = s[0], n1 = s[1];
+    add_x2(n0, n1, v0, v1);                  // s' = s + v
+    float b0 = n0, b1 = n1;
+    sub_x2(b0, b1, s[0], s[1]);              // bb = s' - s
+    float r0 = n0, r1 = n1;
+    sub_x2(r0, r1, b0, b1);                  // s' - bb
+    float a0 = s[0], a1 = s[1];
+    sub_x2(a0, a1, r0, r1);                  // s - (s' - bb)
+    sub_x2(v0, v1, b0, b1);                  // v - bb
+    add_x2(a0, a1, v0, v1);                  // e
+    add_x2(c[0], c[1], a0, a1);              // c += e
+    s[0] = n0;
+    s[1] = n1;
+}
+
 // 2-byte rows of whole aligned groups of four: eight rows in flight kept as
 // raw words (a register carries 4 bytes of DRAM data instead of 2), summed
-// as two trees of four.
+// as two trees of four.  The two columns of a word go through packed f32x2
+// pairs (the products, the trees and the compensated sums), each lane
+// rounded as the scalar code rounds it, so the results are bitwise those
+// of one column at a time with a third fewer instructions.
 template <class T>
 __device__ __forceinline__ void rows_raw(const T *__restrict__ x, const T *__restrict__ dy,
                                          const float *__restrict__ stats, long long r0,
@@ -175,19 +205,37 @@ __device__ __forceinline__ void rows_raw(const T *__restrict__ x, const T *__res
             }
         }
 #pragma unroll
-        for (int j = 0; j < kCols; ++j)
+        for (int w = 0; w < kCols / 2; ++w)          // columns 2w and 2w + 1
 #pragma unroll
             for (int g = 0; g < R / 4; ++g) {
-                float t[4], d[4];
+                float t[4][2], d[4][2];
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     const int q = 4 * g + q4;
-                    const float xc = add_half<T>(xw[q][j >> 1], j & 1, -mu[q]);   // x - mu
-                    d[q4] = widen_half<T>(dw[q][j >> 1], j & 1);
-                    t[q4] = d[q4] * (xc * rs[q]);
+                    float x0 = add_half<T>(xw[q][w], 0, -mu[q]);         // x - mu
+                    float x1 = add_half<T>(xw[q][w], 1, -mu[q]);
+                    mul_x2(x0, x1, rs[q], rs[q]);                        // (x - mu) rstd
+                    d[q4][0] = widen_half<T>(dw[q][w], 0);
+                    d[q4][1] = widen_half<T>(dw[q][w], 1);
+                    t[q4][0] = d[q4][0];
+                    t[q4][1] = d[q4][1];
+                    mul_x2(t[q4][0], t[q4][1], x0, x1);                  // dy xhat
                 }
-                comp_add(sg[j], cg[j], tree4(t[0], t[1], t[2], t[3]));
-                comp_add(sb[j], cb[j], tree4(d[0], d[1], d[2], d[3]));
+                // tree4 on pairs: (a + b) + (c + d)
+                add_x2(t[0][0], t[0][1], t[1][0], t[1][1]);
+                add_x2(t[2][0], t[2][1], t[3][0], t[3][1]);
+                add_x2(t[0][0], t[0][1], t[2][0], t[2][1]);
+                add_x2(d[0][0], d[0][1], d[1][0], d[1][1]);
+                add_x2(d[2][0], d[2][1], d[3][0], d[3][1]);
+                add_x2(d[0][0], d[0][1], d[2][0], d[2][1]);
+                float sgp[2] = {sg[2 * w], sg[2 * w + 1]}, cgp[2] = {cg[2 * w], cg[2 * w + 1]};
+                float sbp[2] = {sb[2 * w], sb[2 * w + 1]}, cbp[2] = {cb[2 * w], cb[2 * w + 1]};
+                comp_add_x2(sgp, cgp, t[0][0], t[0][1]);
+                comp_add_x2(sbp, cbp, d[0][0], d[0][1]);
+                sg[2 * w] = sgp[0]; sg[2 * w + 1] = sgp[1];
+                cg[2 * w] = cgp[0]; cg[2 * w + 1] = cgp[1];
+                sb[2 * w] = sbp[0]; sb[2 * w + 1] = sbp[1];
+                cb[2 * w] = cbp[0]; cb[2 * w + 1] = cbp[1];
             }
     }
 }
