@@ -200,7 +200,10 @@ int tile_run_plan_args_f32(int op, int plan_id, const tile_row_args_t *args, cud
  * only and name low precision as not covered, "Residual LayerNorm
  * shared-Tile materialization search", "Exact command").  Each element is
  * widened exactly to FP32, every reduction and map runs in FP32 as for the
- * FP32 entry points, and outputs are rounded to nearest-even BF16.  gamma,
+ * FP32 entry points (except that the row statistics multiply by 1/width
+ * and take rsqrtf, at most 2 ulp, where the FP32 rows divide and take a
+ * correctly rounded 1/sqrt: a few FP32 ulp, far inside half a BF16 ulp),
+ * and outputs are rounded to nearest-even BF16.  gamma,
  * beta and the row outputs of sum and min/max stay FP32.  Pointers to BF16
  * data must be 2-byte aligned; 16-byte vectors (8 elements) are used when
  * in, residual and out share a 16-byte phase.  Everything else is the
@@ -225,8 +228,9 @@ int tile_row_minmax_bf16(const void *in, float *mins, float *maxs, int rows, int
 /* ---- FP16 rows ----------------------------------------------------------
  * The same row operations on IEEE binary16 data (the "FP16 I/O" of low
  * precision the pages name as not covered, same section as above): each
- * element is widened exactly to FP32, every reduction and map runs in FP32,
- * outputs are rounded to nearest-even binary16 (an output beyond 65504
+ * element is widened exactly to FP32, every reduction and map runs in FP32
+ * (row statistics as for BF16 rows), outputs are rounded to nearest-even
+ * binary16 (an output beyond 65504
  * becomes +-inf, as a binary16 rounding does; normalised rows stay far below
  * it).  Layout, alignment, vectors, plans and errors as the BF16 entry
  * points; gamma, beta and the row outputs of sum and min/max stay FP32. */
@@ -294,7 +298,8 @@ int tile_norm_param_grad_f32(const float *in, const float *dy, const float *row_
 
 /* The backward passes with BF16 or FP16 in / y, dy and dx (2 bytes per
  * element, 2-byte aligned): every element is widened exactly to FP32, the
- * statistics, sums and maps run in FP32 as above, and dx is rounded to
+ * statistics, sums and maps run in FP32 as above (row statistics as for the
+ * 2-byte forward rows), and dx is rounded to
  * nearest-even of its type.  gamma, row_stats, dgamma, dbeta and the
  * workspace stay FP32; tile_norm_param_grad_* uses the same workspace size.
  * 16-byte vectors (8 elements) are used when in, dy and dx share a 16-byte
