@@ -4,7 +4,6 @@ a wrong sign, a wrong denominator, a wrong index or row stride, a missing
 max subtraction.  Nothing here touches the real oracle or a GPU."""
 
 import os
-import shutil
 
 import pytest
 

@@ -15,7 +15,7 @@ import torch
 import oracle
 import synth
 import tile_compiler_row_gb300 as tile
-from parity import ATOL, EPS, RTOL, compare, ref_eps
+from parity import ATOL, EPS, RTOL, ref_eps
 
 pytestmark = pytest.mark.gpu
 
