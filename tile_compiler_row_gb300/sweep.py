@@ -95,7 +95,7 @@ def time_call(call, warmup, iters, stream, graph=False, cutoff=None):
 
 
 def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g=None, y2=None,
-              graph=False, cutoff=None):
+              graph=False, cutoff=None, b=None):
     """Median microseconds per call of forward plan ``plan`` (time_call)."""
     import ctypes
 
@@ -106,7 +106,7 @@ def time_plan(lib, op_code, plan, x, r, y, rows, width, warmup, iters, stream, g
     a.in_, a.out = x.data_ptr(), y.data_ptr()
     a.residual = r.data_ptr() if r is not None else None
     a.gamma = g.data_ptr() if g is not None else None
-    a.beta = None
+    a.beta = b.data_ptr() if b is not None else None
     a.out2 = y2.data_ptr() if y2 is not None else None
     a.rows, a.width, a.eps = rows, width, 1e-5
     a.dtype = {torch.bfloat16: 1, torch.float16: 2}.get(x.dtype, 0)
@@ -137,22 +137,26 @@ def make_tensors(rows, width, dtype):
         x, r = x.to(t), r.to(t)
     return {"x": x, "r": r, "y": torch.empty_like(x),
             "g": torch.rand(width, device="cuda", generator=gen) + 0.5,
+            "b": torch.rand(width, device="cuda", generator=gen) - 0.5,
             "y2": torch.empty(rows, device="cuda")}
 
 
 def sweep_entry(lib, op, dtype, rows, width, t, warmup, iters, stream, graph=False,
-                only=None):
+                only=None, beta=False):
     """Every covering 16-byte-vector plan of ``op`` at one shape, timed (µs,
     median); then the two fastest again in alternating order A B B A: the two
-    runs of A give the A/A noise floor that B's margin is read against."""
+    runs of A give the A/A noise floor that B's margin is read against.
+    ``beta``: affine LayerNorm called with a beta vector as well (the tables
+    are swept without one)."""
     import tile_compiler_row_gb300 as tile
     base = op.split("+")[0]          # "layernorm_affine+residual": with a residual
     code = tile.OPS[base]
     r = t["r"] if (op in USES_RESIDUAL or op.endswith("+residual")) else None
     # the selector's choice, where tile_describe_plan_ex can describe the call
     chosen = tile.tile_describe_plan_ex(base, dtype, rows, width)["id"] if base == op else None
+    bvec = t["b"] if beta and base == "layernorm_affine" else None
     entry = {"op": op, "rows": rows, "width": width, "selected": chosen, "plans": {},
-             "dtype": dtype,
+             "dtype": dtype, "beta": bvec is not None,
              "timing": "cuda graph replay" if graph else "back-to-back launches"}
     for pid in range(tile.tile_plan_count()):
         info = tile.tile_plan_info_ex(pid, base, dtype, rows, width)
@@ -163,7 +167,7 @@ def sweep_entry(lib, op, dtype, rows, width, t, warmup, iters, stream, graph=Fal
         best_so_far = min(entry["plans"].values(), default=None)
         us = time_plan(lib, code, pid, t["x"], r, t["y"], rows, width, warmup, iters, stream,
                        g=t["g"], y2=t["y2"], graph=graph,
-                       cutoff=None if best_so_far is None else 3.0 * best_so_far)
+                       cutoff=None if best_so_far is None else 3.0 * best_so_far, b=bvec)
         entry["plans"][pid] = round(us, 3)
     best = min(entry["plans"], key=entry["plans"].get)
     ranked = sorted(entry["plans"], key=entry["plans"].get)
@@ -173,7 +177,7 @@ def sweep_entry(lib, op, dtype, rows, width, t, warmup, iters, stream, graph=Fal
         for pid in (a, b, b, a):
             rerun[pid].append(round(time_plan(lib, code, pid, t["x"], r, t["y"], rows, width,
                                               warmup, iters, stream, g=t["g"], y2=t["y2"],
-                                              graph=graph), 3))
+                                              graph=graph, b=bvec), 3))
         entry["confirm"] = {
             "order": [a, b, b, a], "us": {str(a): rerun[a], str(b): rerun[b]},
             "aa_noise": round(abs(rerun[a][0] - rerun[a][1]) / min(rerun[a]), 4),
@@ -262,6 +266,8 @@ def main(argv=None):
                     help="time calls replayed from a CUDA graph (no host launch overhead)")
     ap.add_argument("--small", action="store_true", help="only the small workload shapes")
     ap.add_argument("--dtype", default="f32", choices=("f32", "bf16", "f16"))
+    ap.add_argument("--beta", action="store_true",
+                    help="call affine LayerNorm with a beta vector too")
     ap.add_argument("--plans", default=None,
                     help="comma list of plan ids to time (default: every covering plan)")
     args = ap.parse_args(argv)
@@ -284,7 +290,7 @@ def main(argv=None):
         t = make_tensors(rows, width, args.dtype)
         for op in args.ops.split(","):
             entry = sweep_entry(lib, op, args.dtype, rows, width, t, args.warmup, args.iters,
-                                stream, graph=args.graph, only=only)
+                                stream, graph=args.graph, only=only, beta=args.beta)
             results.append(entry)
             print(json.dumps(entry), flush=True)
         del t
