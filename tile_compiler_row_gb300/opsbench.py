@@ -67,6 +67,7 @@ def main(argv=None):
     tile.tile_softmax_f32(x, y2)
     sm = y2.clone()
     smb = sm.to(torch.bfloat16)
+    smh = sm.to(torch.float16)
     tile.tile_layernorm_backward_f32(x, None, r, y, stats)
 
     ops = {
@@ -92,6 +93,8 @@ def main(argv=None):
         "layernorm_f16": (lambda: tile.tile_layernorm_f16(xh, yh), 4),
         "rmsnorm_f16": (lambda: tile.tile_rmsnorm_f16(xh, yh), 4),
         "softmax_f16": (lambda: tile.tile_softmax_f16(xh, yh), 4),
+        "layernorm_affine_f16": (lambda: tile.tile_layernorm_affine_f16(xh, None, g, b, yh), 4),
+        "rmsnorm_weighted_f16": (lambda: tile.tile_rmsnorm_weighted_f16(xh, g, yh), 4),
         "layernorm_backward": (lambda: tile.tile_layernorm_backward_f32(x, g, r, y, stats), 12),
         "rmsnorm_backward": (lambda: tile.tile_rmsnorm_backward_f32(x, g, r, y, stats), 12),
         "softmax_backward": (lambda: tile.tile_softmax_backward_f32(sm, r, y), 12),
@@ -102,6 +105,12 @@ def main(argv=None):
         "softmax_backward_bf16": (lambda: tile.tile_softmax_backward_bf16(smb, rb, yb), 6),
         "norm_param_grad_bf16": (lambda: tile.tile_norm_param_grad_bf16(xb, rb, stats, dg, db, ws),
                                  4),
+        "layernorm_backward_f16": (lambda: tile.tile_layernorm_backward_f16(xh, g, rh, yh, stats),
+                                   6),
+        "rmsnorm_backward_f16": (lambda: tile.tile_rmsnorm_backward_f16(xh, g, rh, yh, stats), 6),
+        "softmax_backward_f16": (lambda: tile.tile_softmax_backward_f16(smh, rh, yh), 6),
+        "norm_param_grad_f16": (lambda: tile.tile_norm_param_grad_f16(xh, rh, stats, dg, db, ws),
+                                4),
     }
     only = set(args.only.split(",")) if args.only else None
     peak, src = measured_hbm_gbs()
