@@ -500,6 +500,18 @@ int tile_plan_info_ex(int id, int op, int dtype, int rows, int width, tile_plan_
  * skip or count, or a zero error with count > 0. */
 int tile_inject_launch_failure(int cuda_error, int skip, int count);
 
+/* Test hook for the whole-vector kernels (the notes have no counterpart).
+ * 2-byte rows that are 16-byte aligned and hold whole 16-byte vectors run
+ * a form of the row kernel (and, on the S = 4, P = 1, K = 4 shape, of the
+ * LayerNorm backward kernel) without a scalar head and tail; its results
+ * are bitwise those of the general form, where a head and tail of no
+ * elements add exact +0 terms (which can change only the sign of a zero
+ * result, after a partial sum of exactly -0).  With `on` nonzero every
+ * later launch takes the general form instead, so a test can compare the
+ * two on the same rows; 0 restores the default.  Process-wide, host only;
+ * returns TILE_OK. */
+int tile_test_force_general_kernels(int on);
+
 /* Test hook for the bounded waits of the shared-memory-staged kernel (the
  * notes have no counterpart: their kernels have no copy engine to wait on).
  * Runs the staged plan `plan_id` (path TILE_PATH_STAGED) of `op` on `args`

@@ -39,7 +39,7 @@ __all__ = [
     "tile_layernorm_backward_bf16", "tile_rmsnorm_backward_bf16", "tile_softmax_backward_bf16",
     "tile_norm_param_grad_bf16", "tile_layernorm_backward_f16", "tile_rmsnorm_backward_f16",
     "tile_softmax_backward_f16", "tile_norm_param_grad_f16", "tile_test_staged_wait_timeout",
-    "tile_inject_launch_failure", "tile_describe_backward_plan",
+    "tile_inject_launch_failure", "tile_describe_backward_plan", "tile_test_force_general_kernels",
     "residual_layernorm", "layernorm", "rmsnorm", "softmax", "run",
 ]
 
@@ -164,6 +164,7 @@ def load():
         "tile_plan_info_ex": [I, I, I, I, I, ctypes.POINTER(TilePlan)],
         "tile_test_staged_wait_timeout": [I, I, ctypes.POINTER(TileRowArgs), ctypes.c_uint, P],
         "tile_inject_launch_failure": [I, I, I],
+        "tile_test_force_general_kernels": [I],
         "tile_describe_backward_plan": [I, I, I, I, ctypes.POINTER(TilePlan)],
     }
     for name, argtypes in sigs.items():
@@ -346,6 +347,13 @@ def tile_inject_launch_failure(cuda_error, skip=0, count=1):
     the host with ``cuda_error`` (``count=0`` disarms)."""
     _check(load().tile_inject_launch_failure(int(cuda_error), int(skip), int(count)),
            "tile_inject_launch_failure")
+
+
+def tile_test_force_general_kernels(on):
+    """Test hook: with ``on`` true, 2-byte launches take the general kernel
+    forms instead of the whole-vector ones (bitwise the same results)."""
+    _check(load().tile_test_force_general_kernels(int(bool(on))),
+           "tile_test_force_general_kernels")
 
 
 def tile_test_staged_wait_timeout(op, plan_id, x, out, spin_limit, residual=None, gamma=None,

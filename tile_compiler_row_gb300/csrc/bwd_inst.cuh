@@ -77,7 +77,8 @@ cudaError_t launch_plan(BwdArgs args, cudaStream_t stream) {
                 // plans 4 and 7 the same kernel measured 3 % and 33 %
                 // slower, at 1024 and 16384 columns within about 1 %.
                 if constexpr (S == 4 && P == 1 && K == 4 && C == 1) {
-                    if ((reinterpret_cast<uintptr_t>(args.x) & 15) == 0 && args.width % EV == 0)
+                    if ((reinterpret_cast<uintptr_t>(args.x) & 15) == 0 && args.width % EV == 0 &&
+                        whole_vector_kernels())
                         return cudaLaunchKernelEx(
                             &cfg, row_bwd_raw_kernel<OP, TILE_BWD_T, S, P, K, C, true, true>,
                             args);

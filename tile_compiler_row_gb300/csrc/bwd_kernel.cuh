@@ -388,7 +388,7 @@ __device__ __forceinline__ void dot_raw8(const unsigned int (&a)[4], const unsig
 // RMSNorm without gamma, whose kernel then has no gamma code).  WH: every
 // row is 16-byte aligned and holds whole vectors, so the kernel carries no
 // scalar head or tail (the same results: a head and tail of no elements add
-// exact zeros).
+// exact +0 terms, which can change only the sign of a zero).
 template <int OP, class T, int S, int P, int K, int C, bool G, bool WH = false>
 __global__ void __launch_bounds__(32 * S * P) row_bwd_raw_kernel(const BwdArgs a) {
     static_assert(sizeof(T) == 2, "2-byte element types");

@@ -151,6 +151,10 @@ int run_host(int op, const float *h_in, const float *h_res, float *h_out, int ro
 // launching.
 cudaError_t injected_launch_failure();
 
+// Whether 2-byte launches may take the whole-vector kernel forms (false
+// while tile_test_force_general_kernels holds them on the general forms).
+bool whole_vector_kernels();
+
 // The cudaError_t behind the last TILE_ERR_CUDA on this host thread.
 void set_last_cuda_error(int err);
 int last_cuda_error();

@@ -64,7 +64,8 @@ cudaError_t launch_plan(RowArgs args, cudaStream_t stream) {
         // 2-byte rows that are 16-byte aligned and hold whole vectors take
         // the kernel without a scalar head and tail (bitwise the same results)
         if constexpr (V == 4 && sizeof(TILE_INST_T) == 2) {
-            if ((reinterpret_cast<uintptr_t>(args.x) & 15) == 0 && args.width % EV == 0)
+            if ((reinterpret_cast<uintptr_t>(args.x) & 15) == 0 && args.width % EV == 0 &&
+                whole_vector_kernels())
                 return cudaLaunchKernelEx(
                     &cfg, row_kernel<TILE_INST_OP, TILE_INST_T, V, S, P, K, C, true>, args);
         }

@@ -528,7 +528,8 @@ constexpr int row_min_blocks() {
 // carries none of their loads, sums and stores.  The launcher takes it when
 // the rows are aligned and the width is a multiple of the vector; the
 // results are bitwise those of the general kernel (a head and tail of zero
-// elements contribute exact zeros).
+// elements contribute exact +0 terms, which can change only the sign of a
+// partial sum that is exactly -0, and so of a zero result).
 template <int OP, class T, int V, int S, int P, int K, int C, bool WH = false>
 __global__ void __launch_bounds__(32 * S * P, (row_min_blocks<T, V, S, P, K>()))
     row_kernel(const RowArgs a) {

@@ -556,7 +556,13 @@ thread_local int t_last_cuda_error = 0;
 std::mutex g_inject_mu;
 std::atomic<int> g_inject_armed{0};
 int g_inject_skip = 0, g_inject_count = 0, g_inject_code = 0;
+
+// tile_test_force_general_kernels: nonzero while the general kernel forms
+// are forced.
+std::atomic<int> g_force_general{0};
 }  // namespace
+
+bool whole_vector_kernels() { return g_force_general.load(std::memory_order_relaxed) == 0; }
 
 void set_last_cuda_error(int err) { t_last_cuda_error = err; }
 int last_cuda_error() { return t_last_cuda_error; }
@@ -862,6 +868,11 @@ int tile_inject_launch_failure(int cuda_error, int skip, int count) {
     tile::g_inject_skip = skip;
     tile::g_inject_count = count;
     tile::g_inject_armed.store(count > 0 ? 1 : 0, std::memory_order_release);
+    return TILE_OK;
+}
+
+int tile_test_force_general_kernels(int on) {
+    tile::g_force_general.store(on != 0 ? 1 : 0, std::memory_order_relaxed);
     return TILE_OK;
 }
 
