@@ -258,6 +258,17 @@ def test_injected_launch_failures_are_reported_without_a_cuda_call(lib):
         assert lib.tile_inject_launch_failure(0, 0, 0) == OK
 
 
+def test_general_kernel_hook_is_host_only(lib):
+    """tile_test_force_general_kernels sets a process-wide host flag: TILE_OK
+    for any value on a machine without a GPU, and 0 restores the default
+    (its effect on the launches is tested on the GPU)."""
+    try:
+        assert lib.tile_test_force_general_kernels(1) == OK
+        assert lib.tile_test_force_general_kernels(7) == OK
+    finally:
+        assert lib.tile_test_force_general_kernels(0) == OK
+
+
 @fake_pointers
 def test_staged_wait_hook_rejects_bad_arguments(lib):
     a = tile.TileRowArgs()
